@@ -1,0 +1,657 @@
+#!/usr/bin/env python3
+"""Benchmark of the MXFP8 training hot path on GB300.
+
+One step = one pass of the hot path over one batch of synthetic input.  The
+default workload is the linear layer X [8192, 4096], W [4096, 4096],
+dY [8192, 4096]: dual-axis 1x32 quantization of X, W and dY, then the
+forward (Y = X W^T), dgrad (dX = dY W) and wgrad (dW = dY^T X) block-scaled
+GEMMs with BF16 output.  Other workloads (--workload): linear_fwd_small,
+weight_32x32 (32x32 weight payload shared by forward and dgrad), moe_grouped
+(128-expert grouped GEMMs), sweep_4096 / sweep_7168 / sweep_16384.
+
+Prints one JSON line.  `value` is the step's GEMM FLOPs divided by the step
+time (quantizers included), inputs resident in HBM, timed with CUDA events
+on the launching stream; L2 is flushed (256 MB write) between timed steps,
+outside the timed intervals.  `e2e` is the same metric through the public
+API with the inputs copied from pinned host memory and the BF16 results
+copied back inside every timed step.  `roofline` covers the GEMM kernel,
+`roofline_quant` the quantizers.  `cpu_baseline` times the oracle on a
+bounded sample.  `--impl reference` times the oracle alone (CPU).
+
+Multi-GPU: the path has no exchange step, so N ranks run N independent
+replicas (weak scaling); the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MXFP8 GEMM TFLOP/s (% dense MXFP8 peak); quantizer TB/s (% HBM), 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+L2_FLUSH_BYTES = 256 << 20   # larger than the 129 MB L2
+GEMM_TRAFFIC_BYTES = None    # filled from an ncu capture of the current GEMM kernel
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ---- distributed plumbing (replicas; only timing crosses ranks) ------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Maximum of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def aggregate_value(flops_per_rank_step: float, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job TFLOP/s: the FLOPs all ranks did divided by the slowest rank's time."""
+    return flops_per_rank_step * steps * world / max_seconds / 1e12
+
+
+# ---- clocks -----------------------------------------------------------------------------
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = [p for (t, p) in self.samples if t0 <= t <= t1] or [p for (_, p) in self.samples]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---- workloads -----------------------------------------------------------------------------
+
+class Workload:
+    """Device tensors, preallocated outputs and the ordered kernel launches of one step."""
+    name = ""
+    inputs: dict
+    outputs: list
+
+    def kernels(self):
+        """[(name, kind, algorithmic units, launch fn)]: kind 'gemm' (units = FLOPs)
+        or 'quant' (units = bytes moved by the algorithm)."""
+        raise NotImplementedError
+
+    @property
+    def gemm_flops(self):
+        """GEMM FLOPs of one step (2 per multiply-add)."""
+        raise NotImplementedError
+
+
+def _dual_bytes(r, c):
+    return r * c * (2 + 1 + 1) + 2 * (r * c // 32)
+
+
+def _row_bytes(r, c):
+    return r * c * (2 + 1) + r * c // 32
+
+
+def _blk_bytes(r, c):
+    return r * c * (2 + 1) + 2 * (r * c // 32)
+
+
+class LinearTrain(Workload):
+    def __init__(self, name, M, N, K, gen, dev=None):
+        import torch
+        from mxfp8_microscaled_precision_gb300 import mxq
+        self.name, self.M, self.N, self.K = name, M, N, K
+        self.inputs = gen(dev or "cpu")
+        if dev is None:          # host-only: the oracle arm
+            return
+        u8 = dict(dtype=torch.uint8, device=dev)
+
+        def dual_out(r, c):
+            return (torch.empty((r, c), **u8), torch.empty(mxq.scale_bytes(r, c), **u8),
+                    torch.empty((c, r), **u8), torch.empty(mxq.scale_bytes(c, r), **u8))
+        self.qx, self.qw, self.qg = dual_out(M, K), dual_out(N, K), dual_out(M, N)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.y, self.dx, self.dw = torch.empty((M, N), **bf), torch.empty((M, K), **bf), torch.empty((N, K), **bf)
+        self.outputs = [self.y, self.dx, self.dw]
+
+    @property
+    def gemm_flops(self):
+        return 3 * 2 * self.M * self.N * self.K
+
+    def kernels(self):
+        from mxfp8_microscaled_precision_gb300 import mxq
+        M, N, K, i = self.M, self.N, self.K, self.inputs
+        xr, xrs, xc, xcs = self.qx
+        wr, wrs, wc, wcs = self.qw
+        gr, grs, gc, gcs = self.qg
+        return [
+            ("quant_X_dual", "quant", _dual_bytes(M, K), lambda: mxq.quant_1x32_dual(i["X"], out=self.qx)),
+            ("quant_W_dual", "quant", _dual_bytes(N, K), lambda: mxq.quant_1x32_dual(i["W"], out=self.qw)),
+            ("quant_dY_dual", "quant", _dual_bytes(M, N), lambda: mxq.quant_1x32_dual(i["dY"], out=self.qg)),
+            ("gemm_fwd", "gemm", 2 * M * N * K, lambda: mxq.gemm(xr, xrs, wr, wrs, M, N, K, out=self.y)),
+            ("gemm_dgrad", "gemm", 2 * M * N * K, lambda: mxq.gemm(gr, grs, wc, wcs, M, K, N, out=self.dx)),
+            ("gemm_wgrad", "gemm", 2 * M * N * K, lambda: mxq.gemm(gc, gcs, xc, xcs, N, K, M, out=self.dw)),
+        ]
+
+    def cpu_sample(self, budget_s):
+        """Times the oracle on row samples of each step part; returns
+        (seconds per full step extrapolated, description)."""
+        from oracle import oracle
+        import numpy as np
+        i = self.inputs
+        x = _host_bits(i["X"][:256])
+        t0 = time.perf_counter()
+        oracle.quant_dual(x)
+        tq = (time.perf_counter() - t0) / x.size          # per element, dual
+        qr, sr = oracle.quant_rows(_host_bits(i["X"][:64]))
+        a = oracle.dequant_rows(qr, sr)
+        wq, ws = oracle.quant_rows(_host_bits(i["W"]))
+        b = oracle.dequant_rows(wq, ws)
+        rows, t_g = 0, 0.0
+        while t_g < budget_s and rows < a.shape[0]:
+            t0 = time.perf_counter()
+            oracle.gemm(a, b, rows=np.array([rows], dtype=np.int64))
+            t_g += time.perf_counter() - t0
+            rows += 1
+        tg = t_g / (2.0 * rows * self.N * self.K)          # per FLOP
+        quant_elems = self.M * self.K + self.N * self.K + self.M * self.N
+        step = tq * quant_elems + tg * self.gemm_flops
+        return step, (f"oracle dual quant of 256 rows of X ({x.size} elements) and FP64 GEMM of "
+                      f"{rows} output rows x {self.N} x {self.K}; extrapolated to the full step "
+                      f"({quant_elems} quantized elements, {self.gemm_flops:.4g} GEMM FLOPs)")
+
+
+class LinearFwdSmall(Workload):
+    def __init__(self, dev=None):
+        import torch
+        from mxfp8_microscaled_precision_gb300 import mxq, workloads
+        self.name, self.M, self.N, self.K = "linear_fwd_small", 256, 512, 512
+        self.inputs = workloads.linear_fwd_small(dev or "cpu")
+        if dev is None:
+            return
+        u8 = dict(dtype=torch.uint8, device=dev)
+        self.qx = (torch.empty((256, 512), **u8), torch.empty(mxq.scale_bytes(256, 512), **u8), None, None)
+        self.qw = (torch.empty((512, 512), **u8), torch.empty(mxq.scale_bytes(512, 512), **u8), None, None)
+        self.y = torch.empty((256, 512), dtype=torch.bfloat16, device=dev)
+        self.outputs = [self.y]
+
+    @property
+    def gemm_flops(self):
+        return 2 * self.M * self.N * self.K
+
+    def kernels(self):
+        from mxfp8_microscaled_precision_gb300 import mxq
+        i = self.inputs
+        return [
+            ("quant_X_row", "quant", _row_bytes(256, 512), lambda: mxq.quant_1x32_dual(i["X"], col=False, out=self.qx)),
+            ("quant_W_row", "quant", _row_bytes(512, 512), lambda: mxq.quant_1x32_dual(i["W"], col=False, out=self.qw)),
+            ("gemm_fwd", "gemm", 2 * 256 * 512 * 512,
+             lambda: mxq.gemm(self.qx[0], self.qx[1], self.qw[0], self.qw[1], 256, 512, 512, out=self.y)),
+        ]
+
+    def cpu_sample(self, budget_s):
+        from oracle import oracle
+        i = self.inputs
+        t0 = time.perf_counter()
+        xq, xs = oracle.quant_rows(_host_bits(i["X"]))
+        wq, ws = oracle.quant_rows(_host_bits(i["W"]))
+        oracle.gemm(oracle.dequant_rows(xq, xs), oracle.dequant_rows(wq, ws))
+        return time.perf_counter() - t0, "the whole step (quantization of X and W, FP64 GEMM)"
+
+
+class Weight32(Workload):
+    def __init__(self, dev=None):
+        import torch
+        from mxfp8_microscaled_precision_gb300 import mxq, workloads
+        self.name, self.M, self.n, self.k = "weight_32x32", 4096, 7168, 7168
+        self.inputs = workloads.weight_32x32(dev or "cpu")
+        if dev is None:
+            return
+        M, n, k = self.M, self.n, self.k
+        u8 = dict(dtype=torch.uint8, device=dev)
+        self.qw = (torch.empty((n, k), **u8), torch.empty(mxq.scale_bytes(n, k), **u8),
+                   torch.empty(mxq.scale_bytes(k, n), **u8))
+        self.qx = (torch.empty((M, k), **u8), torch.empty(mxq.scale_bytes(M, k), **u8), None, None)
+        self.qg = (torch.empty((M, n), **u8), torch.empty(mxq.scale_bytes(M, n), **u8), None, None)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.y, self.dx = torch.empty((M, n), **bf), torch.empty((M, k), **bf)
+        self.outputs = [self.y, self.dx]
+
+    @property
+    def gemm_flops(self):
+        return 2 * 2 * self.M * self.n * self.k
+
+    def kernels(self):
+        from mxfp8_microscaled_precision_gb300 import mxq
+        M, n, k, i = self.M, self.n, self.k, self.inputs
+        q, sf, sb = self.qw
+        return [
+            ("quant_W_32x32", "quant", _blk_bytes(n, k), lambda: mxq.quant_32x32(i["W"], out=self.qw)),
+            ("quant_X_row", "quant", _row_bytes(M, k), lambda: mxq.quant_1x32_dual(i["X"], col=False, out=self.qx)),
+            ("quant_dY_row", "quant", _row_bytes(M, n), lambda: mxq.quant_1x32_dual(i["dY"], col=False, out=self.qg)),
+            ("gemm_fwd", "gemm", 2 * M * n * k, lambda: mxq.gemm(self.qx[0], self.qx[1], q, sf, M, n, k, out=self.y)),
+            ("gemm_dgrad_mn", "gemm", 2 * M * n * k,
+             lambda: mxq.gemm(self.qg[0], self.qg[1], q, sb, M, k, n, b_mn_major=True, out=self.dx)),
+        ]
+
+    def cpu_sample(self, budget_s):
+        from oracle import oracle
+        import numpy as np
+        i = self.inputs
+        w = _host_bits(i["W"][:256])
+        t0 = time.perf_counter()
+        oracle.quant_32x32(w)
+        tq = (time.perf_counter() - t0) / w.size
+        xq, xs = oracle.quant_rows(_host_bits(i["X"][:64]))
+        a = oracle.dequant_rows(xq, xs)
+        oq, osf, _ = oracle.quant_32x32(_host_bits(i["W"]))
+        b = oracle.dequant_rows(oq, osf)
+        rows, t_g = 0, 0.0
+        while t_g < budget_s and rows < a.shape[0]:
+            t0 = time.perf_counter()
+            oracle.gemm(a, b, rows=np.array([rows], dtype=np.int64))
+            t_g += time.perf_counter() - t0
+            rows += 1
+        tg = t_g / (2.0 * rows * self.n * self.k)
+        elems = self.n * self.k + self.M * self.k + self.M * self.n
+        return tq * elems + tg * self.gemm_flops, (
+            f"oracle 32x32 quant of 256 weight rows and FP64 GEMM of {rows} rows x {self.n} x {self.k}; "
+            f"extrapolated to the full step")
+
+
+class MoE(Workload):
+    def __init__(self, dev=None):
+        import torch
+        from mxfp8_microscaled_precision_gb300 import mxq, workloads
+        self.name = "moe_grouped"
+        d = workloads.moe_grouped(dev or "cpu", weights=False)
+        G, H, I = 128, 4096, 2048
+        self.G, self.H, self.I = G, H, I
+        self.Mt = d["A"].shape[0]
+        seed_gu = workloads.seed_for("moe_grouped", "W")
+        seed_dn = workloads.seed_for("moe_grouped", "W_down")
+        if dev is None:          # host-only: the oracle arm needs one expert's weights
+            self.inputs = {"A": d["A"], "Hd": d["H"],
+                           "W_gate_up": workloads.normal((2 * I, H), 0.02, seed_gu)}
+            return
+        self.offsets = d["routing"].offsets.to(dev)
+        self.inputs = {"A": d["A"], "Hd": d["H"],
+                       "W_gate_up": workloads.normal((G * 2 * I, H), 0.02, seed_gu, device=dev),
+                       "W_down": workloads.normal((G * H, I), 0.02, seed_dn, device=dev)}
+        u8 = dict(dtype=torch.uint8, device=dev)
+
+        def row_out(r, c):
+            return (torch.empty((r, c), **u8), torch.empty(mxq.scale_bytes(r, c), **u8), None, None)
+        self.qa, self.qh = row_out(self.Mt, H), row_out(self.Mt, I)
+        self.qgu, self.qdn = row_out(G * 2 * I, H), row_out(G * H, I)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.y1, self.y2 = torch.empty((self.Mt, 2 * I), **bf), torch.empty((self.Mt, H), **bf)
+        self.outputs = [self.y1, self.y2]
+
+    @property
+    def gemm_flops(self):
+        return 2 * self.Mt * 2 * self.I * self.H + 2 * self.Mt * self.H * self.I
+
+    def kernels(self):
+        from mxfp8_microscaled_precision_gb300 import mxq
+        i, G, H, I, Mt = self.inputs, self.G, self.H, self.I, self.Mt
+        return [
+            ("quant_A_row", "quant", _row_bytes(Mt, H), lambda: mxq.quant_1x32_dual(i["A"], col=False, out=self.qa)),
+            ("quant_H_row", "quant", _row_bytes(Mt, I), lambda: mxq.quant_1x32_dual(i["Hd"], col=False, out=self.qh)),
+            ("quant_Wgu_row", "quant", _row_bytes(G * 2 * I, H),
+             lambda: mxq.quant_1x32_dual(i["W_gate_up"], col=False, out=self.qgu)),
+            ("quant_Wdn_row", "quant", _row_bytes(G * H, I),
+             lambda: mxq.quant_1x32_dual(i["W_down"], col=False, out=self.qdn)),
+            ("grouped_gate_up", "gemm", 2 * Mt * 2 * I * H,
+             lambda: mxq.grouped_gemm(self.qa[0], self.qa[1], self.qgu[0], self.qgu[1], self.offsets, 2 * I, H, out=self.y1)),
+            ("grouped_down", "gemm", 2 * Mt * H * I,
+             lambda: mxq.grouped_gemm(self.qh[0], self.qh[1], self.qdn[0], self.qdn[1], self.offsets, H, I, out=self.y2)),
+        ]
+
+    def cpu_sample(self, budget_s):
+        from oracle import oracle
+        import numpy as np
+        i = self.inputs
+        x = _host_bits(i["A"][:256])
+        t0 = time.perf_counter()
+        oracle.quant_rows(x)
+        tq = (time.perf_counter() - t0) / x.size
+        qa, sa = oracle.quant_rows(_host_bits(i["A"][:64]))
+        a = oracle.dequant_rows(qa, sa)
+        qb, sb = oracle.quant_rows(_host_bits(i["W_gate_up"][:2 * self.I]))   # expert 0
+        b = oracle.dequant_rows(qb, sb)
+        rows, t_g = 0, 0.0
+        while t_g < budget_s and rows < a.shape[0]:
+            t0 = time.perf_counter()
+            oracle.gemm(a, b, rows=np.array([rows], dtype=np.int64))
+            t_g += time.perf_counter() - t0
+            rows += 1
+        tg = t_g / (2.0 * rows * 2 * self.I * self.H)
+        elems = self.Mt * (self.H + self.I) + self.G * 2 * self.I * self.H + self.G * self.H * self.I
+        return tq * elems + tg * self.gemm_flops, (
+            f"oracle row quant of 256 routed rows and FP64 GEMM of {rows} rows against one expert "
+            f"(N {2 * self.I}, K {self.H}); extrapolated to the full step")
+
+
+def _host_bits(t):
+    import numpy as np
+    import torch
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def make_workload(name, dev=None):
+    """The workload on device `dev`, or host-only inputs when dev is None."""
+    from mxfp8_microscaled_precision_gb300 import workloads
+    if name == "linear_train":
+        return LinearTrain(name, 8192, 4096, 4096, lambda d: workloads.linear_train(d), dev)
+    if name.startswith("sweep_"):
+        K = int(name.split("_")[1])
+        return LinearTrain(name, 16384, K, K, lambda d: workloads.sweep(K, d), dev)
+    if name == "linear_fwd_small":
+        return LinearFwdSmall(dev)
+    if name == "weight_32x32":
+        return Weight32(dev)
+    if name == "moe_grouped":
+        return MoE(dev)
+    raise SystemExit(f"unknown workload {name}")
+
+
+WORKLOAD_NAMES = ["linear_train", "linear_fwd_small", "weight_32x32", "moe_grouped",
+                  "sweep_4096", "sweep_7168", "sweep_16384"]
+
+
+def workload_config(w):
+    cfg = {"workload": w.name}
+    for k in ("M", "N", "K", "n", "k", "G", "H", "I", "Mt"):
+        if hasattr(w, k):
+            cfg[k] = getattr(w, k)
+    cfg["l2"] = "flushed between timed steps (256 MB device write, outside the timed intervals)"
+    return cfg
+
+
+# ---- the GPU arm ---------------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from mxfp8_microscaled_precision_gb300 import build as mbuild, mxq
+    mbuild.build()
+    mxq.lib()
+    peaks = load_peaks()
+    w = make_workload(args.workload, dev)
+    kern = w.kernels()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for (_, _, _, fn) in kern:
+            fn()
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    st = mxq.get_device_status()
+    if st != 0:
+        raise SystemExit(f"device status {st} after warm-up")
+
+    nk = len(kern)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index if world == 1 else local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(dev)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)                      # evict L2 between steps (not timed)
+        ev[s][0].record(stream)
+        for j, (_, _, _, fn) in enumerate(kern):
+            fn()
+            ev[s][j + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(dev)
+    t_wall1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0 - 0.05, t_wall1 + 0.05)
+
+    per_kernel = [[ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps)] for j in range(nk)]
+    step_ms = [ev[s][0].elapsed_time(ev[s][nk]) for s in range(args.steps)]
+    total_s = sum(step_ms) / 1e3
+    max_total_s = max_over_ranks(total_s, dev if world > 1 else None)
+    value = aggregate_value(w.gemm_flops, args.steps, world, max_total_s)
+
+    kernels_ms = {kern[j][0]: statistics.mean(per_kernel[j]) for j in range(nk)}
+    gemm_idx = [j for j in range(nk) if kern[j][1] == "gemm"]
+    quant_idx = [j for j in range(nk) if kern[j][1] == "quant"]
+    gemm_s = sum(sum(per_kernel[j]) for j in gemm_idx) / 1e3
+    quant_s = sum(sum(per_kernel[j]) for j in quant_idx) / 1e3
+    gemm_flops = sum(kern[j][2] for j in gemm_idx) * args.steps
+    quant_bytes = sum(kern[j][2] for j in quant_idx) * args.steps
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    gemm_tflops = gemm_flops / gemm_s / 1e12
+    quant_gbs = quant_bytes / quant_s / 1e9
+    per_launch_flops = statistics.mean(kern[j][2] for j in gemm_idx)
+    roofline = {"bound": "tensor", "kernel": "gemm_mxf8_kernel", "achieved": round(gemm_tflops, 1),
+                "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
+                "traffic": GEMM_TRAFFIC_BYTES,
+                "units_per_launch": per_launch_flops,
+                "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 ratio)"}
+    roofline_quant = {"bound": "hbm", "kernel": "quant kernels", "achieved": round(quant_gbs, 1),
+                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
+                      "peak_source": peaks["source"] + " copy bandwidth"}
+
+    # ---- end to end through the public API, host buffers, copies inside the timed step
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: v.detach().cpu().pin_memory() for k, v in w.inputs.items()}
+        host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in w.outputs]
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = sum(o.numel() * o.element_size() for o in host_out)
+        e2e_steps = args.steps
+        ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+        for s in range(e2e_steps + 2):
+            if s >= 2:
+                flush.fill_(s & 0xFF)
+                ee[s - 2][0].record(stream)
+            for k, v in host_in.items():
+                w.inputs[k].copy_(v, non_blocking=True)
+            step()
+            for o, h in zip(w.outputs, host_out):
+                h.copy_(o, non_blocking=True)
+            if s >= 2:
+                ee[s - 2][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_total = sum(a.elapsed_time(b) for a, b in ee) / 1e3
+        e2e_total = max_over_ranks(e2e_total, dev if world > 1 else None)
+        e2e = {"value": round(aggregate_value(w.gemm_flops, e2e_steps, world, e2e_total), 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_total / e2e_steps * 1e3, 4)}
+
+    st = mxq.get_device_status()
+    if st != 0:
+        raise SystemExit(f"device status {st} after the timed region")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_budget)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(max_total_s / args.steps * 1e3, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (E8M0 block scales, fp32 accumulate)",
+                "data": "synthetic (seeded generators; shapes of the linear / MoE-expert workloads)",
+                "config": workload_config(w),
+                "gemm_tflops": round(gemm_tflops, 1), "gemm_frac_fp8_peak": round(gemm_tflops / fp8_peak, 4),
+                "quant_tbs": round(quant_gbs / 1e3, 3), "quant_frac_hbm": round(quant_gbs / peaks["hbm_gbs"], 4),
+                "kernels_ms": {k: round(v, 5) for k, v in kernels_ms.items()},
+                "roofline": roofline, "roofline_quant": roofline_quant,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": nk * args.steps, "clocks": clocks,
+                "impl": "mxq"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def cpu_baseline(w, budget_s):
+    from oracle import oracle
+    oracle.build()
+    t_step, sample = w.cpu_sample(budget_s)
+    cores = _omp_threads()
+    return {"value": round(w.gemm_flops / t_step / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "sample": sample, "extrapolated_s_per_step": round(t_step, 3)}
+
+
+def _omp_threads():
+    v = os.environ.get("OMP_NUM_THREADS")
+    if v and v.isdigit():
+        return int(v)
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ---- the reference arm: the oracle on the host cores ------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    from oracle import oracle
+    oracle.build()
+    w = make_workload(args.workload)
+    per_step_budget = max(0.05, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    times = []
+    desc = ""
+    for s in range(args.warmup + args.steps):
+        t, desc = w.cpu_sample(per_step_budget * 0.8)
+        if s >= args.warmup:
+            times.append(t)
+    t_step = statistics.mean(times)
+    value = w.gemm_flops / t_step / 1e12
+    cores = _omp_threads()
+    line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic", "config": workload_config(w), "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": desc + "; each step is this bounded sample, time extrapolated to the full step"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["mxq", "reference"], default="mxq")
+    ap.add_argument("--workload", choices=WORKLOAD_NAMES, default="linear_train")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle GEMM in the CPU baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+/*
+ * mxq.h -- C ABI of libmxq: MXFP8 microscaled quantization and block-scaled
+ * FP8 GEMMs with BF16 output, for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (sources, by page and section):
+ *   - "torchtitan-npu MXFP8/HiF8 low-precision training tutorial", section
+ *     "MXFP8 与 HiF8 架构原理速览": MXFP8 is per-block dynamic quantization in
+ *     which every 32 consecutive elements share one E8M0 (power-of-two)
+ *     scale; the FP8 matmul returns BF16.  Linear layers and MoE expert
+ *     layers (grouped matmul) are quantized.  Section "常用环境变量"
+ *     (MXFP8_DUAL_AXIS_FORWARD): the forward quantizes along both axes.
+ *     Section "第 3 步": the scale rule is "mxfp8_rceil".
+ *   - MindSpeed RFC "Add MXFP8-32x32 quantization support to FSDP":
+ *     section 3.1 (block size [1,32,32]: 32 along input_dim and output_dim,
+ *     token_dim unblocked; forward and backward share one weight), section
+ *     3.3.1 (E4M3 elements, dynamic scaling), section 3.3.3 (dual-axis
+ *     quantization gives separate forward/backward copies; 32x32 gives one
+ *     payload and two scales), section 3.5.2.1 (unsupported block sizes
+ *     raise an error).
+ *
+ * Number formats:
+ *   payload  float8_e4m3fn: bias 7, no Inf, NaN = S.1111.111, max 448.
+ *   scale    E8M0: code c in [0,254] means 2^(c-127); 0xFF is NaN.
+ *   rule     e = ceil(log2(amax/448)) clamped to [-127,127]; amax 0 -> -127.
+ *            q = round-to-nearest-even, saturating E4M3 of x * 2^-e.
+ *            A group holding NaN or Inf gets scale 0xFF and payload
+ *            0x7F | sign(x).
+ *   GEMM     y = sum_k deq(a)[m,k] * deq(b)[n,k] with deq(q) = q * 2^e,
+ *            accumulated in FP32 on the tensor cores, rounded once to BF16.
+ *
+ * Scale layouts (for an operand [R, C] quantized along C, scales [R, C/32]):
+ *   MXQ_SCALE_ROWMAJOR   plain row-major [R][C/32] bytes.
+ *   MXQ_SCALE_MMA_TILED  the layout the block-scaled tensor-core MMA reads:
+ *                        R padded to a multiple of 128 and C/32 to a
+ *                        multiple of 4; 512-byte atoms of 128 rows x 4
+ *                        groups, atoms of one 128-row band consecutive;
+ *                        inside an atom row r, group g sit at byte
+ *                        16*(r%32) + 4*((r%128)/32) + (g%4).  Padding = 0.
+ *   mxq_scale_bytes() gives the size of either.
+ *
+ * Conventions for every call:
+ *   - Pointers named x, w, q*, s*, a*, b*, y, group_offsets are DEVICE
+ *     pointers; the caller owns all memory (the library allocates nothing
+ *     per call) and must keep it alive until the work on `stream` is done.
+ *   - All device pointers must be 16-byte aligned; leading dimensions are
+ *     in elements and must keep rows 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and run on the current CUDA device.
+ *   - Arguments are checked on the host before anything is launched; a
+ *     failed check returns a status and launches nothing.
+ *   - Kernels bound every internal wait; a wait that runs out records
+ *     MXQ_ERR_TIMEOUT in a device status word that mxq_get_device_status()
+ *     reports.
+ */
+#ifndef MXQ_H
+#define MXQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MXQ_ABI_VERSION 1
+
+typedef struct CUstream_st* mxq_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+    MXQ_OK = 0,
+    MXQ_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad enum, misalignment */
+    MXQ_ERR_UNSUPPORTED_SHAPE = 2,  /* a dimension that is not a supported multiple */
+    MXQ_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103 (GB300) */
+    MXQ_ERR_CUDA = 4,               /* a CUDA runtime or driver call failed */
+    MXQ_ERR_TIMEOUT = 5             /* a bounded device-side wait ran out */
+} mxq_status;
+
+typedef enum {
+    MXQ_SCALE_ROWMAJOR = 0,
+    MXQ_SCALE_MMA_TILED = 1
+} mxq_scale_layout;
+
+/* Version of this ABI (MXQ_ABI_VERSION). */
+int mxq_abi_version(void);
+
+/* Static text for a status code. */
+const char* mxq_status_string(mxq_status s);
+
+/* Bytes of the scale matrix of an operand [rows, cols] quantized along cols
+ * (cols % 32 == 0) in the given layout; 0 for invalid arguments. */
+size_t mxq_scale_bytes(int64_t rows, int64_t cols, mxq_scale_layout layout);
+
+/*
+ * 1x32 dual-axis quantization (the "mxfp8" recipe; RFC section 3.3.3
+ * "dual_axis_quant", tutorial "MXFP8_DUAL_AXIS_FORWARD").
+ *
+ * x      bf16 [rows, cols], row stride ld elements (ld >= cols, ld % 8 == 0).
+ * q_row  u8 [rows, cols]       E4M3 payload, groups of 32 along cols.
+ * s_row  u8 scales of q_row    ([rows, cols/32] in `layout`).
+ * q_col  u8 [cols, rows]       E4M3 payload of x transposed: groups of 32
+ *                              along rows; stored cols-major-first so that
+ *                              every GEMM operand is K-major.
+ * s_col  u8 scales of q_col    ([cols, rows/32] in `layout`).
+ * Either pair may be NULL (row-only or column-only); not both.
+ * Shapes: cols % 32 == 0; rows % 32 == 0 when the column pair is asked for;
+ * rows >= 1 otherwise.  Output rows are dense (stride cols resp. rows).
+ * Errors: MXQ_ERR_INVALID_ARG, MXQ_ERR_UNSUPPORTED_SHAPE,
+ * MXQ_ERR_UNSUPPORTED_DEVICE, MXQ_ERR_CUDA (launch failure).
+ */
+mxq_status mxq_quant_1x32_dual(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                               void* q_row, void* s_row, void* q_col, void* s_col,
+                               mxq_scale_layout layout, mxq_stream_t stream);
+
+/*
+ * 32x32 block quantization (the "mxfp8-32x32" recipe; RFC sections 3.1 and
+ * 3.3.3 "block_mx_quant": one payload, forward and backward scales).
+ *
+ * w      bf16 weight [n, k] (output_dim x input_dim), row stride ld.
+ * q      u8 [n, k]  the single E4M3 payload used by forward and backward.
+ * s_fwd  u8 scales for contraction over k: [n, k/32] in `layout`,
+ *        s_fwd[r][j] = t[r/32][j].
+ * s_bwd  u8 scales for contraction over n: [k, n/32] in `layout`,
+ *        s_bwd[c][i] = t[i][c/32].
+ * where t[i][j] is the E8M0 code of 32x32 tile (i, j) (tiles start at 0,0).
+ * s_fwd or s_bwd may be NULL.  Shapes: n % 32 == 0, k % 32 == 0.
+ */
+mxq_status mxq_quant_32x32(const void* w, int64_t n, int64_t k, int64_t ld,
+                           void* q, void* s_fwd, void* s_bwd,
+                           mxq_scale_layout layout, mxq_stream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM with BF16 output: forward Y = X W^T, dgrad and
+ * wgrad (tutorial: "前向用 npu_quant_matmul 执行 FP8 矩阵乘, 输出恢复为 BF16").
+ *
+ *   y[m, n] = sum_k deq(A)[m, k] * deq(B)[n, k]        (0 <= m < M, 0 <= n < N)
+ *
+ * a_q   u8 [M, K] K-major E4M3 payload; a_s its scales [M, K/32], MMA-tiled.
+ * b_q   b_mn_major == 0: u8 [N, K] K-major; b_s scales [N, K/32], MMA-tiled.
+ *       b_mn_major == 1: u8 [K, N] (N contiguous) -- the single 32x32 weight
+ *       payload read for dgrad -- with b_s = its backward scales [N, K/32]
+ *       MMA-tiled (s_bwd of mxq_quant_32x32).
+ * y     bf16 [M, N], row stride ldy (ldy >= N, ldy % 8 == 0).
+ * Shapes: M >= 1; N % 16 == 0 (N % 128 == 0 when b_mn_major); K % 32 == 0
+ * (K % 128 == 0 when b_mn_major).
+ * Operand pairing for training (contraction axis quantized in groups of 32):
+ *   forward  A = X row copy,   B = W row copy           (M tokens, N out, K in)
+ *   dgrad    A = dY row copy,  B = W column copy        (N = in, K = out)
+ *            or, 32x32, B = W payload MN-major with s_bwd
+ *   wgrad    A = dY column copy, B = X column copy      (M = out, N = in, K = tokens)
+ */
+mxq_status mxq_gemm_bf16out(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
+                            int64_t M, int64_t N, int64_t K, int b_mn_major,
+                            void* y, int64_t ldy, mxq_stream_t stream);
+
+/*
+ * Grouped block-scaled GEMM for MoE experts (tutorial: "MoE 专家层 (Grouped
+ * MM)"; RFC section 2.2: gate_up_proj and down_proj).  Tokens are already
+ * sorted by expert.  For each expert g and row r with
+ * group_offsets[g] <= r < group_offsets[g+1]:
+ *
+ *   y[r, n] = sum_k deq(A)[r, k] * deq(B_g)[n, k]
+ *
+ * a_q            u8 [M_total, K] K-major; a_s scales [M_total, K/32] MMA-tiled.
+ * b_q            u8 [G, N, K] K-major; b_s scales of the [G*N, K] stack, MMA-tiled.
+ * group_offsets  DEVICE int64 [G+1]: 0 = off[0] <= off[1] <= ... <= off[G] = M_total.
+ *                Empty experts are allowed.  Offsets are read on the device, so
+ *                the call does not synchronize with the host; offsets that break
+ *                the rule above give unspecified rows (never out-of-bounds access).
+ * y              bf16 [M_total, N], row stride ldy.
+ * Shapes: 1 <= G <= 1024; N % 128 == 0; K % 32 == 0; M_total >= 0.
+ */
+mxq_status mxq_grouped_gemm(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
+                            const int64_t* group_offsets, int32_t G, int64_t M_total,
+                            int64_t N, int64_t K, void* y, int64_t ldy, mxq_stream_t stream);
+
+/* Waits for all work on the current device, then returns MXQ_ERR_TIMEOUT if
+ * any kernel of this library recorded a bounded wait that ran out since the
+ * last call (and clears the record), MXQ_ERR_CUDA if the device reports an
+ * error, MXQ_OK otherwise. */
+mxq_status mxq_get_device_status(void);
+
+/* Test hook for the bounded-wait machinery: launches one small kernel that
+ * waits on a barrier no thread ever completes, giving up after timeout_us
+ * microseconds (1..1000000) and recording MXQ_ERR_TIMEOUT the way every
+ * kernel of the library does.  Returns the launch status. */
+mxq_status mxq_debug_wait_timeout(uint32_t timeout_us, mxq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXQ_H */

@@ -1,0 +1,220 @@
+// api.cu -- the extern "C" entry points of libmxq (declared in include/mxq.h).
+//
+// Each call validates its arguments on the host, checks that the current
+// device is a GB300 (sm_103), and launches one kernel on the caller's
+// stream.  Nothing is allocated per call.
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "mxq.h"
+#include "mxq_internal.h"
+
+// Device status word: kernels record a timed-out bounded wait here.
+__device__ unsigned int g_mxq_device_status = 0u;
+
+namespace mxq {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+bool g_have[kMaxDevices] = {};
+DeviceInfo g_info[kMaxDevices];
+
+}  // namespace
+
+cudaError_t current_device_info(DeviceInfo* info) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_have[dev]) {
+        DeviceInfo d;
+        d.device = dev;
+        if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return e;
+        int optin = 0;
+        if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+            return e;
+        d.smem_optin = static_cast<size_t>(optin);
+        if (d.cc_major == 10 && d.cc_minor == 3) {
+            void* p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_mxq_device_status)) != cudaSuccess) return e;
+            d.status = static_cast<unsigned int*>(p);
+        }
+        g_info[dev] = d;
+        g_have[dev] = true;
+    }
+    *info = g_info[dev];
+    return cudaSuccess;
+}
+
+}  // namespace mxq
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device check shared by every launching call.
+mxq_status device_ok(mxq::DeviceInfo* info) {
+    if (mxq::current_device_info(info) != cudaSuccess) return MXQ_ERR_CUDA;
+    if (info->cc_major != 10 || info->cc_minor != 3 || info->status == nullptr)
+        return MXQ_ERR_UNSUPPORTED_DEVICE;
+    return MXQ_OK;
+}
+
+inline mxq_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return MXQ_OK;
+    if (e == cudaErrorInvalidValue) return MXQ_ERR_INVALID_ARG;
+    return MXQ_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mxq_abi_version(void) { return MXQ_ABI_VERSION; }
+
+const char* mxq_status_string(mxq_status s) {
+    switch (s) {
+        case MXQ_OK: return "ok";
+        case MXQ_ERR_INVALID_ARG: return "invalid argument";
+        case MXQ_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case MXQ_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103 / GB300)";
+        case MXQ_ERR_CUDA: return "CUDA error";
+        case MXQ_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+size_t mxq_scale_bytes(int64_t rows, int64_t cols, mxq_scale_layout layout) {
+    if (rows < 0 || cols < 0 || cols % 32 != 0) return 0;
+    const int64_t groups = cols / 32;
+    if (layout == MXQ_SCALE_ROWMAJOR) return static_cast<size_t>(rows * groups);
+    if (layout == MXQ_SCALE_MMA_TILED)
+        return static_cast<size_t>(((rows + 127) / 128 * 128) * ((groups + 3) / 4 * 4));
+    return 0;
+}
+
+mxq_status mxq_quant_1x32_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q_row,
+                               void* s_row, void* q_col, void* s_col, mxq_scale_layout layout,
+                               mxq_stream_t stream) {
+    if (layout != MXQ_SCALE_ROWMAJOR && layout != MXQ_SCALE_MMA_TILED) return MXQ_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0) return MXQ_ERR_INVALID_ARG;
+    const bool row = q_row != nullptr || s_row != nullptr;
+    const bool col = q_col != nullptr || s_col != nullptr;
+    if (!row && !col) return MXQ_ERR_INVALID_ARG;
+    if (cols % 32 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (col && rows % 32 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0 || cols == 0) return MXQ_OK;
+    if (!x || (row && (!q_row || !s_row)) || (col && (!q_col || !s_col))) return MXQ_ERR_INVALID_ARG;
+    if (ld < cols || ld % 8 != 0) return MXQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || (row && (!aligned16(q_row) || !aligned16(s_row))) ||
+        (col && (!aligned16(q_col) || !aligned16(s_col))))
+        return MXQ_ERR_INVALID_ARG;
+    mxq::DeviceInfo dev;
+    mxq_status st = device_ok(&dev);
+    if (st != MXQ_OK) return st;
+    return from_cuda(mxq::launch_quant_1x32(x, rows, cols, ld, row ? q_row : nullptr,
+                                            row ? s_row : nullptr, col ? q_col : nullptr,
+                                            col ? s_col : nullptr, layout == MXQ_SCALE_MMA_TILED,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxq_status mxq_quant_32x32(const void* w, int64_t n, int64_t k, int64_t ld, void* q, void* s_fwd,
+                           void* s_bwd, mxq_scale_layout layout, mxq_stream_t stream) {
+    if (layout != MXQ_SCALE_ROWMAJOR && layout != MXQ_SCALE_MMA_TILED) return MXQ_ERR_INVALID_ARG;
+    if (n < 0 || k < 0) return MXQ_ERR_INVALID_ARG;
+    if (n % 32 != 0 || k % 32 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (n == 0 || k == 0) return MXQ_OK;
+    if (!w || !q) return MXQ_ERR_INVALID_ARG;
+    if (ld < k || ld % 8 != 0) return MXQ_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(q) || (s_fwd && !aligned16(s_fwd)) || (s_bwd && !aligned16(s_bwd)))
+        return MXQ_ERR_INVALID_ARG;
+    mxq::DeviceInfo dev;
+    mxq_status st = device_ok(&dev);
+    if (st != MXQ_OK) return st;
+    return from_cuda(mxq::launch_quant_32x32(w, n, k, ld, q, s_fwd, s_bwd,
+                                             layout == MXQ_SCALE_MMA_TILED,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxq_status mxq_gemm_bf16out(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
+                            int64_t M, int64_t N, int64_t K, int b_mn_major, void* y, int64_t ldy,
+                            mxq_stream_t stream) {
+    if (M < 0 || N < 0 || K < 0 || (b_mn_major != 0 && b_mn_major != 1)) return MXQ_ERR_INVALID_ARG;
+    if (K % 32 != 0 || N % 16 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (b_mn_major && N % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (M > (int64_t(1) << 31) - 128 || N > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - 128)
+        return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0) return MXQ_OK;
+    if (!y || ldy < N || ldy % 8 != 0 || !aligned16(y)) return MXQ_ERR_INVALID_ARG;
+    mxq::DeviceInfo dev;
+    if (K == 0) {  // empty contraction: y = 0
+        mxq_status st = device_ok(&dev);
+        if (st != MXQ_OK) return st;
+        return from_cuda(cudaMemset2DAsync(y, static_cast<size_t>(ldy) * 2, 0,
+                                           static_cast<size_t>(N) * 2, static_cast<size_t>(M),
+                                           reinterpret_cast<cudaStream_t>(stream)));
+    }
+    if (!a_q || !a_s || !b_q || !b_s) return MXQ_ERR_INVALID_ARG;
+    if (!aligned16(a_q) || !aligned16(a_s) || !aligned16(b_q) || !aligned16(b_s))
+        return MXQ_ERR_INVALID_ARG;
+    mxq_status st = device_ok(&dev);
+    if (st != MXQ_OK) return st;
+    return from_cuda(mxq::launch_gemm(dev, a_q, a_s, b_q, b_s, M, N, K, b_mn_major != 0, y, ldy,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxq_status mxq_grouped_gemm(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
+                            const int64_t* group_offsets, int32_t G, int64_t M_total, int64_t N,
+                            int64_t K, void* y, int64_t ldy, mxq_stream_t stream) {
+    if (G < 1 || M_total < 0 || N < 0 || K < 0) return MXQ_ERR_INVALID_ARG;
+    if (G > 1024) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (N % 128 != 0 || K % 32 != 0 || K == 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (M_total > (int64_t(1) << 31) - 128 || static_cast<int64_t>(G) * N > (int64_t(1) << 31) - 256 ||
+        K > (int64_t(1) << 31) - 128)
+        return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (M_total == 0 || N == 0) return MXQ_OK;
+    if (!a_q || !a_s || !b_q || !b_s || !group_offsets || !y) return MXQ_ERR_INVALID_ARG;
+    if (ldy < N || ldy % 8 != 0) return MXQ_ERR_INVALID_ARG;
+    if (!aligned16(a_q) || !aligned16(a_s) || !aligned16(b_q) || !aligned16(b_s) || !aligned16(y) ||
+        (reinterpret_cast<uintptr_t>(group_offsets) & 7u) != 0)
+        return MXQ_ERR_INVALID_ARG;
+    mxq::DeviceInfo dev;
+    mxq_status st = device_ok(&dev);
+    if (st != MXQ_OK) return st;
+    return from_cuda(mxq::launch_grouped_gemm(dev, a_q, a_s, b_q, b_s, group_offsets, G, M_total, N, K,
+                                              y, ldy, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxq_status mxq_get_device_status(void) {
+    mxq::DeviceInfo dev;
+    mxq_status st = device_ok(&dev);
+    if (st != MXQ_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MXQ_ERR_CUDA;
+    unsigned int v = 0u;
+    if (cudaMemcpyFromSymbol(&v, g_mxq_device_status, sizeof v) != cudaSuccess) return MXQ_ERR_CUDA;
+    if (v != 0u) {
+        const unsigned int zero = 0u;
+        if (cudaMemcpyToSymbol(g_mxq_device_status, &zero, sizeof zero) != cudaSuccess) return MXQ_ERR_CUDA;
+        return MXQ_ERR_TIMEOUT;
+    }
+    return MXQ_OK;
+}
+
+mxq_status mxq_debug_wait_timeout(uint32_t timeout_us, mxq_stream_t stream) {
+    if (timeout_us < 1u || timeout_us > 1000000u) return MXQ_ERR_INVALID_ARG;
+    mxq::DeviceInfo dev;
+    mxq_status st = device_ok(&dev);
+    if (st != MXQ_OK) return st;
+    return from_cuda(mxq::launch_wait_probe(dev, static_cast<uint64_t>(timeout_us) * 1000ull,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

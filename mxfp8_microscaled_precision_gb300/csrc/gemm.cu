@@ -1,0 +1,536 @@
+// gemm.cu -- block-scaled MXFP8 GEMMs with BF16 output for sm_103a.
+//
+//   y[m, n] = sum_k (qa[m,k] * 2^ea[m,k/32]) * (qb[n,k] * 2^eb[n,k/32])
+//
+// The FP8 matmul of the MXFP8 recipe (torchtitan-npu low-precision tutorial,
+// "MXFP8 与 HiF8 架构原理速览": FP8 matmul, output restored to BF16) for the
+// forward, dgrad and wgrad of linear layers, and its grouped form for MoE
+// experts (same page; MindSpeed RFC "Add MXFP8-32x32 quantization support
+// to FSDP", section 2.2, gate_up_proj / down_proj).  With the 32x32 recipe
+// the dgrad reads the one shared weight payload N-major (RFC section 3.1).
+//
+// Design (one CTA per SM, persistent over output tiles of 128 x BN):
+//   warp 0      TMA producer: A and B tiles (128-byte swizzle) and the
+//               512-byte scale atoms, into a ring of STAGES shared-memory
+//               slots guarded by full/empty mbarriers.
+//   warp 1      allocates tensor memory; one lane issues tcgen05.cp of the
+//               scale atoms into per-stage TMEM columns and the
+//               tcgen05.mma.kind::mxf8f6f4.block_scale instructions
+//               (128 x BN x 32 each) into one of two TMEM accumulators.
+//   warps 2-5   epilogue: tcgen05.ld of the FP32 accumulator, RNE to BF16,
+//               16-byte global stores; releases the accumulator so the MMA
+//               warp proceeds with the next tile meanwhile.
+// Every mbarrier wait is bounded (see mxq_device.cuh).
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "mxq_device.cuh"
+#include "mxq_internal.h"
+
+namespace mxq {
+namespace {
+
+constexpr int kBM = 128;          // rows of A per tile (= TMEM lanes)
+constexpr int kBK = 128;          // K elements (= bytes) per pipeline stage
+constexpr int kUmmaK = 32;        // K of one MMA instruction (FP8)
+constexpr int kThreads = 192;     // 6 warps
+constexpr int kAccStages = 2;
+constexpr int kRasterBand = 8;    // m-tiles per raster band (L2 reuse of B)
+constexpr int kMaxGroups = 1024;
+
+struct GemmArgs {
+    const uint8_t* a_s;      // A scales, MMA-tiled
+    const uint8_t* b_s;      // B scales, MMA-tiled
+    uint16_t* y;             // bf16 output
+    int64_t M, N, K, ldy;
+    int64_t k_atoms;         // 4-group scale atoms per 128-row band = ceil(K/128)
+    int64_t b_bands;         // 128-row bands of B scales that exist
+    const int64_t* offsets;  // grouped: [G+1] on the device
+    int G;
+    unsigned int* status;
+    uint64_t wait_limit_ns;
+};
+
+template <int BN, int STAGES>
+struct Layout {
+    static constexpr int kBBytes = BN * kBK;             // per stage
+    static constexpr int kABytes = kBM * kBK;
+    static constexpr int kSfbAtoms = BN / 128;
+    static constexpr int kOffB = 0;                       // B first (see MN-major note)
+    static constexpr int kOffA = kOffB + STAGES * kBBytes;
+    static constexpr int kOffSfa = kOffA + STAGES * kABytes;
+    static constexpr int kOffSfb = kOffSfa + STAGES * 512;
+    static constexpr int kOffBar = kOffSfb + STAGES * 512 * kSfbAtoms;
+    static constexpr int kNumBars = 2 * STAGES + 2 * kAccStages + 1;
+    static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
+    static constexpr int kOffAbort = kOffTmemSlot + 4;
+    static constexpr int kOffSched = (kOffAbort + 4 + 15) / 16 * 16;
+    static constexpr int kSchedBytes = 8 * (kMaxGroups + 1) + 4 * (kMaxGroups + 1) + 4 * kMaxGroups;
+    static constexpr int kBytes = kOffSched + kSchedBytes;
+    static constexpr int kAlloc = kBytes + 1024;          // slack for 1024-byte alignment
+    // TMEM columns: accumulators, then per-stage SFA and SFB slots.
+    static constexpr int kTmemSfa = kAccStages * BN;
+    static constexpr int kTmemSfb = kTmemSfa + 4 * STAGES;
+    static constexpr int kTmemUsed = kTmemSfb + 4 * kSfbAtoms * STAGES;
+    static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
+    static_assert(kTmemUsed <= 512, "tensor memory budget");
+    static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+// Output-tile schedule.  Dense: raster bands of kRasterBand m-tiles, n-tiles
+// inside a band.  Grouped: tiles of expert g cover the 128-row blocks that
+// intersect [off[g], off[g+1]); n-tiles innermost.
+struct TileInfo {
+    int64_t m0;      // first row of the A tile (multiple of 128)
+    int64_t n0;      // first output column
+    int64_t row_lo;  // rows [row_lo, row_hi) of this tile are stored
+    int64_t row_hi;
+    int64_t b_row;   // first row of the B tile in the (stacked) B matrix
+};
+
+struct Schedule {
+    int64_t m_tiles, n_tiles, total;
+    // grouped only (shared memory)
+    const int64_t* off;
+    const int* prefix;    // [G+1] tile prefix
+    const int* first_mt;  // [G]
+    int G;
+};
+
+template <int BN, bool kGrouped>
+__device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs& p, int64_t t) {
+    TileInfo ti;
+    if constexpr (!kGrouped) {
+        const int64_t per_band = static_cast<int64_t>(kRasterBand) * s.n_tiles;
+        const int64_t band = t / per_band, within = t - band * per_band;
+        const int64_t mb = band * kRasterBand;
+        const int64_t bh = min(static_cast<int64_t>(kRasterBand), s.m_tiles - mb);
+        const int64_t m_blk = mb + within % bh, n_blk = within / bh;
+        ti.m0 = m_blk * kBM;
+        ti.n0 = n_blk * BN;
+        ti.row_lo = ti.m0;
+        ti.row_hi = min(ti.m0 + kBM, p.M);
+        ti.b_row = ti.n0;
+    } else {
+        int lo = 0, hi = s.G;  // largest g with prefix[g] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s.prefix[mid] <= t) lo = mid; else hi = mid;
+        }
+        const int g = lo;
+        const int64_t local = t - s.prefix[g];
+        const int64_t m_blk = s.first_mt[g] + local / s.n_tiles;
+        const int64_t n_blk = local % s.n_tiles;
+        ti.m0 = m_blk * kBM;
+        ti.n0 = n_blk * BN;
+        ti.row_lo = max(ti.m0, s.off[g]);
+        ti.row_hi = min(ti.m0 + kBM, s.off[g + 1]);
+        ti.b_row = static_cast<int64_t>(g) * p.N + ti.n0;
+    }
+    return ti;
+}
+
+template <int BN, int STAGES, bool kMnMajor, bool kGrouped>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tma_a,
+                     const __grid_constant__ CUtensorMap tma_b, const GemmArgs p) {
+    using L = Layout<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const uint32_t bar0 = sbase + L::kOffBar;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + kAccStages + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * kAccStages);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+    const WaitGuard guard{abort_flag, p.status, p.wait_limit_ns};
+
+    // ---- set-up -------------------------------------------------------------
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < kAccStages; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);  // one arrive per epilogue warp
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tma_a);
+        prefetch_tensormap(&tma_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + L::kOffTmemSlot, L::kTmemCols);
+        tmem_relinquish();
+    }
+
+    Schedule sch;
+    sch.n_tiles = (p.N + BN - 1) / BN;
+    sch.G = p.G;
+    if constexpr (!kGrouped) {
+        sch.m_tiles = (p.M + kBM - 1) / kBM;
+        sch.total = sch.m_tiles * sch.n_tiles;
+        sch.off = nullptr;
+        sch.prefix = nullptr;
+        sch.first_mt = nullptr;
+    } else {
+        int64_t* s_off = reinterpret_cast<int64_t*>(smem + L::kOffSched);
+        int* s_prefix = reinterpret_cast<int*>(s_off + (kMaxGroups + 1));
+        int* s_first = s_prefix + (kMaxGroups + 1);
+        for (int g = threadIdx.x; g <= p.G; g += kThreads) {
+            int64_t o = p.offsets[g];
+            o = o < 0 ? 0 : (o > p.M ? p.M : o);  // keep malformed offsets in bounds
+            s_off[g] = o;
+        }
+        __syncthreads();
+        if (warp == 0) {  // tile counts and their exclusive prefix, 32 groups at a time
+            int carry = 0;
+            for (int base = 0; base < p.G; base += 32) {
+                const int g = base + lane;
+                int cnt = 0;
+                if (g < p.G) {
+                    const int64_t lo = s_off[g], hi = s_off[g + 1];
+                    const int64_t fm = lo / kBM;
+                    s_first[g] = static_cast<int>(fm);
+                    cnt = hi > lo ? static_cast<int>((hi - 1) / kBM - fm + 1) * static_cast<int>(sch.n_tiles) : 0;
+                }
+                int incl = cnt;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                    if (lane >= d) incl += y;
+                }
+                if (g < p.G) s_prefix[g] = carry + incl - cnt;
+                carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+            }
+            if (lane == 0) s_prefix[p.G] = carry;
+        }
+        sch.off = s_off;
+        sch.prefix = s_prefix;
+        sch.first_mt = s_first;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemSlot);
+    if constexpr (kGrouped) sch.total = sch.prefix[p.G];
+
+    const int num_kb = static_cast<int>((p.K + kBK - 1) / kBK);
+
+    if (warp == 0) {
+        // ---- producer -------------------------------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            for (int64_t t = blockIdx.x; t < sch.total && !*abort_flag; t += gridDim.x) {
+                const TileInfo ti = tile_info<BN, kGrouped>(sch, p, t);
+                const int64_t a_band = ti.m0 / 128;
+                const int64_t b_band0 = ti.b_row / 128;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, guard)) break;
+                    int sfb_atoms = 0;
+                    for (int j = 0; j < L::kSfbAtoms; ++j)
+                        if (b_band0 + j < p.b_bands) ++sfb_atoms;
+                    const uint32_t bytes = L::kABytes + L::kBBytes + 512u + 512u * sfb_atoms;
+                    mbar_arrive_expect_tx(full_bar(stage), bytes);
+                    const uint32_t sa = sbase + L::kOffA + stage * L::kABytes;
+                    const uint32_t sb = sbase + L::kOffB + stage * L::kBBytes;
+                    const int32_t kx = kb * kBK;
+                    tma_load_2d(sa, &tma_a, kx, static_cast<int32_t>(ti.m0), full_bar(stage));
+                    if constexpr (!kMnMajor) {
+                        tma_load_2d(sb, &tma_b, kx, static_cast<int32_t>(ti.b_row), full_bar(stage));
+                    } else {
+                        // B stored [K, N]: boxes of 128 N-bytes x 128 K-rows.
+#pragma unroll
+                        for (int j = 0; j < BN / 128; ++j)
+                            tma_load_2d(sb + j * 128 * kBK, &tma_b,
+                                        static_cast<int32_t>(ti.b_row + 128 * j), kx, full_bar(stage));
+                    }
+                    bulk_load(sbase + L::kOffSfa + stage * 512,
+                              p.a_s + (a_band * p.k_atoms + kb) * 512, 512u, full_bar(stage));
+                    for (int j = 0; j < sfb_atoms; ++j)
+                        bulk_load(sbase + L::kOffSfb + (stage * L::kSfbAtoms + j) * 512,
+                                  p.b_s + ((b_band0 + j) * p.k_atoms + kb) * 512, 512u,
+                                  full_bar(stage));
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (*abort_flag) {
+                // Let copies already in flight land before the CTA exits.
+                const int64_t n = issued < STAGES ? issued : STAGES;
+                int s = stage;
+                uint32_t ph = phase;
+                for (int64_t i = 0; i < n; ++i) {
+                    if (--s < 0) { s = STAGES - 1; ph ^= 1u; }
+                    WaitGuard g2 = guard;
+                    volatile int never = 0;
+                    g2.abort_flag = &never;
+                    (void)mbar_wait(full_bar(s), ph, g2);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer -----------------------------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < sch.total && ok; t += gridDim.x) {
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, guard)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, guard)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem_base + L::kTmemSfa + 4 * stage;
+                    const uint32_t sfb_t = tmem_base + L::kTmemSfb + 4 * L::kSfbAtoms * stage;
+                    tc_cp_32x128b_warpx4(sfa_t, make_smem_desc(sbase + L::kOffSfa + stage * 512, 0, 128, 0));
+#pragma unroll
+                    for (int j = 0; j < L::kSfbAtoms; ++j)
+                        tc_cp_32x128b_warpx4(sfb_t + 4 * j,
+                                             make_smem_desc(sbase + L::kOffSfb + (stage * L::kSfbAtoms + j) * 512,
+                                                            0, 128, 0));
+                    const uint32_t sa = sbase + L::kOffA + stage * L::kABytes;
+                    const uint32_t sb = sbase + L::kOffB + stage * L::kBBytes;
+                    const int64_t k_left = p.K - static_cast<int64_t>(kb) * kBK;
+                    const int ksub = static_cast<int>(k_left < kBK ? k_left : kBK) / kUmmaK;
+#pragma unroll
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        if (k < ksub) {
+                            const uint64_t adesc = make_smem_desc(sa + k * kUmmaK, 16, 1024, 2);
+                            uint64_t bdesc;
+                            if constexpr (!kMnMajor)
+                                bdesc = make_smem_desc(sb + k * kUmmaK, 16, 1024, 2);
+                            else
+                                bdesc = make_smem_desc(sb + k * kUmmaK * 128, 128 * kBK, 1024, 2);
+                            const uint32_t idesc = make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k);
+                            tc_mma_mxf8(d_tmem, adesc, bdesc, idesc, sfa_t, sfb_t,
+                                        (kb > 0 || k > 0) ? 1u : 0u);
+                        }
+                    }
+                    tc_commit(empty_bar(stage));  // frees the slot once these MMAs are done
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(tfull_bar(acc));
+                if (++acc == kAccStages) { acc = 0; acc_phase ^= 1u; }
+            }
+            // Drain: every MMA and copy issued above completes before teardown.
+            tc_commit(drain_bar);
+            WaitGuard g2 = guard;
+            volatile int never = 0;
+            g2.abort_flag = &never;
+            (void)mbar_wait(drain_bar, 0, g2);
+        }
+    } else {
+        // ---- epilogue (warps 2..5) -----------------------------------------
+        const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int64_t t = blockIdx.x; t < sch.total; t += gridDim.x) {
+            const TileInfo ti = tile_info<BN, kGrouped>(sch, p, t);
+            // One lane waits; the warp follows its verdict, so the .sync.aligned
+            // tensor-memory loads below always run with the full warp.
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, guard) ? 1 : 0;
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int64_t row = ti.m0 + 32 * quad + lane;
+            const bool row_ok = row >= ti.row_lo && row < ti.row_hi;
+            uint16_t* yrow = p.y + row * p.ldy;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; c += 2) {
+                uint32_t v0[32], v1[32];
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + acc * BN + c * 32;
+                tmem_ld_32x32b_x32(taddr, v0);
+                tmem_ld_32x32b_x32(taddr + 32, v1);
+                tmem_ld_wait();
+                if (row_ok) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t* v = h ? v1 : v0;
+                        const int64_t n = ti.n0 + (c + h) * 32;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if (n + 8 * q + 8 <= p.N) {
+                                uint4 o;
+                                o.x = cvt_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+                                o.y = cvt_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+                                o.z = cvt_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+                                o.w = cvt_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+                                *reinterpret_cast<uint4*>(yrow + n + 8 * q) = o;
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (++acc == kAccStages) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    // ---- teardown -----------------------------------------------------------
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, L::kTmemCols);
+    }
+}
+
+// ---- tensor maps (driver entry point resolved once) --------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Row-major u8 matrix [rows, cols] (cols contiguous), box [box_rows, 128 bytes],
+// 128-byte swizzle.
+bool make_tma_u8(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {128u, box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, bool kMnMajor, bool kGrouped>
+cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& ta, const CUtensorMap& tb,
+                     const GemmArgs& args, int64_t max_tiles, cudaStream_t stream) {
+    using L = Layout<BN, STAGES>;
+    auto kern = gemm_mxf8_kernel<BN, STAGES, kMnMajor, kGrouped>;
+    static thread_local int configured_device = -1;  // attribute set once per device and thread
+    if (configured_device != dev.device) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        if (e != cudaSuccess) return e;
+        configured_device = dev.device;
+    }
+    int64_t grid = dev.sm_count;
+    if (max_tiles >= 0 && max_tiles < grid) grid = max_tiles;
+    if (grid <= 0) return cudaSuccess;
+    kern<<<static_cast<unsigned>(grid), kThreads, L::kAlloc, stream>>>(ta, tb, args);
+    return cudaGetLastError();
+}
+
+constexpr int kBN = 128;
+constexpr int kStages = 6;
+
+}  // namespace
+
+cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
+                        const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
+                        int64_t ldy, cudaStream_t stream) {
+    CUtensorMap ta, tb;
+    if (!make_tma_u8(&ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kBM))
+        return cudaErrorInvalidValue;
+    if (!b_mn_major) {
+        if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN))
+            return cudaErrorInvalidValue;
+    } else {
+        if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK))
+            return cudaErrorInvalidValue;
+    }
+    GemmArgs args{};
+    args.a_s = static_cast<const uint8_t*>(a_s);
+    args.b_s = static_cast<const uint8_t*>(b_s);
+    args.y = static_cast<uint16_t*>(y);
+    args.M = M; args.N = N; args.K = K; args.ldy = ldy;
+    args.k_atoms = (K + 127) / 128;
+    args.b_bands = (N + 127) / 128;
+    args.offsets = nullptr;
+    args.G = 0;
+    args.status = dev.status;
+    args.wait_limit_ns = kDefaultWaitLimitNs;
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    if (b_mn_major)
+        return launch_t<kBN, kStages, true, false>(dev, ta, tb, args, tiles, stream);
+    return launch_t<kBN, kStages, false, false>(dev, ta, tb, args, tiles, stream);
+}
+
+cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
+                                const void* b_q, const void* b_s, const int64_t* offsets, int G,
+                                int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy,
+                                cudaStream_t stream) {
+    CUtensorMap ta, tb;
+    if (!make_tma_u8(&ta, a_q, static_cast<uint64_t>(M_total), static_cast<uint64_t>(K), kBM))
+        return cudaErrorInvalidValue;
+    if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(G) * static_cast<uint64_t>(N),
+                     static_cast<uint64_t>(K), kBN))
+        return cudaErrorInvalidValue;
+    GemmArgs args{};
+    args.a_s = static_cast<const uint8_t*>(a_s);
+    args.b_s = static_cast<const uint8_t*>(b_s);
+    args.y = static_cast<uint16_t*>(y);
+    args.M = M_total; args.N = N; args.K = K; args.ldy = ldy;
+    args.k_atoms = (K + 127) / 128;
+    args.b_bands = static_cast<int64_t>(G) * N / 128;
+    args.offsets = offsets;
+    args.G = G;
+    args.status = dev.status;
+    args.wait_limit_ns = kDefaultWaitLimitNs;
+    return launch_t<kBN, kStages, false, true>(dev, ta, tb, args, -1, stream);
+}
+
+// ---- bounded-wait probe ---------------------------------------------------------------
+
+namespace {
+__global__ void wait_probe_kernel(unsigned int* status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const WaitGuard g{&abort_flag, status, limit_ns};
+    if (threadIdx.x == 0) (void)mbar_wait(smem_u32(&bar), 0, g);  // nobody arrives
+    __syncthreads();
+}
+}  // namespace
+
+cudaError_t launch_wait_probe(const DeviceInfo& dev, uint64_t limit_ns, cudaStream_t stream) {
+    wait_probe_kernel<<<1, 32, 0, stream>>>(dev.status, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace mxq

@@ -1,0 +1,42 @@
+// mxq_internal.h -- host-side launchers shared between the C ABI (api.cu)
+// and the kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mxq {
+
+// Per-device facts the launchers need.
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    size_t smem_optin = 0;            // max dynamic shared memory per block
+    unsigned int* status = nullptr;   // device status word (timeouts)
+};
+
+// Returns cudaSuccess and fills `info` for the current device.
+cudaError_t current_device_info(DeviceInfo* info);
+
+cudaError_t launch_quant_1x32(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q_row,
+                              void* s_row, void* q_col, void* s_col, bool tiled,
+                              cudaStream_t stream);
+
+cudaError_t launch_quant_32x32(const void* w, int64_t n, int64_t k, int64_t ld, void* q,
+                               void* s_fwd, void* s_bwd, bool tiled, cudaStream_t stream);
+
+// Dense block-scaled GEMM (see mxq_gemm_bf16out).  Returns cudaErrorInvalidValue
+// when a tensor map cannot be encoded for the given shapes.
+cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
+                        const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
+                        int64_t ldy, cudaStream_t stream);
+
+cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
+                                const void* b_q, const void* b_s, const int64_t* offsets, int G,
+                                int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy,
+                                cudaStream_t stream);
+
+cudaError_t launch_wait_probe(const DeviceInfo& dev, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace mxq

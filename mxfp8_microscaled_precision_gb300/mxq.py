@@ -1,0 +1,189 @@
+"""Python binding of libmxq (the C ABI in include/mxq.h).
+
+Argument marshalling only: tensors are allocated by PyTorch on the current
+CUDA device, their pointers and sizes go through ctypes to the C ABI, and
+every step of the computation runs in the library's CUDA kernels on the
+current stream.  There is no fallback: if the library is missing or the
+device is not a GB300 the calls raise.
+
+Names follow the pages: ``quant_1x32_dual`` returns the forward and
+backward copies (q_row, s_row, q_col, s_col) of the mxfp8 recipe,
+``quant_32x32`` the single payload and two scale tensors (q, s_fwd, s_bwd)
+of the mxfp8-32x32 recipe (MindSpeed RFC "Add MXFP8-32x32 quantization
+support to FSDP", sections 3.3.2-3.3.3), ``gemm`` / ``grouped_gemm`` the
+block-scaled FP8 matmuls with BF16 output.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+ROWMAJOR, TILED = 0, 1
+_LAYOUTS = {"rowmajor": ROWMAJOR, "tiled": TILED, ROWMAJOR: ROWMAJOR, TILED: TILED}
+STATUS = {0: "MXQ_OK", 1: "MXQ_ERR_INVALID_ARG", 2: "MXQ_ERR_UNSUPPORTED_SHAPE",
+          3: "MXQ_ERR_UNSUPPORTED_DEVICE", 4: "MXQ_ERR_CUDA", 5: "MXQ_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MXQError(ValueError):
+    """A non-OK status from the C ABI."""
+
+    def __init__(self, what: str, status: int, text: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({text})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library with argument types declared.  Raises if it has
+    not been built (run ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libmxq.so is not built ({path}); run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        P, I64, I32, U32, SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                ctypes.c_uint32, ctypes.c_size_t)
+        S = ctypes.c_int
+        L.mxq_abi_version.argtypes, L.mxq_abi_version.restype = [], ctypes.c_int
+        L.mxq_status_string.argtypes, L.mxq_status_string.restype = [S], ctypes.c_char_p
+        L.mxq_scale_bytes.argtypes, L.mxq_scale_bytes.restype = [I64, I64, S], SZ
+        L.mxq_quant_1x32_dual.argtypes = [P, I64, I64, I64, P, P, P, P, S, P]
+        L.mxq_quant_32x32.argtypes = [P, I64, I64, I64, P, P, P, S, P]
+        L.mxq_gemm_bf16out.argtypes = [P, P, P, P, I64, I64, I64, S, P, I64, P]
+        L.mxq_grouped_gemm.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, I64, P]
+        L.mxq_get_device_status.argtypes = []
+        L.mxq_debug_wait_timeout.argtypes = [U32, P]
+        for f in ("mxq_quant_1x32_dual", "mxq_quant_32x32", "mxq_gemm_bf16out",
+                  "mxq_grouped_gemm", "mxq_get_device_status", "mxq_debug_wait_timeout"):
+            getattr(L, f).restype = S
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().mxq_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise MXQError(what, status, status_string(status))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _layout(layout) -> int:
+    if layout not in _LAYOUTS:
+        raise ValueError(f"unknown scale layout {layout!r}")
+    return _LAYOUTS[layout]
+
+
+def scale_bytes(rows: int, cols: int, layout="tiled") -> int:
+    return int(lib().mxq_scale_bytes(rows, cols, _layout(layout)))
+
+
+def _scale_tensor(rows, cols, layout, device):
+    n = scale_bytes(rows, cols, layout)
+    if _layout(layout) == ROWMAJOR:
+        return torch.empty((rows, cols // 32), dtype=torch.uint8, device=device)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def quant_1x32_dual(x: torch.Tensor, row: bool = True, col: bool = True, layout="tiled",
+                    out=None):
+    """1x32 quantization of a 2-D bf16 CUDA tensor along both axes.
+    Returns (q_row [R,C], s_row, q_col [C,R], s_col); pairs not asked for are
+    None.  `out` may supply the four output tensors (None where not asked for)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda:
+        raise ValueError("x must be a 2-D bfloat16 CUDA tensor")
+    if x.stride(1) != 1:
+        raise ValueError("x must have unit stride along its last axis")
+    R, C = x.shape
+    dev = x.device
+    if out is not None:
+        q_row, s_row, q_col, s_col = out
+    else:
+        q_row = torch.empty((R, C), dtype=torch.uint8, device=dev) if row else None
+        s_row = _scale_tensor(R, C, layout, dev) if row else None
+        q_col = torch.empty((C, R), dtype=torch.uint8, device=dev) if col else None
+        s_col = _scale_tensor(C, R, layout, dev) if col else None
+    _check(lib().mxq_quant_1x32_dual(_ptr(x), R, C, x.stride(0), _ptr(q_row), _ptr(s_row),
+                                     _ptr(q_col), _ptr(s_col), _layout(layout), _stream()),
+           "mxq_quant_1x32_dual")
+    return q_row, s_row, q_col, s_col
+
+
+def quant_32x32(w: torch.Tensor, layout="tiled", out=None):
+    """32x32 block quantization of a bf16 weight [n, k].  Returns
+    (q [n,k], s_fwd ([n,k/32] scales), s_bwd ([k,n/32] scales)); `out` may
+    supply the three output tensors."""
+    if w.dtype != torch.bfloat16 or w.dim() != 2 or not w.is_cuda or w.stride(1) != 1:
+        raise ValueError("w must be a 2-D bfloat16 CUDA tensor with unit last stride")
+    n, k = w.shape
+    dev = w.device
+    if out is not None:
+        q, s_fwd, s_bwd = out
+    else:
+        q = torch.empty((n, k), dtype=torch.uint8, device=dev)
+        s_fwd = _scale_tensor(n, k, layout, dev)
+        s_bwd = _scale_tensor(k, n, layout, dev)
+    _check(lib().mxq_quant_32x32(_ptr(w), n, k, w.stride(0), _ptr(q), _ptr(s_fwd), _ptr(s_bwd),
+                                 _layout(layout), _stream()), "mxq_quant_32x32")
+    return q, s_fwd, s_bwd
+
+
+def gemm(a_q, a_s, b_q, b_s, M: int, N: int, K: int, b_mn_major: bool = False, out=None):
+    """y [M, N] bf16 = deq(A) deq(B)^T with tiled scales (see mxq_gemm_bf16out)."""
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a_q.device)
+    _check(lib().mxq_gemm_bf16out(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K,
+                                  1 if b_mn_major else 0, _ptr(out), out.stride(0), _stream()),
+           "mxq_gemm_bf16out")
+    return out
+
+
+def grouped_gemm(a_q, a_s, b_q, b_s, offsets: torch.Tensor, N: int, K: int, out=None):
+    """Per-expert y[r] = deq(A)[r] deq(B_g)^T for rows of expert g
+    (offsets: int64 CUDA tensor [G+1]).  Returns y [M_total, N] bf16."""
+    if offsets.dtype != torch.int64 or not offsets.is_cuda:
+        raise ValueError("offsets must be an int64 CUDA tensor")
+    G = offsets.numel() - 1
+    M_total = a_q.shape[0]
+    if out is None:
+        out = torch.empty((M_total, N), dtype=torch.bfloat16, device=a_q.device)
+    _check(lib().mxq_grouped_gemm(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(offsets), G,
+                                  M_total, N, K, _ptr(out), out.stride(0), _stream()),
+           "mxq_grouped_gemm")
+    return out
+
+
+def get_device_status() -> int:
+    """Synchronizes the device; returns 0 or the recorded status (e.g. 5 = timeout)."""
+    return int(lib().mxq_get_device_status())
+
+
+def debug_wait_timeout(timeout_us: int) -> int:
+    """Launches the bounded-wait probe (see mxq_debug_wait_timeout); 0 on launch."""
+    _check(lib().mxq_debug_wait_timeout(int(timeout_us), _stream()), "mxq_debug_wait_timeout")
+    return 0

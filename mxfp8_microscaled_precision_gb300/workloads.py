@@ -132,18 +132,22 @@ def weight_32x32(device="cpu", M=4096, N=7168, K=7168):
             "dY": normal((M, N), 1e-3, seed_for(w, "dY"), device=device)}
 
 
-def moe_grouped(device="cpu", tokens=16384, hidden=4096, inter=2048, experts=128, topk=8):
+def moe_grouped(device="cpu", tokens=16384, hidden=4096, inter=2048, experts=128, topk=8,
+                weights=True):
     """Routed inputs for the expert GEMMs: A = X rows gathered in expert order
     [tokens*topk, hidden]; H = the down-projection input [tokens*topk, inter];
-    gate_up weights [E, 2*inter, hidden]; down weights [E, hidden, inter]."""
+    gate_up weights [E, 2*inter, hidden]; down weights [E, hidden, inter]
+    (omitted when weights=False)."""
     w = "moe_grouped"
     routing = moe_routing(tokens, experts, topk, seed_for(w, "routing"))
     x = normal_with_outliers((tokens, hidden), seed_for(w, "X"), device=device)
     a = x.index_select(0, routing.token_of_row.to(device))
     h = normal((tokens * topk, inter), 1.0, seed_for(w, "H"), device=device)
-    w_gu = normal((experts, 2 * inter, hidden), 0.02, seed_for(w, "W"), device=device)
-    w_dn = normal((experts, hidden, inter), 0.02, seed_for(w, "W_down"), device=device)
-    return {"A": a, "H": h, "W_gate_up": w_gu, "W_down": w_dn, "routing": routing}
+    out = {"A": a, "H": h, "routing": routing}
+    if weights:
+        out["W_gate_up"] = normal((experts, 2 * inter, hidden), 0.02, seed_for(w, "W"), device=device)
+        out["W_down"] = normal((experts, hidden, inter), 0.02, seed_for(w, "W_down"), device=device)
+    return out
 
 
 def sweep(K: int, device="cpu", M=16384):

@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads
+and exports every function include/mxq.h declares, and argument validation
+rejects bad calls with the documented status before any CUDA work.
+
+The RFC's interface rejects unsupported configurations with an explicit
+error (MindSpeed RFC "Add MXFP8-32x32 quantization support to FSDP",
+sections 3.4 and 3.5.2.1); the ABI does the same with status codes.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxq.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mxfp8_microscaled_precision_gb300 import build, mxq
+    build.build()
+    return mxq.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_hot_path_calls():
+    names = _declared_functions()
+    for f in ("mxq_quant_1x32_dual", "mxq_quant_32x32", "mxq_gemm_bf16out", "mxq_grouped_gemm"):
+        assert f in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_version_and_strings(L):
+    assert L.mxq_abi_version() == 1
+    for s in range(6):
+        assert L.mxq_status_string(s)
+    assert L.mxq_scale_bytes(256, 512, 0) == 256 * 16
+    assert L.mxq_scale_bytes(1, 32, 1) == 128 * 4
+    assert L.mxq_scale_bytes(130, 160, 1) == 256 * 8
+    assert L.mxq_scale_bytes(4, 33, 0) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)        # 16-byte aligned, never dereferenced
+ODD = ctypes.c_void_p(0x10008)         # misaligned
+
+
+def test_quant_argument_errors(L):
+    q = L.mxq_quant_1x32_dual
+    assert q(FAKE, 64, 48, 48, FAKE, FAKE, None, None, 1, None) == 2      # cols % 32
+    assert q(FAKE, 48, 64, 64, None, None, FAKE, FAKE, 1, None) == 2      # rows % 32 (col copy)
+    assert q(None, 64, 64, 64, FAKE, FAKE, None, None, 1, None) == 1      # null input
+    assert q(FAKE, 64, 64, 64, None, None, None, None, 1, None) == 1      # no output asked
+    assert q(FAKE, 64, 64, 64, FAKE, None, None, None, 1, None) == 1      # half a pair
+    assert q(FAKE, 64, 64, 60, FAKE, FAKE, None, None, 1, None) == 1      # ld < cols
+    assert q(ODD, 64, 64, 64, FAKE, FAKE, None, None, 1, None) == 1       # misaligned
+    assert q(FAKE, 64, 64, 64, FAKE, FAKE, None, None, 7, None) == 1      # bad layout
+    assert q(FAKE, -1, 64, 64, FAKE, FAKE, None, None, 1, None) == 1
+    assert q(FAKE, 0, 64, 64, FAKE, FAKE, None, None, 1, None) == 0       # empty: nothing to do
+    b = L.mxq_quant_32x32
+    assert b(FAKE, 48, 64, 64, FAKE, FAKE, FAKE, 1, None) == 2            # n % 32
+    assert b(FAKE, 64, 40, 40, FAKE, FAKE, FAKE, 1, None) == 2            # k % 32 (block size)
+    assert b(None, 64, 64, 64, FAKE, FAKE, FAKE, 1, None) == 1
+
+
+def test_gemm_argument_errors(L):
+    g = L.mxq_gemm_bf16out
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 128, 48, 0, FAKE, 128, None) == 2   # K % 32
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 120, 64, 0, FAKE, 120, None) == 2   # N % 16
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 144, 64, 1, FAKE, 144, None) == 2   # MN-major N % 128
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 128, 64, 2, FAKE, 128, None) == 1   # bad flag
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 128, 64, 0, FAKE, 100, None) == 1   # ldy < N
+    assert g(None, FAKE, FAKE, FAKE, 64, 128, 64, 0, FAKE, 128, None) == 1
+    assert g(FAKE, FAKE, ODD, FAKE, 64, 128, 64, 0, FAKE, 128, None) == 1
+    assert g(FAKE, FAKE, FAKE, FAKE, 0, 128, 64, 0, FAKE, 128, None) == 0    # empty
+    gg = L.mxq_grouped_gemm
+    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 64, 128, 64, FAKE, 128, None) == 1     # G < 1
+    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 2000, 64, 128, 64, FAKE, 128, None) == 2  # G too big
+    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 192, 64, FAKE, 192, None) == 2     # N % 128
+    assert gg(FAKE, FAKE, FAKE, FAKE, None, 4, 64, 128, 64, FAKE, 128, None) == 1     # no offsets
+    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 0, 128, 64, FAKE, 128, None) == 0      # no rows
+
+
+def test_binding_raises_value_error(L):
+    from mxfp8_microscaled_precision_gb300 import mxq
+    with pytest.raises(ValueError):
+        mxq._check(2, "probe")
+    with pytest.raises(ValueError):
+        mxq._layout("zigzag")
