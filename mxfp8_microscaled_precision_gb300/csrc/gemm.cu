@@ -37,8 +37,6 @@ namespace {
 constexpr int kBM = 128;          // rows of A per tile (= TMEM lanes)
 constexpr int kBK = 128;          // K elements (= bytes) per pipeline stage
 constexpr int kUmmaK = 32;        // K of one MMA instruction (FP8)
-constexpr int kThreads = 192;     // 6 warps
-constexpr int kAccStages = 2;
 constexpr int kRasterBand = 8;    // m-tiles per raster band (L2 reuse of B)
 constexpr int kMaxGroups = 1024;
 
@@ -55,12 +53,22 @@ struct GemmArgs {
     uint64_t wait_limit_ns;
 };
 
+// Compile-time configuration of one kernel instance.
+//   BN = 128: two 128-column TMEM accumulators (the epilogue of tile t
+//             overlaps the main loop of tile t+1), 4 epilogue warps.
+//   BN = 256: one 256-column accumulator (two would leave no TMEM columns
+//             for the scale factors); 8 epilogue warps drain it into
+//             registers at once and release it before converting and
+//             storing, so the next tile's MMAs start after the drain only.
 template <int BN, int STAGES>
-struct Layout {
-    static constexpr int kBBytes = BN * kBK;             // per stage
+struct Cfg {
+    static constexpr int kAccStages = BN == 128 ? 2 : 1;
+    static constexpr int kEpiWarps = 4 * (BN / 128);   // each owns 32 lanes x 128 columns
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kBBytes = BN * kBK;            // per stage
     static constexpr int kABytes = kBM * kBK;
     static constexpr int kSfbAtoms = BN / 128;
-    static constexpr int kOffB = 0;                       // B first (see MN-major note)
+    static constexpr int kOffB = 0;                     // B first: see the N-major note below
     static constexpr int kOffA = kOffB + STAGES * kBBytes;
     static constexpr int kOffSfa = kOffA + STAGES * kABytes;
     static constexpr int kOffSfb = kOffSfa + STAGES * 512;
@@ -71,7 +79,7 @@ struct Layout {
     static constexpr int kOffSched = (kOffAbort + 4 + 15) / 16 * 16;
     static constexpr int kSchedBytes = 8 * (kMaxGroups + 1) + 4 * (kMaxGroups + 1) + 4 * kMaxGroups;
     static constexpr int kBytes = kOffSched + kSchedBytes;
-    static constexpr int kAlloc = kBytes + 1024;          // slack for 1024-byte alignment
+    static constexpr int kAlloc = kBytes + 1024;        // slack for 1024-byte alignment
     // TMEM columns: accumulators, then per-stage SFA and SFB slots.
     static constexpr int kTmemSfa = kAccStages * BN;
     static constexpr int kTmemSfb = kTmemSfa + 4 * STAGES;
@@ -134,11 +142,17 @@ __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs&
     return ti;
 }
 
+// Fast path of a bounded wait: one probe inline, the polling loop out of line.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitGuard& g) {
+    return mbar_try_wait(bar, parity) || mbar_wait(bar, parity, g);
+}
+
 template <int BN, int STAGES, bool kMnMajor, bool kGrouped>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tma_a,
                      const __grid_constant__ CUtensorMap tma_b, const GemmArgs p) {
-    using L = Layout<BN, STAGES>;
+    using L = Cfg<BN, STAGES>;
+    constexpr int kAcc = L::kAccStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -150,8 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + kAccStages + a); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * kAccStages);
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + kAcc + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * kAcc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
     const WaitGuard guard{abort_flag, p.status, p.wait_limit_ns};
 
@@ -161,9 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        for (int a = 0; a < kAccStages; ++a) {
+        for (int a = 0; a < kAcc; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);  // one arrive per epilogue warp
+            mbar_init(tempty_bar(a), L::kEpiWarps);  // one arrive per epilogue warp
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -189,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t* s_off = reinterpret_cast<int64_t*>(smem + L::kOffSched);
         int* s_prefix = reinterpret_cast<int*>(s_off + (kMaxGroups + 1));
         int* s_first = s_prefix + (kMaxGroups + 1);
-        for (int g = threadIdx.x; g <= p.G; g += kThreads) {
+        for (int g = threadIdx.x; g <= p.G; g += L::kThreads) {
             int64_t o = p.offsets[g];
             o = o < 0 ? 0 : (o > p.M ? p.M : o);  // keep malformed offsets in bounds
             s_off[g] = o;
@@ -235,36 +249,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             int64_t issued = 0;
+            const uint32_t full0 = full_bar(0), empty0 = empty_bar(0);
             for (int64_t t = blockIdx.x; t < sch.total && !*abort_flag; t += gridDim.x) {
                 const TileInfo ti = tile_info<BN, kGrouped>(sch, p, t);
-                const int64_t a_band = ti.m0 / 128;
                 const int64_t b_band0 = ti.b_row / 128;
+                int sfb_atoms = 0;
+#pragma unroll
+                for (int j = 0; j < L::kSfbAtoms; ++j)
+                    if (b_band0 + j < p.b_bands) ++sfb_atoms;
+                const uint32_t bytes = L::kABytes + L::kBBytes + 512u + 512u * sfb_atoms;
+                const uint8_t* sfa_src = p.a_s + (ti.m0 / 128) * p.k_atoms * 512;
+                const uint8_t* sfb_src = p.b_s + b_band0 * p.k_atoms * 512;
+                const int64_t sfb_band_stride = p.k_atoms * 512;
+                const int32_t ma = static_cast<int32_t>(ti.m0);
+                const int32_t nb = static_cast<int32_t>(ti.b_row);
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, guard)) break;
-                    int sfb_atoms = 0;
-                    for (int j = 0; j < L::kSfbAtoms; ++j)
-                        if (b_band0 + j < p.b_bands) ++sfb_atoms;
-                    const uint32_t bytes = L::kABytes + L::kBBytes + 512u + 512u * sfb_atoms;
-                    mbar_arrive_expect_tx(full_bar(stage), bytes);
+                    const uint32_t fb = full0 + 8u * stage;
+                    if (!wait_phase(empty0 + 8u * stage, phase ^ 1u, guard)) break;
+                    mbar_arrive_expect_tx(fb, bytes);
                     const uint32_t sa = sbase + L::kOffA + stage * L::kABytes;
                     const uint32_t sb = sbase + L::kOffB + stage * L::kBBytes;
                     const int32_t kx = kb * kBK;
-                    tma_load_2d(sa, &tma_a, kx, static_cast<int32_t>(ti.m0), full_bar(stage));
+                    tma_load_2d(sa, &tma_a, kx, ma, fb);
                     if constexpr (!kMnMajor) {
-                        tma_load_2d(sb, &tma_b, kx, static_cast<int32_t>(ti.b_row), full_bar(stage));
+                        tma_load_2d(sb, &tma_b, kx, nb, fb);
                     } else {
-                        // B stored [K, N]: boxes of 128 N-bytes x 128 K-rows.
+                        // B stored [K, N]: boxes of 128 N-bytes x 128 K-rows, one per 128 columns.
 #pragma unroll
                         for (int j = 0; j < BN / 128; ++j)
-                            tma_load_2d(sb + j * 128 * kBK, &tma_b,
-                                        static_cast<int32_t>(ti.b_row + 128 * j), kx, full_bar(stage));
+                            tma_load_2d(sb + j * 128 * kBK, &tma_b, nb + 128 * j, kx, fb);
                     }
-                    bulk_load(sbase + L::kOffSfa + stage * 512,
-                              p.a_s + (a_band * p.k_atoms + kb) * 512, 512u, full_bar(stage));
+                    bulk_load(sbase + L::kOffSfa + stage * 512, sfa_src + kb * 512, 512u, fb);
                     for (int j = 0; j < sfb_atoms; ++j)
                         bulk_load(sbase + L::kOffSfb + (stage * L::kSfbAtoms + j) * 512,
-                                  p.b_s + ((b_band0 + j) * p.k_atoms + kb) * 512, 512u,
-                                  full_bar(stage));
+                                  sfb_src + j * sfb_band_stride + kb * 512, 512u, fb);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -286,50 +304,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---- MMA issuer -----------------------------------------------------
         if (lane == 0) {
+            // Descriptors of stage 0; other stages and K steps are offsets of them
+            // (the address field holds bytes >> 4 in the low bits).
+            const uint64_t a_desc0 = make_smem_desc(sbase + L::kOffA, 16, 1024, 2);
+            // N-major B (the 32x32 dgrad): 128-column chunks are kBK rows x 128 bytes
+            // apart (leading byte offset); 8-row K groups 1024 bytes apart.
+            const uint64_t b_desc0 = kMnMajor ? make_smem_desc(sbase + L::kOffB, 128 * kBK, 1024, 2)
+                                              : make_smem_desc(sbase + L::kOffB, 16, 1024, 2);
+            const uint64_t sfa_desc0 = make_smem_desc(sbase + L::kOffSfa, 0, 128, 0);
+            const uint64_t sfb_desc0 = make_smem_desc(sbase + L::kOffSfb, 0, 128, 0);
+            constexpr uint32_t kBStepK = kMnMajor ? (kUmmaK * 128) >> 4 : kUmmaK >> 4;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < sch.total && ok; t += gridDim.x) {
-                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, guard)) { ok = false; break; }
+                if (!wait_phase(tempty_bar(acc), acc_phase ^ 1u, guard)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, guard)) { ok = false; break; }
+                    if (!wait_phase(full_bar(stage), phase, guard)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sfa_t = tmem_base + L::kTmemSfa + 4 * stage;
                     const uint32_t sfb_t = tmem_base + L::kTmemSfb + 4 * L::kSfbAtoms * stage;
-                    tc_cp_32x128b_warpx4(sfa_t, make_smem_desc(sbase + L::kOffSfa + stage * 512, 0, 128, 0));
+                    tc_cp_32x128b_warpx4(sfa_t, sfa_desc0 + static_cast<uint64_t>((stage * 512) >> 4));
 #pragma unroll
                     for (int j = 0; j < L::kSfbAtoms; ++j)
                         tc_cp_32x128b_warpx4(sfb_t + 4 * j,
-                                             make_smem_desc(sbase + L::kOffSfb + (stage * L::kSfbAtoms + j) * 512,
-                                                            0, 128, 0));
-                    const uint32_t sa = sbase + L::kOffA + stage * L::kABytes;
-                    const uint32_t sb = sbase + L::kOffB + stage * L::kBBytes;
+                                             sfb_desc0 + static_cast<uint64_t>(((stage * L::kSfbAtoms + j) * 512) >> 4));
+                    const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
+                    const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
                     const int64_t k_left = p.K - static_cast<int64_t>(kb) * kBK;
-                    const int ksub = static_cast<int>(k_left < kBK ? k_left : kBK) / kUmmaK;
+                    if (k_left >= kBK) {
 #pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        if (k < ksub) {
-                            const uint64_t adesc = make_smem_desc(sa + k * kUmmaK, 16, 1024, 2);
-                            uint64_t bdesc;
-                            if constexpr (!kMnMajor)
-                                bdesc = make_smem_desc(sb + k * kUmmaK, 16, 1024, 2);
-                            else
-                                bdesc = make_smem_desc(sb + k * kUmmaK * 128, 128 * kBK, 1024, 2);
-                            const uint32_t idesc = make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k);
-                            tc_mma_mxf8(d_tmem, adesc, bdesc, idesc, sfa_t, sfb_t,
+                        for (int k = 0; k < kBK / kUmmaK; ++k)
+                            tc_mma_mxf8(d_tmem, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
+                                        make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k), sfa_t, sfb_t,
                                         (kb > 0 || k > 0) ? 1u : 0u);
-                        }
+                    } else {
+                        const int ksub = static_cast<int>(k_left) / kUmmaK;
+                        for (int k = 0; k < ksub; ++k)
+                            tc_mma_mxf8(d_tmem, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
+                                        make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k), sfa_t, sfb_t,
+                                        (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     tc_commit(empty_bar(stage));  // frees the slot once these MMAs are done
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
                 tc_commit(tfull_bar(acc));
-                if (++acc == kAccStages) { acc = 0; acc_phase ^= 1u; }
+                if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
             }
             // Drain: every MMA and copy issued above completes before teardown.
             tc_commit(drain_bar);
@@ -339,8 +364,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             (void)mbar_wait(drain_bar, 0, g2);
         }
     } else {
-        // ---- epilogue (warps 2..5) -----------------------------------------
-        const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+        // ---- epilogue (warps 2 .. 2+kEpiWarps-1) ------------------------------
+        // Warp w reads TMEM lanes 32*(w%4).. (its lane quarter) and the
+        // 128-column half (w-2)/4 of the accumulator.
+        const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < sch.total; t += gridDim.x) {
@@ -348,43 +376,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             // One lane waits; the warp follows its verdict, so the .sync.aligned
             // tensor-memory loads below always run with the full warp.
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, guard) ? 1 : 0;
+            if (lane == 0) ok = wait_phase(tfull_bar(acc), acc_phase, guard) ? 1 : 0;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
             tc_fence_after();
+            uint32_t v[4][32];
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + acc * BN + half * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 32 * c, v[c]);
+            tmem_ld_wait();
+            // The accumulator is in registers: hand it back to the MMA warp now.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
+
             const int64_t row = ti.m0 + 32 * quad + lane;
-            const bool row_ok = row >= ti.row_lo && row < ti.row_hi;
-            uint16_t* yrow = p.y + row * p.ldy;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; c += 2) {
-                uint32_t v0[32], v1[32];
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + acc * BN + c * 32;
-                tmem_ld_32x32b_x32(taddr, v0);
-                tmem_ld_32x32b_x32(taddr + 32, v1);
-                tmem_ld_wait();
-                if (row_ok) {
+            if (row >= ti.row_lo && row < ti.row_hi) {
+                uint16_t* yrow = p.y + row * p.ldy;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t* v = h ? v1 : v0;
-                        const int64_t n = ti.n0 + (c + h) * 32;
+                for (int c = 0; c < 4; ++c) {
+                    const int64_t n = ti.n0 + half * 128 + c * 32;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            if (n + 8 * q + 8 <= p.N) {
-                                uint4 o;
-                                o.x = cvt_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-                                o.y = cvt_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-                                o.z = cvt_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-                                o.w = cvt_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-                                *reinterpret_cast<uint4*>(yrow + n + 8 * q) = o;
-                            }
+                    for (int q = 0; q < 4; ++q) {
+                        if (n + 8 * q + 8 <= p.N) {
+                            uint4 o;
+                            o.x = cvt_bf16x2(__uint_as_float(v[c][8 * q + 0]), __uint_as_float(v[c][8 * q + 1]));
+                            o.y = cvt_bf16x2(__uint_as_float(v[c][8 * q + 2]), __uint_as_float(v[c][8 * q + 3]));
+                            o.z = cvt_bf16x2(__uint_as_float(v[c][8 * q + 4]), __uint_as_float(v[c][8 * q + 5]));
+                            o.w = cvt_bf16x2(__uint_as_float(v[c][8 * q + 6]), __uint_as_float(v[c][8 * q + 7]));
+                            *reinterpret_cast<uint4*>(yrow + n + 8 * q) = o;
                         }
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
-            if (++acc == kAccStages) { acc = 0; acc_phase ^= 1u; }
         }
     }
 
@@ -436,7 +462,7 @@ bool make_tma_u8(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
 template <int BN, int STAGES, bool kMnMajor, bool kGrouped>
 cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& ta, const CUtensorMap& tb,
                      const GemmArgs& args, int64_t max_tiles, cudaStream_t stream) {
-    using L = Layout<BN, STAGES>;
+    using L = Cfg<BN, STAGES>;
     auto kern = gemm_mxf8_kernel<BN, STAGES, kMnMajor, kGrouped>;
     static thread_local int configured_device = -1;  // attribute set once per device and thread
     if (configured_device != dev.device) {
@@ -447,12 +473,12 @@ cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& ta, const CUtenso
     int64_t grid = dev.sm_count;
     if (max_tiles >= 0 && max_tiles < grid) grid = max_tiles;
     if (grid <= 0) return cudaSuccess;
-    kern<<<static_cast<unsigned>(grid), kThreads, L::kAlloc, stream>>>(ta, tb, args);
+    kern<<<static_cast<unsigned>(grid), L::kThreads, L::kAlloc, stream>>>(ta, tb, args);
     return cudaGetLastError();
 }
 
-constexpr int kBN = 128;
-constexpr int kStages = 6;
+constexpr int kBN = 256;
+constexpr int kStages = 4;
 
 }  // namespace
 
