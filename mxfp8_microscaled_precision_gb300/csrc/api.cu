@@ -120,7 +120,7 @@ mxq_status mxq_quant_1x32_dual(const void* x, int64_t rows, int64_t cols, int64_
     mxq::DeviceInfo dev;
     mxq_status st = device_ok(&dev);
     if (st != MXQ_OK) return st;
-    return from_cuda(mxq::launch_quant_1x32(x, rows, cols, ld, row ? q_row : nullptr,
+    return from_cuda(mxq::launch_quant_1x32(dev, x, rows, cols, ld, row ? q_row : nullptr,
                                             row ? s_row : nullptr, col ? q_col : nullptr,
                                             col ? s_col : nullptr, layout == MXQ_SCALE_MMA_TILED,
                                             reinterpret_cast<cudaStream_t>(stream)));
@@ -139,7 +139,7 @@ mxq_status mxq_quant_32x32(const void* w, int64_t n, int64_t k, int64_t ld, void
     mxq::DeviceInfo dev;
     mxq_status st = device_ok(&dev);
     if (st != MXQ_OK) return st;
-    return from_cuda(mxq::launch_quant_32x32(w, n, k, ld, q, s_fwd, s_bwd,
+    return from_cuda(mxq::launch_quant_32x32(dev, w, n, k, ld, q, s_fwd, s_bwd,
                                              layout == MXQ_SCALE_MMA_TILED,
                                              reinterpret_cast<cudaStream_t>(stream)));
 }

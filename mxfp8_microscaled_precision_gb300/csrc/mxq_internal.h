@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace mxq {
@@ -19,12 +20,19 @@ struct DeviceInfo {
 // Returns cudaSuccess and fills `info` for the current device.
 cudaError_t current_device_info(DeviceInfo* info);
 
-cudaError_t launch_quant_1x32(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q_row,
-                              void* s_row, void* q_col, void* s_col, bool tiled,
-                              cudaStream_t stream);
+// 2-D tensor map over a row-major matrix [outer, inner] of 1- or 2-byte
+// elements with the given row stride, box [box_outer, box_inner].
+bool encode_tensor_map_2d(CUtensorMap* map, const void* base, bool two_byte_elems, uint64_t inner,
+                          uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                          uint32_t box_outer, bool swizzle_128b);
 
-cudaError_t launch_quant_32x32(const void* w, int64_t n, int64_t k, int64_t ld, void* q,
-                               void* s_fwd, void* s_bwd, bool tiled, cudaStream_t stream);
+cudaError_t launch_quant_1x32(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols,
+                              int64_t ld, void* q_row, void* s_row, void* q_col, void* s_col,
+                              bool tiled, cudaStream_t stream);
+
+cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, int64_t k,
+                               int64_t ld, void* q, void* s_fwd, void* s_bwd, bool tiled,
+                               cudaStream_t stream);
 
 // Dense block-scaled GEMM (see mxq_gemm_bf16out).  Returns cudaErrorInvalidValue
 // when a tensor map cannot be encoded for the given shapes.
