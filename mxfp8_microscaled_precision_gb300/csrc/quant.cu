@@ -7,17 +7,20 @@
 //  * 32x32: one scale per 32x32 tile and a single payload shared by the
 //    forward and backward GEMMs (same RFC, sections 3.1 and 3.3.3).
 //
-// Both are HBM-bound.  Persistent CTAs of 256 threads stream 128x128 BF16
-// tiles through a two-slot shared-memory ring filled by TMA, so the loads of
-// the next tiles overlap the quantization and stores of the current one.
-// The amax of a 32-group is reduced over the four lanes that hold it with
-// two shuffles (row groups) or by one thread over a shared-memory column
-// (column groups); the exponent is the exact rceil rule evaluated on the
-// BF16 bits of amax; the scaling by 2^-e is an exact multiply; one
-// cvt.rn.satfinite instruction rounds two values to E4M3.  The column copy
-// reads the same staged tile, so the input is read from HBM once.  Scales
-// go out plain or in the MMA-tiled layout; the tiled permutation is fused
-// into the scale stores (which also write its zero padding).
+// Both are HBM-bound.  Work is cut into 128x128 BF16 tiles; a CTA of 256
+// threads quantizes a tile.  Kernels that only need the row copy (and the
+// 32x32 kernel) load their tile straight into registers with 16-byte loads
+// issued up front, one tile per CTA.  Kernels that also produce the column
+// copy are persistent and stream tiles through a three-slot shared-memory
+// ring filled by TMA, so the loads of the next tiles overlap the work on the
+// current one; the column groups are read back from the staged tile, so the
+// input is read from HBM once.  The amax of a row group is reduced with
+// packed 16x2 maxima and two shuffles over the four lanes that hold it; a
+// column group is reduced by one thread.  The exponent is the exact rceil
+// rule evaluated on the BF16 bits of amax; the scaling by 2^-e is an exact
+// multiply; one cvt.rn.satfinite instruction rounds two values to E4M3.
+// Scales go out plain or in the MMA-tiled layout; the tiled permutation is
+// fused into the scale stores (which also write its zero padding).
 
 #include <cuda_runtime.h>
 
@@ -34,7 +37,7 @@ constexpr int kThreads = 256;
 constexpr int kLoadsPerThread = kTile * kTile / 8 / kThreads;  // 8 x 16-byte chunks
 constexpr int kRing = 2;                                        // tile slots per CTA
 constexpr int kTileBytes = kTile * kTile * 2;                   // 32 KB of BF16
-constexpr int kCtasPerSm = 3;
+constexpr int kCtasPerSm = 3;                                   // ring kernels
 constexpr int kSmemBytes = kRing * kTileBytes + 1024 + 256;     // ring + alignment + barriers
 
 // E8M0 exponent of a finite, non-negative amax given as BF16 bits
@@ -55,9 +58,18 @@ __device__ __forceinline__ float pow2_neg(int e) { return __int_as_float((127 - 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ uint32_t abs_max_bits(uint32_t w, uint32_t m) {
-    m = max(m, w & 0x7FFFu);
-    return max(m, (w >> 16) & 0x7FFFu);
+// Per-half unsigned maximum of two packed 16-bit pairs (one instruction).
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Largest |x| (as BF16 bits, sign cleared) of 8 BF16 values.
+__device__ __forceinline__ uint32_t amax8_bits(const uint4 v) {
+    const uint32_t m = max_u16x2(max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                 max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    return max(m & 0xFFFFu, m >> 16);
 }
 
 // Quantize 8 BF16 values (4 words) with scale 2^-e -> 8 E4M3 bytes.
@@ -163,14 +175,89 @@ __device__ __forceinline__ void ring_drain(const Ring& r, int i, int64_t tile, i
 }
 
 // ---------------------------------------------------------------------------------
-// 1x32 quantization: row copy and/or column copy, tile by tile.
-// Row pass: thread t takes rows (t/16 + 16 i), i = 0..7, 16-byte chunk t % 16
-// of the tile; the four chunks of one 32-group sit in four consecutive lanes.
+// Row copy of one 128x128 tile held in registers.  Thread t holds rows
+// (t/16 + 16 j), j = 0..7, 16-byte chunk t % 16 of the tile; the four chunks
+// of one 32-group sit in four consecutive lanes.
+// `chunk_of(j)` returns chunk j (registers or shared memory).
+template <bool kTiled, class ChunkOf>
+__device__ __forceinline__ void row_pass(ChunkOf chunk_of, int64_t r0, int64_t c0, int64_t rows,
+                                         int64_t cols, uint8_t* __restrict__ q_row,
+                                         uint8_t* __restrict__ s_row) {
+    const int t = threadIdx.x;
+    const int chunk = t & 15;
+    const int64_t groups = cols >> 5;
+    const int64_t col = c0 + chunk * 8;
+    const bool col_ok = col < cols;
+    const int64_t rows_left = rows - r0 - (t >> 4);  // chunk j is in a real row if 16 j < rows_left
+    uint8_t* qp = q_row + (r0 + (t >> 4)) * cols + col;
+    const int64_t qstep = 16 * cols;
+    // Tiled: the tile's scales fill one 512-byte atom; row r and group g sit at
+    // 16*(r%32) + 4*((r%128)/32) + g%4, i.e. 16*(t/16) + 256*(j%2) + 4*(j/2) + chunk/4.
+    uint8_t* sp = kTiled ? s_row + ((r0 >> 7) * ((groups + 3) >> 2) + (c0 >> 7)) * 512 + ((t >> 4) << 4) +
+                               (chunk >> 2)
+                         : s_row + (r0 + (t >> 4)) * groups + (col >> 5);
+#pragma unroll
+    for (int j = 0; j < kLoadsPerThread; ++j) {
+        const uint4 v = chunk_of(j);
+        uint32_t m = amax8_bits(v);
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        const bool valid = col_ok && 16 * j < rows_left;
+        uint8_t code;
+        uint2 out;
+        if (m >= 0x7F80u) {  // NaN or Inf in the group
+            code = 0xFF;
+            out = nan8(v);
+        } else {
+            const int e = rceil_exponent(m);
+            code = static_cast<uint8_t>(e + 127);
+            out = quant8(v, pow2_neg(e));
+        }
+        if (valid) *reinterpret_cast<uint2*>(qp + j * qstep) = out;
+        if ((chunk & 3) == 0 && (valid || kTiled)) {  // tiled padding gets 0
+            uint8_t* dst = kTiled ? sp + 256 * (j & 1) + 4 * (j >> 1) : sp + j * 16 * groups;
+            *dst = valid ? code : 0;
+        }
+    }
+}
+
+// Loads this thread's 8 chunks of tile (r0, c0) straight from global memory
+// (zeros outside the matrix).
+__device__ __forceinline__ void load_tile_chunks(uint4 (&v)[kLoadsPerThread], const uint16_t* __restrict__ x,
+                                                 int64_t r0, int64_t c0, int64_t rows, int64_t cols,
+                                                 int64_t ld) {
+    const int t = threadIdx.x;
+    const int64_t col = c0 + (t & 15) * 8;
+    const int64_t rows_left = rows - r0 - (t >> 4);
+    const uint16_t* xp = x + (r0 + (t >> 4)) * ld + col;
+#pragma unroll
+    for (int j = 0; j < kLoadsPerThread; ++j) {
+        if (col < cols && 16 * j < rows_left)
+            v[j] = __ldg(reinterpret_cast<const uint4*>(xp + j * 16 * ld));
+        else
+            v[j] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Row copy only: one tile per CTA, loaded straight into registers.
+template <bool kTiled>
+__global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                              int64_t cols, int64_t ld,
+                                                              uint8_t* __restrict__ q_row,
+                                                              uint8_t* __restrict__ s_row, int64_t tiles_c) {
+    const int64_t tile = blockIdx.x;
+    const int64_t r0 = (tile / tiles_c) * kTile, c0 = (tile % tiles_c) * kTile;
+    uint4 v[kLoadsPerThread];
+    load_tile_chunks(v, x, r0, c0, rows, cols, ld);
+    row_pass<kTiled>([&](int j) { return v[j]; }, r0, c0, rows, cols, q_row, s_row);
+}
+
+// Column copy (with or without the row copy): persistent, TMA-fed ring.
 // Column pass: thread t takes the column pair t % 64 and the 32-row group
-// t / 64; a warp reads 128 contiguous bytes of one tile row per step, so the
-// shared-memory reads are conflict-free.
-template <bool kRow, bool kCol, bool kTiled>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_1x32_kernel(
+// t / 64; a warp reads 128 contiguous bytes of one staged row per step, so
+// the shared-memory reads are conflict-free.
+template <bool kRow, bool kTiled>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_kernel(
     const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_t cols,
     uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col,
     uint8_t* __restrict__ s_col, int64_t tiles_c, int64_t n_tiles, unsigned int* status,
@@ -181,8 +268,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_1x32_kernel(
     ring_start(ring, &tmap, n_tiles, tiles_c);
 
     const int t = threadIdx.x;
-    const int chunk = t & 15;
-    const int64_t groups = cols >> 5;
     const int64_t rgroups = rows >> 5;
     int i = 0;
     int64_t tile = blockIdx.x;
@@ -193,97 +278,64 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_1x32_kernel(
         const int64_t c0 = (tile % tiles_c) * kTile;
 
         if constexpr (kRow) {
-            const int64_t col = c0 + chunk * 8;
-            const bool col_ok = col < cols;
-            const int64_t g = col >> 5;
-#pragma unroll
-            for (int j = 0; j < kLoadsPerThread; ++j) {
-                const int lr = (t >> 4) + 16 * j;
-                const uint4 v = reinterpret_cast<const uint4*>(buf)[lr * 16 + chunk];
-                const int64_t r = r0 + lr;
-                uint32_t m = abs_max_bits(v.x, 0u);
-                m = abs_max_bits(v.y, m);
-                m = abs_max_bits(v.z, m);
-                m = abs_max_bits(v.w, m);
-                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-                const bool valid = col_ok && r < rows;
-                uint8_t code;
-                uint2 out;
-                if (m >= 0x7F80u) {  // NaN or Inf in the group
-                    code = 0xFF;
-                    out = nan8(v);
-                } else {
-                    const int e = rceil_exponent(m);
-                    code = static_cast<uint8_t>(e + 127);
-                    out = quant8(v, pow2_neg(e));
-                }
-                if (valid) *reinterpret_cast<uint2*>(q_row + r * cols + col) = out;
-                if ((chunk & 3) == 0) {
-                    if (valid)
-                        store_scale(s_row, r, g, groups, kTiled, code);
-                    else if (kTiled)  // zero padding of the tiled layout
-                        store_scale(s_row, r, g, groups, true, 0);
-                }
-            }
+            const uint4* b4 = reinterpret_cast<const uint4*>(buf) + (t >> 4) * 16 + (t & 15);
+            row_pass<kTiled>([&](int j) { return b4[j * 256]; }, r0, c0, rows, cols, q_row, s_row);
         }
 
-        if constexpr (kCol) {
-            const uint32_t* tw = reinterpret_cast<const uint32_t*>(buf);
-            const int p = t & 63;
-            const int gi = t >> 6;
-            const int64_t cA = c0 + 2 * p;              // output row of q_col
-            const int64_t rbase = r0 + 32 * gi;         // first input row of the group
-            const int64_t g_out = rbase >> 5;
-            const bool ok = cA < cols && rbase < rows;  // rows % 32 == 0 in column mode
-            uint32_t w[32];
-            uint32_t mlo = 0u, mhi = 0u;
+        const uint32_t* tw = reinterpret_cast<const uint32_t*>(buf);
+        const int p = t & 63;
+        const int gi = t >> 6;
+        const int64_t cA = c0 + 2 * p;              // output row of q_col
+        const int64_t rbase = r0 + 32 * gi;         // first input row of the group
+        const int64_t g_out = rbase >> 5;
+        const bool ok = cA < cols && rbase < rows;  // rows % 32 == 0 in column mode
+        uint32_t w[32];
+        uint32_t m2 = 0u;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                w[j] = tw[(32 * gi + j) * 64 + p];
-                mlo = max(mlo, w[j] & 0x7FFFu);
-                mhi = max(mhi, (w[j] >> 16) & 0x7FFFu);
-            }
+        for (int j = 0; j < 32; ++j) {
+            w[j] = tw[(32 * gi + j) * 64 + p];
+            m2 = max_u16x2(m2, w[j] & 0x7FFF7FFFu);
+        }
+        uint8_t* q0 = q_col + cA * rows + rbase;
+        // Scale bytes of rows cA and cA+1 (same 32-row block: cA is even).
+        uint8_t* s0 = kTiled ? s_col + tiled_scale_offset(cA, g_out, rgroups) : s_col + cA * rgroups + g_out;
+        const int64_t s_next = kTiled ? 16 : rgroups;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const uint32_t m = half ? mhi : mlo;
-                const int64_t c = cA + half;
-                uint8_t code;
-                uint32_t o[8];
-                if (m >= 0x7F80u) {
-                    code = 0xFF;
+        for (int half = 0; half < 2; ++half) {
+            const uint32_t m = half ? (m2 >> 16) : (m2 & 0xFFFFu);
+            uint8_t code;
+            uint32_t o[8];
+            if (m >= 0x7F80u) {
+                code = 0xFF;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        uint32_t b = 0x7F7F7F7Fu;
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t b = 0x7F7F7F7Fu;
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const uint32_t h = half ? (w[4 * j + u] >> 16) : (w[4 * j + u] & 0xFFFFu);
-                            b |= ((h >> 15) & 1u) << (8 * u + 7);
-                        }
-                        o[j] = b;
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t h = half ? (w[4 * j + u] >> 16) : (w[4 * j + u] & 0xFFFFu);
+                        b |= ((h >> 15) & 1u) << (8 * u + 7);
                     }
-                } else {
-                    const int e = rceil_exponent(m);
-                    const float sc = pow2_neg(e);
-                    code = static_cast<uint8_t>(e + 127);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float f[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            f[u] = (half ? bf16_hi(w[4 * j + u]) : bf16_lo(w[4 * j + u])) * sc;
-                        o[j] = cvt_e4m3x2(f[0], f[1]) | (cvt_e4m3x2(f[2], f[3]) << 16);
-                    }
+                    o[j] = b;
                 }
-                if (ok) {
-                    uint4* dst = reinterpret_cast<uint4*>(q_col + c * rows + rbase);
-                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-                    store_scale(s_col, c, g_out, rgroups, kTiled, code);
-                } else if (kTiled) {
-                    store_scale(s_col, c, g_out, rgroups, true, 0);
+            } else {
+                const int e = rceil_exponent(m);
+                const float sc = pow2_neg(e);
+                code = static_cast<uint8_t>(e + 127);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float f[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        f[u] = (half ? bf16_hi(w[4 * j + u]) : bf16_lo(w[4 * j + u])) * sc;
+                    o[j] = cvt_e4m3x2(f[0], f[1]) | (cvt_e4m3x2(f[2], f[3]) << 16);
                 }
             }
+            if (ok) {
+                uint4* dst = reinterpret_cast<uint4*>(q0 + half * rows);
+                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            if (ok || kTiled) s0[half * s_next] = ok ? code : 0;
         }
         ring_release(ring, &tmap, i, tile, n_tiles, tiles_c);
     }
@@ -291,97 +343,77 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_1x32_kernel(
 }
 
 // ---------------------------------------------------------------------------------
-// 32x32 block quantization of w [n, k], one 128x128 tile (16 blocks) at a time.
+// 32x32 block quantization of w [n, k]: one 128x128 tile (16 blocks) per CTA.
 template <bool kTiled>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_32x32_kernel(
-    const __grid_constant__ CUtensorMap tmap, int64_t n, int64_t k, uint8_t* __restrict__ q,
-    uint8_t* __restrict__ s_fwd, uint8_t* __restrict__ s_bwd, int64_t tiles_c, int64_t n_tiles,
-    unsigned int* status, uint64_t wait_limit_ns) {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ uint32_t blk_amax[2][4][4];  // [tile parity][32-row block][32-col block]
-    const Ring ring = ring_setup(smem_raw);
-    const WaitGuard guard{ring.abort_flag, status, wait_limit_ns};
+__global__ void __launch_bounds__(kThreads) quant_32x32_kernel(const uint16_t* __restrict__ w, int64_t n,
+                                                               int64_t k, int64_t ld, uint8_t* __restrict__ q,
+                                                               uint8_t* __restrict__ s_fwd,
+                                                               uint8_t* __restrict__ s_bwd, int64_t tiles_c) {
+    __shared__ uint32_t blk_amax[4][4];  // [32-row block][32-col block] of this tile
     const int t = threadIdx.x;
-    if (t < 32) reinterpret_cast<uint32_t*>(blk_amax)[t] = 0u;
-    ring_start(ring, &tmap, n_tiles, tiles_c);
-
+    if (t < 16) blk_amax[t >> 2][t & 3] = 0u;
+    const int64_t tile = blockIdx.x;
+    const int64_t r0 = (tile / tiles_c) * kTile, c0 = (tile % tiles_c) * kTile;
     const int chunk = t & 15;
     const int gcol = chunk >> 2;  // 32-column block within the tile
-    const int64_t kgroups = k >> 5, ngroups = n >> 5;
-    int i = 0;
-    int64_t tile = blockIdx.x;
-    for (; tile < n_tiles; tile += gridDim.x, ++i) {
-        if (!ring_wait(ring, i, guard)) break;
-        const uint4* buf = reinterpret_cast<const uint4*>(ring.buf + (i % kRing) * kTileBytes);
-        uint32_t(*am)[4] = blk_amax[i & 1];
-        const int64_t r0 = (tile / tiles_c) * kTile;
-        const int64_t c0 = (tile % tiles_c) * kTile;
-        const int64_t col = c0 + chunk * 8;
-        const bool col_ok = col < k;
+    uint4 v[kLoadsPerThread];
+    load_tile_chunks(v, w, r0, c0, n, k, ld);
+    __syncthreads();  // blk_amax cleared
 
-        uint4 v[kLoadsPerThread];
+    // Chunk j (row t/16 + 16 j) lies in 32-row block j/2 of the tile.
 #pragma unroll
-        for (int j = 0; j < kLoadsPerThread; ++j) v[j] = buf[((t >> 4) + 16 * j) * 16 + chunk];
-        // Row (t/16 + 16 j) lies in 32-row block j/2 of the tile.
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            uint32_t m = 0u;
-#pragma unroll
-            for (int j = 2 * b; j < 2 * b + 2; ++j) {
-                m = abs_max_bits(v[j].x, m);
-                m = abs_max_bits(v[j].y, m);
-                m = abs_max_bits(v[j].z, m);
-                m = abs_max_bits(v[j].w, m);
-            }
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-            if ((chunk & 3) == 0) atomicMax(&am[b][gcol], m);
-        }
-        __syncthreads();
-        // The other parity's block maxima belong to the next tile: clear them now.
-        if (t < 16) reinterpret_cast<uint32_t*>(blk_amax[(i + 1) & 1])[t] = 0u;
-
-#pragma unroll
-        for (int j = 0; j < kLoadsPerThread; ++j) {
-            const int64_t r = r0 + (t >> 4) + 16 * j;
-            const uint32_t m = am[j >> 1][gcol];
-            const bool valid = col_ok && r < n;
-            uint8_t code;
-            uint2 out;
-            if (m >= 0x7F80u) {
-                code = 0xFF;
-                out = nan8(v[j]);
-            } else {
-                const int e = rceil_exponent(m);
-                code = static_cast<uint8_t>(e + 127);
-                out = quant8(v[j], pow2_neg(e));
-            }
-            if (valid) *reinterpret_cast<uint2*>(q + r * k + col) = out;
-            if (s_fwd && (chunk & 3) == 0) {
-                if (valid)
-                    store_scale(s_fwd, r, col >> 5, kgroups, kTiled, code);
-                else if (kTiled)
-                    store_scale(s_fwd, r, col >> 5, kgroups, true, 0);
-            }
-        }
-        // s_bwd [k, n/32]: row c (a column of w), group = 32-row block of w.
-        if (s_bwd) {
-#pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-                const int idx = t + kThreads * e2;   // 0..511
-                const int cl = idx & 127, b = idx >> 7;
-                const int64_t c = c0 + cl;
-                const int64_t gi = (r0 >> 5) + b;
-                const bool valid = c < k && gi < ngroups;
-                const uint32_t m = am[b][cl >> 5];
-                uint8_t code = 0;
-                if (valid) code = (m >= 0x7F80u) ? 0xFF : static_cast<uint8_t>(rceil_exponent(m) + 127);
-                if (valid || kTiled) store_scale(s_bwd, c, gi, ngroups, kTiled, code);
-            }
-        }
-        ring_release(ring, &tmap, i, tile, n_tiles, tiles_c);
+    for (int b = 0; b < 4; ++b) {
+        uint32_t m = max(amax8_bits(v[2 * b]), amax8_bits(v[2 * b + 1]));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        if ((chunk & 3) == 0) atomicMax(&blk_amax[b][gcol], m);
     }
-    ring_drain(ring, i, tile, n_tiles, guard);
+    __syncthreads();
+
+    const int64_t kgroups = k >> 5, ngroups = n >> 5;
+    const int64_t col = c0 + chunk * 8;
+    const bool col_ok = col < k;
+    const int64_t rows_left = n - r0 - (t >> 4);
+    uint8_t* qp = q + (r0 + (t >> 4)) * k + col;
+    uint8_t* sp = nullptr;
+    if (s_fwd)
+        sp = kTiled ? s_fwd + ((r0 >> 7) * ((kgroups + 3) >> 2) + (c0 >> 7)) * 512 + ((t >> 4) << 4) + (chunk >> 2)
+                    : s_fwd + (r0 + (t >> 4)) * kgroups + (col >> 5);
+#pragma unroll
+    for (int j = 0; j < kLoadsPerThread; ++j) {
+        const uint32_t m = blk_amax[j >> 1][gcol];
+        const bool valid = col_ok && 16 * j < rows_left;
+        uint8_t code;
+        uint2 out;
+        if (m >= 0x7F80u) {
+            code = 0xFF;
+            out = nan8(v[j]);
+        } else {
+            const int e = rceil_exponent(m);
+            code = static_cast<uint8_t>(e + 127);
+            out = quant8(v[j], pow2_neg(e));
+        }
+        if (valid) *reinterpret_cast<uint2*>(qp + j * 16 * k) = out;
+        if (sp && (chunk & 3) == 0 && (valid || kTiled)) {
+            uint8_t* dst = kTiled ? sp + 256 * (j & 1) + 4 * (j >> 1) : sp + j * 16 * kgroups;
+            *dst = valid ? code : 0;
+        }
+    }
+    // s_bwd [k, n/32]: row c (a column of w), group = 32-row block of w.
+    if (s_bwd) {
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+            const int idx = t + kThreads * e2;   // 0..511
+            const int cl = idx & 127, b = idx >> 7;
+            const int64_t c = c0 + cl;
+            const int64_t gi = (r0 >> 5) + b;
+            const bool valid = c < k && gi < ngroups;
+            const uint32_t m = blk_amax[b][cl >> 5];
+            uint8_t code = 0;
+            if (valid) code = (m >= 0x7F80u) ? 0xFF : static_cast<uint8_t>(rceil_exponent(m) + 127);
+            if (valid || kTiled) store_scale(s_bwd, c, gi, ngroups, kTiled, code);
+        }
+    }
 }
 
 // Sets the dynamic shared-memory limit once per device and thread.
@@ -398,10 +430,10 @@ int64_t grid_for(const DeviceInfo& dev, int64_t n_tiles) {
     return n_tiles < cap ? n_tiles : cap;
 }
 
-template <bool kRow, bool kCol, bool kTiled>
-cudaError_t launch_1x32_t(const DeviceInfo& dev, const CUtensorMap& map, int64_t rows, int64_t cols,
+template <bool kRow, bool kTiled>
+cudaError_t launch_cols_t(const DeviceInfo& dev, const CUtensorMap& map, int64_t rows, int64_t cols,
                           void* q_row, void* s_row, void* q_col, void* s_col, cudaStream_t stream) {
-    auto kern = quant_1x32_kernel<kRow, kCol, kTiled>;
+    auto kern = quant_cols_kernel<kRow, kTiled>;
     static thread_local int configured = -1;
     cudaError_t e = configure_once(kern, dev.device, &configured);
     if (e != cudaSuccess) return e;
@@ -411,29 +443,6 @@ cudaError_t launch_1x32_t(const DeviceInfo& dev, const CUtensorMap& map, int64_t
         map, rows, cols, static_cast<uint8_t*>(q_row), static_cast<uint8_t*>(s_row),
         static_cast<uint8_t*>(q_col), static_cast<uint8_t*>(s_col), tiles_c, n_tiles, dev.status,
         kDefaultWaitLimitNs);
-    return cudaGetLastError();
-}
-
-template <bool kRow, bool kCol>
-cudaError_t launch_1x32_l(const DeviceInfo& dev, const CUtensorMap& map, int64_t rows, int64_t cols,
-                          void* q_row, void* s_row, void* q_col, void* s_col, bool tiled,
-                          cudaStream_t stream) {
-    if (tiled) return launch_1x32_t<kRow, kCol, true>(dev, map, rows, cols, q_row, s_row, q_col, s_col, stream);
-    return launch_1x32_t<kRow, kCol, false>(dev, map, rows, cols, q_row, s_row, q_col, s_col, stream);
-}
-
-template <bool kTiled>
-cudaError_t launch_32x32_t(const DeviceInfo& dev, const CUtensorMap& map, int64_t n, int64_t k, void* q,
-                           void* s_fwd, void* s_bwd, cudaStream_t stream) {
-    auto kern = quant_32x32_kernel<kTiled>;
-    static thread_local int configured = -1;
-    cudaError_t e = configure_once(kern, dev.device, &configured);
-    if (e != cudaSuccess) return e;
-    const int64_t tiles_c = (k + kTile - 1) / kTile;
-    const int64_t n_tiles = tiles_c * ((n + kTile - 1) / kTile);
-    kern<<<static_cast<unsigned>(grid_for(dev, n_tiles)), kThreads, kSmemBytes, stream>>>(
-        map, n, k, static_cast<uint8_t*>(q), static_cast<uint8_t*>(s_fwd), static_cast<uint8_t*>(s_bwd),
-        tiles_c, n_tiles, dev.status, kDefaultWaitLimitNs);
     return cudaGetLastError();
 }
 
@@ -448,20 +457,42 @@ bool bf16_tile_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols, 
 cudaError_t launch_quant_1x32(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols,
                               int64_t ld, void* q_row, void* s_row, void* q_col, void* s_col,
                               bool tiled, cudaStream_t stream) {
+    const bool row = q_row != nullptr, col = q_col != nullptr;
+    const int64_t tiles_c = (cols + kTile - 1) / kTile;
+    const int64_t n_tiles = tiles_c * ((rows + kTile - 1) / kTile);
+    if (!col) {  // row copy only: direct loads, one tile per CTA
+        auto xp = static_cast<const uint16_t*>(x);
+        auto qp = static_cast<uint8_t*>(q_row);
+        auto sp = static_cast<uint8_t*>(s_row);
+        if (tiled)
+            quant_rows_kernel<true><<<static_cast<unsigned>(n_tiles), kThreads, 0, stream>>>(xp, rows, cols, ld, qp, sp, tiles_c);
+        else
+            quant_rows_kernel<false><<<static_cast<unsigned>(n_tiles), kThreads, 0, stream>>>(xp, rows, cols, ld, qp, sp, tiles_c);
+        return cudaGetLastError();
+    }
     CUtensorMap map;
     if (!bf16_tile_map(&map, x, rows, cols, ld)) return cudaErrorInvalidValue;
-    const bool row = q_row != nullptr, col = q_col != nullptr;
-    if (row && col) return launch_1x32_l<true, true>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tiled, stream);
-    if (row) return launch_1x32_l<true, false>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tiled, stream);
-    return launch_1x32_l<false, true>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tiled, stream);
+    if (row)
+        return tiled ? launch_cols_t<true, true>(dev, map, rows, cols, q_row, s_row, q_col, s_col, stream)
+                     : launch_cols_t<true, false>(dev, map, rows, cols, q_row, s_row, q_col, s_col, stream);
+    return tiled ? launch_cols_t<false, true>(dev, map, rows, cols, q_row, s_row, q_col, s_col, stream)
+                 : launch_cols_t<false, false>(dev, map, rows, cols, q_row, s_row, q_col, s_col, stream);
 }
 
 cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, int64_t k, int64_t ld,
                                void* q, void* s_fwd, void* s_bwd, bool tiled, cudaStream_t stream) {
-    CUtensorMap map;
-    if (!bf16_tile_map(&map, w, n, k, ld)) return cudaErrorInvalidValue;
-    if (tiled) return launch_32x32_t<true>(dev, map, n, k, q, s_fwd, s_bwd, stream);
-    return launch_32x32_t<false>(dev, map, n, k, q, s_fwd, s_bwd, stream);
+    (void)dev;
+    const int64_t tiles_c = (k + kTile - 1) / kTile;
+    const int64_t n_tiles = tiles_c * ((n + kTile - 1) / kTile);
+    auto wp = static_cast<const uint16_t*>(w);
+    auto qp = static_cast<uint8_t*>(q);
+    auto sf = static_cast<uint8_t*>(s_fwd);
+    auto sb = static_cast<uint8_t*>(s_bwd);
+    if (tiled)
+        quant_32x32_kernel<true><<<static_cast<unsigned>(n_tiles), kThreads, 0, stream>>>(wp, n, k, ld, qp, sf, sb, tiles_c);
+    else
+        quant_32x32_kernel<false><<<static_cast<unsigned>(n_tiles), kThreads, 0, stream>>>(wp, n, k, ld, qp, sf, sb, tiles_c);
+    return cudaGetLastError();
 }
 
 }  // namespace mxq
