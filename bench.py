@@ -40,7 +40,9 @@ METRIC = "MXFP8 GEMM TFLOP/s (% dense MXFP8 peak); quantizer TB/s (% HBM), 1 GB3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 L2_FLUSH_BYTES = 256 << 20   # larger than the 129 MB L2
-GEMM_TRAFFIC_BYTES = None    # filled from an ncu capture of the current GEMM kernel
+# DRAM bytes (read + write) of one GEMM launch, from an ncu capture of the current
+# kernel (profiles/gemm_mxf8_kernel_linear_train.md); None where not captured.
+GEMM_TRAFFIC_BYTES = {"linear_train": 52.4e6 + 23.9e6}
 
 
 def load_peaks():
@@ -524,7 +526,7 @@ def run_gpu(args):
     per_launch_flops = statistics.mean(kern[j][2] for j in gemm_idx)
     roofline = {"bound": "tensor", "kernel": "gemm_mxf8_kernel", "achieved": round(gemm_tflops, 1),
                 "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
-                "traffic": GEMM_TRAFFIC_BYTES,
+                "traffic": GEMM_TRAFFIC_BYTES.get(w.name),
                 "units_per_launch": per_launch_flops,
                 "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 ratio)"}
     roofline_quant = {"bound": "hbm", "kernel": "quant kernels", "achieved": round(quant_gbs, 1),
