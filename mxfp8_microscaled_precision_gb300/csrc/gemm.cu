@@ -61,6 +61,7 @@ struct GemmArgs {
 //             storing, so the next tile's MMAs start after the drain only.
 template <int BN, int STAGES>
 struct Cfg {
+    static constexpr int kCpBatch = 2;                  // stages per scale-copy batch (divides STAGES)
     static constexpr int kAccStages = BN == 128 ? 2 : 1;
     static constexpr int kEpiWarps = 4 * (BN / 128);   // each owns 32 lanes x 128 columns
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -313,6 +314,12 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             const uint64_t sfa_desc0 = make_smem_desc(sbase + L::kOffSfa, 0, 128, 0);
             const uint64_t sfb_desc0 = make_smem_desc(sbase + L::kOffSfb, 0, 128, 0);
             constexpr uint32_t kBStepK = kMnMajor ? (kUmmaK * 128) >> 4 : kUmmaK >> 4;
+            // Scale atoms of kCpBatch consecutive stages are copied together (one
+            // copy-to-MMA switch of the tensor pipe per batch).
+            constexpr int kCpBatch = L::kCpBatch;
+            const int64_t my_tiles = blockIdx.x < sch.total ? (sch.total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+            const int64_t g_total = my_tiles * num_kb;
+            int64_t g = 0;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -322,16 +329,28 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                 if (!wait_phase(tempty_bar(acc), acc_phase ^ 1u, guard)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!wait_phase(full_bar(stage), phase, guard)) { ok = false; break; }
-                    tc_fence_after();
+                for (int kb = 0; kb < num_kb; ++kb, ++g) {
+                    if (g % kCpBatch == 0) {
+                        const int nb = static_cast<int>(min(static_cast<int64_t>(kCpBatch), g_total - g));
+                        for (int j = 0; j < nb && ok; ++j) {
+                            const int sj = (stage + j) % STAGES;
+                            const uint32_t pj = phase ^ ((stage + j) >= STAGES ? 1u : 0u);
+                            if (!wait_phase(full_bar(sj), pj, guard)) ok = false;
+                        }
+                        if (!ok) break;
+                        tc_fence_after();
+                        for (int j = 0; j < nb; ++j) {
+                            const int sj = (stage + j) % STAGES;
+                            tc_cp_32x128b_warpx4(tmem_base + L::kTmemSfa + 4 * sj,
+                                                 sfa_desc0 + static_cast<uint64_t>((sj * 512) >> 4));
+#pragma unroll
+                            for (int a = 0; a < L::kSfbAtoms; ++a)
+                                tc_cp_32x128b_warpx4(tmem_base + L::kTmemSfb + 4 * L::kSfbAtoms * sj + 4 * a,
+                                                     sfb_desc0 + static_cast<uint64_t>(((sj * L::kSfbAtoms + a) * 512) >> 4));
+                        }
+                    }
                     const uint32_t sfa_t = tmem_base + L::kTmemSfa + 4 * stage;
                     const uint32_t sfb_t = tmem_base + L::kTmemSfb + 4 * L::kSfbAtoms * stage;
-                    tc_cp_32x128b_warpx4(sfa_t, sfa_desc0 + static_cast<uint64_t>((stage * 512) >> 4));
-#pragma unroll
-                    for (int j = 0; j < L::kSfbAtoms; ++j)
-                        tc_cp_32x128b_warpx4(sfb_t + 4 * j,
-                                             sfb_desc0 + static_cast<uint64_t>(((stage * L::kSfbAtoms + j) * 512) >> 4));
                     const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
                     const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
                     const int64_t k_left = p.K - static_cast<int64_t>(kb) * kBK;
@@ -423,278 +442,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     }
 }
 
-// ---------------------------------------------------------------------------------------
-// Dense GEMM on CTA pairs (cluster of 2, tcgen05 cta_group::2).  Output tiles are
-// 256 x 256: CTA rank r of the pair owns rows m0 + 128 r and loads its 128 rows of
-// A and its 128-row half of B; the even CTA issues 256 x 256 x 32 pair MMAs that
-// read both halves, so each SM stages 32 KB per 128-deep K step (instead of 48 KB
-// for a 128 x 256 single-CTA tile) and the ring gets six stages.  Scale atoms are
-// loaded by every CTA for its own A rows and for all 256 B rows.  All loads of
-// both CTAs complete on the even CTA's full barrier; the even CTA's commits
-// multicast to both CTAs' empty / accumulator-full barriers; the epilogue warps
-// of both CTAs release the even CTA's accumulator-empty barrier.
-struct PairCfg {
-    static constexpr int kStages = 6;
-    static constexpr int kEpiWarps = 8;
-    static constexpr int kThreads = 64 + 32 * kEpiWarps;
-    static constexpr int kABytes = 128 * kBK;          // own A rows per stage
-    static constexpr int kBBytes = 128 * kBK;          // own half of B per stage
-    static constexpr int kSfbBytes = 2 * 512;          // scale atoms of all 256 B rows
-    static constexpr int kStageBytes = kABytes + kBBytes + 512 + kSfbBytes;   // per CTA
-    static constexpr int kOffB = 0;
-    static constexpr int kOffA = kOffB + kStages * kBBytes;
-    static constexpr int kOffSfa = kOffA + kStages * kABytes;
-    static constexpr int kOffSfb = kOffSfa + kStages * 512;
-    static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
-    static constexpr int kNumBars = 2 * kStages + 3;   // full, empty, tmem-full, tmem-empty, drain
-    static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
-    static constexpr int kOffAbort = kOffTmemSlot + 4;
-    static constexpr int kBytes = kOffAbort + 16;
-    static constexpr int kAlloc = kBytes + 1024;
-    static constexpr int kTmemSfa = 256;               // one 256-column accumulator, then scales
-    static constexpr int kTmemSfb = kTmemSfa + 4 * kStages;
-    static constexpr int kTmemCols = 512;
-    static_assert(kTmemSfb + 8 * kStages <= kTmemCols, "tensor memory budget");
-    static_assert(kAlloc <= 227 * 1024, "shared memory budget");
-};
-
-template <bool kMnMajor>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1)
-    gemm_mxf8_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
-                          const __grid_constant__ CUtensorMap tma_b,
-                          const __grid_constant__ CUtensorMap tma_sfa,
-                          const __grid_constant__ CUtensorMap tma_sfb, const GemmArgs p) {
-    using L = PairCfg;
-    constexpr int STAGES = L::kStages;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t sbase = smem_u32(smem);
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const bool leader = rank == 0;
-
-    const uint32_t bar0 = sbase + L::kOffBar;
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    const uint32_t tfull_bar = bar0 + 8u * (2 * STAGES);
-    const uint32_t tempty_bar = bar0 + 8u * (2 * STAGES + 1);
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
-    const WaitGuard guard{abort_flag, p.status, p.wait_limit_ns};
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);      // the even CTA's producer arrives (with both CTAs' bytes)
-            mbar_init(empty_bar(s), 1);     // the even CTA's multicast commit
-        }
-        mbar_init(tfull_bar, 1);
-        mbar_init(tempty_bar, 2 * L::kEpiWarps);
-        mbar_init(drain_bar, 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-        prefetch_tensormap(&tma_a);
-        prefetch_tensormap(&tma_b);
-        prefetch_tensormap(&tma_sfa);
-        prefetch_tensormap(&tma_sfb);
-    }
-    if (warp == 1) {
-        tmem_alloc_pair(sbase + L::kOffTmemSlot, L::kTmemCols);
-        tmem_relinquish_pair();
-    }
-    tc_fence_before();
-    cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
-    tc_fence_after();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemSlot);
-
-    const int64_t m_tiles = (p.M + 255) / 256;
-    const int64_t n_tiles = (p.N + 255) / 256;
-    const int64_t total = m_tiles * n_tiles;
-    const int64_t pair_id = blockIdx.x >> 1;
-    const int64_t n_pairs = gridDim.x >> 1;
-    const int num_kb = static_cast<int>((p.K + kBK - 1) / kBK);
-    auto tile_of = [&](int64_t t, int64_t& m0, int64_t& n0) {
-        const int64_t per_band = static_cast<int64_t>(kRasterBand) * n_tiles;
-        const int64_t band = t / per_band, within = t - band * per_band;
-        const int64_t mb = band * kRasterBand;
-        const int64_t bh = min(static_cast<int64_t>(kRasterBand), m_tiles - mb);
-        m0 = (mb + within % bh) * 256;
-        n0 = (within / bh) * 256;
-    };
-
-    if (warp == 0) {
-        // ---- producer (both CTAs) -------------------------------------------------------
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            const uint32_t full0 = leader ? full_bar(0) : mapa_shared(full_bar(0), 0);
-            for (int64_t t = pair_id; t < total && !*abort_flag; t += n_pairs) {
-                int64_t m0, n0;
-                tile_of(t, m0, n0);
-                const int32_t ma = static_cast<int32_t>(m0 + 128 * rank);
-                const int32_t nb = static_cast<int32_t>(n0 + 128 * rank);
-                const int32_t sfa_row = static_cast<int32_t>(2 * ((m0 / 128 + rank) * p.k_atoms));
-                const int32_t sfb_row0 = static_cast<int32_t>(2 * ((n0 / 128) * p.k_atoms));
-                const int32_t sfb_row1 = static_cast<int32_t>(2 * ((n0 / 128 + 1) * p.k_atoms));
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!wait_phase(empty_bar(stage), phase ^ 1u, guard)) break;
-                    const uint32_t fb = full0 + 8u * stage;
-                    if (leader) mbar_arrive_expect_tx(fb, 2u * L::kStageBytes);
-                    const uint32_t sa = sbase + L::kOffA + stage * L::kABytes;
-                    const uint32_t sb = sbase + L::kOffB + stage * L::kBBytes;
-                    const uint32_t ssa = sbase + L::kOffSfa + stage * 512;
-                    const uint32_t ssb = sbase + L::kOffSfb + stage * L::kSfbBytes;
-                    const int32_t kx = kb * kBK;
-                    tma_load_2d_pair(sa, &tma_a, kx, ma, fb);
-                    if constexpr (!kMnMajor)
-                        tma_load_2d_pair(sb, &tma_b, kx, nb, fb);
-                    else
-                        tma_load_2d_pair(sb, &tma_b, nb, kx, fb);   // B stored [K, N]
-                    tma_load_2d_pair(ssa, &tma_sfa, 0, sfa_row + 2 * kb, fb);
-                    tma_load_2d_pair(ssb, &tma_sfb, 0, sfb_row0 + 2 * kb, fb);
-                    tma_load_2d_pair(ssb + 512, &tma_sfb, 0, sfb_row1 + 2 * kb, fb);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                }
-            }
-            if (*abort_flag) {  // give loads in flight time to land (bounded)
-                const uint64_t t0 = globaltimer_ns();
-                while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
-            }
-        }
-    } else if (warp == 1) {
-        // ---- MMA issuer (even CTA only) ------------------------------------------------
-        if (lane == 0 && leader) {
-            const uint64_t a_desc0 = make_smem_desc(sbase + L::kOffA, 16, 1024, 2);
-            const uint64_t b_desc0 = kMnMajor ? make_smem_desc(sbase + L::kOffB, 128 * kBK, 1024, 2)
-                                              : make_smem_desc(sbase + L::kOffB, 16, 1024, 2);
-            const uint64_t sfa_desc0 = make_smem_desc(sbase + L::kOffSfa, 0, 128, 0);
-            const uint64_t sfb_desc0 = make_smem_desc(sbase + L::kOffSfb, 0, 128, 0);
-            constexpr uint32_t kBStepK = kMnMajor ? (kUmmaK * 128) >> 4 : kUmmaK >> 4;
-            int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
-            bool ok = true;
-            for (int64_t t = pair_id; t < total && ok; t += n_pairs) {
-                if (!wait_phase(tempty_bar, acc_phase ^ 1u, guard)) { ok = false; break; }
-                tc_fence_after();
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!wait_phase(full_bar(stage), phase, guard)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t sfa_t = tmem_base + L::kTmemSfa + 4 * stage;
-                    const uint32_t sfb_t = tmem_base + L::kTmemSfb + 8 * stage;
-                    tc_cp_32x128b_warpx4_pair(sfa_t, sfa_desc0 + static_cast<uint64_t>((stage * 512) >> 4));
-                    tc_cp_32x128b_warpx4_pair(sfb_t, sfb_desc0 + static_cast<uint64_t>((stage * L::kSfbBytes) >> 4));
-                    tc_cp_32x128b_warpx4_pair(sfb_t + 4,
-                                              sfb_desc0 + static_cast<uint64_t>((stage * L::kSfbBytes + 512) >> 4));
-                    const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
-                    const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
-                    const int64_t k_left = p.K - static_cast<int64_t>(kb) * kBK;
-                    const int ksub = k_left >= kBK ? kBK / kUmmaK : static_cast<int>(k_left) / kUmmaK;
-#pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k)
-                        if (k < ksub)
-                            tc_mma_mxf8_pair(tmem_base, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
-                                             make_idesc_mxf8(256, 256, kMnMajor ? 1u : 0u, k, k), sfa_t, sfb_t,
-                                             (kb > 0 || k > 0) ? 1u : 0u);
-                    tc_commit_pair_multicast(empty_bar(stage), 0x3);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                }
-                if (!ok) break;
-                tc_commit_pair_multicast(tfull_bar, 0x3);
-                acc_phase ^= 1u;
-            }
-            tc_commit_pair(drain_bar);
-            WaitGuard g2 = guard;
-            volatile int never = 0;
-            g2.abort_flag = &never;
-            (void)mbar_wait(drain_bar, 0, g2);
-        }
-    } else {
-        // ---- epilogue (both CTAs) ----------------------------------------------------
-        const int quad = warp & 3;
-        const int half = (warp - 2) >> 2;
-        const uint32_t tempty_leader = leader ? tempty_bar : mapa_shared(tempty_bar, 0);
-        uint32_t acc_phase = 0;
-        for (int64_t t = pair_id; t < total; t += n_pairs) {
-            int64_t m0, n0;
-            tile_of(t, m0, n0);
-            int ok = 1;
-            if (lane == 0) ok = wait_phase(tfull_bar, acc_phase, guard) ? 1 : 0;
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t v[4][32];
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + half * 128;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 32 * c, v[c]);
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(tempty_leader);
-            acc_phase ^= 1u;
-
-            const int64_t row = m0 + 128 * rank + 32 * quad + lane;
-            if (row < p.M) {
-                uint16_t* yrow = p.y + row * p.ldy;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int64_t n = n0 + half * 128 + c * 32;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (n + 8 * q + 8 <= p.N) {
-                            uint4 o;
-                            o.x = cvt_bf16x2(__uint_as_float(v[c][8 * q + 0]), __uint_as_float(v[c][8 * q + 1]));
-                            o.y = cvt_bf16x2(__uint_as_float(v[c][8 * q + 2]), __uint_as_float(v[c][8 * q + 3]));
-                            o.z = cvt_bf16x2(__uint_as_float(v[c][8 * q + 4]), __uint_as_float(v[c][8 * q + 5]));
-                            o.w = cvt_bf16x2(__uint_as_float(v[c][8 * q + 6]), __uint_as_float(v[c][8 * q + 7]));
-                            *reinterpret_cast<uint4*>(yrow + n + 8 * q) = o;
-                        }
-                    }
-                }
-            }
-        }
-    }
-
-    // ---- teardown: nothing may still target the peer when either CTA leaves ----
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();
-    tc_fence_after();
-    if (warp == 1) {
-        __syncwarp();
-        tmem_dealloc_pair(tmem_base, L::kTmemCols);
-    }
-}
-
 // Row-major u8 matrix [rows, cols] (cols contiguous), box [box_rows, 128 bytes],
 // 128-byte swizzle.
 bool make_tma_u8(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
     return encode_tensor_map_2d(map, ptr, false, cols, rows, cols, 128u, box_rows, true);
-}
-
-// MMA-tiled scales of a [rows, K] operand viewed as [bands * k_atoms * 2, 256] bytes:
-// one 512-byte atom is a 256 x 2 box at row 2 * (band * k_atoms + kb).
-bool make_tma_scales(CUtensorMap* map, const void* ptr, int64_t bands, int64_t k_atoms) {
-    return encode_tensor_map_2d(map, ptr, false, 256u, static_cast<uint64_t>(bands * k_atoms * 2), 256u, 256u,
-                                2u, false);
-}
-
-template <bool kMnMajor>
-cudaError_t launch_pair(const DeviceInfo& dev, const CUtensorMap& ta, const CUtensorMap& tb,
-                        const CUtensorMap& tsa, const CUtensorMap& tsb, const GemmArgs& args,
-                        int64_t tiles, cudaStream_t stream) {
-    auto kern = gemm_mxf8_pair_kernel<kMnMajor>;
-    static thread_local int configured_device = -1;
-    if (configured_device != dev.device) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kAlloc);
-        if (e != cudaSuccess) return e;
-        configured_device = dev.device;
-    }
-    int64_t pairs = dev.sm_count / 2;
-    if (tiles < pairs) pairs = tiles;
-    if (pairs <= 0) return cudaSuccess;
-    kern<<<static_cast<unsigned>(2 * pairs), PairCfg::kThreads, PairCfg::kAlloc, stream>>>(ta, tb, tsa, tsb, args);
-    return cudaGetLastError();
 }
 
 template <int BN, int STAGES, bool kMnMajor, bool kGrouped>
@@ -723,34 +474,31 @@ constexpr int kStages = 4;
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
                         const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
                         int64_t ldy, cudaStream_t stream) {
-    CUtensorMap ta, tb, tsa, tsb;
-    const int64_t k_atoms = (K + 127) / 128;
-    if (!make_tma_u8(&ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128))
+    CUtensorMap ta, tb;
+    if (!make_tma_u8(&ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kBM))
         return cudaErrorInvalidValue;
     if (!b_mn_major) {
-        if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 128))
+        if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN))
             return cudaErrorInvalidValue;
     } else {
         if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK))
             return cudaErrorInvalidValue;
     }
-    if (!make_tma_scales(&tsa, a_s, (M + 127) / 128, k_atoms) ||
-        !make_tma_scales(&tsb, b_s, (N + 127) / 128, k_atoms))
-        return cudaErrorInvalidValue;
     GemmArgs args{};
     args.a_s = static_cast<const uint8_t*>(a_s);
     args.b_s = static_cast<const uint8_t*>(b_s);
     args.y = static_cast<uint16_t*>(y);
     args.M = M; args.N = N; args.K = K; args.ldy = ldy;
-    args.k_atoms = k_atoms;
+    args.k_atoms = (K + 127) / 128;
     args.b_bands = (N + 127) / 128;
     args.offsets = nullptr;
     args.G = 0;
     args.status = dev.status;
     args.wait_limit_ns = kDefaultWaitLimitNs;
-    const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    if (b_mn_major) return launch_pair<true>(dev, ta, tb, tsa, tsb, args, tiles, stream);
-    return launch_pair<false>(dev, ta, tb, tsa, tsb, args, tiles, stream);
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    if (b_mn_major)
+        return launch_t<kBN, kStages, true, false>(dev, ta, tb, args, tiles, stream);
+    return launch_t<kBN, kStages, false, false>(dev, ta, tb, args, tiles, stream);
 }
 
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
