@@ -41,8 +41,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 L2_FLUSH_BYTES = 256 << 20   # larger than the 129 MB L2
 # DRAM bytes (read + write) of one GEMM launch, from an ncu capture of the current
-# kernel (profiles/gemm_mxf8_kernel_linear_train.md); None where not captured.
-GEMM_TRAFFIC_BYTES = {"linear_train": 52.4e6 + 23.9e6}
+# kernel (profiles/gemm_mxf8_kernel_linear_train.md); None where not captured for
+# the kernel as it stands.
+GEMM_TRAFFIC_BYTES = {}
 
 
 def load_peaks():
