@@ -228,6 +228,42 @@ void orc_quant_32x32(const uint16_t* w, int64_t n, int64_t k, int64_t ld,
     }
 }
 
+// ---- grouped column quantization (MoE weight gradient) ----------------------
+// x: bf16 bits [rows, cols] (row stride ld) with rows sorted by expert;
+// off: [G+1] expert row offsets.  Expert g's tokens are quantized along the
+// token axis in groups of 32 that start at the expert's first token; a group
+// that runs past the expert's last token is completed with zeros (reading of
+// the unstated padding rule).  Output layout: expert g occupies the column
+// slot [P_g, P_g + L_g) of q_col [cols, capacity] with L_g = m_g rounded up
+// to a multiple of 128 and P_g = sum of L_h over h < g; everything in the slot
+// past the expert's groups is zero payload with scale code 0.  s_col holds the
+// plain scales [cols, capacity/32].  Columns past P_G are left untouched.
+void orc_quant_cols_grouped(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                            const int64_t* off, int32_t G, int64_t capacity,
+                            uint8_t* q_col, uint8_t* s_col) {
+    (void)rows;
+    const int64_t cgroups = capacity / 32;
+    int64_t P = 0;
+    for (int32_t g = 0; g < G; ++g) {
+        const int64_t lo = off[g], m = off[g + 1] - off[g];
+        const int64_t L = (m + 127) / 128 * 128;
+#pragma omp parallel for schedule(static)
+        for (int64_t c = 0; c < cols; ++c) {
+            for (int64_t j = 0; j < L / 32; ++j) {
+                uint8_t* dst = q_col + c * capacity + P + 32 * j;
+                s_col[c * cgroups + P / 32 + j] = quant_shared_scale(
+                    32,
+                    [&](int64_t i) {
+                        const int64_t t = 32 * j + i;
+                        return t < m ? bf16_bits_to_double(x[(lo + t) * ld + c]) : 0.0;
+                    },
+                    [&](int64_t i, uint8_t b) { dst[i] = b; });
+            }
+        }
+        P += L;
+    }
+}
+
 // ---- scale layout: plain -> MMA-tiled ---------------------------------------
 // s: plain [rows, groups].  out: tiled, sized roundup(rows,128) *
 // roundup(groups,4) bytes.  Atoms of 128 rows x 4 groups (512 bytes) are

@@ -68,10 +68,12 @@ def _load():
     lib.orc_quant_dual.argtypes = [P, I64, I64, I64, P, P, P, P]
     lib.orc_quant_32x32.argtypes = [P, I64, I64, I64, P, P, P]
     lib.orc_scale_tiled.argtypes = [P, I64, I64, P]
+    lib.orc_quant_cols_grouped.argtypes = [P, I64, I64, I64, P, ctypes.c_int32, I64, P, P]
     lib.orc_dequant_rows.argtypes = [P, P, I64, I64, P]
     lib.orc_gemm.argtypes = [P, P, I64, I64, I64, P, I64, P]
     lib.orc_grouped_gemm.argtypes = [P, P, P, ctypes.c_int32, I64, I64, P, I64, P]
     for f in ("orc_e4m3_encode_array", "orc_bf16_from_double_array", "orc_quant_rows",
+              "orc_quant_cols_grouped",
               "orc_quant_dual", "orc_quant_32x32", "orc_scale_tiled", "orc_dequant_rows",
               "orc_gemm", "orc_grouped_gemm"):
         getattr(lib, f).restype = None
@@ -169,6 +171,33 @@ def quant_32x32(w_bits: np.ndarray):
     s_bwd = np.empty((K, N // 32), np.uint8)
     lib.orc_quant_32x32(_ptr(w), N, K, K, _ptr(q), _ptr(s_fwd), _ptr(s_bwd))
     return q, s_fwd, s_bwd
+
+
+def padded_slots(offsets: np.ndarray):
+    """(P, L): each expert's 128-aligned token slot start and length."""
+    m = np.diff(np.asarray(offsets, dtype=np.int64))
+    L = (m + 127) // 128 * 128
+    P = np.concatenate([[0], np.cumsum(L)[:-1]]).astype(np.int64)
+    return P, L
+
+
+def quant_cols_grouped(x_bits: np.ndarray, offsets: np.ndarray, capacity: int):
+    """Column (token-axis) quantization per expert with zero padding.
+    x_bits uint16 [M_total, C] (rows sorted by expert), offsets int64 [G+1].
+    Returns (q_col [C, capacity], s_col [C, capacity/32]) -- plain scales;
+    columns past the last expert's slot are returned as 0 / code 0."""
+    lib = _load()
+    x = _c(x_bits, np.uint16)
+    R, C = x.shape
+    off = _c(offsets, np.int64)
+    G = off.size - 1
+    assert capacity % 128 == 0 and off[0] == 0 and off[-1] == R
+    P, L = padded_slots(off)
+    assert int((P[-1] + L[-1]) if G else 0) <= capacity
+    q = np.zeros((C, capacity), np.uint8)
+    s = np.zeros((C, capacity // 32), np.uint8)
+    lib.orc_quant_cols_grouped(_ptr(x), R, C, C, _ptr(off), G, capacity, _ptr(q), _ptr(s))
+    return q, s
 
 
 def scale_tiled(s: np.ndarray) -> np.ndarray:
