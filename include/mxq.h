@@ -112,6 +112,45 @@ mxq_status mxq_quant_1x32_dual(const void* x, int64_t rows, int64_t cols, int64_
                                mxq_scale_layout layout, mxq_stream_t stream);
 
 /*
+ * Batched form of mxq_quant_1x32_dual: `batch` matrices [rows, cols] (row
+ * stride ld, matrix b at x + b * batch_stride elements; batch_stride >=
+ * rows * ld, a multiple of 8, ignored when batch == 1).  The outputs of
+ * matrix b follow those of matrix b-1 with no gap: q_row + b*rows*cols,
+ * s_row + b*mxq_scale_bytes(rows, cols, layout), q_col + b*cols*rows,
+ * s_col + b*mxq_scale_bytes(cols, rows, layout).  Used for the stacked MoE
+ * expert weights [G, N, K]: the row copies give the forward operand and the
+ * column copies [G, K, N] the dgrad operand of mxq_grouped_gemm.  batch <= 65535.
+ */
+mxq_status mxq_quant_1x32_dual_batched(const void* x, int64_t batch, int64_t rows, int64_t cols,
+                                       int64_t ld, int64_t batch_stride, void* q_row, void* s_row,
+                                       void* q_col, void* s_col, mxq_scale_layout layout,
+                                       mxq_stream_t stream);
+
+/*
+ * Token-axis (column) 1x32 quantization inside each MoE expert, the operand
+ * form of the expert weight gradient (dW_g = dY_g^T X_g contracts over the
+ * expert's tokens).  Rows of x [rows, cols] (row stride ld) are tokens sorted
+ * by expert; group_offsets is the DEVICE int64 [G+1] of mxq_grouped_gemm.
+ *
+ * Expert g (m_g = off[g+1] - off[g] tokens) gets the slot [P_g, P_g + L_g) of
+ * the token axis, L_g = m_g rounded up to a multiple of 128, P_g = sum of L_h
+ * for h < g.  Its 32-token groups start at its first token; a group that runs
+ * past its last token is completed with zeros (the pages leave this open; this
+ * is the reading taken), so no scale is shared between experts.
+ *
+ * q_col  u8 [cols, capacity]: column c, slot position p = token P_g + i of expert g.
+ * s_col  u8 scales [cols, capacity/32] in `layout`.
+ * Slot positions past an expert's tokens hold zero payload and scale code 0;
+ * positions past the last slot are not written.
+ * capacity: a multiple of 128, >= rows + 127*G (enough for any offsets).
+ * Shapes: cols % 32 == 0; 1 <= G <= 1024.
+ */
+mxq_status mxq_quant_1x32_cols_grouped(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                       const int64_t* group_offsets, int32_t G, int64_t capacity,
+                                       void* q_col, void* s_col, mxq_scale_layout layout,
+                                       mxq_stream_t stream);
+
+/*
  * 32x32 block quantization (the "mxfp8-32x32" recipe; RFC sections 3.1 and
  * 3.3.3 "block_mx_quant": one payload, forward and backward scales).
  *
@@ -172,6 +211,24 @@ mxq_status mxq_gemm_bf16out(const void* a_q, const void* a_s, const void* b_q, c
 mxq_status mxq_grouped_gemm(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
                             const int64_t* group_offsets, int32_t G, int64_t M_total,
                             int64_t N, int64_t K, void* y, int64_t ldy, mxq_stream_t stream);
+
+/*
+ * Grouped weight-gradient GEMM for MoE experts: for every expert g
+ *
+ *   y[g][m, n] = sum over the slot positions p of expert g of deq(A)[m, p] * deq(B)[n, p]
+ *
+ * i.e. dW_g = dY_g^T X_g with A = dY's token-axis quantization [M, capacity]
+ * and B = X's [N, capacity] (both from mxq_quant_1x32_cols_grouped with the
+ * same group_offsets and capacity; scales MMA-tiled).  The slots are
+ * recomputed from group_offsets on the device, exactly as the quantizer does.
+ * y: bf16 [G, M, N], row stride ldy, expert g at y + g*M*ldy; an empty
+ * expert gets zeros.  Shapes: N % 16 == 0, capacity % 128 == 0 and
+ * capacity >= M_total + 127*G, 1 <= G <= 1024.
+ */
+mxq_status mxq_grouped_gemm_wgrad(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
+                                  const int64_t* group_offsets, int32_t G, int64_t M_total,
+                                  int64_t capacity, int64_t M, int64_t N, void* y, int64_t ldy,
+                                  mxq_stream_t stream);
 
 /* Waits for all work on the current device, then returns MXQ_ERR_TIMEOUT if
  * any kernel of this library recorded a bounded wait that ran out since the

@@ -101,29 +101,62 @@ size_t mxq_scale_bytes(int64_t rows, int64_t cols, mxq_scale_layout layout) {
     return 0;
 }
 
-mxq_status mxq_quant_1x32_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q_row,
-                               void* s_row, void* q_col, void* s_col, mxq_scale_layout layout,
-                               mxq_stream_t stream) {
+mxq_status mxq_quant_1x32_dual_batched(const void* x, int64_t batch, int64_t rows, int64_t cols,
+                                       int64_t ld, int64_t batch_stride, void* q_row, void* s_row,
+                                       void* q_col, void* s_col, mxq_scale_layout layout,
+                                       mxq_stream_t stream) {
     if (layout != MXQ_SCALE_ROWMAJOR && layout != MXQ_SCALE_MMA_TILED) return MXQ_ERR_INVALID_ARG;
-    if (rows < 0 || cols < 0) return MXQ_ERR_INVALID_ARG;
+    if (batch < 0 || rows < 0 || cols < 0) return MXQ_ERR_INVALID_ARG;
     const bool row = q_row != nullptr || s_row != nullptr;
     const bool col = q_col != nullptr || s_col != nullptr;
     if (!row && !col) return MXQ_ERR_INVALID_ARG;
     if (cols % 32 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
     if (col && rows % 32 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
-    if (rows == 0 || cols == 0) return MXQ_OK;
+    if (batch > 65535) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (batch == 0 || rows == 0 || cols == 0) return MXQ_OK;
     if (!x || (row && (!q_row || !s_row)) || (col && (!q_col || !s_col))) return MXQ_ERR_INVALID_ARG;
     if (ld < cols || ld % 8 != 0) return MXQ_ERR_INVALID_ARG;
+    if (batch > 1 && (batch_stride < rows * ld || batch_stride % 8 != 0)) return MXQ_ERR_INVALID_ARG;
     if (!aligned16(x) || (row && (!aligned16(q_row) || !aligned16(s_row))) ||
         (col && (!aligned16(q_col) || !aligned16(s_col))))
         return MXQ_ERR_INVALID_ARG;
     mxq::DeviceInfo dev;
     mxq_status st = device_ok(&dev);
     if (st != MXQ_OK) return st;
-    return from_cuda(mxq::launch_quant_1x32(dev, x, rows, cols, ld, row ? q_row : nullptr,
-                                            row ? s_row : nullptr, col ? q_col : nullptr,
-                                            col ? s_col : nullptr, layout == MXQ_SCALE_MMA_TILED,
+    return from_cuda(mxq::launch_quant_1x32(dev, x, batch, rows, cols, ld, batch > 1 ? batch_stride : rows * ld,
+                                            row ? q_row : nullptr, row ? s_row : nullptr,
+                                            col ? q_col : nullptr, col ? s_col : nullptr,
+                                            layout == MXQ_SCALE_MMA_TILED,
                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxq_status mxq_quant_1x32_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q_row,
+                               void* s_row, void* q_col, void* s_col, mxq_scale_layout layout,
+                               mxq_stream_t stream) {
+    return mxq_quant_1x32_dual_batched(x, 1, rows, cols, ld, 0, q_row, s_row, q_col, s_col, layout, stream);
+}
+
+mxq_status mxq_quant_1x32_cols_grouped(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                       const int64_t* group_offsets, int32_t G, int64_t capacity,
+                                       void* q_col, void* s_col, mxq_scale_layout layout,
+                                       mxq_stream_t stream) {
+    if (layout != MXQ_SCALE_ROWMAJOR && layout != MXQ_SCALE_MMA_TILED) return MXQ_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || G < 1 || capacity < 0) return MXQ_ERR_INVALID_ARG;
+    if (G > 1024) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (cols % 32 != 0 || capacity % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (capacity < rows + 127 * static_cast<int64_t>(G)) return MXQ_ERR_INVALID_ARG;
+    if (cols == 0 || capacity == 0) return MXQ_OK;
+    if (!x || !group_offsets || !q_col || !s_col) return MXQ_ERR_INVALID_ARG;
+    if (ld < cols || ld % 8 != 0) return MXQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q_col) || !aligned16(s_col) ||
+        (reinterpret_cast<uintptr_t>(group_offsets) & 7u) != 0)
+        return MXQ_ERR_INVALID_ARG;
+    mxq::DeviceInfo dev;
+    mxq_status st = device_ok(&dev);
+    if (st != MXQ_OK) return st;
+    return from_cuda(mxq::launch_quant_cols_grouped(dev, x, rows, cols, ld, group_offsets, G, capacity, q_col,
+                                                    s_col, layout == MXQ_SCALE_MMA_TILED,
+                                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mxq_status mxq_quant_32x32(const void* w, int64_t n, int64_t k, int64_t ld, void* q, void* s_fwd,
@@ -191,6 +224,36 @@ mxq_status mxq_grouped_gemm(const void* a_q, const void* a_s, const void* b_q, c
     if (st != MXQ_OK) return st;
     return from_cuda(mxq::launch_grouped_gemm(dev, a_q, a_s, b_q, b_s, group_offsets, G, M_total, N, K,
                                               y, ldy, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxq_status mxq_grouped_gemm_wgrad(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
+                                  const int64_t* group_offsets, int32_t G, int64_t M_total,
+                                  int64_t capacity, int64_t M, int64_t N, void* y, int64_t ldy,
+                                  mxq_stream_t stream) {
+    if (G < 1 || M_total < 0 || M < 0 || N < 0 || capacity < 0) return MXQ_ERR_INVALID_ARG;
+    if (G > 1024) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (N % 16 != 0 || capacity % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (capacity < M_total + 127 * static_cast<int64_t>(G)) return MXQ_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) - 128 || N > (int64_t(1) << 31) - 256 || capacity > (int64_t(1) << 31) - 128 ||
+        static_cast<int64_t>(G) * M > (int64_t(1) << 40))
+        return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0) return MXQ_OK;
+    if (!a_q || !a_s || !b_q || !b_s || !group_offsets || !y) return MXQ_ERR_INVALID_ARG;
+    if (ldy < N || ldy % 8 != 0) return MXQ_ERR_INVALID_ARG;
+    if (!aligned16(a_q) || !aligned16(a_s) || !aligned16(b_q) || !aligned16(b_s) || !aligned16(y) ||
+        (reinterpret_cast<uintptr_t>(group_offsets) & 7u) != 0)
+        return MXQ_ERR_INVALID_ARG;
+    mxq::DeviceInfo dev;
+    mxq_status st = device_ok(&dev);
+    if (st != MXQ_OK) return st;
+    if (capacity == 0) {  // every expert is empty: y = 0
+        return from_cuda(cudaMemset2DAsync(y, static_cast<size_t>(ldy) * 2, 0, static_cast<size_t>(N) * 2,
+                                           static_cast<size_t>(G) * static_cast<size_t>(M),
+                                           reinterpret_cast<cudaStream_t>(stream)));
+    }
+    return from_cuda(mxq::launch_grouped_gemm_wgrad(dev, a_q, a_s, b_q, b_s, group_offsets, G, M_total,
+                                                    capacity, M, N, y, ldy,
+                                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mxq_status mxq_get_device_status(void) {

@@ -39,11 +39,17 @@ constexpr int kUmmaK = 32;        // K of one MMA instruction (FP8)
 constexpr int kRasterBand = 8;    // m-tiles per raster band (L2 reuse of B)
 constexpr int kMaxGroups = 1024;
 
+// Kernel modes.
+constexpr int kDense = 0;         // y = A B^T
+constexpr int kGroupedRows = 1;   // rows of A split by expert, one B per expert (MoE fwd, dgrad)
+constexpr int kGroupedK = 2;      // contraction split by expert (MoE wgrad), y stacked per expert
+
 struct GemmArgs {
     const uint8_t* a_s;      // A scales, MMA-tiled
     const uint8_t* b_s;      // B scales, MMA-tiled
     uint16_t* y;             // bf16 output
     int64_t M, N, K, ldy;
+    int64_t M_total;         // grouped contraction: rows of the token-sorted inputs
     int64_t k_atoms;         // 4-group scale atoms per 128-row band = ceil(K/128)
     int64_t b_bands;         // 128-row bands of B scales that exist
     const int64_t* offsets;  // grouped: [G+1] on the device
@@ -90,29 +96,44 @@ struct Cfg {
 };
 
 // Output-tile schedule.  Dense: raster bands of kRasterBand m-tiles, n-tiles
-// inside a band.  Grouped: tiles of expert g cover the 128-row blocks that
-// intersect [off[g], off[g+1]); n-tiles innermost.
+// inside a band.  Grouped rows: tiles of expert g cover the 128-row blocks that
+// intersect [off[g], off[g+1]); n-tiles innermost.  Grouped contraction: every
+// expert has the full m x n tile grid (rastered as dense); its K range is the
+// expert's 128-aligned token slot.
 struct TileInfo {
     int64_t m0;      // first row of the A tile (multiple of 128)
     int64_t n0;      // first output column
     int64_t row_lo;  // rows [row_lo, row_hi) of this tile are stored
     int64_t row_hi;
     int64_t b_row;   // first row of the B tile in the (stacked) B matrix
+    int64_t kb0;     // first 128-deep K block
+    int nkb;         // K blocks of this tile (0: the tile is all zeros)
+    int64_t y_row0;  // output row of A row 0 (grouped contraction: g * M)
 };
 
 struct Schedule {
     int64_t m_tiles, n_tiles, total;
-    // grouped only (shared memory)
+    int num_kb;           // K blocks of dense / grouped-row tiles
+    // grouped modes only (shared memory)
     const int64_t* off;
-    const int* prefix;    // [G+1] tile prefix
-    const int* first_mt;  // [G]
+    const int* prefix;    // [G+1] grouped rows: tile prefix; grouped K: slot start / 128
+    const int* first_mt;  // [G]   grouped rows: first m-tile; grouped K: slot length / 128
     int G;
 };
 
-template <int BN, bool kGrouped>
+template <int BN, int kMode>
 __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs& p, int64_t t) {
     TileInfo ti;
-    if constexpr (!kGrouped) {
+    ti.kb0 = 0;
+    ti.nkb = s.num_kb;
+    ti.y_row0 = 0;
+    if constexpr (kMode != kGroupedRows) {
+        int64_t g = 0;
+        if constexpr (kMode == kGroupedK) {
+            const int64_t per = s.m_tiles * s.n_tiles;
+            g = t / per;
+            t -= g * per;
+        }
         const int64_t per_band = static_cast<int64_t>(kRasterBand) * s.n_tiles;
         const int64_t band = t / per_band, within = t - band * per_band;
         const int64_t mb = band * kRasterBand;
@@ -123,6 +144,11 @@ __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs&
         ti.row_lo = ti.m0;
         ti.row_hi = min(ti.m0 + kBM, p.M);
         ti.b_row = ti.n0;
+        if constexpr (kMode == kGroupedK) {
+            ti.kb0 = s.prefix[g];
+            ti.nkb = s.first_mt[g];
+            ti.y_row0 = g * p.M;
+        }
     } else {
         int lo = 0, hi = s.G;  // largest g with prefix[g] <= t
         while (hi - lo > 1) {
@@ -147,7 +173,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
     return mbar_try_wait(bar, parity) || mbar_wait(bar, parity, g);
 }
 
-template <int BN, int STAGES, bool kMnMajor, bool kGrouped>
+template <int BN, int STAGES, bool kMnMajor, int kMode>
 __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tma_a,
                      const __grid_constant__ CUtensorMap tma_b, const GemmArgs p) {
@@ -193,7 +219,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     Schedule sch;
     sch.n_tiles = (p.N + BN - 1) / BN;
     sch.G = p.G;
-    if constexpr (!kGrouped) {
+    sch.num_kb = static_cast<int>((p.K + kBK - 1) / kBK);
+    if constexpr (kMode == kDense) {
         sch.m_tiles = (p.M + kBM - 1) / kBM;
         sch.total = sch.m_tiles * sch.n_tiles;
         sch.off = nullptr;
@@ -203,9 +230,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
         int64_t* s_off = reinterpret_cast<int64_t*>(smem + L::kOffSched);
         int* s_prefix = reinterpret_cast<int*>(s_off + (kMaxGroups + 1));
         int* s_first = s_prefix + (kMaxGroups + 1);
+        const int64_t row_limit = kMode == kGroupedRows ? p.M : p.M_total;
         for (int g = threadIdx.x; g <= p.G; g += L::kThreads) {
             int64_t o = p.offsets[g];
-            o = o < 0 ? 0 : (o > p.M ? p.M : o);  // keep malformed offsets in bounds
+            o = o < 0 ? 0 : (o > row_limit ? row_limit : o);  // keep malformed offsets in bounds
             s_off[g] = o;
         }
         __syncthreads();
@@ -216,9 +244,14 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                 int cnt = 0;
                 if (g < p.G) {
                     const int64_t lo = s_off[g], hi = s_off[g + 1];
-                    const int64_t fm = lo / kBM;
-                    s_first[g] = static_cast<int>(fm);
-                    cnt = hi > lo ? static_cast<int>((hi - 1) / kBM - fm + 1) * static_cast<int>(sch.n_tiles) : 0;
+                    if constexpr (kMode == kGroupedRows) {
+                        const int64_t fm = lo / kBM;
+                        s_first[g] = static_cast<int>(fm);
+                        cnt = hi > lo ? static_cast<int>((hi - 1) / kBM - fm + 1) * static_cast<int>(sch.n_tiles) : 0;
+                    } else {  // slot length in 128-token blocks
+                        cnt = hi > lo ? static_cast<int>((hi - lo + kBK - 1) / kBK) : 0;
+                        s_first[g] = cnt;
+                    }
                 }
                 int incl = cnt;
 #pragma unroll
@@ -234,14 +267,18 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
         sch.off = s_off;
         sch.prefix = s_prefix;
         sch.first_mt = s_first;
+        sch.m_tiles = (p.M + kBM - 1) / kBM;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemSlot);
-    if constexpr (kGrouped) sch.total = sch.prefix[p.G];
-
-    const int num_kb = static_cast<int>((p.K + kBK - 1) / kBK);
+    if constexpr (kMode == kGroupedRows) sch.total = sch.prefix[p.G];
+    if constexpr (kMode == kGroupedK) {
+        sch.total = static_cast<int64_t>(p.G) * sch.m_tiles * sch.n_tiles;
+        // the slots must fit the K extent of the operands
+        if (static_cast<int64_t>(sch.prefix[p.G]) * kBK > p.K) sch.total = 0;
+    }
 
     if (warp == 0) {
         // ---- producer -------------------------------------------------------
@@ -251,25 +288,25 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             int64_t issued = 0;
             const uint32_t full0 = full_bar(0), empty0 = empty_bar(0);
             for (int64_t t = blockIdx.x; t < sch.total && !*abort_flag; t += gridDim.x) {
-                const TileInfo ti = tile_info<BN, kGrouped>(sch, p, t);
+                const TileInfo ti = tile_info<BN, kMode>(sch, p, t);
                 const int64_t b_band0 = ti.b_row / 128;
                 int sfb_atoms = 0;
 #pragma unroll
                 for (int j = 0; j < L::kSfbAtoms; ++j)
                     if (b_band0 + j < p.b_bands) ++sfb_atoms;
                 const uint32_t bytes = L::kABytes + L::kBBytes + 512u + 512u * sfb_atoms;
-                const uint8_t* sfa_src = p.a_s + (ti.m0 / 128) * p.k_atoms * 512;
-                const uint8_t* sfb_src = p.b_s + b_band0 * p.k_atoms * 512;
+                const uint8_t* sfa_src = p.a_s + ((ti.m0 / 128) * p.k_atoms + ti.kb0) * 512;
+                const uint8_t* sfb_src = p.b_s + (b_band0 * p.k_atoms + ti.kb0) * 512;
                 const int64_t sfb_band_stride = p.k_atoms * 512;
                 const int32_t ma = static_cast<int32_t>(ti.m0);
                 const int32_t nb = static_cast<int32_t>(ti.b_row);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = 0; kb < ti.nkb; ++kb) {
                     const uint32_t fb = full0 + 8u * stage;
                     if (!wait_phase(empty0 + 8u * stage, phase ^ 1u, guard)) break;
                     mbar_arrive_expect_tx(fb, bytes);
                     const uint32_t sa = sbase + L::kOffA + stage * L::kABytes;
                     const uint32_t sb = sbase + L::kOffB + stage * L::kBBytes;
-                    const int32_t kx = kb * kBK;
+                    const int32_t kx = static_cast<int32_t>((ti.kb0 + kb) * kBK);
                     tma_load_2d(sa, &tma_a, kx, ma, fb);
                     if constexpr (!kMnMajor) {
                         tma_load_2d(sb, &tma_b, kx, nb, fb);
@@ -317,8 +354,14 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             // Scale atoms of kCpBatch consecutive stages are copied together (one
             // copy-to-MMA switch of the tensor pipe per batch).
             constexpr int kCpBatch = L::kCpBatch;
-            const int64_t my_tiles = blockIdx.x < sch.total ? (sch.total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-            const int64_t g_total = my_tiles * num_kb;
+            int64_t g_total = 0;   // stages this CTA consumes
+            if constexpr (kMode == kGroupedK) {
+                for (int64_t t = blockIdx.x; t < sch.total; t += gridDim.x)
+                    g_total += tile_info<BN, kMode>(sch, p, t).nkb;
+            } else {
+                const int64_t my_tiles = blockIdx.x < sch.total ? (sch.total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+                g_total = my_tiles * sch.num_kb;
+            }
             int64_t g = 0;
             int stage = 0;
             uint32_t phase = 0;
@@ -329,7 +372,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                 if (!wait_phase(tempty_bar(acc), acc_phase ^ 1u, guard)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < num_kb; ++kb, ++g) {
+                const int nkb = kMode == kGroupedK ? tile_info<BN, kMode>(sch, p, t).nkb : sch.num_kb;
+                for (int kb = 0; kb < nkb; ++kb, ++g) {
                     if (g % kCpBatch == 0) {
                         const int nb = static_cast<int>(min(static_cast<int64_t>(kCpBatch), g_total - g));
                         for (int j = 0; j < nb && ok; ++j) {
@@ -353,7 +397,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                     const uint32_t sfb_t = tmem_base + L::kTmemSfb + 4 * L::kSfbAtoms * stage;
                     const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
                     const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
-                    const int64_t k_left = p.K - static_cast<int64_t>(kb) * kBK;
+                    const int64_t k_left = kMode == kGroupedK ? static_cast<int64_t>(nkb - kb) * kBK
+                                                              : p.K - static_cast<int64_t>(kb) * kBK;
                     if (k_left >= kBK) {
 #pragma unroll
                         for (int k = 0; k < kBK / kUmmaK; ++k)
@@ -390,7 +435,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < sch.total; t += gridDim.x) {
-            const TileInfo ti = tile_info<BN, kGrouped>(sch, p, t);
+            const TileInfo ti = tile_info<BN, kMode>(sch, p, t);
             // One lane waits; the warp follows its verdict, so the .sync.aligned
             // tensor-memory loads below always run with the full warp.
             int ok = 1;
@@ -410,9 +455,15 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             if (lane == 0) mbar_arrive(tempty_bar(acc));
             if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
 
+            if (ti.nkb == 0) {  // no K blocks (an empty expert): the tile is zero
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[c][j] = 0u;
+            }
             const int64_t row = ti.m0 + 32 * quad + lane;
             if (row >= ti.row_lo && row < ti.row_hi) {
-                uint16_t* yrow = p.y + row * p.ldy;
+                uint16_t* yrow = p.y + (ti.y_row0 + row) * p.ldy;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int64_t n = ti.n0 + half * 128 + c * 32;
@@ -448,11 +499,11 @@ bool make_tma_u8(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
     return encode_tensor_map_2d(map, ptr, false, cols, rows, cols, 128u, box_rows, true);
 }
 
-template <int BN, int STAGES, bool kMnMajor, bool kGrouped>
+template <int BN, int STAGES, bool kMnMajor, int kMode>
 cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& ta, const CUtensorMap& tb,
                      const GemmArgs& args, int64_t max_tiles, cudaStream_t stream) {
     using L = Cfg<BN, STAGES>;
-    auto kern = gemm_mxf8_kernel<BN, STAGES, kMnMajor, kGrouped>;
+    auto kern = gemm_mxf8_kernel<BN, STAGES, kMnMajor, kMode>;
     static thread_local int configured_device = -1;  // attribute set once per device and thread
     if (configured_device != dev.device) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
@@ -497,8 +548,8 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
     args.wait_limit_ns = kDefaultWaitLimitNs;
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
     if (b_mn_major)
-        return launch_t<kBN, kStages, true, false>(dev, ta, tb, args, tiles, stream);
-    return launch_t<kBN, kStages, false, false>(dev, ta, tb, args, tiles, stream);
+        return launch_t<kBN, kStages, true, kDense>(dev, ta, tb, args, tiles, stream);
+    return launch_t<kBN, kStages, false, kDense>(dev, ta, tb, args, tiles, stream);
 }
 
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
@@ -522,7 +573,31 @@ cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const vo
     args.G = G;
     args.status = dev.status;
     args.wait_limit_ns = kDefaultWaitLimitNs;
-    return launch_t<kBN, kStages, false, true>(dev, ta, tb, args, -1, stream);
+    return launch_t<kBN, kStages, false, kGroupedRows>(dev, ta, tb, args, -1, stream);
+}
+
+cudaError_t launch_grouped_gemm_wgrad(const DeviceInfo& dev, const void* a_q, const void* a_s,
+                                      const void* b_q, const void* b_s, const int64_t* offsets, int G,
+                                      int64_t M_total, int64_t capacity, int64_t M, int64_t N, void* y,
+                                      int64_t ldy, cudaStream_t stream) {
+    CUtensorMap ta, tb;
+    if (!make_tma_u8(&ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(capacity), kBM))
+        return cudaErrorInvalidValue;
+    if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(capacity), kBN))
+        return cudaErrorInvalidValue;
+    GemmArgs args{};
+    args.a_s = static_cast<const uint8_t*>(a_s);
+    args.b_s = static_cast<const uint8_t*>(b_s);
+    args.y = static_cast<uint16_t*>(y);
+    args.M = M; args.N = N; args.K = capacity; args.ldy = ldy;
+    args.M_total = M_total;
+    args.k_atoms = capacity / 128;
+    args.b_bands = (N + 127) / 128;
+    args.offsets = offsets;
+    args.G = G;
+    args.status = dev.status;
+    args.wait_limit_ns = kDefaultWaitLimitNs;
+    return launch_t<kBN, kStages, false, kGroupedK>(dev, ta, tb, args, -1, stream);
 }
 
 // ---- bounded-wait probe ---------------------------------------------------------------

@@ -26,9 +26,22 @@ bool encode_tensor_map_2d(CUtensorMap* map, const void* base, bool two_byte_elem
                           uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
                           uint32_t box_outer, bool swizzle_128b);
 
-cudaError_t launch_quant_1x32(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols,
-                              int64_t ld, void* q_row, void* s_row, void* q_col, void* s_col,
-                              bool tiled, cudaStream_t stream);
+// 3-D tensor map [outer, mid, inner], box [1, box_mid, box_inner], no swizzle.
+bool encode_tensor_map_3d(CUtensorMap* map, const void* base, bool two_byte_elems, uint64_t inner,
+                          uint64_t mid, uint64_t outer, uint64_t mid_stride_bytes,
+                          uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_mid);
+
+// 1x32 quantization of `batch` matrices [rows, cols] (row stride ld, matrix
+// stride batch_stride elements); outputs of matrix b follow each other.
+cudaError_t launch_quant_1x32(const DeviceInfo& dev, const void* x, int64_t batch, int64_t rows,
+                              int64_t cols, int64_t ld, int64_t batch_stride, void* q_row,
+                              void* s_row, void* q_col, void* s_col, bool tiled, cudaStream_t stream);
+
+// Token-axis 1x32 quantization inside each expert (zero-padded, 128-aligned slots).
+cudaError_t launch_quant_cols_grouped(const DeviceInfo& dev, const void* x, int64_t rows,
+                                      int64_t cols, int64_t ld, const int64_t* offsets, int G,
+                                      int64_t capacity, void* q_col, void* s_col, bool tiled,
+                                      cudaStream_t stream);
 
 cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, int64_t k,
                                int64_t ld, void* q, void* s_fwd, void* s_bwd, bool tiled,
@@ -44,6 +57,13 @@ cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const vo
                                 const void* b_q, const void* b_s, const int64_t* offsets, int G,
                                 int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy,
                                 cudaStream_t stream);
+
+// Grouped contraction (MoE weight gradient): y[g] = A_g B_g^T where the K range
+// of expert g is its 128-aligned token slot; A [M, capacity], B [N, capacity].
+cudaError_t launch_grouped_gemm_wgrad(const DeviceInfo& dev, const void* a_q, const void* a_s,
+                                      const void* b_q, const void* b_s, const int64_t* offsets, int G,
+                                      int64_t M_total, int64_t capacity, int64_t M, int64_t N, void* y,
+                                      int64_t ldy, cudaStream_t stream);
 
 cudaError_t launch_wait_probe(const DeviceInfo& dev, uint64_t limit_ns, cudaStream_t stream);
 

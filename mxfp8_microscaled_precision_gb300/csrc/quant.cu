@@ -116,18 +116,31 @@ __device__ __forceinline__ Ring ring_setup(uint8_t* smem_raw) {
     return r;
 }
 
-// Issue the TMA load of tile `tile` (tiles_c tiles per 128-row band) into slot s.
+// Tile numbering of a batch of matrices: tile = b * tiles_per_batch +
+// (row band) * tiles_c + (column block).
+struct TileGrid {
+    int64_t tiles_c, tiles_per_batch, n_tiles;
+    __device__ __forceinline__ void at(int64_t tile, int64_t& b, int64_t& r0, int64_t& c0) const {
+        b = tile / tiles_per_batch;
+        const int64_t local = tile - b * tiles_per_batch;
+        r0 = (local / tiles_c) * kTile;
+        c0 = (local % tiles_c) * kTile;
+    }
+};
+
+// Issue the TMA load of `tile` into slot s (3-D map {cols, rows, batch}).
 __device__ __forceinline__ void ring_load(const Ring& r, const CUtensorMap* map, int s, int64_t tile,
-                                          int64_t tiles_c) {
+                                          const TileGrid& tg) {
+    int64_t b, r0, c0;
+    tg.at(tile, b, r0, c0);
     const uint32_t bar = r.bar0 + 8u * s;
     mbar_arrive_expect_tx(bar, kTileBytes);
-    tma_load_2d(smem_u32(r.buf + s * kTileBytes), map, static_cast<int32_t>((tile % tiles_c) * kTile),
-                static_cast<int32_t>((tile / tiles_c) * kTile), bar);
+    tma_load_3d(smem_u32(r.buf + s * kTileBytes), map, static_cast<int32_t>(c0), static_cast<int32_t>(r0),
+                static_cast<int32_t>(b), bar);
 }
 
 // Thread 0 initialises the barriers and issues the first kRing loads.
-__device__ __forceinline__ void ring_start(const Ring& r, const CUtensorMap* map, int64_t n_tiles,
-                                           int64_t tiles_c) {
+__device__ __forceinline__ void ring_start(const Ring& r, const CUtensorMap* map, const TileGrid& tg) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRing; ++s) mbar_init(r.bar0 + 8u * s, 1);
         *r.abort_flag = 0;
@@ -135,7 +148,7 @@ __device__ __forceinline__ void ring_start(const Ring& r, const CUtensorMap* map
         prefetch_tensormap(map);
         for (int s = 0; s < kRing; ++s) {
             const int64_t tile = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
-            if (tile < n_tiles) ring_load(r, map, s, tile, tiles_c);
+            if (tile < tg.n_tiles) ring_load(r, map, s, tile, tg);
         }
     }
     __syncthreads();
@@ -152,11 +165,11 @@ __device__ __forceinline__ bool ring_wait(const Ring& r, int i, const WaitGuard&
 // After every thread is done with slot i % kRing: refill it with the tile
 // kRing iterations ahead.
 __device__ __forceinline__ void ring_release(const Ring& r, const CUtensorMap* map, int i, int64_t tile,
-                                             int64_t n_tiles, int64_t tiles_c) {
+                                             const TileGrid& tg) {
     __syncthreads();
     if (threadIdx.x == 0) {
         const int64_t next = tile + static_cast<int64_t>(kRing) * gridDim.x;
-        if (next < n_tiles) ring_load(r, map, i % kRing, next, tiles_c);
+        if (next < tg.n_tiles) ring_load(r, map, i % kRing, next, tg);
     }
 }
 
@@ -239,17 +252,91 @@ __device__ __forceinline__ void load_tile_chunks(uint4 (&v)[kLoadsPerThread], co
     }
 }
 
+// Output strides between the matrices of a batch (bytes), input stride (elements).
+struct BatchStrides {
+    int64_t x, q_row, s_row, q_col, s_col;
+};
+
 // Row copy only: one tile per CTA, loaded straight into registers.
 template <bool kTiled>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                               int64_t cols, int64_t ld,
                                                               uint8_t* __restrict__ q_row,
-                                                              uint8_t* __restrict__ s_row, int64_t tiles_c) {
-    const int64_t tile = blockIdx.x;
-    const int64_t r0 = (tile / tiles_c) * kTile, c0 = (tile % tiles_c) * kTile;
+                                                              uint8_t* __restrict__ s_row, TileGrid tg,
+                                                              BatchStrides bs) {
+    int64_t b, r0, c0;
+    tg.at(blockIdx.x, b, r0, c0);
     uint4 v[kLoadsPerThread];
-    load_tile_chunks(v, x, r0, c0, rows, cols, ld);
-    row_pass<kTiled>([&](int j) { return v[j]; }, r0, c0, rows, cols, q_row, s_row);
+    load_tile_chunks(v, x + b * bs.x, r0, c0, rows, cols, ld);
+    row_pass<kTiled>([&](int j) { return v[j]; }, r0, c0, rows, cols, q_row + b * bs.q_row,
+                     s_row + b * bs.s_row);
+}
+
+// Column copy of one staged tile: thread t takes the column pair t % 64 and
+// the 32-token group t / 64; a warp reads 128 contiguous bytes of one staged
+// row per step (conflict-free).  The group's first token is tok0 + 32 (t/64)
+// in the output (row stride out_ld, out_ld/32 scale groups); groups at or past
+// tok_limit are not written (tiled layout: their scale is padding, 0).
+template <bool kTiled>
+__device__ __forceinline__ void col_pass(const uint32_t* tw, int64_t c0, int64_t cols, int64_t out_ld,
+                                         int64_t tok0, int64_t tok_limit, uint8_t* __restrict__ q_col,
+                                         uint8_t* __restrict__ s_col) {
+    const int t = threadIdx.x;
+    const int p = t & 63;
+    const int gi = t >> 6;
+    const int64_t cA = c0 + 2 * p;              // output row of q_col
+    const int64_t tok = tok0 + 32 * gi;         // first token of the group
+    const int64_t ogroups = out_ld >> 5;
+    const int64_t g_out = tok >> 5;
+    const bool ok = cA < cols && tok < tok_limit;
+    uint32_t w[32];
+    uint32_t m2 = 0u;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        w[j] = tw[(32 * gi + j) * 64 + p];
+        m2 = max_u16x2(m2, w[j] & 0x7FFF7FFFu);
+    }
+    uint8_t* q0 = q_col + cA * out_ld + tok;
+    // Scale bytes of rows cA and cA+1 (same 32-row block: cA is even).
+    uint8_t* s0 = kTiled ? s_col + tiled_scale_offset(cA, g_out, ogroups) : s_col + cA * ogroups + g_out;
+    const int64_t s_next = kTiled ? 16 : ogroups;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const uint32_t m = half ? (m2 >> 16) : (m2 & 0xFFFFu);
+        uint8_t code;
+        uint32_t o[8];
+        if (m >= 0x7F80u) {
+            code = 0xFF;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint32_t bt = 0x7F7F7F7Fu;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t h = half ? (w[4 * j + u] >> 16) : (w[4 * j + u] & 0xFFFFu);
+                    bt |= ((h >> 15) & 1u) << (8 * u + 7);
+                }
+                o[j] = bt;
+            }
+        } else {
+            const int e = rceil_exponent(m);
+            const float sc = pow2_neg(e);
+            code = static_cast<uint8_t>(e + 127);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float f[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    f[u] = (half ? bf16_hi(w[4 * j + u]) : bf16_lo(w[4 * j + u])) * sc;
+                o[j] = cvt_e4m3x2(f[0], f[1]) | (cvt_e4m3x2(f[2], f[3]) << 16);
+            }
+        }
+        if (ok) {
+            uint4* dst = reinterpret_cast<uint4*>(q0 + half * out_ld);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        if (ok || kTiled) s0[half * s_next] = ok ? code : 0;
+    }
 }
 
 // Column copy (with or without the row copy): persistent, TMA-fed ring.
@@ -260,86 +347,104 @@ template <bool kRow, bool kTiled>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_kernel(
     const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_t cols,
     uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col,
-    uint8_t* __restrict__ s_col, int64_t tiles_c, int64_t n_tiles, unsigned int* status,
+    uint8_t* __restrict__ s_col, TileGrid tg, BatchStrides bs, unsigned int* status,
     uint64_t wait_limit_ns) {
     extern __shared__ uint8_t smem_raw[];
     const Ring ring = ring_setup(smem_raw);
     const WaitGuard guard{ring.abort_flag, status, wait_limit_ns};
-    ring_start(ring, &tmap, n_tiles, tiles_c);
+    ring_start(ring, &tmap, tg);
 
     const int t = threadIdx.x;
-    const int64_t rgroups = rows >> 5;
     int i = 0;
     int64_t tile = blockIdx.x;
-    for (; tile < n_tiles; tile += gridDim.x, ++i) {
+    for (; tile < tg.n_tiles; tile += gridDim.x, ++i) {
         if (!ring_wait(ring, i, guard)) break;
         const uint8_t* buf = ring.buf + (i % kRing) * kTileBytes;
-        const int64_t r0 = (tile / tiles_c) * kTile;
-        const int64_t c0 = (tile % tiles_c) * kTile;
-
+        int64_t b, r0, c0;
+        tg.at(tile, b, r0, c0);
         if constexpr (kRow) {
             const uint4* b4 = reinterpret_cast<const uint4*>(buf) + (t >> 4) * 16 + (t & 15);
-            row_pass<kTiled>([&](int j) { return b4[j * 256]; }, r0, c0, rows, cols, q_row, s_row);
+            row_pass<kTiled>([&](int j) { return b4[j * 256]; }, r0, c0, rows, cols, q_row + b * bs.q_row,
+                             s_row + b * bs.s_row);
         }
-
-        const uint32_t* tw = reinterpret_cast<const uint32_t*>(buf);
-        const int p = t & 63;
-        const int gi = t >> 6;
-        const int64_t cA = c0 + 2 * p;              // output row of q_col
-        const int64_t rbase = r0 + 32 * gi;         // first input row of the group
-        const int64_t g_out = rbase >> 5;
-        const bool ok = cA < cols && rbase < rows;  // rows % 32 == 0 in column mode
-        uint32_t w[32];
-        uint32_t m2 = 0u;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            w[j] = tw[(32 * gi + j) * 64 + p];
-            m2 = max_u16x2(m2, w[j] & 0x7FFF7FFFu);
-        }
-        uint8_t* q0 = q_col + cA * rows + rbase;
-        // Scale bytes of rows cA and cA+1 (same 32-row block: cA is even).
-        uint8_t* s0 = kTiled ? s_col + tiled_scale_offset(cA, g_out, rgroups) : s_col + cA * rgroups + g_out;
-        const int64_t s_next = kTiled ? 16 : rgroups;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const uint32_t m = half ? (m2 >> 16) : (m2 & 0xFFFFu);
-            uint8_t code;
-            uint32_t o[8];
-            if (m >= 0x7F80u) {
-                code = 0xFF;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t b = 0x7F7F7F7Fu;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const uint32_t h = half ? (w[4 * j + u] >> 16) : (w[4 * j + u] & 0xFFFFu);
-                        b |= ((h >> 15) & 1u) << (8 * u + 7);
-                    }
-                    o[j] = b;
-                }
-            } else {
-                const int e = rceil_exponent(m);
-                const float sc = pow2_neg(e);
-                code = static_cast<uint8_t>(e + 127);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float f[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        f[u] = (half ? bf16_hi(w[4 * j + u]) : bf16_lo(w[4 * j + u])) * sc;
-                    o[j] = cvt_e4m3x2(f[0], f[1]) | (cvt_e4m3x2(f[2], f[3]) << 16);
-                }
-            }
-            if (ok) {
-                uint4* dst = reinterpret_cast<uint4*>(q0 + half * rows);
-                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-            }
-            if (ok || kTiled) s0[half * s_next] = ok ? code : 0;
-        }
-        ring_release(ring, &tmap, i, tile, n_tiles, tiles_c);
+        col_pass<kTiled>(reinterpret_cast<const uint32_t*>(buf), c0, cols, rows, r0, rows,
+                         q_col + b * bs.q_col, s_col + b * bs.s_col);
+        ring_release(ring, &tmap, i, tile, tg);
     }
-    ring_drain(ring, i, tile, n_tiles, guard);
+    ring_drain(ring, i, tile, tg.n_tiles, guard);
+}
+
+// Token-axis (column) quantization inside each expert for the MoE weight
+// gradient.  Expert g's tokens go to the slot [P_g, P_g + L_g) of q_col
+// [cols, capacity], L_g = m_g rounded up to 128, P_g = sum of earlier L; each
+// 32-token group starts at the expert's first token and is zero-padded past
+// its last.  The slots are computed from the device offsets by every CTA (in
+// shared memory); the CTAs then walk the (slot block, column block) tiles.
+template <bool kTiled>
+__global__ void __launch_bounds__(kThreads) quant_cols_grouped_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
+    const int64_t* __restrict__ offsets, int G, int64_t capacity, uint8_t* __restrict__ q_col,
+    uint8_t* __restrict__ s_col) {
+    extern __shared__ uint8_t smem_raw[];
+    uint32_t* tile = reinterpret_cast<uint32_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    int64_t* s_off = reinterpret_cast<int64_t*>(tile + kTile * kTile / 2);  // [G+1]
+    int64_t* s_slot = s_off + (G + 1);                                      // [G+1]
+    const int t = threadIdx.x;
+    const int warp = t >> 5, lane = t & 31;
+    for (int g = t; g <= G; g += kThreads) {
+        int64_t o = offsets[g];
+        s_off[g] = o < 0 ? 0 : (o > rows ? rows : o);  // malformed offsets stay in bounds
+    }
+    __syncthreads();
+    if (warp == 0) {  // exclusive prefix of the slot lengths, 32 experts at a time
+        int64_t carry = 0;
+        for (int base = 0; base < G; base += 32) {
+            const int g = base + lane;
+            int64_t len = 0;
+            if (g < G) {
+                const int64_t m = s_off[g + 1] - s_off[g];
+                len = m > 0 ? (m + kTile - 1) / kTile * kTile : 0;
+            }
+            int64_t incl = len;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= d) incl += y;
+            }
+            if (g < G) s_slot[g] = carry + incl - len;
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) s_slot[G] = carry;
+    }
+    __syncthreads();
+    const int64_t used = s_slot[G] < capacity ? s_slot[G] : capacity;
+    const int64_t tiles_c = (cols + kTile - 1) / kTile;
+    const int64_t n_tiles = (used / kTile) * tiles_c;
+    const int chunk = t & 15;
+    for (int64_t tl = blockIdx.x; tl < n_tiles; tl += gridDim.x) {
+        const int64_t pos = (tl / tiles_c) * kTile;   // slot position of this 128-token block
+        const int64_t c0 = (tl % tiles_c) * kTile;
+        int lo = 0, hi = G;  // owner: largest g with s_slot[g] <= pos
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_slot[mid] <= pos) lo = mid; else hi = mid;
+        }
+        const int64_t row0 = s_off[lo] + (pos - s_slot[lo]);
+        const int64_t row_end = s_off[lo + 1];
+        const int64_t col = c0 + chunk * 8;
+        const uint16_t* xp = x + row0 * ld + col;
+#pragma unroll
+        for (int j = 0; j < kLoadsPerThread; ++j) {
+            const int lr = (t >> 4) + 16 * j;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (col < cols && row0 + lr < row_end) v = __ldg(reinterpret_cast<const uint4*>(xp + lr * ld));
+            reinterpret_cast<uint4*>(tile)[lr * 16 + chunk] = v;
+        }
+        __syncthreads();
+        col_pass<kTiled>(tile, c0, cols, capacity, pos, capacity, q_col, s_col);
+        __syncthreads();
+    }
 }
 
 // ---------------------------------------------------------------------------------
@@ -432,51 +537,92 @@ int64_t grid_for(const DeviceInfo& dev, int64_t n_tiles) {
 
 template <bool kRow, bool kTiled>
 cudaError_t launch_cols_t(const DeviceInfo& dev, const CUtensorMap& map, int64_t rows, int64_t cols,
-                          void* q_row, void* s_row, void* q_col, void* s_col, cudaStream_t stream) {
+                          void* q_row, void* s_row, void* q_col, void* s_col, const TileGrid& tg,
+                          const BatchStrides& bs, cudaStream_t stream) {
     auto kern = quant_cols_kernel<kRow, kTiled>;
     static thread_local int configured = -1;
     cudaError_t e = configure_once(kern, dev.device, &configured);
     if (e != cudaSuccess) return e;
-    const int64_t tiles_c = (cols + kTile - 1) / kTile;
-    const int64_t n_tiles = tiles_c * ((rows + kTile - 1) / kTile);
-    kern<<<static_cast<unsigned>(grid_for(dev, n_tiles)), kThreads, kSmemBytes, stream>>>(
+    kern<<<static_cast<unsigned>(grid_for(dev, tg.n_tiles)), kThreads, kSmemBytes, stream>>>(
         map, rows, cols, static_cast<uint8_t*>(q_row), static_cast<uint8_t*>(s_row),
-        static_cast<uint8_t*>(q_col), static_cast<uint8_t*>(s_col), tiles_c, n_tiles, dev.status,
-        kDefaultWaitLimitNs);
+        static_cast<uint8_t*>(q_col), static_cast<uint8_t*>(s_col), tg, bs, dev.status, kDefaultWaitLimitNs);
     return cudaGetLastError();
 }
 
-// BF16 [rows, cols] with row stride ld elements, 128 x 128 boxes, no swizzle.
-bool bf16_tile_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols, int64_t ld) {
-    return encode_tensor_map_2d(map, x, true, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
-                                static_cast<uint64_t>(ld) * 2, kTile, kTile, false);
+int64_t scale_bytes(int64_t rows, int64_t cols, bool tiled) {
+    const int64_t groups = cols / 32;
+    return tiled ? ((rows + 127) / 128 * 128) * ((groups + 3) / 4 * 4) : rows * groups;
 }
 
 }  // namespace
 
-cudaError_t launch_quant_1x32(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols,
-                              int64_t ld, void* q_row, void* s_row, void* q_col, void* s_col,
-                              bool tiled, cudaStream_t stream) {
+cudaError_t launch_quant_1x32(const DeviceInfo& dev, const void* x, int64_t batch, int64_t rows,
+                              int64_t cols, int64_t ld, int64_t batch_stride, void* q_row,
+                              void* s_row, void* q_col, void* s_col, bool tiled, cudaStream_t stream) {
     const bool row = q_row != nullptr, col = q_col != nullptr;
-    const int64_t tiles_c = (cols + kTile - 1) / kTile;
-    const int64_t n_tiles = tiles_c * ((rows + kTile - 1) / kTile);
+    TileGrid tg;
+    tg.tiles_c = (cols + kTile - 1) / kTile;
+    tg.tiles_per_batch = tg.tiles_c * ((rows + kTile - 1) / kTile);
+    tg.n_tiles = tg.tiles_per_batch * batch;
+    BatchStrides bs;
+    bs.x = batch_stride;
+    bs.q_row = rows * cols;
+    bs.s_row = scale_bytes(rows, cols, tiled);
+    bs.q_col = cols * rows;
+    bs.s_col = scale_bytes(cols, rows, tiled);
     if (!col) {  // row copy only: direct loads, one tile per CTA
         auto xp = static_cast<const uint16_t*>(x);
         auto qp = static_cast<uint8_t*>(q_row);
         auto sp = static_cast<uint8_t*>(s_row);
         if (tiled)
-            quant_rows_kernel<true><<<static_cast<unsigned>(n_tiles), kThreads, 0, stream>>>(xp, rows, cols, ld, qp, sp, tiles_c);
+            quant_rows_kernel<true><<<static_cast<unsigned>(tg.n_tiles), kThreads, 0, stream>>>(xp, rows, cols, ld, qp, sp, tg, bs);
         else
-            quant_rows_kernel<false><<<static_cast<unsigned>(n_tiles), kThreads, 0, stream>>>(xp, rows, cols, ld, qp, sp, tiles_c);
+            quant_rows_kernel<false><<<static_cast<unsigned>(tg.n_tiles), kThreads, 0, stream>>>(xp, rows, cols, ld, qp, sp, tg, bs);
         return cudaGetLastError();
     }
     CUtensorMap map;
-    if (!bf16_tile_map(&map, x, rows, cols, ld)) return cudaErrorInvalidValue;
+    if (!encode_tensor_map_3d(&map, x, true, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                              static_cast<uint64_t>(batch), static_cast<uint64_t>(ld) * 2,
+                              static_cast<uint64_t>(batch_stride) * 2, kTile, kTile))
+        return cudaErrorInvalidValue;
     if (row)
-        return tiled ? launch_cols_t<true, true>(dev, map, rows, cols, q_row, s_row, q_col, s_col, stream)
-                     : launch_cols_t<true, false>(dev, map, rows, cols, q_row, s_row, q_col, s_col, stream);
-    return tiled ? launch_cols_t<false, true>(dev, map, rows, cols, q_row, s_row, q_col, s_col, stream)
-                 : launch_cols_t<false, false>(dev, map, rows, cols, q_row, s_row, q_col, s_col, stream);
+        return tiled ? launch_cols_t<true, true>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tg, bs, stream)
+                     : launch_cols_t<true, false>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tg, bs, stream);
+    return tiled ? launch_cols_t<false, true>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tg, bs, stream)
+                 : launch_cols_t<false, false>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tg, bs, stream);
+}
+
+cudaError_t launch_quant_cols_grouped(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols,
+                                      int64_t ld, const int64_t* offsets, int G, int64_t capacity,
+                                      void* q_col, void* s_col, bool tiled, cudaStream_t stream) {
+    const size_t smem = kTile * kTile * 2 + 128 + 2 * 8 * static_cast<size_t>(G + 1);
+    auto xp = static_cast<const uint16_t*>(x);
+    auto qp = static_cast<uint8_t*>(q_col);
+    auto sp = static_cast<uint8_t*>(s_col);
+    const int64_t max_tiles = (capacity / kTile) * ((cols + kTile - 1) / kTile);
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * 4;
+    const unsigned grid = static_cast<unsigned>(max_tiles < cap ? max_tiles : cap);
+    if (grid == 0) return cudaSuccess;
+    if (tiled) {
+        static thread_local int configured = -1;
+        if (configured != dev.device) {
+            cudaError_t e = cudaFuncSetAttribute(quant_cols_grouped_kernel<true>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+            if (e != cudaSuccess) return e;
+            configured = dev.device;
+        }
+        quant_cols_grouped_kernel<true><<<grid, kThreads, smem, stream>>>(xp, rows, cols, ld, offsets, G, capacity, qp, sp);
+    } else {
+        static thread_local int configured = -1;
+        if (configured != dev.device) {
+            cudaError_t e = cudaFuncSetAttribute(quant_cols_grouped_kernel<false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+            if (e != cudaSuccess) return e;
+            configured = dev.device;
+        }
+        quant_cols_grouped_kernel<false><<<grid, kThreads, smem, stream>>>(xp, rows, cols, ld, offsets, G, capacity, qp, sp);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, int64_t k, int64_t ld,

@@ -33,6 +33,21 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
+bool encode_tensor_map_3d(CUtensorMap* map, const void* base, bool two_byte_elems, uint64_t inner,
+                          uint64_t mid, uint64_t outer, uint64_t mid_stride_bytes,
+                          uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_mid) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || inner == 0 || mid == 0 || outer == 0) return false;
+    const cuuint64_t dims[3] = {inner, mid, outer};
+    const cuuint64_t strides[2] = {mid_stride_bytes, outer_stride_bytes};
+    const cuuint32_t box[3] = {box_inner, box_mid, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(map, two_byte_elems ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tensor_map_2d(CUtensorMap* map, const void* base, bool two_byte_elems, uint64_t inner,
                           uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
                           uint32_t box_outer, bool swizzle_128b) {

@@ -64,13 +64,18 @@ def lib() -> ctypes.CDLL:
         L.mxq_status_string.argtypes, L.mxq_status_string.restype = [S], ctypes.c_char_p
         L.mxq_scale_bytes.argtypes, L.mxq_scale_bytes.restype = [I64, I64, S], SZ
         L.mxq_quant_1x32_dual.argtypes = [P, I64, I64, I64, P, P, P, P, S, P]
+        L.mxq_quant_1x32_dual_batched.argtypes = [P, I64, I64, I64, I64, I64, P, P, P, P, S, P]
+        L.mxq_quant_1x32_cols_grouped.argtypes = [P, I64, I64, I64, P, I32, I64, P, P, S, P]
+        L.mxq_grouped_gemm_wgrad.argtypes = [P, P, P, P, P, I32, I64, I64, I64, I64, P, I64, P]
         L.mxq_quant_32x32.argtypes = [P, I64, I64, I64, P, P, P, S, P]
         L.mxq_gemm_bf16out.argtypes = [P, P, P, P, I64, I64, I64, S, P, I64, P]
         L.mxq_grouped_gemm.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, I64, P]
         L.mxq_get_device_status.argtypes = []
         L.mxq_debug_wait_timeout.argtypes = [U32, P]
         for f in ("mxq_quant_1x32_dual", "mxq_quant_32x32", "mxq_gemm_bf16out",
-                  "mxq_grouped_gemm", "mxq_get_device_status", "mxq_debug_wait_timeout"):
+                  "mxq_grouped_gemm", "mxq_get_device_status", "mxq_debug_wait_timeout",
+                  "mxq_quant_1x32_dual_batched", "mxq_quant_1x32_cols_grouped",
+                  "mxq_grouped_gemm_wgrad"):
             getattr(L, f).restype = S
         _lib = L
         return L
@@ -132,6 +137,65 @@ def quant_1x32_dual(x: torch.Tensor, row: bool = True, col: bool = True, layout=
                                      _ptr(q_col), _ptr(s_col), _layout(layout), _stream()),
            "mxq_quant_1x32_dual")
     return q_row, s_row, q_col, s_col
+
+
+def quant_1x32_dual_batched(x: torch.Tensor, row: bool = True, col: bool = True, layout="tiled"):
+    """1x32 quantization of every matrix of a 3-D bf16 CUDA tensor [B, R, C]
+    (e.g. stacked expert weights).  Returns (q_row [B,R,C], s_row [B, bytes],
+    q_col [B,C,R], s_col [B, bytes]); pairs not asked for are None."""
+    if x.dtype != torch.bfloat16 or x.dim() != 3 or not x.is_cuda or x.stride(2) != 1:
+        raise ValueError("x must be a 3-D bfloat16 CUDA tensor with unit last stride")
+    B, R, C = x.shape
+    dev = x.device
+    u8 = dict(dtype=torch.uint8, device=dev)
+    q_row = torch.empty((B, R, C), **u8) if row else None
+    s_row = torch.empty((B, scale_bytes(R, C, layout)), **u8) if row else None
+    q_col = torch.empty((B, C, R), **u8) if col else None
+    s_col = torch.empty((B, scale_bytes(C, R, layout)), **u8) if col else None
+    _check(lib().mxq_quant_1x32_dual_batched(_ptr(x), B, R, C, x.stride(1), x.stride(0), _ptr(q_row),
+                                             _ptr(s_row), _ptr(q_col), _ptr(s_col), _layout(layout),
+                                             _stream()), "mxq_quant_1x32_dual_batched")
+    return q_row, s_row, q_col, s_col
+
+
+def grouped_capacity(M_total: int, G: int) -> int:
+    """Token-slot capacity that fits any offsets: M_total + 127 G, rounded up to 128."""
+    return (M_total + 127 * G + 127) // 128 * 128
+
+
+def quant_cols_grouped(x: torch.Tensor, offsets: torch.Tensor, capacity: int = None, layout="tiled"):
+    """Token-axis quantization inside each expert (see mxq_quant_1x32_cols_grouped).
+    x: bf16 [M_total, C] sorted by expert; offsets: int64 CUDA [G+1].
+    Returns (q_col [C, capacity], s_col)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D bfloat16 CUDA tensor with unit last stride")
+    if offsets.dtype != torch.int64 or not offsets.is_cuda:
+        raise ValueError("offsets must be an int64 CUDA tensor")
+    R, C = x.shape
+    G = offsets.numel() - 1
+    if capacity is None:
+        capacity = grouped_capacity(R, G)
+    q_col = torch.empty((C, capacity), dtype=torch.uint8, device=x.device)
+    s_col = _scale_tensor(C, capacity, layout, x.device)
+    _check(lib().mxq_quant_1x32_cols_grouped(_ptr(x), R, C, x.stride(0), _ptr(offsets), G, capacity,
+                                             _ptr(q_col), _ptr(s_col), _layout(layout), _stream()),
+           "mxq_quant_1x32_cols_grouped")
+    return q_col, s_col
+
+
+def grouped_gemm_wgrad(a_q, a_s, b_q, b_s, offsets: torch.Tensor, M_total: int, out=None):
+    """Per-expert y[g] = A_g B_g^T over each expert's token slot (see
+    mxq_grouped_gemm_wgrad).  a_q [M, capacity], b_q [N, capacity] from
+    quant_cols_grouped.  Returns y bf16 [G, M, N]."""
+    M, capacity = a_q.shape
+    N = b_q.shape[0]
+    G = offsets.numel() - 1
+    if out is None:
+        out = torch.empty((G, M, N), dtype=torch.bfloat16, device=a_q.device)
+    _check(lib().mxq_grouped_gemm_wgrad(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(offsets), G,
+                                        M_total, capacity, M, N, _ptr(out), out.stride(-2), _stream()),
+           "mxq_grouped_gemm_wgrad")
+    return out
 
 
 def quant_32x32(w: torch.Tensor, layout="tiled", out=None):

@@ -90,6 +90,22 @@ def test_gemm_argument_errors(L):
     assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 0, 128, 64, FAKE, 128, None) == 0      # no rows
 
 
+def test_moe_backward_argument_errors(L):
+    b = L.mxq_quant_1x32_dual_batched
+    assert b(FAKE, 2, 64, 48, 48, 64 * 48, FAKE, FAKE, None, None, 1, None) == 2     # cols % 32
+    assert b(FAKE, 2, 64, 64, 64, 100, FAKE, FAKE, None, None, 1, None) == 1         # stride < rows*ld
+    assert b(FAKE, 0, 64, 64, 64, 4096, FAKE, FAKE, None, None, 1, None) == 0        # empty batch
+    c = L.mxq_quant_1x32_cols_grouped
+    assert c(FAKE, 300, 64, 64, FAKE, 4, 384, FAKE, FAKE, 1, None) == 1   # capacity < rows + 127 G
+    assert c(FAKE, 300, 64, 64, FAKE, 4, 1000, FAKE, FAKE, 1, None) == 2  # capacity % 128
+    assert c(FAKE, 300, 48, 48, FAKE, 4, 1024, FAKE, FAKE, 1, None) == 2  # cols % 32
+    assert c(FAKE, 300, 64, 64, None, 4, 1024, FAKE, FAKE, 1, None) == 1  # no offsets
+    w = L.mxq_grouped_gemm_wgrad
+    assert w(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 300, 1024, 128, 120, FAKE, 120, None) == 2   # N % 16
+    assert w(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 300, 512, 128, 128, FAKE, 128, None) == 1    # capacity small
+    assert w(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 300, 1024, 128, 128, FAKE, 128, None) == 1   # G < 1
+
+
 def test_binding_raises_value_error(L):
     from mxfp8_microscaled_precision_gb300 import mxq
     with pytest.raises(ValueError):
