@@ -143,7 +143,7 @@ mxq_status mxq_quant_1x32_dual_batched(const void* x, int64_t batch, int64_t row
  * Slot positions past an expert's tokens hold zero payload and scale code 0;
  * positions past the last slot are not written.
  * capacity: a multiple of 128, >= rows + 127*G (enough for any offsets).
- * Shapes: cols % 32 == 0; 1 <= G <= 1024.
+ * Shapes: cols % 32 == 0; 1 <= G <= 1024.  rows == 0 writes nothing.
  */
 mxq_status mxq_quant_1x32_cols_grouped(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                        const int64_t* group_offsets, int32_t G, int64_t capacity,

@@ -145,7 +145,7 @@ mxq_status mxq_quant_1x32_cols_grouped(const void* x, int64_t rows, int64_t cols
     if (G > 1024) return MXQ_ERR_UNSUPPORTED_SHAPE;
     if (cols % 32 != 0 || capacity % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
     if (capacity < rows + 127 * static_cast<int64_t>(G)) return MXQ_ERR_INVALID_ARG;
-    if (cols == 0 || capacity == 0) return MXQ_OK;
+    if (rows == 0 || cols == 0 || capacity == 0) return MXQ_OK;   // no tokens: every slot is empty
     if (!x || !group_offsets || !q_col || !s_col) return MXQ_ERR_INVALID_ARG;
     if (ld < cols || ld % 8 != 0) return MXQ_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(q_col) || !aligned16(s_col) ||
