@@ -394,6 +394,10 @@ class MoE(Workload):
              lambda: mxq.grouped_gemm(self.qh[0], self.qh[1], self.qdn[0], self.qdn[1], self.offsets, H, I, out=self.y2)),
         ]
 
+    def expert0_gate_up(self):
+        """Expert 0's gate_up weight [2I, H] (stacked rows on the device, alone on the host)."""
+        return self.inputs["W_gate_up"][:2 * self.I]
+
     def cpu_sample(self, budget_s):
         from oracle import oracle
         import numpy as np
@@ -404,7 +408,7 @@ class MoE(Workload):
         tq = (time.perf_counter() - t0) / x.size
         qa, sa = oracle.quant_rows(_host_bits(i["A"][:64]))
         a = oracle.dequant_rows(qa, sa)
-        qb, sb = oracle.quant_rows(_host_bits(i["W_gate_up"][:2 * self.I]))   # expert 0
+        qb, sb = oracle.quant_rows(_host_bits(self.expert0_gate_up()))
         b = oracle.dequant_rows(qb, sb)
         rows, t_g = 0, 0.0
         while t_g < budget_s and rows < a.shape[0]:
@@ -417,6 +421,121 @@ class MoE(Workload):
         return tq * elems + tg * self.gemm_flops, (
             f"oracle row quant of 256 routed rows and FP64 GEMM of {rows} rows against one expert "
             f"(N {2 * self.I}, K {self.H}); extrapolated to the full step")
+
+
+class MoETrain(Workload):
+    """One MoE expert-layer training pass over the 128-expert workload:
+    forward (gate_up, down), dgrad (dA = dY1 W_gu, dH = dY2 W_dn) and wgrad
+    (dW_gu = dY1^T A, dW_dn = dY2^T H) per expert.  dY1 / dY2 are synthetic
+    output gradients (the activation between the projections is not part of
+    the MXFP8 path)."""
+
+    def __init__(self, dev=None):
+        import torch
+        from mxfp8_microscaled_precision_gb300 import mxq, workloads
+        self.name = "moe_train"
+        d = workloads.moe_grouped(dev or "cpu", weights=False)
+        G, H, I = 128, 4096, 2048
+        self.G, self.H, self.I = G, H, I
+        self.Mt = d["A"].shape[0]
+        w = "moe_grouped"
+        seed_gu, seed_dn = workloads.seed_for(w, "W"), workloads.seed_for(w, "W_down")
+        if dev is None:
+            self.inputs = {"A": d["A"], "Hd": d["H"],
+                           "W_gate_up": workloads.normal((2 * I, H), 0.02, seed_gu)}
+            return
+        Mt = self.Mt
+        self.offsets = d["routing"].offsets.to(dev)
+        self.inputs = {"A": d["A"], "Hd": d["H"],
+                       "W_gate_up": workloads.normal((G, 2 * I, H), 0.02, seed_gu, device=dev),
+                       "W_down": workloads.normal((G, H, I), 0.02, seed_dn, device=dev),
+                       "dY1": workloads.normal((Mt, 2 * I), 1e-3, seed_gu + 50, device=dev),
+                       "dY2": workloads.normal((Mt, H), 1e-3, seed_dn + 50, device=dev)}
+        u8 = dict(dtype=torch.uint8, device=dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        sb = mxq.scale_bytes
+        self.cap = mxq.grouped_capacity(Mt, G)
+        cap = self.cap
+
+        def rows(r, c):
+            return (torch.empty((r, c), **u8), torch.empty(sb(r, c), **u8), None, None)
+
+        def cols_g(c):
+            return torch.empty((c, cap), **u8), torch.empty(sb(c, cap), **u8)
+        self.qa, self.qh = rows(Mt, H), rows(Mt, I)
+        self.qg1, self.qg2 = rows(Mt, 2 * I), rows(Mt, H)
+        self.wgu = (torch.empty((G, 2 * I, H), **u8), torch.empty((G, sb(2 * I, H)), **u8),
+                    torch.empty((G, H, 2 * I), **u8), torch.empty((G, sb(H, 2 * I)), **u8))
+        self.wdn = (torch.empty((G, H, I), **u8), torch.empty((G, sb(H, I)), **u8),
+                    torch.empty((G, I, H), **u8), torch.empty((G, sb(I, H)), **u8))
+        self.c_g1, self.c_a, self.c_g2, self.c_h = cols_g(2 * I), cols_g(H), cols_g(H), cols_g(I)
+        self.y1, self.y2 = torch.empty((Mt, 2 * I), **bf), torch.empty((Mt, H), **bf)
+        self.da, self.dh = torch.empty((Mt, H), **bf), torch.empty((Mt, I), **bf)
+        self.dwgu, self.dwdn = torch.empty((G, 2 * I, H), **bf), torch.empty((G, H, I), **bf)
+        self.outputs = [self.y1, self.y2, self.da, self.dh, self.dwgu, self.dwdn]
+
+    @property
+    def gemm_flops(self):
+        return 3 * (2 * self.Mt * 2 * self.I * self.H + 2 * self.Mt * self.H * self.I)
+
+    def _quant_batched(self, w, out):
+        from mxfp8_microscaled_precision_gb300 import mxq
+        B, R, C = w.shape
+        lib = mxq.lib()
+        mxq._check(lib.mxq_quant_1x32_dual_batched(mxq._ptr(w), B, R, C, w.stride(1), w.stride(0),
+                                                   *[mxq._ptr(t) for t in out], 1, mxq._stream()),
+                   "mxq_quant_1x32_dual_batched")
+
+    def _quant_cols(self, x, out):
+        from mxfp8_microscaled_precision_gb300 import mxq
+        lib = mxq.lib()
+        R, C = x.shape
+        mxq._check(lib.mxq_quant_1x32_cols_grouped(mxq._ptr(x), R, C, x.stride(0), mxq._ptr(self.offsets),
+                                                   self.G, self.cap, mxq._ptr(out[0]), mxq._ptr(out[1]), 1,
+                                                   mxq._stream()), "mxq_quant_1x32_cols_grouped")
+
+    def kernels(self):
+        from mxfp8_microscaled_precision_gb300 import mxq
+        i, G, H, I, Mt, off = self.inputs, self.G, self.H, self.I, self.Mt, self.offsets
+        wgu, wdn = self.wgu, self.wdn
+        f_gu, f_dn = 2 * Mt * 2 * I * H, 2 * Mt * H * I
+
+        def colsb(c):
+            return Mt * c * 3 + Mt * c // 32
+        return [
+            ("quant_A_row", "quant", _row_bytes(Mt, H), lambda: mxq.quant_1x32_dual(i["A"], col=False, out=self.qa)),
+            ("quant_H_row", "quant", _row_bytes(Mt, I), lambda: mxq.quant_1x32_dual(i["Hd"], col=False, out=self.qh)),
+            ("quant_Wgu_dual", "quant", _dual_bytes(G * 2 * I, H), lambda: self._quant_batched(i["W_gate_up"], wgu)),
+            ("quant_Wdn_dual", "quant", _dual_bytes(G * H, I), lambda: self._quant_batched(i["W_down"], wdn)),
+            ("grouped_fwd_gate_up", "gemm", f_gu,
+             lambda: mxq.grouped_gemm(self.qa[0], self.qa[1], wgu[0].view(G * 2 * I, H), wgu[1].view(-1), off, 2 * I, H, out=self.y1)),
+            ("grouped_fwd_down", "gemm", f_dn,
+             lambda: mxq.grouped_gemm(self.qh[0], self.qh[1], wdn[0].view(G * H, I), wdn[1].view(-1), off, H, I, out=self.y2)),
+            ("quant_dY1_row", "quant", _row_bytes(Mt, 2 * I), lambda: mxq.quant_1x32_dual(i["dY1"], col=False, out=self.qg1)),
+            ("quant_dY2_row", "quant", _row_bytes(Mt, H), lambda: mxq.quant_1x32_dual(i["dY2"], col=False, out=self.qg2)),
+            ("grouped_dgrad_gate_up", "gemm", f_gu,
+             lambda: mxq.grouped_gemm(self.qg1[0], self.qg1[1], wgu[2].view(G * H, 2 * I), wgu[3].view(-1), off, H, 2 * I, out=self.da)),
+            ("grouped_dgrad_down", "gemm", f_dn,
+             lambda: mxq.grouped_gemm(self.qg2[0], self.qg2[1], wdn[2].view(G * I, H), wdn[3].view(-1), off, I, H, out=self.dh)),
+            ("quant_dY1_cols", "quant", colsb(2 * I), lambda: self._quant_cols(i["dY1"], self.c_g1)),
+            ("quant_A_cols", "quant", colsb(H), lambda: self._quant_cols(i["A"], self.c_a)),
+            ("quant_dY2_cols", "quant", colsb(H), lambda: self._quant_cols(i["dY2"], self.c_g2)),
+            ("quant_H_cols", "quant", colsb(I), lambda: self._quant_cols(i["Hd"], self.c_h)),
+            ("grouped_wgrad_gate_up", "gemm", f_gu,
+             lambda: mxq.grouped_gemm_wgrad(self.c_g1[0], self.c_g1[1], self.c_a[0], self.c_a[1], off, Mt, out=self.dwgu)),
+            ("grouped_wgrad_down", "gemm", f_dn,
+             lambda: mxq.grouped_gemm_wgrad(self.c_g2[0], self.c_g2[1], self.c_h[0], self.c_h[1], off, Mt, out=self.dwdn)),
+        ]
+
+    def expert0_gate_up(self):
+        w = self.inputs["W_gate_up"]
+        return w[0] if w.dim() == 3 else w
+
+    def cpu_sample(self, budget_s):
+        # MoE.cpu_sample measures per-element and per-FLOP oracle rates and scales
+        # the FLOP part by self.gemm_flops (here the whole training step).
+        t_step, desc = MoE.cpu_sample(self, budget_s)
+        return t_step, desc + " (GEMM rate applied to the forward + dgrad + wgrad FLOPs)"
 
 
 def _host_bits(t):
@@ -439,16 +558,18 @@ def make_workload(name, dev=None):
         return Weight32(dev)
     if name == "moe_grouped":
         return MoE(dev)
+    if name == "moe_train":
+        return MoETrain(dev)
     raise SystemExit(f"unknown workload {name}")
 
 
-WORKLOAD_NAMES = ["linear_train", "linear_fwd_small", "weight_32x32", "moe_grouped",
+WORKLOAD_NAMES = ["linear_train", "linear_fwd_small", "weight_32x32", "moe_grouped", "moe_train",
                   "sweep_4096", "sweep_7168", "sweep_16384"]
 
 
 def workload_config(w):
     cfg = {"workload": w.name}
-    for k in ("M", "N", "K", "n", "k", "G", "H", "I", "Mt"):
+    for k in ("M", "N", "K", "n", "k", "G", "H", "I", "Mt", "cap"):
         if hasattr(w, k):
             cfg[k] = getattr(w, k)
     cfg["l2"] = "flushed between timed steps (256 MB device write, outside the timed intervals)"
