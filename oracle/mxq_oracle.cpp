@@ -27,6 +27,8 @@
 //    NaN = S.1111.111, largest finite 448.  Conversion is round to nearest,
 //    ties to even, saturating to +-448; the sign of zero is kept.
 //  * E8M0 code c in [0,254] means 2^(c-127); 0xFF is NaN.
+//  * The RFC also allows dst_type E5M2 (section 3.5.2.3): OCP float8_e5m2,
+//    bias 15, max finite 57344, RNE saturating; rceil then uses 57344.
 //  * rceil: e = ceil(log2(amax / 448)), clamped to [-127, 127]; amax == 0
 //    gives e = -127.  Evaluated exactly: with amax = f * 2^k, f in [0.5,1),
 //    448 = 0.875 * 2^9, so e = k - 9 + (f > 0.875).
@@ -110,17 +112,50 @@ uint8_t e4m3_encode(double v) {
     return sign | static_cast<uint8_t>((E << 3) | m);
 }
 
+// ---- E5M2 (float8_e5m2) ---------------------------------------------------------
+// Bias 15, 2 mantissa bits; S.11111.00 = Inf, S.11111.xx (xx != 0) = NaN;
+// largest finite 57344 = 1.75 * 2^15, smallest normal 2^-14, subnormal spacing 2^-16.
+
+double e5m2_decode(uint8_t c) {
+    int s = c >> 7, E = (c >> 2) & 0x1F, m = c & 0x3;
+    double mag;
+    if (E == 0x1F) mag = m == 0 ? HUGE_VAL : std::nan("");
+    else if (E == 0) mag = std::ldexp(static_cast<double>(m), -16);
+    else mag = std::ldexp(static_cast<double>(4 + m), E - 17);
+    return s ? -mag : mag;
+}
+
+// Round-to-nearest-even, saturating (to +-57344) encode of an exact double.
+uint8_t e5m2_encode(double v) {
+    uint8_t sign = std::signbit(v) ? 0x80 : 0;
+    if (std::isnan(v)) return sign | 0x7F;
+    double a = std::fabs(v);
+    if (a >= 57344.0) return sign | 0x7B;
+    if (a == 0.0) return sign;
+    int k;
+    std::frexp(a, &k);
+    int lead = k - 1;
+    if (lead < -14) lead = -14;
+    double quantum = std::ldexp(1.0, lead - 2);  // 2 mantissa bits
+    double n = std::nearbyint(a / quantum);      // integer in [0, 8]
+    if (lead == -14 && n < 4) return sign | static_cast<uint8_t>(n);
+    if (n == 8) { n = 4; lead += 1; }
+    // a < 57344 rounds at most to 57344 (E = 30, m = 3).
+    return sign | static_cast<uint8_t>(((lead + 15) << 2) | (static_cast<int>(n) - 4));
+}
+
 double e8m0_decode(uint8_t c) {
     if (c == 0xFF) return std::nan("");
     return std::ldexp(1.0, static_cast<int>(c) - 127);
 }
 
-// rceil scale exponent of a finite, non-negative amax.
-int rceil_exponent(double amax) {
+// rceil scale exponent of a finite, non-negative amax: ceil(log2(amax / max))
+// with max = 448 = 0.875 * 2^9 (E4M3) or 57344 = 0.875 * 2^16 (E5M2).
+int rceil_exponent(double amax, int fmt = 0) {
     if (amax == 0.0) return -127;
     int k;
     double f = std::frexp(amax, &k);
-    int e = k - 9 + (f > 0.875 ? 1 : 0);
+    int e = k - (fmt == 0 ? 9 : 16) + (f > 0.875 ? 1 : 0);
     if (e < -127) e = -127;
     if (e > 127) e = 127;
     return e;
@@ -129,7 +164,7 @@ int rceil_exponent(double amax) {
 // Quantize a set of n values that share one scale.  Writes the payload bytes
 // via `put(i, byte)` and returns the E8M0 scale code.
 template <class Get, class Put>
-uint8_t quant_shared_scale(int64_t n, Get get, Put put) {
+uint8_t quant_shared_scale(int64_t n, Get get, Put put, int fmt = 0) {
     double amax = 0.0;
     bool nonfinite = false;
     for (int64_t i = 0; i < n; ++i) {
@@ -141,8 +176,11 @@ uint8_t quant_shared_scale(int64_t n, Get get, Put put) {
         for (int64_t i = 0; i < n; ++i) put(i, static_cast<uint8_t>((std::signbit(get(i)) ? 0x80 : 0) | 0x7F));
         return 0xFF;
     }
-    int e = rceil_exponent(amax);
-    for (int64_t i = 0; i < n; ++i) put(i, e4m3_encode(std::ldexp(get(i), -e)));  // x * 2^-e is exact
+    int e = rceil_exponent(amax, fmt);
+    for (int64_t i = 0; i < n; ++i) {  // x * 2^-e is exact
+        const double v = std::ldexp(get(i), -e);
+        put(i, fmt == 0 ? e4m3_encode(v) : e5m2_encode(v));
+    }
     return static_cast<uint8_t>(e + 127);
 }
 
@@ -156,6 +194,13 @@ double orc_e4m3_decode(uint8_t c) { return e4m3_decode(c); }
 uint8_t orc_e4m3_encode(double v) { return e4m3_encode(v); }
 double orc_e8m0_decode(uint8_t c) { return e8m0_decode(c); }
 int orc_rceil_exponent(double amax) { return rceil_exponent(amax); }
+double orc_e5m2_decode(uint8_t c) { return e5m2_decode(c); }
+int orc_rceil_exponent_fmt(double amax, int fmt) { return rceil_exponent(amax, fmt); }
+
+void orc_e5m2_encode_array(const double* v, int64_t n, uint8_t* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = e5m2_encode(v[i]);
+}
 uint16_t orc_bf16_from_double(double v) { return double_to_bf16_bits(v); }
 double orc_bf16_to_double(uint16_t b) { return bf16_bits_to_double(b); }
 
@@ -173,8 +218,8 @@ void orc_bf16_from_double_array(const double* v, int64_t n, uint16_t* out) {
 // x: bf16 bits [rows, cols] with row stride ld (elements); cols % 32 == 0.
 // q: [rows, cols] payload; s: [rows, cols/32] scale codes (plain row-major).
 // Each group is 32 consecutive elements of one row.
-void orc_quant_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
-                    uint8_t* q, uint8_t* s) {
+void orc_quant_rows_fmt(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                        uint8_t* q, uint8_t* s, int fmt) {
     const int64_t groups = cols / 32;
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r) {
@@ -183,9 +228,14 @@ void orc_quant_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
             uint8_t* dst = q + r * cols + g * 32;
             s[r * groups + g] = quant_shared_scale(
                 32, [&](int64_t i) { return bf16_bits_to_double(src[i]); },
-                [&](int64_t i, uint8_t b) { dst[i] = b; });
+                [&](int64_t i, uint8_t b) { dst[i] = b; }, fmt);
         }
     }
+}
+
+void orc_quant_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                    uint8_t* q, uint8_t* s) {
+    orc_quant_rows_fmt(x, rows, cols, ld, q, s, 0);
 }
 
 // Dual-axis 1x32 quantization: the row copy is orc_quant_rows(x); the column
@@ -285,7 +335,17 @@ void orc_scale_tiled(const uint8_t* s, int64_t rows, int64_t groups, uint8_t* ou
 }
 
 // ---- dequantization ----------------------------------------------------------
-// out[r][c] = e4m3(q[r][c]) * 2^(s[r][c/32] - 127)   (plain scales)
+// out[r][c] = fp8(q[r][c]) * 2^(s[r][c/32] - 127)   (plain scales)
+void orc_dequant_rows_fmt(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t cols, double* out,
+                          int fmt) {
+    const int64_t groups = cols / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c)
+            out[r * cols + c] = (fmt == 0 ? e4m3_decode(q[r * cols + c]) : e5m2_decode(q[r * cols + c])) *
+                                e8m0_decode(s[r * groups + c / 32]);
+}
+
 void orc_dequant_rows(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t cols, double* out) {
     const int64_t groups = cols / 32;
 #pragma omp parallel for schedule(static)

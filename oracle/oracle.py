@@ -54,6 +54,13 @@ def _load():
     lib.orc_e4m3_decode.restype = ctypes.c_double
     lib.orc_e4m3_encode.argtypes = [ctypes.c_double]
     lib.orc_e4m3_encode.restype = ctypes.c_uint8
+    lib.orc_e5m2_decode.argtypes = [ctypes.c_uint8]
+    lib.orc_e5m2_decode.restype = ctypes.c_double
+    lib.orc_rceil_exponent_fmt.argtypes = [ctypes.c_double, ctypes.c_int]
+    lib.orc_rceil_exponent_fmt.restype = ctypes.c_int
+    lib.orc_e5m2_encode_array.argtypes = [P, I64, P]
+    lib.orc_quant_rows_fmt.argtypes = [P, I64, I64, I64, P, P, ctypes.c_int]
+    lib.orc_dequant_rows_fmt.argtypes = [P, P, I64, I64, P, ctypes.c_int]
     lib.orc_e8m0_decode.argtypes = [ctypes.c_uint8]
     lib.orc_e8m0_decode.restype = ctypes.c_double
     lib.orc_rceil_exponent.argtypes = [ctypes.c_double]
@@ -73,7 +80,8 @@ def _load():
     lib.orc_gemm.argtypes = [P, P, I64, I64, I64, P, I64, P]
     lib.orc_grouped_gemm.argtypes = [P, P, P, ctypes.c_int32, I64, I64, P, I64, P]
     for f in ("orc_e4m3_encode_array", "orc_bf16_from_double_array", "orc_quant_rows",
-              "orc_quant_cols_grouped",
+              "orc_quant_cols_grouped", "orc_e5m2_encode_array", "orc_quant_rows_fmt",
+              "orc_dequant_rows_fmt",
               "orc_quant_dual", "orc_quant_32x32", "orc_scale_tiled", "orc_dequant_rows",
               "orc_gemm", "orc_grouped_gemm"):
         getattr(lib, f).restype = None
@@ -105,6 +113,27 @@ def e4m3_encode(values) -> np.ndarray:
     out = np.empty(v.shape, np.uint8)
     lib.orc_e4m3_encode_array(_ptr(v), v.size, _ptr(out))
     return out.reshape(np.shape(values))
+
+
+def e5m2_decode(codes) -> np.ndarray:
+    """Value of each float8_e5m2 code (Inf for 0x7C/0xFC, NaN for the other E=31 codes)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.orc_e5m2_decode(int(v)) for v in c]).reshape(np.shape(codes))
+
+
+def e5m2_encode(values) -> np.ndarray:
+    """Round-to-nearest-even, saturating float8_e5m2 code of each double."""
+    lib = _load()
+    v = _c(values, np.float64).ravel()
+    out = np.empty(v.shape, np.uint8)
+    lib.orc_e5m2_encode_array(_ptr(v), v.size, _ptr(out))
+    return out.reshape(np.shape(values))
+
+
+def rceil_exponent_fmt(amax: float, fmt: int) -> int:
+    """ceil(log2(amax / max_fmt)), max 448 (fmt 0, E4M3) or 57344 (fmt 1, E5M2)."""
+    return _load().orc_rceil_exponent_fmt(float(amax), int(fmt))
 
 
 def e8m0_decode(code: int) -> float:
@@ -143,6 +172,27 @@ def quant_rows(x_bits: np.ndarray):
     s = np.empty((R, C // 32), np.uint8)
     lib.orc_quant_rows(_ptr(x), R, C, C, _ptr(q), _ptr(s))
     return q, s
+
+
+def quant_rows_fmt(x_bits: np.ndarray, fmt: int):
+    """quant_rows with the payload format fmt (0 E4M3, 1 E5M2)."""
+    lib = _load()
+    x = _c(x_bits, np.uint16)
+    R, C = x.shape
+    q = np.empty((R, C), np.uint8)
+    s = np.empty((R, C // 32), np.uint8)
+    lib.orc_quant_rows_fmt(_ptr(x), R, C, C, _ptr(q), _ptr(s), int(fmt))
+    return q, s
+
+
+def dequant_rows_fmt(q: np.ndarray, s: np.ndarray, fmt: int) -> np.ndarray:
+    lib = _load()
+    q = _c(q, np.uint8)
+    s = _c(s, np.uint8)
+    R, C = q.shape
+    out = np.empty((R, C), np.float64)
+    lib.orc_dequant_rows_fmt(_ptr(q), _ptr(s), R, C, _ptr(out), int(fmt))
+    return out
 
 
 def quant_dual(x_bits: np.ndarray, want_row: bool = True, want_col: bool = True):
