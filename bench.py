@@ -483,7 +483,7 @@ class MoETrain(Workload):
         B, R, C = w.shape
         lib = mxq.lib()
         mxq._check(lib.mxq_quant_1x32_dual_batched(mxq._ptr(w), B, R, C, w.stride(1), w.stride(0),
-                                                   *[mxq._ptr(t) for t in out], 1, mxq._stream()),
+                                                   *[mxq._ptr(t) for t in out], 1, 0, mxq._stream()),
                    "mxq_quant_1x32_dual_batched")
 
     def _quant_cols(self, x, out):

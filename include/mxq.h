@@ -80,6 +80,14 @@ typedef enum {
     MXQ_SCALE_MMA_TILED = 1
 } mxq_scale_layout;
 
+/* FP8 payload format (RFC section 3.5.2.3: dst_type E4M3 or E5M2).
+ * E4M3 = float8_e4m3fn (max 448), the default of every call;
+ * E5M2 = float8_e5m2 (bias 15, max 57344; rceil then uses 57344). */
+typedef enum {
+    MXQ_FP8_E4M3 = 0,
+    MXQ_FP8_E5M2 = 1
+} mxq_fp8_format;
+
 /* Version of this ABI (MXQ_ABI_VERSION). */
 int mxq_abi_version(void);
 
@@ -120,11 +128,12 @@ mxq_status mxq_quant_1x32_dual(const void* x, int64_t rows, int64_t cols, int64_
  * s_col + b*mxq_scale_bytes(cols, rows, layout).  Used for the stacked MoE
  * expert weights [G, N, K]: the row copies give the forward operand and the
  * column copies [G, K, N] the dgrad operand of mxq_grouped_gemm.  batch <= 65535.
+ * fmt selects the payload format (mxq_quant_1x32_dual is fmt = MXQ_FP8_E4M3).
  */
 mxq_status mxq_quant_1x32_dual_batched(const void* x, int64_t batch, int64_t rows, int64_t cols,
                                        int64_t ld, int64_t batch_stride, void* q_row, void* s_row,
                                        void* q_col, void* s_col, mxq_scale_layout layout,
-                                       mxq_stream_t stream);
+                                       mxq_fp8_format fmt, mxq_stream_t stream);
 
 /*
  * Token-axis (column) 1x32 quantization inside each MoE expert, the operand
@@ -190,6 +199,13 @@ mxq_status mxq_quant_32x32(const void* w, int64_t n, int64_t k, int64_t ld,
 mxq_status mxq_gemm_bf16out(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
                             int64_t M, int64_t N, int64_t K, int b_mn_major,
                             void* y, int64_t ldy, mxq_stream_t stream);
+
+/* mxq_gemm_bf16out with the payload format of each operand (E4M3 or E5M2,
+ * e.g. E5M2 gradients against E4M3 weights); mxq_gemm_bf16out is E4M3 x E4M3. */
+mxq_status mxq_gemm_bf16out_fmt(const void* a_q, const void* a_s, mxq_fp8_format a_fmt,
+                                const void* b_q, const void* b_s, mxq_fp8_format b_fmt,
+                                int64_t M, int64_t N, int64_t K, int b_mn_major,
+                                void* y, int64_t ldy, mxq_stream_t stream);
 
 /*
  * Grouped block-scaled GEMM for MoE experts (tutorial: "MoE 专家层 (Grouped

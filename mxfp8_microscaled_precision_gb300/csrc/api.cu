@@ -104,8 +104,9 @@ size_t mxq_scale_bytes(int64_t rows, int64_t cols, mxq_scale_layout layout) {
 mxq_status mxq_quant_1x32_dual_batched(const void* x, int64_t batch, int64_t rows, int64_t cols,
                                        int64_t ld, int64_t batch_stride, void* q_row, void* s_row,
                                        void* q_col, void* s_col, mxq_scale_layout layout,
-                                       mxq_stream_t stream) {
+                                       mxq_fp8_format fmt, mxq_stream_t stream) {
     if (layout != MXQ_SCALE_ROWMAJOR && layout != MXQ_SCALE_MMA_TILED) return MXQ_ERR_INVALID_ARG;
+    if (fmt != MXQ_FP8_E4M3 && fmt != MXQ_FP8_E5M2) return MXQ_ERR_INVALID_ARG;
     if (batch < 0 || rows < 0 || cols < 0) return MXQ_ERR_INVALID_ARG;
     const bool row = q_row != nullptr || s_row != nullptr;
     const bool col = q_col != nullptr || s_col != nullptr;
@@ -126,14 +127,15 @@ mxq_status mxq_quant_1x32_dual_batched(const void* x, int64_t batch, int64_t row
     return from_cuda(mxq::launch_quant_1x32(dev, x, batch, rows, cols, ld, batch > 1 ? batch_stride : rows * ld,
                                             row ? q_row : nullptr, row ? s_row : nullptr,
                                             col ? q_col : nullptr, col ? s_col : nullptr,
-                                            layout == MXQ_SCALE_MMA_TILED,
+                                            layout == MXQ_SCALE_MMA_TILED, static_cast<int>(fmt),
                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mxq_status mxq_quant_1x32_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q_row,
                                void* s_row, void* q_col, void* s_col, mxq_scale_layout layout,
                                mxq_stream_t stream) {
-    return mxq_quant_1x32_dual_batched(x, 1, rows, cols, ld, 0, q_row, s_row, q_col, s_col, layout, stream);
+    return mxq_quant_1x32_dual_batched(x, 1, rows, cols, ld, 0, q_row, s_row, q_col, s_col, layout,
+                                       MXQ_FP8_E4M3, stream);
 }
 
 mxq_status mxq_quant_1x32_cols_grouped(const void* x, int64_t rows, int64_t cols, int64_t ld,
@@ -180,7 +182,16 @@ mxq_status mxq_quant_32x32(const void* w, int64_t n, int64_t k, int64_t ld, void
 mxq_status mxq_gemm_bf16out(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
                             int64_t M, int64_t N, int64_t K, int b_mn_major, void* y, int64_t ldy,
                             mxq_stream_t stream) {
+    return mxq_gemm_bf16out_fmt(a_q, a_s, MXQ_FP8_E4M3, b_q, b_s, MXQ_FP8_E4M3, M, N, K, b_mn_major, y, ldy,
+                                stream);
+}
+
+mxq_status mxq_gemm_bf16out_fmt(const void* a_q, const void* a_s, mxq_fp8_format a_fmt, const void* b_q,
+                                const void* b_s, mxq_fp8_format b_fmt, int64_t M, int64_t N, int64_t K,
+                                int b_mn_major, void* y, int64_t ldy, mxq_stream_t stream) {
     if (M < 0 || N < 0 || K < 0 || (b_mn_major != 0 && b_mn_major != 1)) return MXQ_ERR_INVALID_ARG;
+    if ((a_fmt != MXQ_FP8_E4M3 && a_fmt != MXQ_FP8_E5M2) || (b_fmt != MXQ_FP8_E4M3 && b_fmt != MXQ_FP8_E5M2))
+        return MXQ_ERR_INVALID_ARG;
     if (K % 32 != 0 || N % 16 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
     if (b_mn_major && N % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
     if (M > (int64_t(1) << 31) - 128 || N > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - 128)
@@ -201,6 +212,7 @@ mxq_status mxq_gemm_bf16out(const void* a_q, const void* a_s, const void* b_q, c
     mxq_status st = device_ok(&dev);
     if (st != MXQ_OK) return st;
     return from_cuda(mxq::launch_gemm(dev, a_q, a_s, b_q, b_s, M, N, K, b_mn_major != 0, y, ldy,
+                                      static_cast<int>(a_fmt), static_cast<int>(b_fmt),
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 

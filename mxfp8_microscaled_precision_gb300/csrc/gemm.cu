@@ -54,6 +54,7 @@ struct GemmArgs {
     int64_t b_bands;         // 128-row bands of B scales that exist
     const int64_t* offsets;  // grouped: [G+1] on the device
     int G;
+    uint32_t fmt_bits;       // operand formats in the instruction descriptor (0 = E4M3, E4M3)
     unsigned int* status;
     uint64_t wait_limit_ns;
 };
@@ -403,13 +404,13 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
 #pragma unroll
                         for (int k = 0; k < kBK / kUmmaK; ++k)
                             tc_mma_mxf8(d_tmem, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
-                                        make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k), sfa_t, sfb_t,
+                                        make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k) | p.fmt_bits, sfa_t, sfb_t,
                                         (kb > 0 || k > 0) ? 1u : 0u);
                     } else {
                         const int ksub = static_cast<int>(k_left) / kUmmaK;
                         for (int k = 0; k < ksub; ++k)
                             tc_mma_mxf8(d_tmem, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
-                                        make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k), sfa_t, sfb_t,
+                                        make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k) | p.fmt_bits, sfa_t, sfb_t,
                                         (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     tc_commit(empty_bar(stage));  // frees the slot once these MMAs are done
@@ -524,7 +525,7 @@ constexpr int kStages = 4;
 
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
                         const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
-                        int64_t ldy, cudaStream_t stream) {
+                        int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream) {
     CUtensorMap ta, tb;
     if (!make_tma_u8(&ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kBM))
         return cudaErrorInvalidValue;
@@ -544,6 +545,8 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
     args.b_bands = (N + 127) / 128;
     args.offsets = nullptr;
     args.G = 0;
+    // kind::mxf8f6f4 format codes: E4M3 = 0, E5M2 = 1 (A at bits 7-9, B at 10-12)
+    args.fmt_bits = (static_cast<uint32_t>(a_fmt) << 7) | (static_cast<uint32_t>(b_fmt) << 10);
     args.status = dev.status;
     args.wait_limit_ns = kDefaultWaitLimitNs;
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);

@@ -230,6 +230,14 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return r;
 }
 
+// Two floats -> two float8_e5m2 codes, round to nearest even, saturating to
+// +-57344 (NaN stays NaN).  `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t cvt_e5m2x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // Two floats -> packed bf16x2, round to nearest even; `lo` in the low half.
 __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
     uint32_t r;

@@ -33,9 +33,11 @@ bool encode_tensor_map_3d(CUtensorMap* map, const void* base, bool two_byte_elem
 
 // 1x32 quantization of `batch` matrices [rows, cols] (row stride ld, matrix
 // stride batch_stride elements); outputs of matrix b follow each other.
+// fmt: 0 = E4M3, 1 = E5M2.
 cudaError_t launch_quant_1x32(const DeviceInfo& dev, const void* x, int64_t batch, int64_t rows,
                               int64_t cols, int64_t ld, int64_t batch_stride, void* q_row,
-                              void* s_row, void* q_col, void* s_col, bool tiled, cudaStream_t stream);
+                              void* s_row, void* q_col, void* s_col, bool tiled, int fmt,
+                              cudaStream_t stream);
 
 // Token-axis 1x32 quantization inside each expert (zero-padded, 128-aligned slots).
 cudaError_t launch_quant_cols_grouped(const DeviceInfo& dev, const void* x, int64_t rows,
@@ -51,7 +53,7 @@ cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, 
 // when a tensor map cannot be encoded for the given shapes.
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
                         const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
-                        int64_t ldy, cudaStream_t stream);
+                        int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream);
 
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
                                 const void* b_q, const void* b_s, const int64_t* offsets, int G,

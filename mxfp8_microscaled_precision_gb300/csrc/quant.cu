@@ -45,11 +45,20 @@ constexpr int kSmemBytes = kRing * kTileBytes + 1024 + 256;     // ring + alignm
 // With amax = 1.m * 2^(E-127): amax/448 = (1.m/1.75) * 2^(E-135), and the
 // ceiling steps up exactly when the 7-bit mantissa exceeds 1.75 (m > 96).
 // Subnormal and zero amax (E == 0) fall below -127 and are clamped.
+//
+// Payload formats: kFmt 0 = E4M3 (max 448), 1 = E5M2 (max 57344 = 1.75 * 2^15,
+// so the same mantissa test with the exponent offset 142 instead of 135).
+template <int kFmt = 0>
 __device__ __forceinline__ int rceil_exponent(uint32_t amax_bits) {
     const int E = static_cast<int>(amax_bits >> 7);
     const int m = static_cast<int>(amax_bits & 0x7Fu);
-    const int e = E - 135 + (m > 96 ? 1 : 0);
+    const int e = E - (kFmt == 0 ? 135 : 142) + (m > 96 ? 1 : 0);
     return e < -127 ? -127 : e;
+}
+
+template <int kFmt>
+__device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
+    return kFmt == 0 ? cvt_e4m3x2(lo, hi) : cvt_e5m2x2(lo, hi);
 }
 
 // 2^-e as a float for e in [-127, 120] (always a normal number).
@@ -72,13 +81,14 @@ __device__ __forceinline__ uint32_t amax8_bits(const uint4 v) {
     return max(m & 0xFFFFu, m >> 16);
 }
 
-// Quantize 8 BF16 values (4 words) with scale 2^-e -> 8 E4M3 bytes.
+// Quantize 8 BF16 values (4 words) with scale 2^-e -> 8 FP8 bytes.
+template <int kFmt = 0>
 __device__ __forceinline__ uint2 quant8(const uint4 v, float sc) {
     uint2 o;
-    o.x = cvt_e4m3x2(bf16_lo(v.x) * sc, bf16_hi(v.x) * sc) |
-          (cvt_e4m3x2(bf16_lo(v.y) * sc, bf16_hi(v.y) * sc) << 16);
-    o.y = cvt_e4m3x2(bf16_lo(v.z) * sc, bf16_hi(v.z) * sc) |
-          (cvt_e4m3x2(bf16_lo(v.w) * sc, bf16_hi(v.w) * sc) << 16);
+    o.x = cvt_fp8x2<kFmt>(bf16_lo(v.x) * sc, bf16_hi(v.x) * sc) |
+          (cvt_fp8x2<kFmt>(bf16_lo(v.y) * sc, bf16_hi(v.y) * sc) << 16);
+    o.y = cvt_fp8x2<kFmt>(bf16_lo(v.z) * sc, bf16_hi(v.z) * sc) |
+          (cvt_fp8x2<kFmt>(bf16_lo(v.w) * sc, bf16_hi(v.w) * sc) << 16);
     return o;
 }
 
@@ -192,7 +202,7 @@ __device__ __forceinline__ void ring_drain(const Ring& r, int i, int64_t tile, i
 // (t/16 + 16 j), j = 0..7, 16-byte chunk t % 16 of the tile; the four chunks
 // of one 32-group sit in four consecutive lanes.
 // `chunk_of(j)` returns chunk j (registers or shared memory).
-template <bool kTiled, class ChunkOf>
+template <bool kTiled, int kFmt, class ChunkOf>
 __device__ __forceinline__ void row_pass(ChunkOf chunk_of, int64_t r0, int64_t c0, int64_t rows,
                                          int64_t cols, uint8_t* __restrict__ q_row,
                                          uint8_t* __restrict__ s_row) {
@@ -222,9 +232,9 @@ __device__ __forceinline__ void row_pass(ChunkOf chunk_of, int64_t r0, int64_t c
             code = 0xFF;
             out = nan8(v);
         } else {
-            const int e = rceil_exponent(m);
+            const int e = rceil_exponent<kFmt>(m);
             code = static_cast<uint8_t>(e + 127);
-            out = quant8(v, pow2_neg(e));
+            out = quant8<kFmt>(v, pow2_neg(e));
         }
         if (valid) *reinterpret_cast<uint2*>(qp + j * qstep) = out;
         if ((chunk & 3) == 0 && (valid || kTiled)) {  // tiled padding gets 0
@@ -258,7 +268,7 @@ struct BatchStrides {
 };
 
 // Row copy only: one tile per CTA, loaded straight into registers.
-template <bool kTiled>
+template <bool kTiled, int kFmt>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                               int64_t cols, int64_t ld,
                                                               uint8_t* __restrict__ q_row,
@@ -268,7 +278,7 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t* __
     tg.at(blockIdx.x, b, r0, c0);
     uint4 v[kLoadsPerThread];
     load_tile_chunks(v, x + b * bs.x, r0, c0, rows, cols, ld);
-    row_pass<kTiled>([&](int j) { return v[j]; }, r0, c0, rows, cols, q_row + b * bs.q_row,
+    row_pass<kTiled, kFmt>([&](int j) { return v[j]; }, r0, c0, rows, cols, q_row + b * bs.q_row,
                      s_row + b * bs.s_row);
 }
 
@@ -277,7 +287,7 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t* __
 // row per step (conflict-free).  The group's first token is tok0 + 32 (t/64)
 // in the output (row stride out_ld, out_ld/32 scale groups); groups at or past
 // tok_limit are not written (tiled layout: their scale is padding, 0).
-template <bool kTiled>
+template <bool kTiled, int kFmt>
 __device__ __forceinline__ void col_pass(const uint32_t* tw, int64_t c0, int64_t cols, int64_t out_ld,
                                          int64_t tok0, int64_t tok_limit, uint8_t* __restrict__ q_col,
                                          uint8_t* __restrict__ s_col) {
@@ -318,7 +328,7 @@ __device__ __forceinline__ void col_pass(const uint32_t* tw, int64_t c0, int64_t
                 o[j] = bt;
             }
         } else {
-            const int e = rceil_exponent(m);
+            const int e = rceil_exponent<kFmt>(m);
             const float sc = pow2_neg(e);
             code = static_cast<uint8_t>(e + 127);
 #pragma unroll
@@ -327,7 +337,7 @@ __device__ __forceinline__ void col_pass(const uint32_t* tw, int64_t c0, int64_t
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     f[u] = (half ? bf16_hi(w[4 * j + u]) : bf16_lo(w[4 * j + u])) * sc;
-                o[j] = cvt_e4m3x2(f[0], f[1]) | (cvt_e4m3x2(f[2], f[3]) << 16);
+                o[j] = cvt_fp8x2<kFmt>(f[0], f[1]) | (cvt_fp8x2<kFmt>(f[2], f[3]) << 16);
             }
         }
         if (ok) {
@@ -343,7 +353,7 @@ __device__ __forceinline__ void col_pass(const uint32_t* tw, int64_t c0, int64_t
 // Column pass: thread t takes the column pair t % 64 and the 32-row group
 // t / 64; a warp reads 128 contiguous bytes of one staged row per step, so
 // the shared-memory reads are conflict-free.
-template <bool kRow, bool kTiled>
+template <bool kRow, bool kTiled, int kFmt>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_kernel(
     const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_t cols,
     uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col,
@@ -364,10 +374,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_kernel(
         tg.at(tile, b, r0, c0);
         if constexpr (kRow) {
             const uint4* b4 = reinterpret_cast<const uint4*>(buf) + (t >> 4) * 16 + (t & 15);
-            row_pass<kTiled>([&](int j) { return b4[j * 256]; }, r0, c0, rows, cols, q_row + b * bs.q_row,
+            row_pass<kTiled, kFmt>([&](int j) { return b4[j * 256]; }, r0, c0, rows, cols, q_row + b * bs.q_row,
                              s_row + b * bs.s_row);
         }
-        col_pass<kTiled>(reinterpret_cast<const uint32_t*>(buf), c0, cols, rows, r0, rows,
+        col_pass<kTiled, kFmt>(reinterpret_cast<const uint32_t*>(buf), c0, cols, rows, r0, rows,
                          q_col + b * bs.q_col, s_col + b * bs.s_col);
         ring_release(ring, &tmap, i, tile, tg);
     }
@@ -442,7 +452,7 @@ __global__ void __launch_bounds__(kThreads) quant_cols_grouped_kernel(
             reinterpret_cast<uint4*>(tile)[lr * 16 + chunk] = v;
         }
         __syncthreads();
-        col_pass<kTiled>(tile, c0, cols, capacity, pos, capacity, q_col, s_col);
+        col_pass<kTiled, 0>(tile, c0, cols, capacity, pos, capacity, q_col, s_col);
         __syncthreads();
     }
 }
@@ -535,11 +545,11 @@ int64_t grid_for(const DeviceInfo& dev, int64_t n_tiles) {
     return n_tiles < cap ? n_tiles : cap;
 }
 
-template <bool kRow, bool kTiled>
+template <bool kRow, bool kTiled, int kFmt>
 cudaError_t launch_cols_t(const DeviceInfo& dev, const CUtensorMap& map, int64_t rows, int64_t cols,
                           void* q_row, void* s_row, void* q_col, void* s_col, const TileGrid& tg,
                           const BatchStrides& bs, cudaStream_t stream) {
-    auto kern = quant_cols_kernel<kRow, kTiled>;
+    auto kern = quant_cols_kernel<kRow, kTiled, kFmt>;
     static thread_local int configured = -1;
     cudaError_t e = configure_once(kern, dev.device, &configured);
     if (e != cudaSuccess) return e;
@@ -547,6 +557,34 @@ cudaError_t launch_cols_t(const DeviceInfo& dev, const CUtensorMap& map, int64_t
         map, rows, cols, static_cast<uint8_t*>(q_row), static_cast<uint8_t*>(s_row),
         static_cast<uint8_t*>(q_col), static_cast<uint8_t*>(s_col), tg, bs, dev.status, kDefaultWaitLimitNs);
     return cudaGetLastError();
+}
+
+template <int kFmt>
+cudaError_t launch_1x32_fmt(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                            int64_t batch, int64_t batch_stride, void* q_row, void* s_row, void* q_col,
+                            void* s_col, bool tiled, const TileGrid& tg, const BatchStrides& bs,
+                            cudaStream_t stream) {
+    const bool row = q_row != nullptr, col = q_col != nullptr;
+    if (!col) {  // row copy only: direct loads, one tile per CTA
+        auto xp = static_cast<const uint16_t*>(x);
+        auto qp = static_cast<uint8_t*>(q_row);
+        auto sp = static_cast<uint8_t*>(s_row);
+        if (tiled)
+            quant_rows_kernel<true, kFmt><<<static_cast<unsigned>(tg.n_tiles), kThreads, 0, stream>>>(xp, rows, cols, ld, qp, sp, tg, bs);
+        else
+            quant_rows_kernel<false, kFmt><<<static_cast<unsigned>(tg.n_tiles), kThreads, 0, stream>>>(xp, rows, cols, ld, qp, sp, tg, bs);
+        return cudaGetLastError();
+    }
+    CUtensorMap map;
+    if (!encode_tensor_map_3d(&map, x, true, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                              static_cast<uint64_t>(batch), static_cast<uint64_t>(ld) * 2,
+                              static_cast<uint64_t>(batch_stride) * 2, kTile, kTile))
+        return cudaErrorInvalidValue;
+    if (row)
+        return tiled ? launch_cols_t<true, true, kFmt>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tg, bs, stream)
+                     : launch_cols_t<true, false, kFmt>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tg, bs, stream);
+    return tiled ? launch_cols_t<false, true, kFmt>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tg, bs, stream)
+                 : launch_cols_t<false, false, kFmt>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tg, bs, stream);
 }
 
 int64_t scale_bytes(int64_t rows, int64_t cols, bool tiled) {
@@ -558,8 +596,8 @@ int64_t scale_bytes(int64_t rows, int64_t cols, bool tiled) {
 
 cudaError_t launch_quant_1x32(const DeviceInfo& dev, const void* x, int64_t batch, int64_t rows,
                               int64_t cols, int64_t ld, int64_t batch_stride, void* q_row,
-                              void* s_row, void* q_col, void* s_col, bool tiled, cudaStream_t stream) {
-    const bool row = q_row != nullptr, col = q_col != nullptr;
+                              void* s_row, void* q_col, void* s_col, bool tiled, int fmt,
+                              cudaStream_t stream) {
     TileGrid tg;
     tg.tiles_c = (cols + kTile - 1) / kTile;
     tg.tiles_per_batch = tg.tiles_c * ((rows + kTile - 1) / kTile);
@@ -570,26 +608,9 @@ cudaError_t launch_quant_1x32(const DeviceInfo& dev, const void* x, int64_t batc
     bs.s_row = scale_bytes(rows, cols, tiled);
     bs.q_col = cols * rows;
     bs.s_col = scale_bytes(cols, rows, tiled);
-    if (!col) {  // row copy only: direct loads, one tile per CTA
-        auto xp = static_cast<const uint16_t*>(x);
-        auto qp = static_cast<uint8_t*>(q_row);
-        auto sp = static_cast<uint8_t*>(s_row);
-        if (tiled)
-            quant_rows_kernel<true><<<static_cast<unsigned>(tg.n_tiles), kThreads, 0, stream>>>(xp, rows, cols, ld, qp, sp, tg, bs);
-        else
-            quant_rows_kernel<false><<<static_cast<unsigned>(tg.n_tiles), kThreads, 0, stream>>>(xp, rows, cols, ld, qp, sp, tg, bs);
-        return cudaGetLastError();
-    }
-    CUtensorMap map;
-    if (!encode_tensor_map_3d(&map, x, true, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
-                              static_cast<uint64_t>(batch), static_cast<uint64_t>(ld) * 2,
-                              static_cast<uint64_t>(batch_stride) * 2, kTile, kTile))
-        return cudaErrorInvalidValue;
-    if (row)
-        return tiled ? launch_cols_t<true, true>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tg, bs, stream)
-                     : launch_cols_t<true, false>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tg, bs, stream);
-    return tiled ? launch_cols_t<false, true>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tg, bs, stream)
-                 : launch_cols_t<false, false>(dev, map, rows, cols, q_row, s_row, q_col, s_col, tg, bs, stream);
+    if (fmt == 1)
+        return launch_1x32_fmt<1>(dev, x, rows, cols, ld, batch, batch_stride, q_row, s_row, q_col, s_col, tiled, tg, bs, stream);
+    return launch_1x32_fmt<0>(dev, x, rows, cols, ld, batch, batch_stride, q_row, s_row, q_col, s_col, tiled, tg, bs, stream);
 }
 
 cudaError_t launch_quant_cols_grouped(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols,

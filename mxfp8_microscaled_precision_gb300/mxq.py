@@ -24,6 +24,8 @@ import torch
 from . import build as _build
 
 ROWMAJOR, TILED = 0, 1
+E4M3, E5M2 = 0, 1
+_FORMATS = {"e4m3": E4M3, "e5m2": E5M2, E4M3: E4M3, E5M2: E5M2}
 _LAYOUTS = {"rowmajor": ROWMAJOR, "tiled": TILED, ROWMAJOR: ROWMAJOR, TILED: TILED}
 STATUS = {0: "MXQ_OK", 1: "MXQ_ERR_INVALID_ARG", 2: "MXQ_ERR_UNSUPPORTED_SHAPE",
           3: "MXQ_ERR_UNSUPPORTED_DEVICE", 4: "MXQ_ERR_CUDA", 5: "MXQ_ERR_TIMEOUT"}
@@ -64,7 +66,8 @@ def lib() -> ctypes.CDLL:
         L.mxq_status_string.argtypes, L.mxq_status_string.restype = [S], ctypes.c_char_p
         L.mxq_scale_bytes.argtypes, L.mxq_scale_bytes.restype = [I64, I64, S], SZ
         L.mxq_quant_1x32_dual.argtypes = [P, I64, I64, I64, P, P, P, P, S, P]
-        L.mxq_quant_1x32_dual_batched.argtypes = [P, I64, I64, I64, I64, I64, P, P, P, P, S, P]
+        L.mxq_quant_1x32_dual_batched.argtypes = [P, I64, I64, I64, I64, I64, P, P, P, P, S, S, P]
+        L.mxq_gemm_bf16out_fmt.argtypes = [P, P, S, P, P, S, I64, I64, I64, S, P, I64, P]
         L.mxq_quant_1x32_cols_grouped.argtypes = [P, I64, I64, I64, P, I32, I64, P, P, S, P]
         L.mxq_grouped_gemm_wgrad.argtypes = [P, P, P, P, P, I32, I64, I64, I64, I64, P, I64, P]
         L.mxq_quant_32x32.argtypes = [P, I64, I64, I64, P, P, P, S, P]
@@ -75,7 +78,7 @@ def lib() -> ctypes.CDLL:
         for f in ("mxq_quant_1x32_dual", "mxq_quant_32x32", "mxq_gemm_bf16out",
                   "mxq_grouped_gemm", "mxq_get_device_status", "mxq_debug_wait_timeout",
                   "mxq_quant_1x32_dual_batched", "mxq_quant_1x32_cols_grouped",
-                  "mxq_grouped_gemm_wgrad"):
+                  "mxq_grouped_gemm_wgrad", "mxq_gemm_bf16out_fmt"):
             getattr(L, f).restype = S
         _lib = L
         return L
@@ -139,10 +142,20 @@ def quant_1x32_dual(x: torch.Tensor, row: bool = True, col: bool = True, layout=
     return q_row, s_row, q_col, s_col
 
 
-def quant_1x32_dual_batched(x: torch.Tensor, row: bool = True, col: bool = True, layout="tiled"):
+def _fmt(fmt) -> int:
+    if fmt not in _FORMATS:
+        raise ValueError(f"unknown FP8 format {fmt!r} (e4m3 or e5m2)")
+    return _FORMATS[fmt]
+
+
+def quant_1x32_dual_batched(x: torch.Tensor, row: bool = True, col: bool = True, layout="tiled",
+                            fmt="e4m3"):
     """1x32 quantization of every matrix of a 3-D bf16 CUDA tensor [B, R, C]
-    (e.g. stacked expert weights).  Returns (q_row [B,R,C], s_row [B, bytes],
+    (e.g. stacked expert weights; B = 1 for a single matrix) with payload
+    format fmt ("e4m3" or "e5m2").  Returns (q_row [B,R,C], s_row [B, bytes],
     q_col [B,C,R], s_col [B, bytes]); pairs not asked for are None."""
+    if x.dim() == 2:
+        x = x.unsqueeze(0)
     if x.dtype != torch.bfloat16 or x.dim() != 3 or not x.is_cuda or x.stride(2) != 1:
         raise ValueError("x must be a 3-D bfloat16 CUDA tensor with unit last stride")
     B, R, C = x.shape
@@ -154,7 +167,7 @@ def quant_1x32_dual_batched(x: torch.Tensor, row: bool = True, col: bool = True,
     s_col = torch.empty((B, scale_bytes(C, R, layout)), **u8) if col else None
     _check(lib().mxq_quant_1x32_dual_batched(_ptr(x), B, R, C, x.stride(1), x.stride(0), _ptr(q_row),
                                              _ptr(s_row), _ptr(q_col), _ptr(s_col), _layout(layout),
-                                             _stream()), "mxq_quant_1x32_dual_batched")
+                                             _fmt(fmt), _stream()), "mxq_quant_1x32_dual_batched")
     return q_row, s_row, q_col, s_col
 
 
@@ -224,6 +237,16 @@ def gemm(a_q, a_s, b_q, b_s, M: int, N: int, K: int, b_mn_major: bool = False, o
     _check(lib().mxq_gemm_bf16out(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K,
                                   1 if b_mn_major else 0, _ptr(out), out.stride(0), _stream()),
            "mxq_gemm_bf16out")
+    return out
+
+
+def gemm_fmt(a_q, a_s, a_fmt, b_q, b_s, b_fmt, M: int, N: int, K: int, b_mn_major: bool = False, out=None):
+    """gemm with per-operand payload formats ("e4m3" / "e5m2")."""
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a_q.device)
+    _check(lib().mxq_gemm_bf16out_fmt(_ptr(a_q), _ptr(a_s), _fmt(a_fmt), _ptr(b_q), _ptr(b_s), _fmt(b_fmt),
+                                      M, N, K, 1 if b_mn_major else 0, _ptr(out), out.stride(0), _stream()),
+           "mxq_gemm_bf16out_fmt")
     return out
 
 

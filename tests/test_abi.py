@@ -92,9 +92,13 @@ def test_gemm_argument_errors(L):
 
 def test_moe_backward_argument_errors(L):
     b = L.mxq_quant_1x32_dual_batched
-    assert b(FAKE, 2, 64, 48, 48, 64 * 48, FAKE, FAKE, None, None, 1, None) == 2     # cols % 32
-    assert b(FAKE, 2, 64, 64, 64, 100, FAKE, FAKE, None, None, 1, None) == 1         # stride < rows*ld
-    assert b(FAKE, 0, 64, 64, 64, 4096, FAKE, FAKE, None, None, 1, None) == 0        # empty batch
+    assert b(FAKE, 2, 64, 48, 48, 64 * 48, FAKE, FAKE, None, None, 1, 0, None) == 2     # cols % 32
+    assert b(FAKE, 2, 64, 64, 64, 100, FAKE, FAKE, None, None, 1, 0, None) == 1         # stride < rows*ld
+    assert b(FAKE, 0, 64, 64, 64, 4096, FAKE, FAKE, None, None, 1, 0, None) == 0        # empty batch
+    assert b(FAKE, 2, 64, 64, 64, 4096, FAKE, FAKE, None, None, 1, 7, None) == 1        # bad format
+    f = L.mxq_gemm_bf16out_fmt
+    assert f(FAKE, FAKE, 2, FAKE, FAKE, 0, 64, 128, 64, 0, FAKE, 128, None) == 1       # bad format
+    assert f(FAKE, FAKE, 1, FAKE, FAKE, 0, 64, 128, 48, 0, FAKE, 128, None) == 2       # K % 32
     c = L.mxq_quant_1x32_cols_grouped
     assert c(FAKE, 300, 64, 64, FAKE, 4, 384, FAKE, FAKE, 1, None) == 1   # capacity < rows + 127 G
     assert c(FAKE, 300, 64, 64, FAKE, 4, 1000, FAKE, FAKE, 1, None) == 2  # capacity % 128
