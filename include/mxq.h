@@ -208,6 +208,29 @@ mxq_status mxq_gemm_bf16out_fmt(const void* a_q, const void* a_s, mxq_fp8_format
                                 void* y, int64_t ldy, mxq_stream_t stream);
 
 /*
+ * Block-scaled FP8 GEMM whose epilogue also quantizes its output: the BF16
+ * result y (as mxq_gemm_bf16out computes it) is rounded to BF16 and each run
+ * of 32 consecutive columns of a row gets the 1x32 rceil E8M0 scale and E4M3
+ * payload, written straight from the accumulator registers.  This removes the
+ * HBM round trip of quantizing y in a separate pass (DeepSeek-V4 Ascend
+ * training write-up, "AutoFuse 收益分析": fused kernels keep intermediates on
+ * chip instead of re-reading HBM); the bytes equal those of
+ * mxq_quant_1x32_dual's row copy of y with the MMA-tiled layout.
+ *
+ * a_q, a_s, b_q, b_s, M, N, K, b_mn_major  as for mxq_gemm_bf16out (E4M3 x E4M3).
+ * y     optional bf16 [M, N], row stride ldy (ldy >= N, ldy % 8 == 0); NULL to
+ *       keep only the quantized output (ldy then ignored).
+ * y_q   u8 [M, N] E4M3 payload, row stride N (required, 16-byte aligned).
+ * y_s   u8 scales [M, N/32], MMA-tiled (mxq_scale_bytes(M, N, MXQ_SCALE_MMA_TILED)
+ *       bytes, padding rows and groups written as zero).
+ * Shapes: N % 32 == 0 (N % 128 == 0 when b_mn_major); K % 32 == 0 and K >= 32.
+ * M == 0 or N == 0 writes nothing.  Errors: as mxq_gemm_bf16out.
+ */
+mxq_status mxq_gemm_mxfp8out(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
+                             int64_t M, int64_t N, int64_t K, int b_mn_major,
+                             void* y, int64_t ldy, void* y_q, void* y_s, mxq_stream_t stream);
+
+/*
  * Grouped block-scaled GEMM for MoE experts (tutorial: "MoE 专家层 (Grouped
  * MM)"; RFC section 2.2: gate_up_proj and down_proj).  Tokens are already
  * sorted by expert.  For each expert g and row r with

@@ -216,6 +216,27 @@ mxq_status mxq_gemm_bf16out_fmt(const void* a_q, const void* a_s, mxq_fp8_format
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
+mxq_status mxq_gemm_mxfp8out(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
+                             int64_t M, int64_t N, int64_t K, int b_mn_major, void* y, int64_t ldy,
+                             void* y_q, void* y_s, mxq_stream_t stream) {
+    if (M < 0 || N < 0 || K < 0 || (b_mn_major != 0 && b_mn_major != 1)) return MXQ_ERR_INVALID_ARG;
+    if (K % 32 != 0 || K == 0 || N % 32 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (b_mn_major && N % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (M > (int64_t(1) << 31) - 128 || N > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - 128)
+        return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0) return MXQ_OK;
+    if (y && (ldy < N || ldy % 8 != 0 || !aligned16(y))) return MXQ_ERR_INVALID_ARG;
+    if (!a_q || !a_s || !b_q || !b_s || !y_q || !y_s) return MXQ_ERR_INVALID_ARG;
+    if (!aligned16(a_q) || !aligned16(a_s) || !aligned16(b_q) || !aligned16(b_s) || !aligned16(y_q) ||
+        !aligned16(y_s))
+        return MXQ_ERR_INVALID_ARG;
+    mxq::DeviceInfo dev;
+    mxq_status st = device_ok(&dev);
+    if (st != MXQ_OK) return st;
+    return from_cuda(mxq::launch_gemm_quant(dev, a_q, a_s, b_q, b_s, M, N, K, b_mn_major != 0, y, ldy, y_q,
+                                            y_s, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 mxq_status mxq_grouped_gemm(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
                             const int64_t* group_offsets, int32_t G, int64_t M_total, int64_t N,
                             int64_t K, void* y, int64_t ldy, mxq_stream_t stream) {

@@ -29,6 +29,7 @@
 
 #include "mxq_device.cuh"
 #include "mxq_internal.h"
+#include "mxq_quant_math.cuh"
 
 namespace mxq {
 namespace {
@@ -43,6 +44,7 @@ constexpr int kMaxGroups = 1024;
 constexpr int kDense = 0;         // y = A B^T
 constexpr int kGroupedRows = 1;   // rows of A split by expert, one B per expert (MoE fwd, dgrad)
 constexpr int kGroupedK = 2;      // contraction split by expert (MoE wgrad), y stacked per expert
+constexpr int kDenseQuant = 3;    // dense, epilogue also emits the 1x32 MXFP8 quantization of y
 
 struct GemmArgs {
     const uint8_t* a_s;      // A scales, MMA-tiled
@@ -55,6 +57,8 @@ struct GemmArgs {
     const int64_t* offsets;  // grouped: [G+1] on the device
     int G;
     uint32_t fmt_bits;       // operand formats in the instruction descriptor (0 = E4M3, E4M3)
+    uint8_t* yq;             // quantizing epilogue: E4M3 payload [M, N] (row stride N)
+    uint8_t* ys;             //   and its MMA-tiled scales [M, N/32]
     unsigned int* status;
     uint64_t wait_limit_ns;
 };
@@ -221,7 +225,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     sch.n_tiles = (p.N + BN - 1) / BN;
     sch.G = p.G;
     sch.num_kb = static_cast<int>((p.K + kBK - 1) / kBK);
-    if constexpr (kMode == kDense) {
+    if constexpr (kMode == kDense || kMode == kDenseQuant) {
         sch.m_tiles = (p.M + kBM - 1) / kBM;
         sch.total = sch.m_tiles * sch.n_tiles;
         sch.off = nullptr;
@@ -463,7 +467,58 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                     for (int j = 0; j < 32; ++j) v[c][j] = 0u;
             }
             const int64_t row = ti.m0 + 32 * quad + lane;
-            if (row >= ti.row_lo && row < ti.row_hi) {
+            if constexpr (kMode == kDenseQuant) {
+                // Round to BF16, then quantize each 32-column group of this row in
+                // registers (rceil E8M0 scale, E4M3 payload): the same bytes as
+                // quantizing the BF16 output, without its round trip through HBM.
+                const bool row_in = row < ti.row_hi;
+                const int64_t ngroups = p.N >> 5;
+                const int64_t g0 = (ti.n0 + half * 128) >> 5;    // a multiple of 4
+                uint32_t codes = 0u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int64_t n = ti.n0 + half * 128 + c * 32;
+                    const bool grp_ok = row_in && n < p.N;
+                    uint32_t b[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        b[i] = cvt_bf16x2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1]));
+                    if (grp_ok && p.y != nullptr) {
+                        uint4* yd = reinterpret_cast<uint4*>(p.y + row * p.ldy + n);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) yd[q] = make_uint4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+                    }
+                    uint32_t m2 = 0u;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) m2 = max_u16x2(m2, b[i] & 0x7FFF7FFFu);
+                    const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+                    uint32_t o[8];
+                    uint32_t code;
+                    if (m >= 0x7F80u) {  // NaN or Inf in the group
+                        code = 0xFFu;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) o[j] = nan_bytes4(b[2 * j], b[2 * j + 1]);
+                    } else {
+                        const int e = rceil_exponent<0>(m);
+                        const float sc = pow2_neg(e);
+                        code = static_cast<uint32_t>(e + 127);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            o[j] = cvt_fp8x2<0>(bf16_lo(b[2 * j]) * sc, bf16_hi(b[2 * j]) * sc) |
+                                   (cvt_fp8x2<0>(bf16_lo(b[2 * j + 1]) * sc, bf16_hi(b[2 * j + 1]) * sc) << 16);
+                    }
+                    if (grp_ok) {
+                        uint4* qd = reinterpret_cast<uint4*>(p.yq + row * p.N + n);
+                        qd[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                        qd[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                    codes |= (grp_ok ? code : 0u) << (8 * c);
+                }
+                // The 4 groups are 4 consecutive bytes of one tiled scale atom (zero
+                // where the row or group lies past the matrix: the layout's padding).
+                if (g0 < ((ngroups + 3) & ~static_cast<int64_t>(3)))
+                    *reinterpret_cast<uint32_t*>(p.ys + tiled_scale_offset(row, g0, ngroups)) = codes;
+            } else if (row >= ti.row_lo && row < ti.row_hi) {
                 uint16_t* yrow = p.y + (ti.y_row0 + row) * p.ldy;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -553,6 +608,37 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
     if (b_mn_major)
         return launch_t<kBN, kStages, true, kDense>(dev, ta, tb, args, tiles, stream);
     return launch_t<kBN, kStages, false, kDense>(dev, ta, tb, args, tiles, stream);
+}
+
+cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
+                              const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
+                              int64_t ldy, void* y_q, void* y_s, cudaStream_t stream) {
+    CUtensorMap ta, tb;
+    if (!make_tma_u8(&ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kBM))
+        return cudaErrorInvalidValue;
+    if (!b_mn_major) {
+        if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN))
+            return cudaErrorInvalidValue;
+    } else {
+        if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK))
+            return cudaErrorInvalidValue;
+    }
+    GemmArgs args{};
+    args.a_s = static_cast<const uint8_t*>(a_s);
+    args.b_s = static_cast<const uint8_t*>(b_s);
+    args.y = static_cast<uint16_t*>(y);
+    args.M = M; args.N = N; args.K = K; args.ldy = ldy;
+    args.k_atoms = (K + 127) / 128;
+    args.b_bands = (N + 127) / 128;
+    args.fmt_bits = 0;
+    args.yq = static_cast<uint8_t*>(y_q);
+    args.ys = static_cast<uint8_t*>(y_s);
+    args.status = dev.status;
+    args.wait_limit_ns = kDefaultWaitLimitNs;
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    if (b_mn_major)
+        return launch_t<kBN, kStages, true, kDenseQuant>(dev, ta, tb, args, tiles, stream);
+    return launch_t<kBN, kStages, false, kDenseQuant>(dev, ta, tb, args, tiles, stream);
 }
 
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,

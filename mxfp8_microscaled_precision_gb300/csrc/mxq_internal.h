@@ -55,6 +55,12 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
                         const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
                         int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream);
 
+// Dense GEMM whose epilogue also writes the 1x32 E4M3 quantization of the BF16
+// output (y may be null: quantized output only).
+cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
+                              const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
+                              int64_t ldy, void* y_q, void* y_s, cudaStream_t stream);
+
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
                                 const void* b_q, const void* b_s, const int64_t* offsets, int G,
                                 int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy,

@@ -28,6 +28,7 @@
 
 #include "mxq_device.cuh"
 #include "mxq_internal.h"
+#include "mxq_quant_math.cuh"
 
 namespace mxq {
 namespace {
@@ -40,47 +41,6 @@ constexpr int kTileBytes = kTile * kTile * 2;                   // 32 KB of BF16
 constexpr int kCtasPerSm = 3;                                   // ring kernels
 constexpr int kSmemBytes = kRing * kTileBytes + 1024 + 256;     // ring + alignment + barriers
 
-// E8M0 exponent of a finite, non-negative amax given as BF16 bits
-// (sign cleared): e = ceil(log2(amax/448)), clamped below at -127.
-// With amax = 1.m * 2^(E-127): amax/448 = (1.m/1.75) * 2^(E-135), and the
-// ceiling steps up exactly when the 7-bit mantissa exceeds 1.75 (m > 96).
-// Subnormal and zero amax (E == 0) fall below -127 and are clamped.
-//
-// Payload formats: kFmt 0 = E4M3 (max 448), 1 = E5M2 (max 57344 = 1.75 * 2^15,
-// so the same mantissa test with the exponent offset 142 instead of 135).
-template <int kFmt = 0>
-__device__ __forceinline__ int rceil_exponent(uint32_t amax_bits) {
-    const int E = static_cast<int>(amax_bits >> 7);
-    const int m = static_cast<int>(amax_bits & 0x7Fu);
-    const int e = E - (kFmt == 0 ? 135 : 142) + (m > 96 ? 1 : 0);
-    return e < -127 ? -127 : e;
-}
-
-template <int kFmt>
-__device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
-    return kFmt == 0 ? cvt_e4m3x2(lo, hi) : cvt_e5m2x2(lo, hi);
-}
-
-// 2^-e as a float for e in [-127, 120] (always a normal number).
-__device__ __forceinline__ float pow2_neg(int e) { return __int_as_float((127 - e) << 23); }
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Per-half unsigned maximum of two packed 16-bit pairs (one instruction).
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-// Largest |x| (as BF16 bits, sign cleared) of 8 BF16 values.
-__device__ __forceinline__ uint32_t amax8_bits(const uint4 v) {
-    const uint32_t m = max_u16x2(max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                                 max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-    return max(m & 0xFFFFu, m >> 16);
-}
-
 // Quantize 8 BF16 values (4 words) with scale 2^-e -> 8 FP8 bytes.
 template <int kFmt = 0>
 __device__ __forceinline__ uint2 quant8(const uint4 v, float sc) {
@@ -90,12 +50,6 @@ __device__ __forceinline__ uint2 quant8(const uint4 v, float sc) {
     o.y = cvt_fp8x2<kFmt>(bf16_lo(v.z) * sc, bf16_hi(v.z) * sc) |
           (cvt_fp8x2<kFmt>(bf16_lo(v.w) * sc, bf16_hi(v.w) * sc) << 16);
     return o;
-}
-
-// Payload of a group holding NaN or Inf: every byte 0x7F | sign.
-__device__ __forceinline__ uint32_t nan_bytes4(uint32_t w0, uint32_t w1) {
-    return 0x7F7F7F7Fu | ((w0 >> 8) & 0x80u) | ((w0 >> 16) & 0x8000u) | ((w1 << 8) & 0x800000u) |
-           (w1 & 0x80000000u);
 }
 
 __device__ __forceinline__ uint2 nan8(const uint4 v) {

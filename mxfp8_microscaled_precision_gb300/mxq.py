@@ -73,12 +73,13 @@ def lib() -> ctypes.CDLL:
         L.mxq_quant_32x32.argtypes = [P, I64, I64, I64, P, P, P, S, P]
         L.mxq_gemm_bf16out.argtypes = [P, P, P, P, I64, I64, I64, S, P, I64, P]
         L.mxq_grouped_gemm.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, I64, P]
+        L.mxq_gemm_mxfp8out.argtypes = [P, P, P, P, I64, I64, I64, S, P, I64, P, P, P]
         L.mxq_get_device_status.argtypes = []
         L.mxq_debug_wait_timeout.argtypes = [U32, P]
         for f in ("mxq_quant_1x32_dual", "mxq_quant_32x32", "mxq_gemm_bf16out",
                   "mxq_grouped_gemm", "mxq_get_device_status", "mxq_debug_wait_timeout",
                   "mxq_quant_1x32_dual_batched", "mxq_quant_1x32_cols_grouped",
-                  "mxq_grouped_gemm_wgrad", "mxq_gemm_bf16out_fmt"):
+                  "mxq_grouped_gemm_wgrad", "mxq_gemm_bf16out_fmt", "mxq_gemm_mxfp8out"):
             getattr(L, f).restype = S
         _lib = L
         return L
@@ -248,6 +249,24 @@ def gemm_fmt(a_q, a_s, a_fmt, b_q, b_s, b_fmt, M: int, N: int, K: int, b_mn_majo
                                       M, N, K, 1 if b_mn_major else 0, _ptr(out), out.stride(0), _stream()),
            "mxq_gemm_bf16out_fmt")
     return out
+
+
+def gemm_mxfp8out(a_q, a_s, b_q, b_s, M: int, N: int, K: int, b_mn_major: bool = False,
+                  want_bf16: bool = True, out=None):
+    """gemm whose epilogue also emits the 1x32 E4M3 quantization of its BF16
+    output (MMA-tiled scales).  Returns (y or None, y_q [M, N] u8, y_s u8)."""
+    dev = a_q.device
+    if out is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev) if want_bf16 else None
+        y_q = torch.empty((M, N), dtype=torch.uint8, device=dev)
+        y_s = torch.empty(scale_bytes(M, N, TILED), dtype=torch.uint8, device=dev)
+    else:
+        y, y_q, y_s = out
+    _check(lib().mxq_gemm_mxfp8out(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K,
+                                   1 if b_mn_major else 0, _ptr(y),
+                                   y.stride(0) if y is not None else 0, _ptr(y_q), _ptr(y_s), _stream()),
+           "mxq_gemm_mxfp8out")
+    return y, y_q, y_s
 
 
 def grouped_gemm(a_q, a_s, b_q, b_s, offsets: torch.Tensor, N: int, K: int, out=None):

@@ -110,6 +110,18 @@ def test_moe_backward_argument_errors(L):
     assert w(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 300, 1024, 128, 128, FAKE, 128, None) == 1   # G < 1
 
 
+def test_fused_quant_gemm_argument_errors(L):
+    g = L.mxq_gemm_mxfp8out
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 48, 64, 0, FAKE, 48, FAKE, FAKE, None) == 2    # N % 32
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 64, 0, 0, FAKE, 64, FAKE, FAKE, None) == 2     # K == 0
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 96, 64, 1, FAKE, 96, FAKE, FAKE, None) == 2    # MN-major N % 128
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 64, 64, 0, FAKE, 64, None, FAKE, None) == 1    # no payload
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 64, 64, 0, FAKE, 64, FAKE, ODD, None) == 1     # misaligned scales
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 64, 64, 0, FAKE, 60, FAKE, FAKE, None) == 1    # ldy < N
+    assert g(FAKE, FAKE, FAKE, FAKE, 0, 64, 64, 0, None, 0, None, None, None) == 0      # no rows
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 64, 64, 2, FAKE, 64, FAKE, FAKE, None) == 1    # bad flag
+
+
 def test_binding_raises_value_error(L):
     from mxfp8_microscaled_precision_gb300 import mxq
     with pytest.raises(ValueError):
