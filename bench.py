@@ -345,6 +345,110 @@ class Weight32(Workload):
             f"extrapolated to the full step")
 
 
+class FsdpWeight(Workload):
+    """One fully sharded linear layer seen from rank 0 of `world` ranks (MindSpeed
+    RFC "Add MXFP8-32x32 quantization support to FSDP", section 3.3.2): quantize
+    the local weight shard straight into its all-gather payload, receive the other
+    ranks' payloads (device copies stand in for the collective on one GPU), rebuild
+    the full operands, then the forward and dgrad GEMMs of the 7168x7168 layer
+    with X and dY [4096, 7168] row-quantized.  recipe "mxfp8" gathers four tensors
+    per rank, "mxfp8-32x32" three."""
+
+    def __init__(self, recipe, dev=None, world=8):
+        import torch
+        from mxfp8_microscaled_precision_gb300 import mxq, workloads
+        self.recipe = recipe
+        self.name = "fsdp_" + recipe.replace("-", "_")
+        self.M, self.n, self.k, self.world = 4096, 7168, 7168, world
+        ns = self.n // world
+        d = workloads.weight_32x32(dev or "cpu")
+        self.inputs = {"W_shard": d["W"][:ns].contiguous(), "X": d["X"], "dY": d["dY"]}
+        if dev is None:
+            self.W_host = d["W"]
+            return
+        M, n, k = self.M, self.n, self.k
+        u8 = dict(dtype=torch.uint8, device=dev)
+        self.off, self.P = mxq.fsdp_payload_layout(recipe, n, k, world)
+        self.gathered = torch.zeros(world * self.P, **u8)
+        self.remote = torch.zeros((world - 1) * self.P, **u8)     # the other ranks' send buffers
+        for r in range(1, world):
+            mxq.fsdp_quant_shard(d["W"][r * ns:(r + 1) * ns], recipe, n, world,
+                                 self.remote[(r - 1) * self.P:r * self.P])
+        del d["W"]
+        dual = recipe == "mxfp8"
+        self.full = (torch.empty((n, k), **u8), torch.empty(mxq.scale_bytes(n, k), **u8),
+                     torch.empty((k, n), **u8) if dual else None, torch.empty(mxq.scale_bytes(k, n), **u8))
+        self.qx = (torch.empty((M, k), **u8), torch.empty(mxq.scale_bytes(M, k), **u8), None, None)
+        self.qg = (torch.empty((M, n), **u8), torch.empty(mxq.scale_bytes(M, n), **u8), None, None)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.y, self.dx = torch.empty((M, n), **bf), torch.empty((M, k), **bf)
+        self.outputs = [self.y, self.dx]
+        torch.cuda.synchronize()
+
+    @property
+    def gemm_flops(self):
+        return 2 * 2 * self.M * self.n * self.k
+
+    def extra(self):
+        n, k, W, P = self.n, self.k, self.world, self.P
+        return {"fsdp": {"recipe": self.recipe, "world": W, "tensors_per_rank": sum(o >= 0 for o in self.off),
+                         "payload_bytes_per_rank": P, "gathered_bytes": W * P,
+                         "bytes_per_weight_element": round(W * P / (n * k), 5),
+                         "collective": "stood in for by one device copy of the other ranks' payloads"}}
+
+    def kernels(self):
+        from mxfp8_microscaled_precision_gb300 import mxq
+        M, n, k, W, P, i = self.M, self.n, self.k, self.world, self.P, self.inputs
+        ns = n // W
+        q, sf, qc, sb = self.full
+        dual = self.recipe == "mxfp8"
+        own = self.gathered[:P]
+        if dual:
+            dgrad = ("gemm_dgrad", "gemm", 2 * M * n * k,
+                     lambda: mxq.gemm(self.qg[0], self.qg[1], qc, sb, M, k, n, out=self.dx))
+        else:
+            dgrad = ("gemm_dgrad_mn", "gemm", 2 * M * n * k,
+                     lambda: mxq.gemm(self.qg[0], self.qg[1], q, sb, M, k, n, b_mn_major=True, out=self.dx))
+        return [
+            ("quant_W_shard", "quant", _dual_bytes(ns, k) if dual else _blk_bytes(ns, k),
+             lambda: mxq.fsdp_quant_shard(i["W_shard"], self.recipe, n, W, own)),
+            ("allgather_copy", "collective", 2 * (W - 1) * P, lambda: self.gathered[P:].copy_(self.remote)),
+            ("fsdp_unpack", "copy", 2 * W * P,
+             lambda: mxq.fsdp_unpack(self.recipe, self.gathered, n, k, W, out=self.full)),
+            ("quant_X_row", "quant", _row_bytes(M, k), lambda: mxq.quant_1x32_dual(i["X"], col=False, out=self.qx)),
+            ("quant_dY_row", "quant", _row_bytes(M, n), lambda: mxq.quant_1x32_dual(i["dY"], col=False, out=self.qg)),
+            ("gemm_fwd", "gemm", 2 * M * n * k, lambda: mxq.gemm(self.qx[0], self.qx[1], q, sf, M, n, k, out=self.y)),
+            dgrad,
+        ]
+
+    def cpu_sample(self, budget_s):
+        from oracle import oracle
+        import numpy as np
+        i = self.inputs
+        w = _host_bits(i["W_shard"][:256])
+        t0 = time.perf_counter()
+        if self.recipe == "mxfp8":
+            oracle.quant_dual(w)
+        else:
+            oracle.quant_32x32(w)
+        tq = (time.perf_counter() - t0) / w.size
+        xq, xs = oracle.quant_rows(_host_bits(i["X"][:64]))
+        a = oracle.dequant_rows(xq, xs)
+        wq, ws = oracle.quant_rows(_host_bits(self.W_host))
+        b = oracle.dequant_rows(wq, ws)
+        rows, t_g = 0, 0.0
+        while t_g < budget_s and rows < a.shape[0]:
+            t0 = time.perf_counter()
+            oracle.gemm(a, b, rows=np.array([rows], dtype=np.int64))
+            t_g += time.perf_counter() - t0
+            rows += 1
+        tg = t_g / (2.0 * rows * self.n * self.k)
+        elems = self.n * self.k // self.world + self.M * self.k + self.M * self.n
+        return tq * elems + tg * self.gemm_flops, (
+            f"oracle {self.recipe} quant of 256 shard rows and FP64 GEMM of {rows} rows x {self.n} x {self.k}; "
+            f"extrapolated to the full step (the gather and unpack move bytes only and are not timed on the CPU)")
+
+
 class MoE(Workload):
     def __init__(self, dev=None):
         import torch
@@ -560,16 +664,19 @@ def make_workload(name, dev=None):
         return MoE(dev)
     if name == "moe_train":
         return MoETrain(dev)
+    if name in ("fsdp_mxfp8", "fsdp_mxfp8_32x32"):
+        return FsdpWeight("mxfp8" if name == "fsdp_mxfp8" else "mxfp8-32x32", dev)
     raise SystemExit(f"unknown workload {name}")
 
 
 WORKLOAD_NAMES = ["linear_train", "linear_fwd_small", "weight_32x32", "moe_grouped", "moe_train",
+                  "fsdp_mxfp8", "fsdp_mxfp8_32x32",
                   "sweep_4096", "sweep_7168", "sweep_16384"]
 
 
 def workload_config(w):
     cfg = {"workload": w.name}
-    for k in ("M", "N", "K", "n", "k", "G", "H", "I", "Mt", "cap"):
+    for k in ("M", "N", "K", "n", "k", "G", "H", "I", "Mt", "cap", "world", "recipe"):
         if hasattr(w, k):
             cfg[k] = getattr(w, k)
     cfg["l2"] = "flushed between timed steps (256 MB device write, outside the timed intervals)"
@@ -654,6 +761,13 @@ def run_gpu(args):
     roofline_quant = {"bound": "hbm", "kernel": "quant kernels", "achieved": round(quant_gbs, 1),
                       "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
                       "peak_source": peaks["source"] + " copy bandwidth"}
+    other_hbm = {}
+    for j in range(nk):
+        if kern[j][1] not in ("gemm", "quant"):
+            gbs = kern[j][2] * args.steps / (sum(per_kernel[j]) / 1e3) / 1e9
+            other_hbm[kern[j][0]] = {"kind": kern[j][1], "bytes_per_launch": kern[j][2],
+                                     "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    own_launches = sum(1 for j in range(nk) if kern[j][1] != "collective")
 
     # ---- end to end through the public API, host buffers, copies inside the timed step
     e2e = None
@@ -701,8 +815,12 @@ def run_gpu(args):
                 "quant_tbs": round(quant_gbs / 1e3, 3), "quant_frac_hbm": round(quant_gbs / peaks["hbm_gbs"], 4),
                 "kernels_ms": {k: round(v, 5) for k, v in kernels_ms.items()},
                 "roofline": roofline, "roofline_quant": roofline_quant,
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": nk * args.steps, "clocks": clocks,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": own_launches * args.steps, "clocks": clocks,
                 "impl": "mxq"}
+        if other_hbm:
+            line["hbm_kernels"] = other_hbm
+        if hasattr(w, "extra"):
+            line.update(w.extra())
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -231,6 +231,56 @@ mxq_status mxq_gemm_mxfp8out(const void* a_q, const void* a_s, const void* b_q, 
                              void* y, int64_t ldy, void* y_q, void* y_s, mxq_stream_t stream);
 
 /*
+ * Pre-quantized weight all-gather for fully sharded data parallelism
+ * (MindSpeed RFC "Add MXFP8-32x32 quantization support to FSDP", section
+ * 3.3.2: before the all-gather each rank quantizes its shard; the mxfp8
+ * recipe gathers (weight_fwd, scale_fwd, weight_bwd, scale_bwd), the
+ * mxfp8-32x32 recipe (weight, scale_fwd, scale_bwd), one weight tensor fewer;
+ * after the gather the full tensors are rebuilt).
+ *
+ * A weight W [n, k] (bf16) is split into `world` shards of n_s = n / world
+ * consecutive rows.  Rank r's payload is one contiguous byte buffer holding
+ * its shard's quantized tensors at the offsets mxq_fsdp_payload_layout gives:
+ *   MXQ_FSDP_1X32_DUAL  offsets[0] row payload [n_s, k]
+ *                       offsets[1] row scales  tiled [n_s, k/32]
+ *                       offsets[2] col payload [k, n_s]
+ *                       offsets[3] col scales  tiled [k, n_s/32]
+ *                       (= mxq_quant_1x32_dual of the shard, MMA-tiled)
+ *   MXQ_FSDP_32X32      offsets[0] payload [n_s, k], offsets[1] s_fwd tiled
+ *                       [n_s, k/32], offsets[2] = -1, offsets[3] s_bwd tiled
+ *                       [k, n_s/32]  (= mxq_quant_32x32 of the shard)
+ * so packing is the quantizer call itself with those output pointers.  The
+ * gathered buffer is the world payloads back to back (rank r at
+ * r * payload_bytes), as an all-gather into one buffer leaves them.
+ * Shapes: n % (128 * world) == 0 (no scale atom spans two ranks), k % 32 == 0.
+ */
+typedef enum {
+    MXQ_FSDP_1X32_DUAL = 0,
+    MXQ_FSDP_32X32 = 1
+} mxq_fsdp_recipe;
+
+/* Host only.  offsets: 4 host int64 slots (offsets[2] = -1 for 32x32);
+ * payload_bytes: one rank's payload size (a multiple of 512).  Returns
+ * MXQ_ERR_UNSUPPORTED_SHAPE for unsupported n, k, world, MXQ_ERR_INVALID_ARG
+ * for a bad recipe or NULL outputs. */
+mxq_status mxq_fsdp_payload_layout(mxq_fsdp_recipe recipe, int64_t n, int64_t k, int32_t world,
+                                   int64_t* offsets, int64_t* payload_bytes);
+
+/*
+ * Rebuilds the full-weight GEMM operands from the gathered buffer
+ * (world * payload_bytes bytes, device).  Outputs (device):
+ *   q_fwd  u8 [n, k]          row payload (32x32: the single payload)
+ *   s_fwd  u8 tiled [n, k/32] mxq_scale_bytes(n, k, MXQ_SCALE_MMA_TILED) bytes
+ *   q_bwd  u8 [k, n]          column payload (1x32 only; must be NULL for 32x32)
+ *   s_bwd  u8 tiled [k, n/32]
+ * The bytes equal those of quantizing the whole of W in one call.  One
+ * kernel, HBM-bound: reads and writes world * payload_bytes bytes.
+ */
+mxq_status mxq_fsdp_unpack(mxq_fsdp_recipe recipe, int64_t n, int64_t k, int32_t world,
+                           const void* gathered, void* q_fwd, void* s_fwd, void* q_bwd, void* s_bwd,
+                           mxq_stream_t stream);
+
+/*
  * Grouped block-scaled GEMM for MoE experts (tutorial: "MoE 专家层 (Grouped
  * MM)"; RFC section 2.2: gate_up_proj and down_proj).  Tokens are already
  * sorted by expert.  For each expert g and row r with

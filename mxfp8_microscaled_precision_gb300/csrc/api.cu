@@ -237,6 +237,35 @@ mxq_status mxq_gemm_mxfp8out(const void* a_q, const void* a_s, const void* b_q, 
                                             y_s, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+mxq_status mxq_fsdp_payload_layout(mxq_fsdp_recipe recipe, int64_t n, int64_t k, int32_t world,
+                                   int64_t* offsets, int64_t* payload_bytes) {
+    if ((recipe != MXQ_FSDP_1X32_DUAL && recipe != MXQ_FSDP_32X32) || !offsets || !payload_bytes)
+        return MXQ_ERR_INVALID_ARG;
+    if (world < 1 || n <= 0 || k <= 0 || n > (int64_t(1) << 31) || k > (int64_t(1) << 31))
+        return MXQ_ERR_UNSUPPORTED_SHAPE;
+    return mxq::fsdp_payload_layout(static_cast<int>(recipe), n, k, world, offsets, payload_bytes)
+               ? MXQ_OK
+               : MXQ_ERR_UNSUPPORTED_SHAPE;
+}
+
+mxq_status mxq_fsdp_unpack(mxq_fsdp_recipe recipe, int64_t n, int64_t k, int32_t world, const void* gathered,
+                           void* q_fwd, void* s_fwd, void* q_bwd, void* s_bwd, mxq_stream_t stream) {
+    int64_t off[4], payload = 0;
+    const mxq_status lay = mxq_fsdp_payload_layout(recipe, n, k, world, off, &payload);
+    if (lay != MXQ_OK) return lay;
+    if (static_cast<int64_t>(world) * payload / 16 >= (int64_t(1) << 31)) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    const bool dual = recipe == MXQ_FSDP_1X32_DUAL;
+    if (!gathered || !q_fwd || !s_fwd || !s_bwd || (dual != (q_bwd != nullptr))) return MXQ_ERR_INVALID_ARG;
+    if (!aligned16(gathered) || !aligned16(q_fwd) || !aligned16(s_fwd) || !aligned16(s_bwd) ||
+        (dual && !aligned16(q_bwd)))
+        return MXQ_ERR_INVALID_ARG;
+    mxq::DeviceInfo dev;
+    mxq_status st = device_ok(&dev);
+    if (st != MXQ_OK) return st;
+    return from_cuda(mxq::launch_fsdp_unpack(dev, static_cast<int>(recipe), n, k, world, gathered, q_fwd, s_fwd,
+                                             q_bwd, s_bwd, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 mxq_status mxq_grouped_gemm(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
                             const int64_t* group_offsets, int32_t G, int64_t M_total, int64_t N,
                             int64_t K, void* y, int64_t ldy, mxq_stream_t stream) {

@@ -61,6 +61,15 @@ cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void
                               const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
                               int64_t ldy, void* y_q, void* y_s, cudaStream_t stream);
 
+// All-gather payload of a pre-quantized weight shard: tensor byte offsets in
+// one rank's payload (offsets[2] = -1 for the 32x32 recipe) and its size.
+// False when the shape is not supported (n % (128*world), k % 32).
+bool fsdp_payload_layout(int recipe, int64_t n, int64_t k, int32_t world, int64_t offsets[4],
+                         int64_t* payload_bytes);
+cudaError_t launch_fsdp_unpack(const DeviceInfo& dev, int recipe, int64_t n, int64_t k, int32_t world,
+                               const void* gathered, void* q_fwd, void* s_fwd, void* q_bwd, void* s_bwd,
+                               cudaStream_t stream);
+
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
                                 const void* b_q, const void* b_s, const int64_t* offsets, int G,
                                 int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy,

@@ -74,12 +74,15 @@ def lib() -> ctypes.CDLL:
         L.mxq_gemm_bf16out.argtypes = [P, P, P, P, I64, I64, I64, S, P, I64, P]
         L.mxq_grouped_gemm.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, I64, P]
         L.mxq_gemm_mxfp8out.argtypes = [P, P, P, P, I64, I64, I64, S, P, I64, P, P, P]
+        L.mxq_fsdp_payload_layout.argtypes = [S, I64, I64, I32, ctypes.POINTER(I64), ctypes.POINTER(I64)]
+        L.mxq_fsdp_unpack.argtypes = [S, I64, I64, I32, P, P, P, P, P, P]
         L.mxq_get_device_status.argtypes = []
         L.mxq_debug_wait_timeout.argtypes = [U32, P]
         for f in ("mxq_quant_1x32_dual", "mxq_quant_32x32", "mxq_gemm_bf16out",
                   "mxq_grouped_gemm", "mxq_get_device_status", "mxq_debug_wait_timeout",
                   "mxq_quant_1x32_dual_batched", "mxq_quant_1x32_cols_grouped",
-                  "mxq_grouped_gemm_wgrad", "mxq_gemm_bf16out_fmt", "mxq_gemm_mxfp8out"):
+                  "mxq_grouped_gemm_wgrad", "mxq_gemm_bf16out_fmt", "mxq_gemm_mxfp8out",
+                  "mxq_fsdp_payload_layout", "mxq_fsdp_unpack"):
             getattr(L, f).restype = S
         _lib = L
         return L
@@ -267,6 +270,65 @@ def gemm_mxfp8out(a_q, a_s, b_q, b_s, M: int, N: int, K: int, b_mn_major: bool =
                                    y.stride(0) if y is not None else 0, _ptr(y_q), _ptr(y_s), _stream()),
            "mxq_gemm_mxfp8out")
     return y, y_q, y_s
+
+
+FSDP_1X32_DUAL, FSDP_32X32 = 0, 1
+_RECIPES = {"mxfp8": FSDP_1X32_DUAL, "mxfp8-32x32": FSDP_32X32,
+            FSDP_1X32_DUAL: FSDP_1X32_DUAL, FSDP_32X32: FSDP_32X32}
+
+
+def _recipe(r) -> int:
+    if r not in _RECIPES:
+        raise ValueError(f"unknown recipe {r!r}")
+    return _RECIPES[r]
+
+
+def fsdp_payload_layout(recipe, n: int, k: int, world: int):
+    """(offsets [4] (offsets[2] = -1 for 32x32), payload_bytes) of one rank's
+    all-gather payload for a weight [n, k] split into `world` row shards."""
+    off = (ctypes.c_int64 * 4)()
+    size = ctypes.c_int64()
+    _check(lib().mxq_fsdp_payload_layout(_recipe(recipe), n, k, world, off, ctypes.byref(size)),
+           "mxq_fsdp_payload_layout")
+    return tuple(int(v) for v in off), int(size.value)
+
+
+def fsdp_quant_shard(w_shard: torch.Tensor, recipe, n: int, world: int, payload: torch.Tensor):
+    """Quantizes a rank's weight shard [n/world, k] straight into its payload
+    (a uint8 CUDA tensor of payload_bytes): the quantizer's outputs are views
+    at the layout's offsets, so the payload needs no separate packing."""
+    ns, k = w_shard.shape
+    off, size = fsdp_payload_layout(recipe, n, k, world)
+    if ns * world != n or payload.dtype != torch.uint8 or payload.numel() < size:
+        raise ValueError("shard or payload does not match the layout")
+
+    def view(o, nbytes, shape=None):
+        t = payload[o:o + nbytes]
+        return t.view(shape) if shape else t
+
+    sf, sb = scale_bytes(ns, k, TILED), scale_bytes(k, ns, TILED)
+    if _recipe(recipe) == FSDP_1X32_DUAL:
+        quant_1x32_dual(w_shard, out=(view(off[0], ns * k, (ns, k)), view(off[1], sf),
+                                      view(off[2], ns * k, (k, ns)), view(off[3], sb)))
+    else:
+        quant_32x32(w_shard, out=(view(off[0], ns * k, (ns, k)), view(off[1], sf), view(off[3], sb)))
+    return payload
+
+
+def fsdp_unpack(recipe, gathered: torch.Tensor, n: int, k: int, world: int, out=None):
+    """Full-weight operands from the gathered payloads: (q_fwd [n,k], s_fwd,
+    q_bwd [k,n] or None for 32x32, s_bwd), tiled scales."""
+    dual = _recipe(recipe) == FSDP_1X32_DUAL
+    dev = gathered.device
+    if out is None:
+        out = (torch.empty((n, k), dtype=torch.uint8, device=dev),
+               torch.empty(scale_bytes(n, k, TILED), dtype=torch.uint8, device=dev),
+               torch.empty((k, n), dtype=torch.uint8, device=dev) if dual else None,
+               torch.empty(scale_bytes(k, n, TILED), dtype=torch.uint8, device=dev))
+    q_fwd, s_fwd, q_bwd, s_bwd = out
+    _check(lib().mxq_fsdp_unpack(_recipe(recipe), n, k, world, _ptr(gathered), _ptr(q_fwd), _ptr(s_fwd),
+                                 _ptr(q_bwd), _ptr(s_bwd), _stream()), "mxq_fsdp_unpack")
+    return out
 
 
 def grouped_gemm(a_q, a_s, b_q, b_s, offsets: torch.Tensor, N: int, K: int, out=None):

@@ -122,6 +122,45 @@ def test_fused_quant_gemm_argument_errors(L):
     assert g(FAKE, FAKE, FAKE, FAKE, 64, 64, 64, 2, FAKE, 64, FAKE, FAKE, None) == 1    # bad flag
 
 
+def _layout(L, recipe, n, k, world):
+    off = (ctypes.c_int64 * 4)()
+    size = ctypes.c_int64()
+    st = L.mxq_fsdp_payload_layout(recipe, n, k, world, off, ctypes.byref(size))
+    return st, list(off), size.value
+
+
+@pytest.mark.parametrize("n,k,world", [(7168, 7168, 8), (1024, 320, 8), (4096, 4096, 1), (512, 96, 2)])
+def test_fsdp_payload_layout(L, n, k, world):
+    """One rank's all-gather payload: its shard's tensors back to back, 4 of
+    them for mxfp8 and 3 for mxfp8-32x32 (the counts the RFC states), the
+    32x32 payload smaller by exactly one shard payload."""
+    import json
+    facts = json.load(open(os.path.join(ROOT, "tests", "golden", "page_facts.json")))["allgather_tensor_count"]
+    ns = n // world
+    sf, sb = L.mxq_scale_bytes(ns, k, 1), L.mxq_scale_bytes(k, ns, 1)
+    st, off, size = _layout(L, 0, n, k, world)
+    assert st == 0 and off == [0, ns * k, ns * k + sf, 2 * ns * k + sf] and size == 2 * ns * k + sf + sb
+    assert sum(o >= 0 for o in off) == facts["value"]["mxfp8"]
+    st, off32, size32 = _layout(L, 1, n, k, world)
+    assert st == 0 and off32 == [0, ns * k, -1, ns * k + sf] and size32 == ns * k + sf + sb
+    assert sum(o >= 0 for o in off32) == facts["value"]["mxfp8-32x32"]
+    assert size - size32 == ns * k
+    assert all(o % 512 == 0 for o in off + off32 if o >= 0) and size % 512 == 0
+
+
+def test_fsdp_argument_errors(L):
+    assert _layout(L, 0, 1000, 64, 1)[0] == 2           # n % 128
+    assert _layout(L, 0, 1024, 64, 16)[0] == 2          # n % (128 world)
+    assert _layout(L, 0, 1024, 48, 1)[0] == 2           # k % 32
+    assert _layout(L, 0, 1024, 64, 0)[0] == 2           # world < 1
+    assert _layout(L, 3, 1024, 64, 1)[0] == 1           # recipe
+    u = L.mxq_fsdp_unpack
+    assert u(1, 1024, 64, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1    # 32x32 takes no q_bwd
+    assert u(0, 1024, 64, 2, FAKE, FAKE, FAKE, None, FAKE, None) == 1    # 1x32 needs q_bwd
+    assert u(0, 1024, 64, 2, ODD, FAKE, FAKE, FAKE, FAKE, None) == 1     # misaligned source
+    assert u(0, 1024, 64, 3, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 2    # shard not 128-aligned
+
+
 def test_binding_raises_value_error(L):
     from mxfp8_microscaled_precision_gb300 import mxq
     with pytest.raises(ValueError):
