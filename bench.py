@@ -40,10 +40,9 @@ METRIC = "MXFP8 GEMM TFLOP/s (% dense MXFP8 peak); quantizer TB/s (% HBM), 1 GB3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 L2_FLUSH_BYTES = 256 << 20   # larger than the 129 MB L2
-# DRAM bytes (read + write) of one GEMM launch, from an ncu capture of the current
-# kernel (profiles/gemm_mxf8_kernel_linear_train.md); None where not captured for
-# the kernel as it stands.
-GEMM_TRAFFIC_BYTES = {}
+# DRAM bytes (read + write) of one GEMM launch (the forward GEMM of the step), from
+# an ncu --set full capture of the kernel as it stands; None where not captured.
+GEMM_TRAFFIC_BYTES = {"linear_train": 76926464}
 
 
 def load_peaks():
