@@ -20,6 +20,12 @@
 //   warps 2-5   epilogue: tcgen05.ld of the FP32 accumulator, RNE to BF16,
 //               16-byte global stores; releases the accumulator so the MMA
 //               warp proceeds with the next tile meanwhile.
+// Dense modes run in clusters of kCM CTAs along M: the kCM CTAs of a cluster
+// compute vertically adjacent tiles that share one B tile, and each loads 1/kCM
+// of it with a TMA multicast into all of their shared memories (L2 reads of B
+// divided by kCM).  A slot is refilled only after every CTA of the cluster has
+// consumed it: each MMA warp's commit arrives on the empty barrier of all of
+// them.
 // Every mbarrier wait is bounded (see mxq_device.cuh).
 
 #include <cuda.h>
@@ -39,6 +45,10 @@ constexpr int kBK = 128;          // K elements (= bytes) per pipeline stage
 constexpr int kUmmaK = 32;        // K of one MMA instruction (FP8)
 constexpr int kRasterBand = 8;    // m-tiles per raster band (L2 reuse of B)
 constexpr int kMaxGroups = 1024;
+#ifndef MXQ_GEMM_CLUSTER_M
+#define MXQ_GEMM_CLUSTER_M 2
+#endif
+constexpr int kClusterM = MXQ_GEMM_CLUSTER_M;   // CTAs per cluster in the dense modes (1, 2 or 4)
 
 // Kernel modes.
 constexpr int kDense = 0;         // y = A B^T
@@ -126,8 +136,10 @@ struct Schedule {
     int G;
 };
 
-template <int BN, int kMode>
-__device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs& p, int64_t t) {
+// t indexes cluster tiles (kCM vertically adjacent m-tiles x one n-tile);
+// `rank` picks this CTA's m-tile in it (m_tiles counts cluster rows here).
+template <int BN, int kMode, int kCM>
+__device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs& p, int64_t t, int rank) {
     TileInfo ti;
     ti.kb0 = 0;
     ti.nkb = s.num_kb;
@@ -139,11 +151,12 @@ __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs&
             g = t / per;
             t -= g * per;
         }
-        const int64_t per_band = static_cast<int64_t>(kRasterBand) * s.n_tiles;
+        constexpr int kBand = kRasterBand / kCM > 0 ? kRasterBand / kCM : 1;
+        const int64_t per_band = static_cast<int64_t>(kBand) * s.n_tiles;
         const int64_t band = t / per_band, within = t - band * per_band;
-        const int64_t mb = band * kRasterBand;
-        const int64_t bh = min(static_cast<int64_t>(kRasterBand), s.m_tiles - mb);
-        const int64_t m_blk = mb + within % bh, n_blk = within / bh;
+        const int64_t mb = band * kBand;
+        const int64_t bh = min(static_cast<int64_t>(kBand), s.m_tiles - mb);
+        const int64_t m_blk = (mb + within % bh) * kCM + rank, n_blk = within / bh;
         ti.m0 = m_blk * kBM;
         ti.n0 = n_blk * BN;
         ti.row_lo = ti.m0;
@@ -178,12 +191,17 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
     return mbar_try_wait(bar, parity) || mbar_wait(bar, parity, g);
 }
 
-template <int BN, int STAGES, bool kMnMajor, int kMode>
+template <int BN, int STAGES, bool kMnMajor, int kMode, int kCM>
 __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tma_a,
                      const __grid_constant__ CUtensorMap tma_b, const GemmArgs p) {
     using L = Cfg<BN, STAGES>;
     constexpr int kAcc = L::kAccStages;
+    static_assert(kCM == 1 || ((kMode == kDense || kMode == kDenseQuant) && BN == 256 && (kCM == 2 || kCM == 4)),
+                  "clusters: dense modes, 256-column tiles, 2 or 4 CTAs");
+    constexpr uint16_t kMask = static_cast<uint16_t>((1u << kCM) - 1u);
+    const int rank = kCM > 1 ? static_cast<int>(blockIdx.x % kCM) : 0;   // rank in the cluster
+    const int64_t cid = blockIdx.x / kCM, ncl = gridDim.x / kCM;          // cluster id, clusters
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -204,7 +222,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), kCM);   // one commit from each CTA of the cluster
         }
         for (int a = 0; a < kAcc; ++a) {
             mbar_init(tfull_bar(a), 1);
@@ -226,7 +244,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     sch.G = p.G;
     sch.num_kb = static_cast<int>((p.K + kBK - 1) / kBK);
     if constexpr (kMode == kDense || kMode == kDenseQuant) {
-        sch.m_tiles = (p.M + kBM - 1) / kBM;
+        sch.m_tiles = ((p.M + kBM - 1) / kBM + kCM - 1) / kCM;   // cluster rows
         sch.total = sch.m_tiles * sch.n_tiles;
         sch.off = nullptr;
         sch.prefix = nullptr;
@@ -276,6 +294,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (kCM > 1) cluster_sync();   // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemSlot);
     if constexpr (kMode == kGroupedRows) sch.total = sch.prefix[p.G];
@@ -292,14 +311,17 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             const uint32_t full0 = full_bar(0), empty0 = empty_bar(0);
-            for (int64_t t = blockIdx.x; t < sch.total && !*abort_flag; t += gridDim.x) {
-                const TileInfo ti = tile_info<BN, kMode>(sch, p, t);
+            for (int64_t t = cid; t < sch.total && !*abort_flag; t += ncl) {
+                const TileInfo ti = tile_info<BN, kMode, kCM>(sch, p, t, rank);
                 const int64_t b_band0 = ti.b_row / 128;
                 int sfb_atoms = 0;
 #pragma unroll
                 for (int j = 0; j < L::kSfbAtoms; ++j)
                     if (b_band0 + j < p.b_bands) ++sfb_atoms;
-                const uint32_t bytes = L::kABytes + L::kBBytes + 512u + 512u * sfb_atoms;
+                // A cluster's last tile row may lie wholly below M: its A box reads the
+                // fill value, its scale atoms do not exist and are not loaded.
+                const bool sfa_ok = ti.m0 < p.M || kCM == 1;
+                const uint32_t bytes = L::kABytes + L::kBBytes + (sfa_ok ? 512u : 0u) + 512u * sfb_atoms;
                 const uint8_t* sfa_src = p.a_s + ((ti.m0 / 128) * p.k_atoms + ti.kb0) * 512;
                 const uint8_t* sfb_src = p.b_s + (b_band0 * p.k_atoms + ti.kb0) * 512;
                 const int64_t sfb_band_stride = p.k_atoms * 512;
@@ -313,7 +335,19 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                     const uint32_t sb = sbase + L::kOffB + stage * L::kBBytes;
                     const int32_t kx = static_cast<int32_t>((ti.kb0 + kb) * kBK);
                     tma_load_2d(sa, &tma_a, kx, ma, fb);
-                    if constexpr (!kMnMajor) {
+                    if constexpr (kCM > 1) {
+                        // This CTA's 1/kCM of the shared B tile, to every CTA of the cluster.
+                        if constexpr (!kMnMajor) {
+                            constexpr int kRows = BN / kCM;
+                            tma_load_2d_multicast(sb + rank * kRows * kBK, &tma_b, kx, nb + rank * kRows, fb, kMask);
+                        } else {
+                            constexpr int kSplit = kCM / (BN / 128);     // K-row pieces per 128-column chunk
+                            constexpr int kKRows = kBK / kSplit;
+                            const int j = rank / kSplit, kr = (rank % kSplit) * kKRows;
+                            tma_load_2d_multicast(sb + j * 128 * kBK + kr * 128, &tma_b, nb + 128 * j, kx + kr, fb,
+                                                  kMask);
+                        }
+                    } else if constexpr (!kMnMajor) {
                         tma_load_2d(sb, &tma_b, kx, nb, fb);
                     } else {
                         // B stored [K, N]: boxes of 128 N-bytes x 128 K-rows, one per 128 columns.
@@ -321,7 +355,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                         for (int j = 0; j < BN / 128; ++j)
                             tma_load_2d(sb + j * 128 * kBK, &tma_b, nb + 128 * j, kx, fb);
                     }
-                    bulk_load(sbase + L::kOffSfa + stage * 512, sfa_src + kb * 512, 512u, fb);
+                    if (sfa_ok) bulk_load(sbase + L::kOffSfa + stage * 512, sfa_src + kb * 512, 512u, fb);
                     for (int j = 0; j < sfb_atoms; ++j)
                         bulk_load(sbase + L::kOffSfb + (stage * L::kSfbAtoms + j) * 512,
                                   sfb_src + j * sfb_band_stride + kb * 512, 512u, fb);
@@ -361,10 +395,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             constexpr int kCpBatch = L::kCpBatch;
             int64_t g_total = 0;   // stages this CTA consumes
             if constexpr (kMode == kGroupedK) {
-                for (int64_t t = blockIdx.x; t < sch.total; t += gridDim.x)
-                    g_total += tile_info<BN, kMode>(sch, p, t).nkb;
+                for (int64_t t = cid; t < sch.total; t += ncl)
+                    g_total += tile_info<BN, kMode, kCM>(sch, p, t, rank).nkb;
             } else {
-                const int64_t my_tiles = blockIdx.x < sch.total ? (sch.total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+                const int64_t my_tiles = cid < sch.total ? (sch.total - cid + ncl - 1) / ncl : 0;
                 g_total = my_tiles * sch.num_kb;
             }
             int64_t g = 0;
@@ -373,11 +407,11 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < sch.total && ok; t += gridDim.x) {
+            for (int64_t t = cid; t < sch.total && ok; t += ncl) {
                 if (!wait_phase(tempty_bar(acc), acc_phase ^ 1u, guard)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                const int nkb = kMode == kGroupedK ? tile_info<BN, kMode>(sch, p, t).nkb : sch.num_kb;
+                const int nkb = kMode == kGroupedK ? tile_info<BN, kMode, kCM>(sch, p, t, rank).nkb : sch.num_kb;
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
                     if (g % kCpBatch == 0) {
                         const int nb = static_cast<int>(min(static_cast<int64_t>(kCpBatch), g_total - g));
@@ -417,7 +451,9 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                                         make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k) | p.fmt_bits, sfa_t, sfb_t,
                                         (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    tc_commit(empty_bar(stage));  // frees the slot once these MMAs are done
+                    // frees the slot (in every CTA of the cluster) once these MMAs are done
+                    if constexpr (kCM > 1) tc_commit_multicast(empty_bar(stage), kMask);
+                    else tc_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
@@ -439,8 +475,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
         const int half = (warp - 2) >> 2;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int64_t t = blockIdx.x; t < sch.total; t += gridDim.x) {
-            const TileInfo ti = tile_info<BN, kMode>(sch, p, t);
+        for (int64_t t = cid; t < sch.total; t += ncl) {
+            const TileInfo ti = tile_info<BN, kMode, kCM>(sch, p, t, rank);
             // One lane waits; the warp follows its verdict, so the .sync.aligned
             // tensor-memory loads below always run with the full warp.
             int ok = 1;
@@ -516,7 +552,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                 }
                 // The 4 groups are 4 consecutive bytes of one tiled scale atom (zero
                 // where the row or group lies past the matrix: the layout's padding).
-                if (g0 < ((ngroups + 3) & ~static_cast<int64_t>(3)))
+                if (ti.m0 < p.M && g0 < ((ngroups + 3) & ~static_cast<int64_t>(3)))
                     *reinterpret_cast<uint32_t*>(p.ys + tiled_scale_offset(row, g0, ngroups)) = codes;
             } else if (row >= ti.row_lo && row < ti.row_hi) {
                 uint16_t* yrow = p.y + (ti.y_row0 + row) * p.ldy;
@@ -542,6 +578,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     // ---- teardown -----------------------------------------------------------
     tc_fence_before();
     __syncthreads();
+    // No CTA leaves while a peer may still write its shared memory or barriers.
+    if constexpr (kCM > 1) cluster_sync();
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
@@ -555,26 +593,67 @@ bool make_tma_u8(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
     return encode_tensor_map_2d(map, ptr, false, cols, rows, cols, 128u, box_rows, true);
 }
 
-template <int BN, int STAGES, bool kMnMajor, int kMode>
+template <int BN, int STAGES, bool kMnMajor, int kMode, int kCM = 1>
 cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& ta, const CUtensorMap& tb,
                      const GemmArgs& args, int64_t max_tiles, cudaStream_t stream) {
     using L = Cfg<BN, STAGES>;
-    auto kern = gemm_mxf8_kernel<BN, STAGES, kMnMajor, kMode>;
-    static thread_local int configured_device = -1;  // attribute set once per device and thread
+    auto kern = gemm_mxf8_kernel<BN, STAGES, kMnMajor, kMode, kCM>;
+    static thread_local int configured_device = -1;  // attributes set once per device and thread
+    static thread_local int max_clusters = 0;
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(L::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCM;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = kCM > 1 ? 1 : 0;
     if (configured_device != dev.device) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
         if (e != cudaSuccess) return e;
+        max_clusters = dev.sm_count;
+        if (kCM > 1) {
+            cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count / kCM * kCM), 1, 1);
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            if (e != cudaSuccess) return e;
+            if (n < 1) return cudaErrorInvalidConfiguration;
+            max_clusters = n;
+        }
         configured_device = dev.device;
     }
-    int64_t grid = dev.sm_count;
-    if (max_tiles >= 0 && max_tiles < grid) grid = max_tiles;
-    if (grid <= 0) return cudaSuccess;
-    kern<<<static_cast<unsigned>(grid), L::kThreads, L::kAlloc, stream>>>(ta, tb, args);
+    // max_tiles counts cluster tiles (one per cluster at a time); < 0: no limit.
+    int64_t clusters = max_clusters;
+    if (max_tiles >= 0 && max_tiles < clusters) clusters = max_tiles;
+    if (clusters <= 0) return cudaSuccess;
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * kCM), 1, 1);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, args);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 constexpr int kBN = 256;
 constexpr int kStages = 4;
+
+// Tensor maps of the dense modes.  A: boxes of 128 rows x 128 K-bytes.  B, K-major
+// [N, K]: boxes of 256/kClusterM rows (one CTA's share of the tile); MN-major [K, N]:
+// boxes of 128 N-bytes x (128 * 2 / kClusterM, at most 128) K-rows.
+bool make_dense_maps(CUtensorMap* ta, CUtensorMap* tb, const void* a_q, const void* b_q, int64_t M, int64_t N,
+                     int64_t K, bool b_mn_major) {
+    if (!make_tma_u8(ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kBM)) return false;
+    if (!b_mn_major)
+        return make_tma_u8(tb, b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN / kClusterM);
+    const uint32_t krows = kClusterM <= 2 ? kBK : kBK * 2 / kClusterM;
+    return make_tma_u8(tb, b_q, static_cast<uint64_t>(K), static_cast<uint64_t>(N), krows);
+}
+
+int64_t dense_cluster_tiles(int64_t M, int64_t N) {
+    const int64_t m_tiles = (M + kBM - 1) / kBM;
+    return (m_tiles + kClusterM - 1) / kClusterM * ((N + kBN - 1) / kBN);
+}
 
 }  // namespace
 
@@ -582,15 +661,7 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
                         const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
                         int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream) {
     CUtensorMap ta, tb;
-    if (!make_tma_u8(&ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kBM))
-        return cudaErrorInvalidValue;
-    if (!b_mn_major) {
-        if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN))
-            return cudaErrorInvalidValue;
-    } else {
-        if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK))
-            return cudaErrorInvalidValue;
-    }
+    if (!make_dense_maps(&ta, &tb, a_q, b_q, M, N, K, b_mn_major)) return cudaErrorInvalidValue;
     GemmArgs args{};
     args.a_s = static_cast<const uint8_t*>(a_s);
     args.b_s = static_cast<const uint8_t*>(b_s);
@@ -604,25 +675,17 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
     args.fmt_bits = (static_cast<uint32_t>(a_fmt) << 7) | (static_cast<uint32_t>(b_fmt) << 10);
     args.status = dev.status;
     args.wait_limit_ns = kDefaultWaitLimitNs;
-    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    const int64_t tiles = dense_cluster_tiles(M, N);
     if (b_mn_major)
-        return launch_t<kBN, kStages, true, kDense>(dev, ta, tb, args, tiles, stream);
-    return launch_t<kBN, kStages, false, kDense>(dev, ta, tb, args, tiles, stream);
+        return launch_t<kBN, kStages, true, kDense, kClusterM>(dev, ta, tb, args, tiles, stream);
+    return launch_t<kBN, kStages, false, kDense, kClusterM>(dev, ta, tb, args, tiles, stream);
 }
 
 cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
                               const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
                               int64_t ldy, void* y_q, void* y_s, cudaStream_t stream) {
     CUtensorMap ta, tb;
-    if (!make_tma_u8(&ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kBM))
-        return cudaErrorInvalidValue;
-    if (!b_mn_major) {
-        if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN))
-            return cudaErrorInvalidValue;
-    } else {
-        if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK))
-            return cudaErrorInvalidValue;
-    }
+    if (!make_dense_maps(&ta, &tb, a_q, b_q, M, N, K, b_mn_major)) return cudaErrorInvalidValue;
     GemmArgs args{};
     args.a_s = static_cast<const uint8_t*>(a_s);
     args.b_s = static_cast<const uint8_t*>(b_s);
@@ -635,10 +698,10 @@ cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void
     args.ys = static_cast<uint8_t*>(y_s);
     args.status = dev.status;
     args.wait_limit_ns = kDefaultWaitLimitNs;
-    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    const int64_t tiles = dense_cluster_tiles(M, N);
     if (b_mn_major)
-        return launch_t<kBN, kStages, true, kDenseQuant>(dev, ta, tb, args, tiles, stream);
-    return launch_t<kBN, kStages, false, kDenseQuant>(dev, ta, tb, args, tiles, stream);
+        return launch_t<kBN, kStages, true, kDenseQuant, kClusterM>(dev, ta, tb, args, tiles, stream);
+    return launch_t<kBN, kStages, false, kDenseQuant, kClusterM>(dev, ta, tb, args, tiles, stream);
 }
 
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
