@@ -20,12 +20,6 @@
 //   warps 2-5   epilogue: tcgen05.ld of the FP32 accumulator, RNE to BF16,
 //               16-byte global stores; releases the accumulator so the MMA
 //               warp proceeds with the next tile meanwhile.
-// Dense modes run in clusters of kCM CTAs along M: the kCM CTAs of a cluster
-// compute vertically adjacent tiles that share one B tile, and each loads 1/kCM
-// of it with a TMA multicast into all of their shared memories (L2 reads of B
-// divided by kCM).  A slot is refilled only after every CTA of the cluster has
-// consumed it: each MMA warp's commit arrives on the empty barrier of all of
-// them.
 // Every mbarrier wait is bounded (see mxq_device.cuh).
 
 #include <cuda.h>
@@ -45,10 +39,6 @@ constexpr int kBK = 128;          // K elements (= bytes) per pipeline stage
 constexpr int kUmmaK = 32;        // K of one MMA instruction (FP8)
 constexpr int kRasterBand = 8;    // m-tiles per raster band (L2 reuse of B)
 constexpr int kMaxGroups = 1024;
-#ifndef MXQ_GEMM_CLUSTER_M
-#define MXQ_GEMM_CLUSTER_M 2
-#endif
-constexpr int kClusterM = MXQ_GEMM_CLUSTER_M;   // CTAs per cluster in the dense modes (1, 2 or 4)
 
 // Kernel modes.
 constexpr int kDense = 0;         // y = A B^T
@@ -136,10 +126,8 @@ struct Schedule {
     int G;
 };
 
-// t indexes cluster tiles (kCM vertically adjacent m-tiles x one n-tile);
-// `rank` picks this CTA's m-tile in it (m_tiles counts cluster rows here).
-template <int BN, int kMode, int kCM>
-__device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs& p, int64_t t, int rank) {
+template <int BN, int kMode>
+__device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs& p, int64_t t) {
     TileInfo ti;
     ti.kb0 = 0;
     ti.nkb = s.num_kb;
@@ -151,12 +139,11 @@ __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs&
             g = t / per;
             t -= g * per;
         }
-        constexpr int kBand = kRasterBand / kCM > 0 ? kRasterBand / kCM : 1;
-        const int64_t per_band = static_cast<int64_t>(kBand) * s.n_tiles;
+        const int64_t per_band = static_cast<int64_t>(kRasterBand) * s.n_tiles;
         const int64_t band = t / per_band, within = t - band * per_band;
-        const int64_t mb = band * kBand;
-        const int64_t bh = min(static_cast<int64_t>(kBand), s.m_tiles - mb);
-        const int64_t m_blk = (mb + within % bh) * kCM + rank, n_blk = within / bh;
+        const int64_t mb = band * kRasterBand;
+        const int64_t bh = min(static_cast<int64_t>(kRasterBand), s.m_tiles - mb);
+        const int64_t m_blk = mb + within % bh, n_blk = within / bh;
         ti.m0 = m_blk * kBM;
         ti.n0 = n_blk * BN;
         ti.row_lo = ti.m0;
@@ -186,22 +173,99 @@ __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs&
     return ti;
 }
 
+// One epilogue thread's share of a finished tile: 128 accumulator columns
+// (starting at n) of output row `row`, stored when row_lo <= row < row_hi.
+// kDenseQuant rounds them to BF16 (stored when y is given) and writes their
+// 1x32 MXFP8 quantization: 32-byte payload runs and one 4-byte word of a tiled
+// scale atom (zero for rows or groups past the matrix: the layout's padding,
+// written for every row of a band that lies in the matrix, tile_in).
+template <int kMode>
+__device__ __forceinline__ void store_row(const GemmArgs& p, uint32_t (&v)[4][32], int64_t row, int64_t row_lo,
+                                          int64_t row_hi, int64_t y_row0, int64_t n, bool tile_in) {
+    if constexpr (kMode == kDenseQuant) {
+        // Round to BF16, then quantize each 32-column group of this row in
+        // registers (rceil E8M0 scale, E4M3 payload): the same bytes as
+        // quantizing the BF16 output, without its round trip through HBM.
+        const bool row_in = row >= row_lo && row < row_hi;
+        const int64_t ngroups = p.N >> 5;
+        const int64_t g0 = n >> 5;    // a multiple of 4
+        uint32_t codes = 0u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int64_t nc = n + c * 32;
+            const bool grp_ok = row_in && nc < p.N;
+            uint32_t b[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                b[i] = cvt_bf16x2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1]));
+            if (grp_ok && p.y != nullptr) {
+                uint4* yd = reinterpret_cast<uint4*>(p.y + row * p.ldy + nc);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) yd[q] = make_uint4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+            }
+            uint32_t m2 = 0u;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m2 = max_u16x2(m2, b[i] & 0x7FFF7FFFu);
+            const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+            uint32_t o[8];
+            uint32_t code;
+            if (m >= 0x7F80u) {  // NaN or Inf in the group
+                code = 0xFFu;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[j] = nan_bytes4(b[2 * j], b[2 * j + 1]);
+            } else {
+                const int e = rceil_exponent<0>(m);
+                const float sc = pow2_neg(e);
+                code = static_cast<uint32_t>(e + 127);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    o[j] = cvt_fp8x2<0>(bf16_lo(b[2 * j]) * sc, bf16_hi(b[2 * j]) * sc) |
+                           (cvt_fp8x2<0>(bf16_lo(b[2 * j + 1]) * sc, bf16_hi(b[2 * j + 1]) * sc) << 16);
+            }
+            if (grp_ok) {
+                uint4* qd = reinterpret_cast<uint4*>(p.yq + row * p.N + nc);
+                qd[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                qd[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            codes |= (grp_ok ? code : 0u) << (8 * c);
+        }
+        // The 4 groups are 4 consecutive bytes of one tiled scale atom.
+        if (tile_in && g0 < ((ngroups + 3) & ~static_cast<int64_t>(3)))
+            *reinterpret_cast<uint32_t*>(p.ys + tiled_scale_offset(row, g0, ngroups)) = codes;
+    } else {
+        (void)tile_in;
+        if (row >= row_lo && row < row_hi) {
+            uint16_t* yrow = p.y + (y_row0 + row) * p.ldy;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int64_t nc = n + c * 32;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (nc + 8 * q + 8 <= p.N) {
+                        uint4 o;
+                        o.x = cvt_bf16x2(__uint_as_float(v[c][8 * q + 0]), __uint_as_float(v[c][8 * q + 1]));
+                        o.y = cvt_bf16x2(__uint_as_float(v[c][8 * q + 2]), __uint_as_float(v[c][8 * q + 3]));
+                        o.z = cvt_bf16x2(__uint_as_float(v[c][8 * q + 4]), __uint_as_float(v[c][8 * q + 5]));
+                        o.w = cvt_bf16x2(__uint_as_float(v[c][8 * q + 6]), __uint_as_float(v[c][8 * q + 7]));
+                        *reinterpret_cast<uint4*>(yrow + nc + 8 * q) = o;
+                    }
+                }
+            }
+        }
+    }
+}
+
 // Fast path of a bounded wait: one probe inline, the polling loop out of line.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitGuard& g) {
     return mbar_try_wait(bar, parity) || mbar_wait(bar, parity, g);
 }
 
-template <int BN, int STAGES, bool kMnMajor, int kMode, int kCM>
+template <int BN, int STAGES, bool kMnMajor, int kMode>
 __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tma_a,
                      const __grid_constant__ CUtensorMap tma_b, const GemmArgs p) {
     using L = Cfg<BN, STAGES>;
     constexpr int kAcc = L::kAccStages;
-    static_assert(kCM == 1 || ((kMode == kDense || kMode == kDenseQuant) && BN == 256 && (kCM == 2 || kCM == 4)),
-                  "clusters: dense modes, 256-column tiles, 2 or 4 CTAs");
-    constexpr uint16_t kMask = static_cast<uint16_t>((1u << kCM) - 1u);
-    const int rank = kCM > 1 ? static_cast<int>(blockIdx.x % kCM) : 0;   // rank in the cluster
-    const int64_t cid = blockIdx.x / kCM, ncl = gridDim.x / kCM;          // cluster id, clusters
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -222,7 +286,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), kCM);   // one commit from each CTA of the cluster
+            mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < kAcc; ++a) {
             mbar_init(tfull_bar(a), 1);
@@ -244,7 +308,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     sch.G = p.G;
     sch.num_kb = static_cast<int>((p.K + kBK - 1) / kBK);
     if constexpr (kMode == kDense || kMode == kDenseQuant) {
-        sch.m_tiles = ((p.M + kBM - 1) / kBM + kCM - 1) / kCM;   // cluster rows
+        sch.m_tiles = (p.M + kBM - 1) / kBM;
         sch.total = sch.m_tiles * sch.n_tiles;
         sch.off = nullptr;
         sch.prefix = nullptr;
@@ -294,7 +358,6 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (kCM > 1) cluster_sync();   // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemSlot);
     if constexpr (kMode == kGroupedRows) sch.total = sch.prefix[p.G];
@@ -311,17 +374,14 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             const uint32_t full0 = full_bar(0), empty0 = empty_bar(0);
-            for (int64_t t = cid; t < sch.total && !*abort_flag; t += ncl) {
-                const TileInfo ti = tile_info<BN, kMode, kCM>(sch, p, t, rank);
+            for (int64_t t = blockIdx.x; t < sch.total && !*abort_flag; t += gridDim.x) {
+                const TileInfo ti = tile_info<BN, kMode>(sch, p, t);
                 const int64_t b_band0 = ti.b_row / 128;
                 int sfb_atoms = 0;
 #pragma unroll
                 for (int j = 0; j < L::kSfbAtoms; ++j)
                     if (b_band0 + j < p.b_bands) ++sfb_atoms;
-                // A cluster's last tile row may lie wholly below M: its A box reads the
-                // fill value, its scale atoms do not exist and are not loaded.
-                const bool sfa_ok = ti.m0 < p.M || kCM == 1;
-                const uint32_t bytes = L::kABytes + L::kBBytes + (sfa_ok ? 512u : 0u) + 512u * sfb_atoms;
+                const uint32_t bytes = L::kABytes + L::kBBytes + 512u + 512u * sfb_atoms;
                 const uint8_t* sfa_src = p.a_s + ((ti.m0 / 128) * p.k_atoms + ti.kb0) * 512;
                 const uint8_t* sfb_src = p.b_s + (b_band0 * p.k_atoms + ti.kb0) * 512;
                 const int64_t sfb_band_stride = p.k_atoms * 512;
@@ -335,19 +395,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                     const uint32_t sb = sbase + L::kOffB + stage * L::kBBytes;
                     const int32_t kx = static_cast<int32_t>((ti.kb0 + kb) * kBK);
                     tma_load_2d(sa, &tma_a, kx, ma, fb);
-                    if constexpr (kCM > 1) {
-                        // This CTA's 1/kCM of the shared B tile, to every CTA of the cluster.
-                        if constexpr (!kMnMajor) {
-                            constexpr int kRows = BN / kCM;
-                            tma_load_2d_multicast(sb + rank * kRows * kBK, &tma_b, kx, nb + rank * kRows, fb, kMask);
-                        } else {
-                            constexpr int kSplit = kCM / (BN / 128);     // K-row pieces per 128-column chunk
-                            constexpr int kKRows = kBK / kSplit;
-                            const int j = rank / kSplit, kr = (rank % kSplit) * kKRows;
-                            tma_load_2d_multicast(sb + j * 128 * kBK + kr * 128, &tma_b, nb + 128 * j, kx + kr, fb,
-                                                  kMask);
-                        }
-                    } else if constexpr (!kMnMajor) {
+                    if constexpr (!kMnMajor) {
                         tma_load_2d(sb, &tma_b, kx, nb, fb);
                     } else {
                         // B stored [K, N]: boxes of 128 N-bytes x 128 K-rows, one per 128 columns.
@@ -355,7 +403,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                         for (int j = 0; j < BN / 128; ++j)
                             tma_load_2d(sb + j * 128 * kBK, &tma_b, nb + 128 * j, kx, fb);
                     }
-                    if (sfa_ok) bulk_load(sbase + L::kOffSfa + stage * 512, sfa_src + kb * 512, 512u, fb);
+                    bulk_load(sbase + L::kOffSfa + stage * 512, sfa_src + kb * 512, 512u, fb);
                     for (int j = 0; j < sfb_atoms; ++j)
                         bulk_load(sbase + L::kOffSfb + (stage * L::kSfbAtoms + j) * 512,
                                   sfb_src + j * sfb_band_stride + kb * 512, 512u, fb);
@@ -395,10 +443,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             constexpr int kCpBatch = L::kCpBatch;
             int64_t g_total = 0;   // stages this CTA consumes
             if constexpr (kMode == kGroupedK) {
-                for (int64_t t = cid; t < sch.total; t += ncl)
-                    g_total += tile_info<BN, kMode, kCM>(sch, p, t, rank).nkb;
+                for (int64_t t = blockIdx.x; t < sch.total; t += gridDim.x)
+                    g_total += tile_info<BN, kMode>(sch, p, t).nkb;
             } else {
-                const int64_t my_tiles = cid < sch.total ? (sch.total - cid + ncl - 1) / ncl : 0;
+                const int64_t my_tiles = blockIdx.x < sch.total ? (sch.total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
                 g_total = my_tiles * sch.num_kb;
             }
             int64_t g = 0;
@@ -407,11 +455,11 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int64_t t = cid; t < sch.total && ok; t += ncl) {
+            for (int64_t t = blockIdx.x; t < sch.total && ok; t += gridDim.x) {
                 if (!wait_phase(tempty_bar(acc), acc_phase ^ 1u, guard)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                const int nkb = kMode == kGroupedK ? tile_info<BN, kMode, kCM>(sch, p, t, rank).nkb : sch.num_kb;
+                const int nkb = kMode == kGroupedK ? tile_info<BN, kMode>(sch, p, t).nkb : sch.num_kb;
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
                     if (g % kCpBatch == 0) {
                         const int nb = static_cast<int>(min(static_cast<int64_t>(kCpBatch), g_total - g));
@@ -451,9 +499,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                                         make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k) | p.fmt_bits, sfa_t, sfb_t,
                                         (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    // frees the slot (in every CTA of the cluster) once these MMAs are done
-                    if constexpr (kCM > 1) tc_commit_multicast(empty_bar(stage), kMask);
-                    else tc_commit(empty_bar(stage));
+                    tc_commit(empty_bar(stage));  // frees the slot once these MMAs are done
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
@@ -475,8 +521,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
         const int half = (warp - 2) >> 2;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int64_t t = cid; t < sch.total; t += ncl) {
-            const TileInfo ti = tile_info<BN, kMode, kCM>(sch, p, t, rank);
+        for (int64_t t = blockIdx.x; t < sch.total; t += gridDim.x) {
+            const TileInfo ti = tile_info<BN, kMode>(sch, p, t);
             // One lane waits; the warp follows its verdict, so the .sync.aligned
             // tensor-memory loads below always run with the full warp.
             int ok = 1;
@@ -502,88 +548,276 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[c][j] = 0u;
             }
-            const int64_t row = ti.m0 + 32 * quad + lane;
-            if constexpr (kMode == kDenseQuant) {
-                // Round to BF16, then quantize each 32-column group of this row in
-                // registers (rceil E8M0 scale, E4M3 payload): the same bytes as
-                // quantizing the BF16 output, without its round trip through HBM.
-                const bool row_in = row < ti.row_hi;
-                const int64_t ngroups = p.N >> 5;
-                const int64_t g0 = (ti.n0 + half * 128) >> 5;    // a multiple of 4
-                uint32_t codes = 0u;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int64_t n = ti.n0 + half * 128 + c * 32;
-                    const bool grp_ok = row_in && n < p.N;
-                    uint32_t b[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        b[i] = cvt_bf16x2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1]));
-                    if (grp_ok && p.y != nullptr) {
-                        uint4* yd = reinterpret_cast<uint4*>(p.y + row * p.ldy + n);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) yd[q] = make_uint4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
-                    }
-                    uint32_t m2 = 0u;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) m2 = max_u16x2(m2, b[i] & 0x7FFF7FFFu);
-                    const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-                    uint32_t o[8];
-                    uint32_t code;
-                    if (m >= 0x7F80u) {  // NaN or Inf in the group
-                        code = 0xFFu;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) o[j] = nan_bytes4(b[2 * j], b[2 * j + 1]);
-                    } else {
-                        const int e = rceil_exponent<0>(m);
-                        const float sc = pow2_neg(e);
-                        code = static_cast<uint32_t>(e + 127);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            o[j] = cvt_fp8x2<0>(bf16_lo(b[2 * j]) * sc, bf16_hi(b[2 * j]) * sc) |
-                                   (cvt_fp8x2<0>(bf16_lo(b[2 * j + 1]) * sc, bf16_hi(b[2 * j + 1]) * sc) << 16);
-                    }
-                    if (grp_ok) {
-                        uint4* qd = reinterpret_cast<uint4*>(p.yq + row * p.N + n);
-                        qd[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                        qd[1] = make_uint4(o[4], o[5], o[6], o[7]);
-                    }
-                    codes |= (grp_ok ? code : 0u) << (8 * c);
-                }
-                // The 4 groups are 4 consecutive bytes of one tiled scale atom (zero
-                // where the row or group lies past the matrix: the layout's padding).
-                if (ti.m0 < p.M && g0 < ((ngroups + 3) & ~static_cast<int64_t>(3)))
-                    *reinterpret_cast<uint32_t*>(p.ys + tiled_scale_offset(row, g0, ngroups)) = codes;
-            } else if (row >= ti.row_lo && row < ti.row_hi) {
-                uint16_t* yrow = p.y + (ti.y_row0 + row) * p.ldy;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int64_t n = ti.n0 + half * 128 + c * 32;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (n + 8 * q + 8 <= p.N) {
-                            uint4 o;
-                            o.x = cvt_bf16x2(__uint_as_float(v[c][8 * q + 0]), __uint_as_float(v[c][8 * q + 1]));
-                            o.y = cvt_bf16x2(__uint_as_float(v[c][8 * q + 2]), __uint_as_float(v[c][8 * q + 3]));
-                            o.z = cvt_bf16x2(__uint_as_float(v[c][8 * q + 4]), __uint_as_float(v[c][8 * q + 5]));
-                            o.w = cvt_bf16x2(__uint_as_float(v[c][8 * q + 6]), __uint_as_float(v[c][8 * q + 7]));
-                            *reinterpret_cast<uint4*>(yrow + n + 8 * q) = o;
-                        }
-                    }
-                }
-            }
+            store_row<kMode>(p, v, ti.m0 + 32 * quad + lane, ti.row_lo, ti.row_hi, ti.y_row0,
+                             ti.n0 + half * 128, ti.m0 < p.M);
         }
     }
 
     // ---- teardown -----------------------------------------------------------
     tc_fence_before();
     __syncthreads();
-    // No CTA leaves while a peer may still write its shared memory or barriers.
-    if constexpr (kCM > 1) cluster_sync();
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
         tmem_dealloc(tmem_base, L::kTmemCols);
+    }
+}
+
+// ---- dense GEMM on CTA pairs (cluster of 2, tcgen05 cta_group::2) --------------------
+//
+// Output tiles of 256 x 256.  CTA rank r of the pair owns rows m0 + 128 r: it
+// loads its 128 rows of A, its 128-row half of the B tile, its A scale atom and
+// both B scale atoms, all completing on the even CTA's full barrier.  The even
+// CTA's MMA warp issues 256 x 256 x 32 pair MMAs that read A and B from both
+// CTAs' shared memory and write each CTA's 128 accumulator rows into its own
+// tensor memory, and pair scale copies (each CTA's atoms into its own tensor
+// memory); its commits arrive on both CTAs' barriers.  Per SM and 128-deep K
+// step this stages 32 KB of operands (48 KB for a single-CTA 128 x 256 tile)
+// and issues half the scale copies per multiply-add.  The epilogue warps of
+// both CTAs release the even CTA's accumulator-empty barrier.
+struct PairCfg {
+    static constexpr int kStages = 6;
+    static constexpr int kCpBatch = 2;                 // stages per scale-copy batch (divides kStages)
+    static constexpr int kEpiWarps = 8;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kABytes = 128 * kBK;          // own A rows per stage
+    static constexpr int kBBytes = 128 * kBK;          // own half of B per stage
+    static constexpr int kSfbBytes = 2 * 512;          // scale atoms of all 256 B rows
+    static constexpr int kStageBytes = kABytes + kBBytes + 512 + kSfbBytes;   // per CTA
+    static constexpr int kOffB = 0;
+    static constexpr int kOffA = kOffB + kStages * kBBytes;
+    static constexpr int kOffSfa = kOffA + kStages * kABytes;
+    static constexpr int kOffSfb = kOffSfa + kStages * 512;
+    static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
+    static constexpr int kNumBars = 2 * kStages + 3;   // full, empty, tmem-full, tmem-empty, drain
+    static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
+    static constexpr int kOffAbort = kOffTmemSlot + 4;
+    static constexpr int kBytes = kOffAbort + 16;
+    static constexpr int kAlloc = kBytes + 1024;
+    static constexpr int kTmemSfa = 256;               // one 256-column accumulator, then scales
+    static constexpr int kTmemSfb = kTmemSfa + 4 * kStages;
+    static constexpr int kTmemCols = 512;
+    static_assert(kStages % kCpBatch == 0, "copy batches tile the ring");
+    static_assert(kTmemSfb + 8 * kStages <= kTmemCols, "tensor memory budget");
+    static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+template <bool kMnMajor, int kMode>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1)
+    gemm_mxf8_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
+                          const __grid_constant__ CUtensorMap tma_b,
+                          const __grid_constant__ CUtensorMap tma_sfa,
+                          const __grid_constant__ CUtensorMap tma_sfb, const GemmArgs p) {
+    static_assert(kMode == kDense || kMode == kDenseQuant, "pair kernel: dense modes");
+    using L = PairCfg;
+    constexpr int STAGES = L::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = blockIdx.x & 1u;   // rank in the cluster of two
+    const bool leader = rank == 0;
+
+    const uint32_t bar0 = sbase + L::kOffBar;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t tfull_bar = bar0 + 8u * (2 * STAGES);
+    const uint32_t tempty_bar = bar0 + 8u * (2 * STAGES + 1);
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+    const WaitGuard guard{abort_flag, p.status, p.wait_limit_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);      // the even CTA's producer arrives (with both CTAs' bytes)
+            mbar_init(empty_bar(s), 1);     // the even CTA's multicast commit
+        }
+        mbar_init(tfull_bar, 1);
+        mbar_init(tempty_bar, 2 * L::kEpiWarps);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tma_a);
+        prefetch_tensormap(&tma_b);
+        prefetch_tensormap(&tma_sfa);
+        prefetch_tensormap(&tma_sfb);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(sbase + L::kOffTmemSlot, L::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // barriers of both CTAs initialised, tensor memory allocated
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemSlot);
+
+    const int64_t m_tiles = (p.M + 255) / 256;
+    const int64_t n_tiles = (p.N + 255) / 256;
+    const int64_t total = m_tiles * n_tiles;
+    const int64_t pair_id = blockIdx.x >> 1;
+    const int64_t n_pairs = gridDim.x >> 1;
+    const int num_kb = static_cast<int>((p.K + kBK - 1) / kBK);
+    constexpr int kBand = kRasterBand / 2;   // 256-row tile rows per raster band
+    auto tile_of = [&](int64_t t, int64_t& m0, int64_t& n0) {
+        const int64_t per_band = static_cast<int64_t>(kBand) * n_tiles;
+        const int64_t band = t / per_band, within = t - band * per_band;
+        const int64_t mb = band * kBand;
+        const int64_t bh = min(static_cast<int64_t>(kBand), m_tiles - mb);
+        m0 = (mb + within % bh) * 256;
+        n0 = (within / bh) * 256;
+    };
+
+    if (warp == 0) {
+        // ---- producer (both CTAs) ------------------------------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            const uint32_t full0 = leader ? full_bar(0) : mapa_shared(full_bar(0), 0);
+            for (int64_t t = pair_id; t < total && !*abort_flag; t += n_pairs) {
+                int64_t m0, n0;
+                tile_of(t, m0, n0);
+                const int32_t ma = static_cast<int32_t>(m0 + 128 * rank);
+                const int32_t nb = static_cast<int32_t>(n0 + 128 * rank);
+                // scale atoms viewed as rows of 256 bytes: atom (band, kb) is rows 2 (band k_atoms + kb) + {0, 1}
+                const int32_t sfa_row = static_cast<int32_t>(2 * ((m0 / 128 + rank) * p.k_atoms));
+                const int32_t sfb_row0 = static_cast<int32_t>(2 * ((n0 / 128) * p.k_atoms));
+                const int32_t sfb_row1 = static_cast<int32_t>(2 * ((n0 / 128 + 1) * p.k_atoms));
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!wait_phase(empty_bar(stage), phase ^ 1u, guard)) break;
+                    const uint32_t fb = full0 + 8u * stage;
+                    if (leader) mbar_arrive_expect_tx(fb, 2u * L::kStageBytes);
+                    const uint32_t sa = sbase + L::kOffA + stage * L::kABytes;
+                    const uint32_t sb = sbase + L::kOffB + stage * L::kBBytes;
+                    const uint32_t ssa = sbase + L::kOffSfa + stage * 512;
+                    const uint32_t ssb = sbase + L::kOffSfb + stage * L::kSfbBytes;
+                    const int32_t kx = kb * kBK;
+                    tma_load_2d_pair(sa, &tma_a, kx, ma, fb);
+                    if constexpr (!kMnMajor)
+                        tma_load_2d_pair(sb, &tma_b, kx, nb, fb);
+                    else
+                        tma_load_2d_pair(sb, &tma_b, nb, kx, fb);   // B stored [K, N]
+                    tma_load_2d_pair(ssa, &tma_sfa, 0, sfa_row + 2 * kb, fb);
+                    tma_load_2d_pair(ssb, &tma_sfb, 0, sfb_row0 + 2 * kb, fb);
+                    tma_load_2d_pair(ssb + 512, &tma_sfb, 0, sfb_row1 + 2 * kb, fb);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (*abort_flag) {
+                // Loads in flight complete on the even CTA's barrier, which this CTA
+                // cannot wait on: give them a bounded while to land.
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
+            }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer (even CTA only) --------------------------------------------------
+        if (lane == 0 && leader) {
+            const uint64_t a_desc0 = make_smem_desc(sbase + L::kOffA, 16, 1024, 2);
+            const uint64_t b_desc0 = kMnMajor ? make_smem_desc(sbase + L::kOffB, 128 * kBK, 1024, 2)
+                                              : make_smem_desc(sbase + L::kOffB, 16, 1024, 2);
+            const uint64_t sfa_desc0 = make_smem_desc(sbase + L::kOffSfa, 0, 128, 0);
+            const uint64_t sfb_desc0 = make_smem_desc(sbase + L::kOffSfb, 0, 128, 0);
+            constexpr uint32_t kBStepK = kMnMajor ? (kUmmaK * 128) >> 4 : kUmmaK >> 4;
+            constexpr int kCpBatch = L::kCpBatch;
+            const int64_t my_tiles = pair_id < total ? (total - pair_id + n_pairs - 1) / n_pairs : 0;
+            const int64_t g_total = my_tiles * num_kb;   // stages this pair consumes
+            int64_t g = 0;
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int64_t t = pair_id; t < total && ok; t += n_pairs) {
+                if (!wait_phase(tempty_bar, acc_phase ^ 1u, guard)) { ok = false; break; }
+                tc_fence_after();
+                for (int kb = 0; kb < num_kb; ++kb, ++g) {
+                    if (g % kCpBatch == 0) {
+                        // scale atoms of the next kCpBatch stages, copied together
+                        const int nb = static_cast<int>(min(static_cast<int64_t>(kCpBatch), g_total - g));
+                        for (int j = 0; j < nb && ok; ++j) {
+                            const int sj = (stage + j) % STAGES;
+                            const uint32_t pj = phase ^ ((stage + j) >= STAGES ? 1u : 0u);
+                            if (!wait_phase(full_bar(sj), pj, guard)) ok = false;
+                        }
+                        if (!ok) break;
+                        tc_fence_after();
+                        for (int j = 0; j < nb; ++j) {
+                            const int sj = (stage + j) % STAGES;
+                            tc_cp_32x128b_warpx4_pair(tmem_base + L::kTmemSfa + 4 * sj,
+                                                      sfa_desc0 + static_cast<uint64_t>((sj * 512) >> 4));
+                            tc_cp_32x128b_warpx4_pair(tmem_base + L::kTmemSfb + 8 * sj,
+                                                      sfb_desc0 + static_cast<uint64_t>((sj * L::kSfbBytes) >> 4));
+                            tc_cp_32x128b_warpx4_pair(tmem_base + L::kTmemSfb + 8 * sj + 4,
+                                                      sfb_desc0 + static_cast<uint64_t>((sj * L::kSfbBytes + 512) >> 4));
+                        }
+                    }
+                    const uint32_t sfa_t = tmem_base + L::kTmemSfa + 4 * stage;
+                    const uint32_t sfb_t = tmem_base + L::kTmemSfb + 8 * stage;
+                    const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
+                    const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
+                    const int64_t k_left = p.K - static_cast<int64_t>(kb) * kBK;
+                    const int ksub = k_left >= kBK ? kBK / kUmmaK : static_cast<int>(k_left) / kUmmaK;
+#pragma unroll
+                    for (int k = 0; k < kBK / kUmmaK; ++k)
+                        if (k < ksub)
+                            tc_mma_mxf8_pair(tmem_base, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
+                                             make_idesc_mxf8(256, 256, kMnMajor ? 1u : 0u, k, k) | p.fmt_bits, sfa_t,
+                                             sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
+                    tc_commit_pair_multicast(empty_bar(stage), 0x3);   // frees the slot in both CTAs
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit_pair_multicast(tfull_bar, 0x3);
+                acc_phase ^= 1u;
+            }
+            // Drain: every MMA and copy issued above completes before teardown.
+            tc_commit_pair(drain_bar);
+            WaitGuard g2 = guard;
+            volatile int never = 0;
+            g2.abort_flag = &never;
+            (void)mbar_wait(drain_bar, 0, g2);
+        }
+    } else {
+        // ---- epilogue (both CTAs; warps 2..9) ----------------------------------------------
+        const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const uint32_t tempty_leader = leader ? tempty_bar : mapa_shared(tempty_bar, 0);
+        uint32_t acc_phase = 0;
+        for (int64_t t = pair_id; t < total; t += n_pairs) {
+            int64_t m0, n0;
+            tile_of(t, m0, n0);
+            int ok = 1;
+            if (lane == 0) ok = wait_phase(tfull_bar, acc_phase, guard) ? 1 : 0;
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t v[4][32];
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + half * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 32 * c, v[c]);
+            tmem_ld_wait();
+            // The accumulator is in registers: hand it back to the MMA warp now.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive(tempty_bar);
+                else mbar_arrive_cluster(tempty_leader);
+            }
+            acc_phase ^= 1u;
+            const int64_t mc = m0 + 128 * rank;   // this CTA's first row
+            store_row<kMode>(p, v, mc + 32 * quad + lane, mc, min(mc + 128, p.M), 0, n0 + half * 128, mc < p.M);
+        }
+    }
+
+    // ---- teardown: nothing may still target the peer when either CTA leaves ----
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc_pair(tmem_base, L::kTmemCols);
     }
 }
 
@@ -593,75 +827,85 @@ bool make_tma_u8(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
     return encode_tensor_map_2d(map, ptr, false, cols, rows, cols, 128u, box_rows, true);
 }
 
-template <int BN, int STAGES, bool kMnMajor, int kMode, int kCM = 1>
+template <int BN, int STAGES, bool kMnMajor, int kMode>
 cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& ta, const CUtensorMap& tb,
                      const GemmArgs& args, int64_t max_tiles, cudaStream_t stream) {
     using L = Cfg<BN, STAGES>;
-    auto kern = gemm_mxf8_kernel<BN, STAGES, kMnMajor, kMode, kCM>;
-    static thread_local int configured_device = -1;  // attributes set once per device and thread
-    static thread_local int max_clusters = 0;
-    cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(L::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = L::kAlloc;
-    cfg.stream = stream;
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCM;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = kCM > 1 ? 1 : 0;
+    auto kern = gemm_mxf8_kernel<BN, STAGES, kMnMajor, kMode>;
+    static thread_local int configured_device = -1;  // attribute set once per device and thread
     if (configured_device != dev.device) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
         if (e != cudaSuccess) return e;
-        max_clusters = dev.sm_count;
-        if (kCM > 1) {
-            cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count / kCM * kCM), 1, 1);
-            int n = 0;
-            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-            if (e != cudaSuccess) return e;
-            if (n < 1) return cudaErrorInvalidConfiguration;
-            max_clusters = n;
-        }
         configured_device = dev.device;
     }
-    // max_tiles counts cluster tiles (one per cluster at a time); < 0: no limit.
-    int64_t clusters = max_clusters;
-    if (max_tiles >= 0 && max_tiles < clusters) clusters = max_tiles;
-    if (clusters <= 0) return cudaSuccess;
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * kCM), 1, 1);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, args);
-    if (e != cudaSuccess) return e;
+    int64_t grid = dev.sm_count;
+    if (max_tiles >= 0 && max_tiles < grid) grid = max_tiles;
+    if (grid <= 0) return cudaSuccess;
+    kern<<<static_cast<unsigned>(grid), L::kThreads, L::kAlloc, stream>>>(ta, tb, args);
     return cudaGetLastError();
+}
+
+// MMA-tiled scales of a [rows, K] operand viewed as [bands * k_atoms * 2, 256] bytes:
+// one 512-byte atom is a 2 x 256 box at row 2 (band * k_atoms + kb).
+bool make_tma_scales(CUtensorMap* map, const void* ptr, int64_t bands, int64_t k_atoms) {
+    return encode_tensor_map_2d(map, ptr, false, 256u, static_cast<uint64_t>(bands * k_atoms * 2), 256u, 256u,
+                                2u, false);
+}
+
+template <bool kMnMajor, int kMode>
+cudaError_t launch_pair(const DeviceInfo& dev, const CUtensorMap& ta, const CUtensorMap& tb,
+                        const CUtensorMap& tsa, const CUtensorMap& tsb, const GemmArgs& args,
+                        int64_t tiles, cudaStream_t stream) {
+    auto kern = gemm_mxf8_pair_kernel<kMnMajor, kMode>;
+    static thread_local int configured_device = -1;  // attributes set once per device and thread
+    static thread_local int max_pairs = 0;
+    if (configured_device != dev.device) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kAlloc);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count / 2 * 2), 1, 1);
+        cfg.blockDim = dim3(PairCfg::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = PairCfg::kAlloc;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        max_pairs = n;
+        configured_device = dev.device;
+    }
+    int64_t pairs = max_pairs;
+    if (tiles < pairs) pairs = tiles;
+    if (pairs <= 0) return cudaSuccess;
+    kern<<<static_cast<unsigned>(2 * pairs), PairCfg::kThreads, PairCfg::kAlloc, stream>>>(ta, tb, tsa, tsb, args);
+    return cudaGetLastError();
+}
+
+// Tensor maps of the pair kernel: A boxes of 128 rows, B boxes of one CTA's
+// 128-row half (K-major) or 128-column chunk (MN-major), scale atoms.
+bool make_pair_maps(CUtensorMap* ta, CUtensorMap* tb, CUtensorMap* tsa, CUtensorMap* tsb, const void* a_q,
+                    const void* a_s, const void* b_q, const void* b_s, int64_t M, int64_t N, int64_t K,
+                    bool b_mn_major) {
+    const int64_t k_atoms = (K + 127) / 128;
+    if (!make_tma_u8(ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128)) return false;
+    if (!b_mn_major) {
+        if (!make_tma_u8(tb, b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 128)) return false;
+    } else {
+        if (!make_tma_u8(tb, b_q, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK)) return false;
+    }
+    return make_tma_scales(tsa, a_s, (M + 127) / 128, k_atoms) && make_tma_scales(tsb, b_s, (N + 127) / 128, k_atoms);
 }
 
 constexpr int kBN = 256;
 constexpr int kStages = 4;
-
-// Tensor maps of the dense modes.  A: boxes of 128 rows x 128 K-bytes.  B, K-major
-// [N, K]: boxes of 256/kClusterM rows (one CTA's share of the tile); MN-major [K, N]:
-// boxes of 128 N-bytes x (128 * 2 / kClusterM, at most 128) K-rows.
-bool make_dense_maps(CUtensorMap* ta, CUtensorMap* tb, const void* a_q, const void* b_q, int64_t M, int64_t N,
-                     int64_t K, bool b_mn_major) {
-    if (!make_tma_u8(ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kBM)) return false;
-    if (!b_mn_major)
-        return make_tma_u8(tb, b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN / kClusterM);
-    const uint32_t krows = kClusterM <= 2 ? kBK : kBK * 2 / kClusterM;
-    return make_tma_u8(tb, b_q, static_cast<uint64_t>(K), static_cast<uint64_t>(N), krows);
-}
-
-int64_t dense_cluster_tiles(int64_t M, int64_t N) {
-    const int64_t m_tiles = (M + kBM - 1) / kBM;
-    return (m_tiles + kClusterM - 1) / kClusterM * ((N + kBN - 1) / kBN);
-}
 
 }  // namespace
 
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
                         const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
                         int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream) {
-    CUtensorMap ta, tb;
-    if (!make_dense_maps(&ta, &tb, a_q, b_q, M, N, K, b_mn_major)) return cudaErrorInvalidValue;
+    CUtensorMap ta, tb, tsa, tsb;
+    if (!make_pair_maps(&ta, &tb, &tsa, &tsb, a_q, a_s, b_q, b_s, M, N, K, b_mn_major))
+        return cudaErrorInvalidValue;
     GemmArgs args{};
     args.a_s = static_cast<const uint8_t*>(a_s);
     args.b_s = static_cast<const uint8_t*>(b_s);
@@ -675,17 +919,18 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
     args.fmt_bits = (static_cast<uint32_t>(a_fmt) << 7) | (static_cast<uint32_t>(b_fmt) << 10);
     args.status = dev.status;
     args.wait_limit_ns = kDefaultWaitLimitNs;
-    const int64_t tiles = dense_cluster_tiles(M, N);
+    const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
     if (b_mn_major)
-        return launch_t<kBN, kStages, true, kDense, kClusterM>(dev, ta, tb, args, tiles, stream);
-    return launch_t<kBN, kStages, false, kDense, kClusterM>(dev, ta, tb, args, tiles, stream);
+        return launch_pair<true, kDense>(dev, ta, tb, tsa, tsb, args, tiles, stream);
+    return launch_pair<false, kDense>(dev, ta, tb, tsa, tsb, args, tiles, stream);
 }
 
 cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
                               const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
                               int64_t ldy, void* y_q, void* y_s, cudaStream_t stream) {
-    CUtensorMap ta, tb;
-    if (!make_dense_maps(&ta, &tb, a_q, b_q, M, N, K, b_mn_major)) return cudaErrorInvalidValue;
+    CUtensorMap ta, tb, tsa, tsb;
+    if (!make_pair_maps(&ta, &tb, &tsa, &tsb, a_q, a_s, b_q, b_s, M, N, K, b_mn_major))
+        return cudaErrorInvalidValue;
     GemmArgs args{};
     args.a_s = static_cast<const uint8_t*>(a_s);
     args.b_s = static_cast<const uint8_t*>(b_s);
@@ -698,10 +943,10 @@ cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void
     args.ys = static_cast<uint8_t*>(y_s);
     args.status = dev.status;
     args.wait_limit_ns = kDefaultWaitLimitNs;
-    const int64_t tiles = dense_cluster_tiles(M, N);
+    const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
     if (b_mn_major)
-        return launch_t<kBN, kStages, true, kDenseQuant, kClusterM>(dev, ta, tb, args, tiles, stream);
-    return launch_t<kBN, kStages, false, kDenseQuant, kClusterM>(dev, ta, tb, args, tiles, stream);
+        return launch_pair<true, kDenseQuant>(dev, ta, tb, tsa, tsb, args, tiles, stream);
+    return launch_pair<false, kDenseQuant>(dev, ta, tb, tsa, tsb, args, tiles, stream);
 }
 
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
