@@ -570,14 +570,13 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
 // both B scale atoms, all completing on the even CTA's full barrier.  The even
 // CTA's MMA warp issues 256 x 256 x 32 pair MMAs that read A and B from both
 // CTAs' shared memory and write each CTA's 128 accumulator rows into its own
-// tensor memory, and pair scale copies (each CTA's atoms into its own tensor
-// memory); its commits arrive on both CTAs' barriers.  Per SM and 128-deep K
+// tensor memory, and per stage the pair scale copies (each CTA's atoms into its
+// own tensor memory); its commits arrive on both CTAs' barriers.  Per SM and 128-deep K
 // step this stages 32 KB of operands (48 KB for a single-CTA 128 x 256 tile)
 // and issues half the scale copies per multiply-add.  The epilogue warps of
 // both CTAs release the even CTA's accumulator-empty barrier.
 struct PairCfg {
     static constexpr int kStages = 6;
-    static constexpr int kCpBatch = 2;                 // stages per scale-copy batch (divides kStages)
     static constexpr int kEpiWarps = 8;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
     static constexpr int kABytes = 128 * kBK;          // own A rows per stage
@@ -597,7 +596,6 @@ struct PairCfg {
     static constexpr int kTmemSfa = 256;               // one 256-column accumulator, then scales
     static constexpr int kTmemSfb = kTmemSfa + 4 * kStages;
     static constexpr int kTmemCols = 512;
-    static_assert(kStages % kCpBatch == 0, "copy batches tile the ring");
     static_assert(kTmemSfb + 8 * kStages <= kTmemCols, "tensor memory budget");
     static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
@@ -721,37 +719,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
             const uint64_t sfa_desc0 = make_smem_desc(sbase + L::kOffSfa, 0, 128, 0);
             const uint64_t sfb_desc0 = make_smem_desc(sbase + L::kOffSfb, 0, 128, 0);
             constexpr uint32_t kBStepK = kMnMajor ? (kUmmaK * 128) >> 4 : kUmmaK >> 4;
-            constexpr int kCpBatch = L::kCpBatch;
-            const int64_t my_tiles = pair_id < total ? (total - pair_id + n_pairs - 1) / n_pairs : 0;
-            const int64_t g_total = my_tiles * num_kb;   // stages this pair consumes
-            int64_t g = 0;
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int64_t t = pair_id; t < total && ok; t += n_pairs) {
                 if (!wait_phase(tempty_bar, acc_phase ^ 1u, guard)) { ok = false; break; }
                 tc_fence_after();
-                for (int kb = 0; kb < num_kb; ++kb, ++g) {
-                    if (g % kCpBatch == 0) {
-                        // scale atoms of the next kCpBatch stages, copied together
-                        const int nb = static_cast<int>(min(static_cast<int64_t>(kCpBatch), g_total - g));
-                        for (int j = 0; j < nb && ok; ++j) {
-                            const int sj = (stage + j) % STAGES;
-                            const uint32_t pj = phase ^ ((stage + j) >= STAGES ? 1u : 0u);
-                            if (!wait_phase(full_bar(sj), pj, guard)) ok = false;
-                        }
-                        if (!ok) break;
-                        tc_fence_after();
-                        for (int j = 0; j < nb; ++j) {
-                            const int sj = (stage + j) % STAGES;
-                            tc_cp_32x128b_warpx4_pair(tmem_base + L::kTmemSfa + 4 * sj,
-                                                      sfa_desc0 + static_cast<uint64_t>((sj * 512) >> 4));
-                            tc_cp_32x128b_warpx4_pair(tmem_base + L::kTmemSfb + 8 * sj,
-                                                      sfb_desc0 + static_cast<uint64_t>((sj * L::kSfbBytes) >> 4));
-                            tc_cp_32x128b_warpx4_pair(tmem_base + L::kTmemSfb + 8 * sj + 4,
-                                                      sfb_desc0 + static_cast<uint64_t>((sj * L::kSfbBytes + 512) >> 4));
-                        }
-                    }
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!wait_phase(full_bar(stage), phase, guard)) { ok = false; break; }
+                    tc_fence_after();
+                    // this stage's scale atoms into its tensor-memory columns (each CTA its own)
+                    tc_cp_32x128b_warpx4_pair(tmem_base + L::kTmemSfa + 4 * stage,
+                                              sfa_desc0 + static_cast<uint64_t>((stage * 512) >> 4));
+                    tc_cp_32x128b_warpx4_pair(tmem_base + L::kTmemSfb + 8 * stage,
+                                              sfb_desc0 + static_cast<uint64_t>((stage * L::kSfbBytes) >> 4));
+                    tc_cp_32x128b_warpx4_pair(tmem_base + L::kTmemSfb + 8 * stage + 4,
+                                              sfb_desc0 + static_cast<uint64_t>((stage * L::kSfbBytes + 512) >> 4));
                     const uint32_t sfa_t = tmem_base + L::kTmemSfa + 4 * stage;
                     const uint32_t sfb_t = tmem_base + L::kTmemSfb + 8 * stage;
                     const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
