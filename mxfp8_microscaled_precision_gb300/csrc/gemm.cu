@@ -13,13 +13,13 @@
 //   warp 0      TMA producer: A and B tiles (128-byte swizzle) and the
 //               512-byte scale atoms, into a ring of STAGES shared-memory
 //               slots guarded by full/empty mbarriers.
-//   warp 1      allocates tensor memory; one lane issues tcgen05.cp of the
-//               scale atoms into per-stage TMEM columns and the
-//               tcgen05.mma.kind::mxf8f6f4.block_scale instructions
-//               (128 x BN x 32 each) into one of two TMEM accumulators.
-//   warps 2-5   epilogue: tcgen05.ld of the FP32 accumulator, RNE to BF16,
-//               16-byte global stores; releases the accumulator so the MMA
-//               warp proceeds with the next tile meanwhile.
+//   warp 1      allocates tensor memory; one lane issues, per stage,
+//               tcgen05.cp of the scale atoms into that stage's TMEM columns
+//               and the tcgen05.mma.kind::mxf8f6f4.block_scale instructions
+//               (128 x BN x 32 each) into the TMEM accumulator.
+//   warps 2-9   epilogue: tcgen05.ld of the FP32 accumulator, which is then
+//               released to the MMA warp; RNE to BF16 (and, in the quantizing
+//               mode, the 1x32 MXFP8 quantization), 16-byte global stores.
 // Every mbarrier wait is bounded (see mxq_device.cuh).
 
 #include <cuda.h>
@@ -72,7 +72,6 @@ struct GemmArgs {
 //             storing, so the next tile's MMAs start after the drain only.
 template <int BN, int STAGES>
 struct Cfg {
-    static constexpr int kCpBatch = 2;                  // stages per scale-copy batch (divides STAGES)
     static constexpr int kAccStages = BN == 128 ? 2 : 1;
     static constexpr int kEpiWarps = 4 * (BN / 128);   // each owns 32 lanes x 128 columns
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -438,18 +437,6 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             const uint64_t sfa_desc0 = make_smem_desc(sbase + L::kOffSfa, 0, 128, 0);
             const uint64_t sfb_desc0 = make_smem_desc(sbase + L::kOffSfb, 0, 128, 0);
             constexpr uint32_t kBStepK = kMnMajor ? (kUmmaK * 128) >> 4 : kUmmaK >> 4;
-            // Scale atoms of kCpBatch consecutive stages are copied together (one
-            // copy-to-MMA switch of the tensor pipe per batch).
-            constexpr int kCpBatch = L::kCpBatch;
-            int64_t g_total = 0;   // stages this CTA consumes
-            if constexpr (kMode == kGroupedK) {
-                for (int64_t t = blockIdx.x; t < sch.total; t += gridDim.x)
-                    g_total += tile_info<BN, kMode>(sch, p, t).nkb;
-            } else {
-                const int64_t my_tiles = blockIdx.x < sch.total ? (sch.total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-                g_total = my_tiles * sch.num_kb;
-            }
-            int64_t g = 0;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -460,26 +447,16 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 const int nkb = kMode == kGroupedK ? tile_info<BN, kMode>(sch, p, t).nkb : sch.num_kb;
-                for (int kb = 0; kb < nkb; ++kb, ++g) {
-                    if (g % kCpBatch == 0) {
-                        const int nb = static_cast<int>(min(static_cast<int64_t>(kCpBatch), g_total - g));
-                        for (int j = 0; j < nb && ok; ++j) {
-                            const int sj = (stage + j) % STAGES;
-                            const uint32_t pj = phase ^ ((stage + j) >= STAGES ? 1u : 0u);
-                            if (!wait_phase(full_bar(sj), pj, guard)) ok = false;
-                        }
-                        if (!ok) break;
-                        tc_fence_after();
-                        for (int j = 0; j < nb; ++j) {
-                            const int sj = (stage + j) % STAGES;
-                            tc_cp_32x128b_warpx4(tmem_base + L::kTmemSfa + 4 * sj,
-                                                 sfa_desc0 + static_cast<uint64_t>((sj * 512) >> 4));
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!wait_phase(full_bar(stage), phase, guard)) { ok = false; break; }
+                    tc_fence_after();
+                    // this stage's scale atoms into its tensor-memory columns
+                    tc_cp_32x128b_warpx4(tmem_base + L::kTmemSfa + 4 * stage,
+                                         sfa_desc0 + static_cast<uint64_t>((stage * 512) >> 4));
 #pragma unroll
-                            for (int a = 0; a < L::kSfbAtoms; ++a)
-                                tc_cp_32x128b_warpx4(tmem_base + L::kTmemSfb + 4 * L::kSfbAtoms * sj + 4 * a,
-                                                     sfb_desc0 + static_cast<uint64_t>(((sj * L::kSfbAtoms + a) * 512) >> 4));
-                        }
-                    }
+                    for (int a = 0; a < L::kSfbAtoms; ++a)
+                        tc_cp_32x128b_warpx4(tmem_base + L::kTmemSfb + 4 * L::kSfbAtoms * stage + 4 * a,
+                                             sfb_desc0 + static_cast<uint64_t>(((stage * L::kSfbAtoms + a) * 512) >> 4));
                     const uint32_t sfa_t = tmem_base + L::kTmemSfa + 4 * stage;
                     const uint32_t sfb_t = tmem_base + L::kTmemSfb + 4 * L::kSfbAtoms * stage;
                     const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
@@ -563,247 +540,6 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     }
 }
 
-// ---- dense GEMM on CTA pairs (cluster of 2, tcgen05 cta_group::2) --------------------
-//
-// Output tiles of 256 x 256.  CTA rank r of the pair owns rows m0 + 128 r: it
-// loads its 128 rows of A, its 128-row half of the B tile, its A scale atom and
-// both B scale atoms, all completing on the even CTA's full barrier.  The even
-// CTA's MMA warp issues 256 x 256 x 32 pair MMAs that read A and B from both
-// CTAs' shared memory and write each CTA's 128 accumulator rows into its own
-// tensor memory, and per stage the pair scale copies (each CTA's atoms into its
-// own tensor memory); its commits arrive on both CTAs' barriers.  Per SM and 128-deep K
-// step this stages 32 KB of operands (48 KB for a single-CTA 128 x 256 tile)
-// and issues half the scale copies per multiply-add.  The epilogue warps of
-// both CTAs release the even CTA's accumulator-empty barrier.
-struct PairCfg {
-    static constexpr int kStages = 6;
-    static constexpr int kEpiWarps = 8;
-    static constexpr int kThreads = 64 + 32 * kEpiWarps;
-    static constexpr int kABytes = 128 * kBK;          // own A rows per stage
-    static constexpr int kBBytes = 128 * kBK;          // own half of B per stage
-    static constexpr int kSfbBytes = 2 * 512;          // scale atoms of all 256 B rows
-    static constexpr int kStageBytes = kABytes + kBBytes + 512 + kSfbBytes;   // per CTA
-    static constexpr int kOffB = 0;
-    static constexpr int kOffA = kOffB + kStages * kBBytes;
-    static constexpr int kOffSfa = kOffA + kStages * kABytes;
-    static constexpr int kOffSfb = kOffSfa + kStages * 512;
-    static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
-    static constexpr int kNumBars = 2 * kStages + 3;   // full, empty, tmem-full, tmem-empty, drain
-    static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
-    static constexpr int kOffAbort = kOffTmemSlot + 4;
-    static constexpr int kBytes = kOffAbort + 16;
-    static constexpr int kAlloc = kBytes + 1024;
-    static constexpr int kTmemSfa = 256;               // one 256-column accumulator, then scales
-    static constexpr int kTmemSfb = kTmemSfa + 4 * kStages;
-    static constexpr int kTmemCols = 512;
-    static_assert(kTmemSfb + 8 * kStages <= kTmemCols, "tensor memory budget");
-    static_assert(kAlloc <= 227 * 1024, "shared memory budget");
-};
-
-template <bool kMnMajor, int kMode>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1)
-    gemm_mxf8_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
-                          const __grid_constant__ CUtensorMap tma_b,
-                          const __grid_constant__ CUtensorMap tma_sfa,
-                          const __grid_constant__ CUtensorMap tma_sfb, const GemmArgs p) {
-    static_assert(kMode == kDense || kMode == kDenseQuant, "pair kernel: dense modes");
-    using L = PairCfg;
-    constexpr int STAGES = L::kStages;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t sbase = smem_u32(smem);
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const uint32_t rank = blockIdx.x & 1u;   // rank in the cluster of two
-    const bool leader = rank == 0;
-
-    const uint32_t bar0 = sbase + L::kOffBar;
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    const uint32_t tfull_bar = bar0 + 8u * (2 * STAGES);
-    const uint32_t tempty_bar = bar0 + 8u * (2 * STAGES + 1);
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
-    const WaitGuard guard{abort_flag, p.status, p.wait_limit_ns};
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);      // the even CTA's producer arrives (with both CTAs' bytes)
-            mbar_init(empty_bar(s), 1);     // the even CTA's multicast commit
-        }
-        mbar_init(tfull_bar, 1);
-        mbar_init(tempty_bar, 2 * L::kEpiWarps);
-        mbar_init(drain_bar, 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-        prefetch_tensormap(&tma_a);
-        prefetch_tensormap(&tma_b);
-        prefetch_tensormap(&tma_sfa);
-        prefetch_tensormap(&tma_sfb);
-    }
-    if (warp == 1) {
-        tmem_alloc_pair(sbase + L::kOffTmemSlot, L::kTmemCols);
-        tmem_relinquish_pair();
-    }
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();   // barriers of both CTAs initialised, tensor memory allocated
-    tc_fence_after();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemSlot);
-
-    const int64_t m_tiles = (p.M + 255) / 256;
-    const int64_t n_tiles = (p.N + 255) / 256;
-    const int64_t total = m_tiles * n_tiles;
-    const int64_t pair_id = blockIdx.x >> 1;
-    const int64_t n_pairs = gridDim.x >> 1;
-    const int num_kb = static_cast<int>((p.K + kBK - 1) / kBK);
-    constexpr int kBand = kRasterBand / 2;   // 256-row tile rows per raster band
-    auto tile_of = [&](int64_t t, int64_t& m0, int64_t& n0) {
-        const int64_t per_band = static_cast<int64_t>(kBand) * n_tiles;
-        const int64_t band = t / per_band, within = t - band * per_band;
-        const int64_t mb = band * kBand;
-        const int64_t bh = min(static_cast<int64_t>(kBand), m_tiles - mb);
-        m0 = (mb + within % bh) * 256;
-        n0 = (within / bh) * 256;
-    };
-
-    if (warp == 0) {
-        // ---- producer (both CTAs) ------------------------------------------------------
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            const uint32_t full0 = leader ? full_bar(0) : mapa_shared(full_bar(0), 0);
-            for (int64_t t = pair_id; t < total && !*abort_flag; t += n_pairs) {
-                int64_t m0, n0;
-                tile_of(t, m0, n0);
-                const int32_t ma = static_cast<int32_t>(m0 + 128 * rank);
-                const int32_t nb = static_cast<int32_t>(n0 + 128 * rank);
-                // scale atoms viewed as rows of 256 bytes: atom (band, kb) is rows 2 (band k_atoms + kb) + {0, 1}
-                const int32_t sfa_row = static_cast<int32_t>(2 * ((m0 / 128 + rank) * p.k_atoms));
-                const int32_t sfb_row0 = static_cast<int32_t>(2 * ((n0 / 128) * p.k_atoms));
-                const int32_t sfb_row1 = static_cast<int32_t>(2 * ((n0 / 128 + 1) * p.k_atoms));
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!wait_phase(empty_bar(stage), phase ^ 1u, guard)) break;
-                    const uint32_t fb = full0 + 8u * stage;
-                    if (leader) mbar_arrive_expect_tx(fb, 2u * L::kStageBytes);
-                    const uint32_t sa = sbase + L::kOffA + stage * L::kABytes;
-                    const uint32_t sb = sbase + L::kOffB + stage * L::kBBytes;
-                    const uint32_t ssa = sbase + L::kOffSfa + stage * 512;
-                    const uint32_t ssb = sbase + L::kOffSfb + stage * L::kSfbBytes;
-                    const int32_t kx = kb * kBK;
-                    tma_load_2d_pair(sa, &tma_a, kx, ma, fb);
-                    if constexpr (!kMnMajor)
-                        tma_load_2d_pair(sb, &tma_b, kx, nb, fb);
-                    else
-                        tma_load_2d_pair(sb, &tma_b, nb, kx, fb);   // B stored [K, N]
-                    tma_load_2d_pair(ssa, &tma_sfa, 0, sfa_row + 2 * kb, fb);
-                    tma_load_2d_pair(ssb, &tma_sfb, 0, sfb_row0 + 2 * kb, fb);
-                    tma_load_2d_pair(ssb + 512, &tma_sfb, 0, sfb_row1 + 2 * kb, fb);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                }
-            }
-            if (*abort_flag) {
-                // Loads in flight complete on the even CTA's barrier, which this CTA
-                // cannot wait on: give them a bounded while to land.
-                const uint64_t t0 = globaltimer_ns();
-                while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
-            }
-        }
-    } else if (warp == 1) {
-        // ---- MMA issuer (even CTA only) --------------------------------------------------
-        if (lane == 0 && leader) {
-            const uint64_t a_desc0 = make_smem_desc(sbase + L::kOffA, 16, 1024, 2);
-            const uint64_t b_desc0 = kMnMajor ? make_smem_desc(sbase + L::kOffB, 128 * kBK, 1024, 2)
-                                              : make_smem_desc(sbase + L::kOffB, 16, 1024, 2);
-            const uint64_t sfa_desc0 = make_smem_desc(sbase + L::kOffSfa, 0, 128, 0);
-            const uint64_t sfb_desc0 = make_smem_desc(sbase + L::kOffSfb, 0, 128, 0);
-            constexpr uint32_t kBStepK = kMnMajor ? (kUmmaK * 128) >> 4 : kUmmaK >> 4;
-            int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
-            bool ok = true;
-            for (int64_t t = pair_id; t < total && ok; t += n_pairs) {
-                if (!wait_phase(tempty_bar, acc_phase ^ 1u, guard)) { ok = false; break; }
-                tc_fence_after();
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!wait_phase(full_bar(stage), phase, guard)) { ok = false; break; }
-                    tc_fence_after();
-                    // this stage's scale atoms into its tensor-memory columns (each CTA its own)
-                    tc_cp_32x128b_warpx4_pair(tmem_base + L::kTmemSfa + 4 * stage,
-                                              sfa_desc0 + static_cast<uint64_t>((stage * 512) >> 4));
-                    tc_cp_32x128b_warpx4_pair(tmem_base + L::kTmemSfb + 8 * stage,
-                                              sfb_desc0 + static_cast<uint64_t>((stage * L::kSfbBytes) >> 4));
-                    tc_cp_32x128b_warpx4_pair(tmem_base + L::kTmemSfb + 8 * stage + 4,
-                                              sfb_desc0 + static_cast<uint64_t>((stage * L::kSfbBytes + 512) >> 4));
-                    const uint32_t sfa_t = tmem_base + L::kTmemSfa + 4 * stage;
-                    const uint32_t sfb_t = tmem_base + L::kTmemSfb + 8 * stage;
-                    const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
-                    const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
-                    const int64_t k_left = p.K - static_cast<int64_t>(kb) * kBK;
-                    const int ksub = k_left >= kBK ? kBK / kUmmaK : static_cast<int>(k_left) / kUmmaK;
-#pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k)
-                        if (k < ksub)
-                            tc_mma_mxf8_pair(tmem_base, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
-                                             make_idesc_mxf8(256, 256, kMnMajor ? 1u : 0u, k, k) | p.fmt_bits, sfa_t,
-                                             sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
-                    tc_commit_pair_multicast(empty_bar(stage), 0x3);   // frees the slot in both CTAs
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                }
-                if (!ok) break;
-                tc_commit_pair_multicast(tfull_bar, 0x3);
-                acc_phase ^= 1u;
-            }
-            // Drain: every MMA and copy issued above completes before teardown.
-            tc_commit_pair(drain_bar);
-            WaitGuard g2 = guard;
-            volatile int never = 0;
-            g2.abort_flag = &never;
-            (void)mbar_wait(drain_bar, 0, g2);
-        }
-    } else {
-        // ---- epilogue (both CTAs; warps 2..9) ----------------------------------------------
-        const int quad = warp & 3;
-        const int half = (warp - 2) >> 2;
-        const uint32_t tempty_leader = leader ? tempty_bar : mapa_shared(tempty_bar, 0);
-        uint32_t acc_phase = 0;
-        for (int64_t t = pair_id; t < total; t += n_pairs) {
-            int64_t m0, n0;
-            tile_of(t, m0, n0);
-            int ok = 1;
-            if (lane == 0) ok = wait_phase(tfull_bar, acc_phase, guard) ? 1 : 0;
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t v[4][32];
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + half * 128;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 32 * c, v[c]);
-            tmem_ld_wait();
-            // The accumulator is in registers: hand it back to the MMA warp now.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (leader) mbar_arrive(tempty_bar);
-                else mbar_arrive_cluster(tempty_leader);
-            }
-            acc_phase ^= 1u;
-            const int64_t mc = m0 + 128 * rank;   // this CTA's first row
-            store_row<kMode>(p, v, mc + 32 * quad + lane, mc, min(mc + 128, p.M), 0, n0 + half * 128, mc < p.M);
-        }
-    }
-
-    // ---- teardown: nothing may still target the peer when either CTA leaves ----
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();
-    tc_fence_after();
-    if (warp == 1) {
-        __syncwarp();
-        tmem_dealloc_pair(tmem_base, L::kTmemCols);
-    }
-}
-
 // Row-major u8 matrix [rows, cols] (cols contiguous), box [box_rows, 128 bytes],
 // 128-byte swizzle.
 bool make_tma_u8(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
@@ -828,67 +564,25 @@ cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& ta, const CUtenso
     return cudaGetLastError();
 }
 
-// MMA-tiled scales of a [rows, K] operand viewed as [bands * k_atoms * 2, 256] bytes:
-// one 512-byte atom is a 2 x 256 box at row 2 (band * k_atoms + kb).
-bool make_tma_scales(CUtensorMap* map, const void* ptr, int64_t bands, int64_t k_atoms) {
-    return encode_tensor_map_2d(map, ptr, false, 256u, static_cast<uint64_t>(bands * k_atoms * 2), 256u, 256u,
-                                2u, false);
-}
-
-template <bool kMnMajor, int kMode>
-cudaError_t launch_pair(const DeviceInfo& dev, const CUtensorMap& ta, const CUtensorMap& tb,
-                        const CUtensorMap& tsa, const CUtensorMap& tsb, const GemmArgs& args,
-                        int64_t tiles, cudaStream_t stream) {
-    auto kern = gemm_mxf8_pair_kernel<kMnMajor, kMode>;
-    static thread_local int configured_device = -1;  // attributes set once per device and thread
-    static thread_local int max_pairs = 0;
-    if (configured_device != dev.device) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kAlloc);
-        if (e != cudaSuccess) return e;
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count / 2 * 2), 1, 1);
-        cfg.blockDim = dim3(PairCfg::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = PairCfg::kAlloc;
-        int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        if (n < 1) return cudaErrorInvalidConfiguration;
-        max_pairs = n;
-        configured_device = dev.device;
-    }
-    int64_t pairs = max_pairs;
-    if (tiles < pairs) pairs = tiles;
-    if (pairs <= 0) return cudaSuccess;
-    kern<<<static_cast<unsigned>(2 * pairs), PairCfg::kThreads, PairCfg::kAlloc, stream>>>(ta, tb, tsa, tsb, args);
-    return cudaGetLastError();
-}
-
-// Tensor maps of the pair kernel: A boxes of 128 rows, B boxes of one CTA's
-// 128-row half (K-major) or 128-column chunk (MN-major), scale atoms.
-bool make_pair_maps(CUtensorMap* ta, CUtensorMap* tb, CUtensorMap* tsa, CUtensorMap* tsb, const void* a_q,
-                    const void* a_s, const void* b_q, const void* b_s, int64_t M, int64_t N, int64_t K,
-                    bool b_mn_major) {
-    const int64_t k_atoms = (K + 127) / 128;
-    if (!make_tma_u8(ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128)) return false;
-    if (!b_mn_major) {
-        if (!make_tma_u8(tb, b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 128)) return false;
-    } else {
-        if (!make_tma_u8(tb, b_q, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK)) return false;
-    }
-    return make_tma_scales(tsa, a_s, (M + 127) / 128, k_atoms) && make_tma_scales(tsb, b_s, (N + 127) / 128, k_atoms);
-}
-
 constexpr int kBN = 256;
 constexpr int kStages = 4;
+
+// Tensor maps of the dense modes: A boxes of 128 rows x 128 K-bytes; B K-major
+// [N, K] boxes of 256 rows, MN-major [K, N] boxes of 128 N-bytes x 128 K-rows.
+bool make_dense_maps(CUtensorMap* ta, CUtensorMap* tb, const void* a_q, const void* b_q, int64_t M, int64_t N,
+                     int64_t K, bool b_mn_major) {
+    if (!make_tma_u8(ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kBM)) return false;
+    if (!b_mn_major) return make_tma_u8(tb, b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN);
+    return make_tma_u8(tb, b_q, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK);
+}
 
 }  // namespace
 
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
                         const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
                         int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream) {
-    CUtensorMap ta, tb, tsa, tsb;
-    if (!make_pair_maps(&ta, &tb, &tsa, &tsb, a_q, a_s, b_q, b_s, M, N, K, b_mn_major))
-        return cudaErrorInvalidValue;
+    CUtensorMap ta, tb;
+    if (!make_dense_maps(&ta, &tb, a_q, b_q, M, N, K, b_mn_major)) return cudaErrorInvalidValue;
     GemmArgs args{};
     args.a_s = static_cast<const uint8_t*>(a_s);
     args.b_s = static_cast<const uint8_t*>(b_s);
@@ -902,18 +596,17 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
     args.fmt_bits = (static_cast<uint32_t>(a_fmt) << 7) | (static_cast<uint32_t>(b_fmt) << 10);
     args.status = dev.status;
     args.wait_limit_ns = kDefaultWaitLimitNs;
-    const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
     if (b_mn_major)
-        return launch_pair<true, kDense>(dev, ta, tb, tsa, tsb, args, tiles, stream);
-    return launch_pair<false, kDense>(dev, ta, tb, tsa, tsb, args, tiles, stream);
+        return launch_t<kBN, kStages, true, kDense>(dev, ta, tb, args, tiles, stream);
+    return launch_t<kBN, kStages, false, kDense>(dev, ta, tb, args, tiles, stream);
 }
 
 cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
                               const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
                               int64_t ldy, void* y_q, void* y_s, cudaStream_t stream) {
-    CUtensorMap ta, tb, tsa, tsb;
-    if (!make_pair_maps(&ta, &tb, &tsa, &tsb, a_q, a_s, b_q, b_s, M, N, K, b_mn_major))
-        return cudaErrorInvalidValue;
+    CUtensorMap ta, tb;
+    if (!make_dense_maps(&ta, &tb, a_q, b_q, M, N, K, b_mn_major)) return cudaErrorInvalidValue;
     GemmArgs args{};
     args.a_s = static_cast<const uint8_t*>(a_s);
     args.b_s = static_cast<const uint8_t*>(b_s);
@@ -926,10 +619,10 @@ cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void
     args.ys = static_cast<uint8_t*>(y_s);
     args.status = dev.status;
     args.wait_limit_ns = kDefaultWaitLimitNs;
-    const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
     if (b_mn_major)
-        return launch_pair<true, kDenseQuant>(dev, ta, tb, tsa, tsb, args, tiles, stream);
-    return launch_pair<false, kDenseQuant>(dev, ta, tb, tsa, tsb, args, tiles, stream);
+        return launch_t<kBN, kStages, true, kDenseQuant>(dev, ta, tb, args, tiles, stream);
+    return launch_t<kBN, kStages, false, kDenseQuant>(dev, ta, tb, args, tiles, stream);
 }
 
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
