@@ -42,7 +42,7 @@ FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 L2_FLUSH_BYTES = 256 << 20   # larger than the 129 MB L2
 # DRAM bytes (read + write) of one GEMM launch (the forward GEMM of the step), from
 # an ncu --set full capture of the kernel as it stands; None where not captured.
-GEMM_TRAFFIC_BYTES = {"linear_train": 76926464}
+GEMM_TRAFFIC_BYTES = {"linear_train": 75995136}
 
 
 def load_peaks():
