@@ -338,32 +338,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_kernel(
     ring_drain(ring, i, tile, tg.n_tiles, guard);
 }
 
-// Column copy (with or without the row copy), one tile per CTA: the tile is
-// loaded straight into registers (16-byte loads issued up front), the row
-// copy is made from the registers, and the tile is staged in shared memory
-// for the column pass.  Many resident CTAs in different phases hide the load
-// latency, with no ring to fill at the start or drain at the end.
-template <bool kRow, bool kTiled, int kFmt>
-__global__ void __launch_bounds__(kThreads, 3) quant_cols_direct_kernel(
-    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, uint8_t* __restrict__ q_row,
-    uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, TileGrid tg,
-    BatchStrides bs) {
-    __shared__ __align__(16) uint32_t tile_s[kTile * kTile / 2];
-    int64_t b, r0, c0;
-    tg.at(blockIdx.x, b, r0, c0);
-    uint4 v[kLoadsPerThread];
-    load_tile_chunks(v, x + b * bs.x, r0, c0, rows, cols, ld);
-    const int t = threadIdx.x;
-#pragma unroll
-    for (int j = 0; j < kLoadsPerThread; ++j)
-        reinterpret_cast<uint4*>(tile_s)[((t >> 4) + 16 * j) * 16 + (t & 15)] = v[j];
-    if constexpr (kRow)
-        row_pass<kTiled, kFmt>([&](int j) { return v[j]; }, r0, c0, rows, cols, q_row + b * bs.q_row,
-                               s_row + b * bs.s_row);
-    __syncthreads();
-    col_pass<kTiled, kFmt>(tile_s, c0, cols, rows, r0, rows, q_col + b * bs.q_col, s_col + b * bs.s_col);
-}
-
 // Token-axis (column) quantization inside each expert for the MoE weight
 // gradient.  Expert g's tokens go to the slot [P_g, P_g + L_g) of q_col
 // [cols, capacity], L_g = m_g rounded up to 128, P_g = sum of earlier L; each
@@ -553,23 +527,6 @@ cudaError_t launch_1x32_fmt(const DeviceInfo& dev, const void* x, int64_t rows, 
             quant_rows_kernel<true, kFmt><<<static_cast<unsigned>(tg.n_tiles), kThreads, 0, stream>>>(xp, rows, cols, ld, qp, sp, tg, bs);
         else
             quant_rows_kernel<false, kFmt><<<static_cast<unsigned>(tg.n_tiles), kThreads, 0, stream>>>(xp, rows, cols, ld, qp, sp, tg, bs);
-        return cudaGetLastError();
-    }
-    {  // column copy, with or without the row copy: one tile per CTA
-        auto xp = static_cast<const uint16_t*>(x);
-        auto qr = static_cast<uint8_t*>(q_row);
-        auto sr = static_cast<uint8_t*>(s_row);
-        auto qc = static_cast<uint8_t*>(q_col);
-        auto sc = static_cast<uint8_t*>(s_col);
-        const unsigned grid = static_cast<unsigned>(tg.n_tiles);
-        if (row && tiled)
-            quant_cols_direct_kernel<true, true, kFmt><<<grid, kThreads, 0, stream>>>(xp, rows, cols, ld, qr, sr, qc, sc, tg, bs);
-        else if (row)
-            quant_cols_direct_kernel<true, false, kFmt><<<grid, kThreads, 0, stream>>>(xp, rows, cols, ld, qr, sr, qc, sc, tg, bs);
-        else if (tiled)
-            quant_cols_direct_kernel<false, true, kFmt><<<grid, kThreads, 0, stream>>>(xp, rows, cols, ld, qr, sr, qc, sc, tg, bs);
-        else
-            quant_cols_direct_kernel<false, false, kFmt><<<grid, kThreads, 0, stream>>>(xp, rows, cols, ld, qr, sr, qc, sc, tg, bs);
         return cudaGetLastError();
     }
     CUtensorMap map;
