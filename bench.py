@@ -546,12 +546,12 @@ class MoETrain(Workload):
     the MXFP8 path)."""
     state_keys = ("W_gate_up", "W_down")
 
-    def __init__(self, dev=None):
+    def __init__(self, dev=None, tokens=16384, experts=128, name="moe_train"):
         import torch
         from mxfp8_microscaled_precision_gb300 import mxq, workloads
-        self.name = "moe_train"
-        d = workloads.moe_grouped(dev or "cpu", weights=False)
-        G, H, I = 128, 4096, 2048
+        self.name = name
+        d = workloads.moe_grouped(dev or "cpu", tokens=tokens, experts=experts, weights=False)
+        G, H, I = experts, 4096, 2048
         self.G, self.H, self.I = G, H, I
         self.Mt = d["A"].shape[0]
         w = "moe_grouped"
@@ -676,12 +676,14 @@ def make_workload(name, dev=None):
         return MoE(dev)
     if name == "moe_train":
         return MoETrain(dev)
+    if name == "moe_train_small":   # 2048 tokens over 16 experts: the per-expert sizes of moe_train, a few GB
+        return MoETrain(dev, tokens=2048, experts=16, name=name)
     if name in ("fsdp_mxfp8", "fsdp_mxfp8_32x32"):
         return FsdpWeight("mxfp8" if name == "fsdp_mxfp8" else "mxfp8-32x32", dev)
     raise SystemExit(f"unknown workload {name}")
 
 
-WORKLOAD_NAMES = ["linear_train", "linear_fwd_small", "weight_32x32", "moe_grouped", "moe_train",
+WORKLOAD_NAMES = ["linear_train", "linear_fwd_small", "weight_32x32", "moe_grouped", "moe_train", "moe_train_small",
                   "fsdp_mxfp8", "fsdp_mxfp8_32x32",
                   "sweep_4096", "sweep_7168", "sweep_16384"]
 
