@@ -208,31 +208,6 @@ mxq_status mxq_gemm_bf16out_fmt(const void* a_q, const void* a_s, mxq_fp8_format
                                 void* y, int64_t ldy, mxq_stream_t stream);
 
 /*
- * mxq_gemm_bf16out with a caller-provided workspace for stream-K scheduling
- * (E4M3 x E4M3).  The pages describe no scheduling; this is a GB300
- * implementation need: whole waves of 128 x 256 output tiles run one tile per
- * SM, and the tiles of the last, partial wave are cut into 128-deep K blocks
- * shared evenly by all SMs; the SM holding a tile's first K block adds the
- * others' FP32 partials (in a fixed order: results are deterministic for a
- * given shape and device) and writes y.  The sum is the same mathematical
- * product as mxq_gemm_bf16out's, associated differently, so the two agree
- * within the GEMM tolerance, not bit for bit.
- *
- * workspace   device memory, 256-byte aligned, owned by the caller; at least
- *             mxq_gemm_workspace_bytes(M, N, K) bytes for stream-K to be used.
- *             NULL, or fewer bytes: the GEMM runs on whole tiles only
- *             (identical to mxq_gemm_bf16out).  The call clears the flags it
- *             needs at its start on `stream`; two calls that run at the same
- *             time must not share a workspace.
- * Other arguments, shapes and errors: as mxq_gemm_bf16out.
- */
-size_t mxq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
-mxq_status mxq_gemm_bf16out_ws(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
-                               int64_t M, int64_t N, int64_t K, int b_mn_major,
-                               void* y, int64_t ldy, void* workspace, size_t workspace_bytes,
-                               mxq_stream_t stream);
-
-/*
  * Block-scaled FP8 GEMM whose epilogue also quantizes its output: the BF16
  * result y (as mxq_gemm_bf16out computes it) is rounded to BF16 and each run
  * of 32 consecutive columns of a row gets the 1x32 rceil E8M0 scale and E4M3

@@ -212,36 +212,8 @@ mxq_status mxq_gemm_bf16out_fmt(const void* a_q, const void* a_s, mxq_fp8_format
     mxq_status st = device_ok(&dev);
     if (st != MXQ_OK) return st;
     return from_cuda(mxq::launch_gemm(dev, a_q, a_s, b_q, b_s, M, N, K, b_mn_major != 0, y, ldy,
-                                      static_cast<int>(a_fmt), static_cast<int>(b_fmt), nullptr, 0,
+                                      static_cast<int>(a_fmt), static_cast<int>(b_fmt),
                                       reinterpret_cast<cudaStream_t>(stream)));
-}
-
-size_t mxq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    if (M <= 0 || N <= 0 || K <= 0) return 0;
-    mxq::DeviceInfo dev;
-    if (device_ok(&dev) != MXQ_OK) return 0;
-    return mxq::gemm_workspace_bytes(dev, M, N, K);
-}
-
-mxq_status mxq_gemm_bf16out_ws(const void* a_q, const void* a_s, const void* b_q, const void* b_s, int64_t M,
-                               int64_t N, int64_t K, int b_mn_major, void* y, int64_t ldy, void* workspace,
-                               size_t workspace_bytes, mxq_stream_t stream) {
-    if (M < 0 || N < 0 || K < 0 || (b_mn_major != 0 && b_mn_major != 1)) return MXQ_ERR_INVALID_ARG;
-    if (K % 32 != 0 || N % 16 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
-    if (b_mn_major && N % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
-    if (M > (int64_t(1) << 31) - 128 || N > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - 128)
-        return MXQ_ERR_UNSUPPORTED_SHAPE;
-    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MXQ_ERR_INVALID_ARG;
-    if (M == 0 || N == 0 || K == 0)   // nothing to share: the plain entry point handles these
-        return mxq_gemm_bf16out(a_q, a_s, b_q, b_s, M, N, K, b_mn_major, y, ldy, stream);
-    if (!y || ldy < N || ldy % 8 != 0 || !aligned16(y)) return MXQ_ERR_INVALID_ARG;
-    if (!a_q || !a_s || !b_q || !b_s) return MXQ_ERR_INVALID_ARG;
-    if (!aligned16(a_q) || !aligned16(a_s) || !aligned16(b_q) || !aligned16(b_s)) return MXQ_ERR_INVALID_ARG;
-    mxq::DeviceInfo dev;
-    mxq_status st = device_ok(&dev);
-    if (st != MXQ_OK) return st;
-    return from_cuda(mxq::launch_gemm(dev, a_q, a_s, b_q, b_s, M, N, K, b_mn_major != 0, y, ldy, 0, 0, workspace,
-                                      workspace ? workspace_bytes : 0, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mxq_status mxq_gemm_mxfp8out(const void* a_q, const void* a_s, const void* b_q, const void* b_s,

@@ -59,12 +59,6 @@ struct GemmArgs {
     uint32_t fmt_bits;       // operand formats in the instruction descriptor (0 = E4M3, E4M3)
     uint8_t* yq;             // quantizing epilogue: E4M3 payload [M, N] (row stride N)
     uint8_t* ys;             //   and its MMA-tiled scales [M, N/32]
-    // Stream-K remainder of the dense modes (sk_units == 0: every tile whole).
-    int64_t sk_tile0;        // tiles [0, sk_tile0) are whole, dealt round robin
-    int64_t sk_units;        // U = (tiles - sk_tile0) * K blocks per tile
-    int sk_ctas;             // CTAs [0, sk_ctas) share the U units in equal ranges
-    float* sk_partial;       // [sk_ctas][256 columns][128 rows] FP32 partial accumulators
-    unsigned int* sk_flags;  // per stream-K tile: partials landed (zero at launch)
     unsigned int* status;
     uint64_t wait_limit_ns;
 };
@@ -89,7 +83,7 @@ struct Cfg {
     static constexpr int kOffSfa = kOffA + STAGES * kABytes;
     static constexpr int kOffSfb = kOffSfa + STAGES * 512;
     static constexpr int kOffBar = kOffSfb + STAGES * 512 * kSfbAtoms;
-    static constexpr int kNumBars = 2 * STAGES + 2 * kAccStages + 3;   // + drain, stream-K done / go
+    static constexpr int kNumBars = 2 * STAGES + 2 * kAccStages + 1;
     static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kOffSched = (kOffAbort + 4 + 15) / 16 * 16;
@@ -260,87 +254,6 @@ __device__ __forceinline__ void store_row(const GemmArgs& p, uint32_t (&v)[4][32
     }
 }
 
-// ---- work items ----------------------------------------------------------------------
-// A CTA's work: the whole tiles blockIdx.x, blockIdx.x + gridDim.x, ... below
-// sk_tile0 (all tiles when stream-K is off), then its share [u0, u1) of the
-// stream-K units of the remaining tiles (a unit is one 128-deep K block of one
-// tile, tile-major), cut at tile boundaries.  A stream-K tile is finished by
-// the CTA holding its first K block, which adds the FP32 partials of the CTAs
-// holding the rest (contributors).  A contributor's part is always the first
-// segment of its range and a finisher's the last, so every CTA publishes its
-// partial before it waits for anyone else's: no chain of waits forms.
-constexpr int kRoleWhole = 0, kRoleContrib = 1, kRoleFinish = 2;
-
-struct WorkItem {
-    int64_t t;      // tile (tile_info order)
-    int kb0, nkb;   // stream-K: K blocks [kb0, kb0 + nkb) of the tile
-    int role;
-    int64_t sk;     // stream-K tile index (-1: whole tile)
-    int c_first, c_last;   // CTAs covering the stream-K tile (c_first finishes it)
-};
-
-struct WorkIter {
-    int64_t t, t_end, step;   // whole-tile phase
-    int64_t u, u1;            // stream-K phase
-    int64_t kb, U;
-    int G;
-    __device__ __forceinline__ int owner(int64_t x) const {   // CTA whose range holds unit x
-        return static_cast<int>(((x + 1) * G - 1) / U);
-    }
-    __device__ __forceinline__ bool next(const GemmArgs& p, WorkItem& w) {
-        if (t < t_end) {
-            w.t = t; w.kb0 = 0; w.nkb = 0; w.role = kRoleWhole; w.sk = -1; w.c_first = w.c_last = 0;
-            t += step;
-            return true;
-        }
-        if (u >= u1) return false;
-        const int64_t s = u / kb;
-        const int64_t seg_end = min(u1, (s + 1) * kb);
-        w.t = p.sk_tile0 + s;
-        w.kb0 = static_cast<int>(u - s * kb);
-        w.nkb = static_cast<int>(seg_end - u);
-        w.sk = s;
-        w.c_first = owner(s * kb);
-        w.c_last = owner((s + 1) * kb - 1);
-        w.role = w.nkb == kb ? kRoleWhole : (w.kb0 == 0 ? kRoleFinish : kRoleContrib);
-        u = seg_end;
-        return true;
-    }
-};
-
-__device__ __forceinline__ WorkIter make_work_iter(const GemmArgs& p, int64_t total, int num_kb) {
-    WorkIter it;
-    it.step = gridDim.x;
-    it.t = blockIdx.x;
-    it.kb = num_kb > 0 ? num_kb : 1;
-    it.U = p.sk_units;
-    it.G = p.sk_ctas > 0 ? p.sk_ctas : 1;
-    it.t_end = p.sk_units > 0 ? p.sk_tile0 : total;
-    it.u = it.u1 = 0;
-    if (p.sk_units > 0 && static_cast<int>(blockIdx.x) < p.sk_ctas) {
-        it.u = static_cast<int64_t>(blockIdx.x) * p.sk_units / p.sk_ctas;
-        it.u1 = (static_cast<int64_t>(blockIdx.x) + 1) * p.sk_units / p.sk_ctas;
-    }
-    return it;
-}
-
-// The tile of a work item, with a stream-K item's K range.
-template <int BN, int kMode>
-__device__ __forceinline__ TileInfo item_tile(const Schedule& s, const GemmArgs& p, const WorkItem& w) {
-    TileInfo ti = tile_info<BN, kMode>(s, p, w.t);
-    if (w.sk >= 0) {
-        ti.kb0 = w.kb0;
-        ti.nkb = w.nkb;
-    }
-    return ti;
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* ptr) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
-    return v;
-}
-
 // Wait for the accumulator hand-off between the MMA warp and the epilogue, on
 // the critical path between tiles: busy polling without suspending the thread
 // (measured 1-4% faster than the suspending probe), bounded, then the timed wait.
@@ -374,8 +287,6 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + kAcc + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * kAcc);
-    const uint32_t sk_done_bar = bar0 + 8u * (2 * STAGES + 2 * kAcc + 1);   // epilogue warps stored a partial
-    const uint32_t sk_go_bar = bar0 + 8u * (2 * STAGES + 2 * kAcc + 2);     // a stream-K tile's partials landed
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
     const WaitGuard guard{abort_flag, p.status, p.wait_limit_ns};
 
@@ -390,8 +301,6 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             mbar_init(tempty_bar(a), L::kEpiWarps);  // one arrive per epilogue warp
         }
         mbar_init(drain_bar, 1);
-        mbar_init(sk_done_bar, L::kEpiWarps);
-        mbar_init(sk_go_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&tma_a);
@@ -473,10 +382,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             const uint32_t full0 = full_bar(0), empty0 = empty_bar(0);
-            WorkIter it = make_work_iter(p, sch.total, sch.num_kb);
-            WorkItem w;
-            while (!*abort_flag && it.next(p, w)) {
-                const TileInfo ti = item_tile<BN, kMode>(sch, p, w);
+            for (int64_t t = blockIdx.x; t < sch.total && !*abort_flag; t += gridDim.x) {
+                const TileInfo ti = tile_info<BN, kMode>(sch, p, t);
                 const int64_t b_band0 = ti.b_row / 128;
                 int sfb_atoms = 0;
 #pragma unroll
@@ -544,14 +451,11 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            WorkIter it = make_work_iter(p, sch.total, sch.num_kb);
-            WorkItem w;
-            while (ok && it.next(p, w)) {
+            for (int64_t t = blockIdx.x; t < sch.total && ok; t += gridDim.x) {
                 if (!spin_phase(tempty_bar(acc), acc_phase ^ 1u, guard)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                const TileInfo ti = item_tile<BN, kMode>(sch, p, w);
-                const int nkb = ti.nkb;
+                const int nkb = kMode == kGroupedK ? tile_info<BN, kMode>(sch, p, t).nkb : sch.num_kb;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!wait_phase(full_bar(stage), phase, guard)) { ok = false; break; }
                     tc_fence_after();
@@ -567,7 +471,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                     const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
                     const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
                     const int64_t k_left = kMode == kGroupedK ? static_cast<int64_t>(nkb - kb) * kBK
-                                                              : p.K - static_cast<int64_t>(ti.kb0 + kb) * kBK;
+                                                              : p.K - static_cast<int64_t>(kb) * kBK;
                     if (k_left >= kBK) {
 #pragma unroll
                         for (int k = 0; k < kBK / kUmmaK; ++k)
@@ -603,13 +507,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
         const int half = (warp - 2) >> 2;
         int acc = 0;
         uint32_t acc_phase = 0;
-        uint32_t done_phase = 0, go_phase = 0;
-        const bool sk_leader = warp == 2 && lane == 0;
-        const int64_t prow = 32 * quad + lane;   // this thread's row of a partial
-        WorkIter it = make_work_iter(p, sch.total, sch.num_kb);
-        WorkItem w;
-        while (it.next(p, w)) {
-            const TileInfo ti = item_tile<BN, kMode>(sch, p, w);
+        for (int64_t t = blockIdx.x; t < sch.total; t += gridDim.x) {
+            const TileInfo ti = tile_info<BN, kMode>(sch, p, t);
             // One lane waits; the warp follows its verdict, so the .sync.aligned
             // tensor-memory loads below always run with the full warp.
             int ok = 1;
@@ -634,60 +533,6 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[c][j] = 0u;
-            }
-            if (w.role == kRoleContrib) {
-                // Publish this CTA's partial (column-major, so a warp's 32 rows of one
-                // column are 128 contiguous bytes), then count it on the tile's flag.
-                float* part = p.sk_partial + (static_cast<int64_t>(blockIdx.x) * 256 + half * 128) * 128 + prow;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) part[(c * 32 + j) * 128] = __uint_as_float(v[c][j]);
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sk_done_bar);
-                if (sk_leader) {
-                    if (wait_phase(sk_done_bar, done_phase, guard)) {
-                        __threadfence();
-                        atomicAdd(p.sk_flags + w.sk, 1u);
-                    }
-                }
-                done_phase ^= 1u;
-                continue;
-            }
-            if (w.role == kRoleFinish) {
-                // Wait (bounded) until every contributor's partial has landed, then add
-                // them in CTA order: the sum does not depend on timing.
-                const unsigned int need = static_cast<unsigned int>(w.c_last - w.c_first);
-                if (sk_leader) {
-                    const uint64_t t0 = globaltimer_ns();
-                    bool landed = true;
-                    while (ld_acquire_u32(p.sk_flags + w.sk) < need) {
-                        if (*abort_flag || globaltimer_ns() - t0 > p.wait_limit_ns) {
-                            *abort_flag = 1;
-                            atomicExch(p.status, kDevStatusTimeout);
-                            landed = false;
-                            break;
-                        }
-                    }
-                    (void)landed;
-                    mbar_arrive(sk_go_bar);
-                }
-                int go = 1;
-                if (lane == 0) go = wait_phase(sk_go_bar, go_phase, guard) ? 1 : 0;
-                go = __shfl_sync(0xFFFFFFFFu, go, 0);
-                go_phase ^= 1u;
-                __threadfence();
-                if (go) {
-                    for (int c2 = w.c_first + 1; c2 <= w.c_last; ++c2) {
-                        const float* part = p.sk_partial + (static_cast<int64_t>(c2) * 256 + half * 128) * 128 + prow;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                v[c][j] = __float_as_uint(__uint_as_float(v[c][j]) + __ldcg(part + (c * 32 + j) * 128));
-                    }
-                }
             }
             store_row<kMode>(p, v, ti.m0 + 32 * quad + lane, ti.row_lo, ti.row_hi, ti.y_row0,
                              ti.n0 + half * 128, ti.m0 < p.M);
@@ -730,64 +575,6 @@ cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& ta, const CUtenso
 
 constexpr int kBN = 256;
 constexpr int kStages = 4;
-constexpr int64_t kSkMinUnits = 4;   // fewest K blocks a stream-K CTA takes on
-
-// Stream-K plan of a dense GEMM on one device: the whole waves of 128 x 256
-// tiles are dealt round robin; the tiles of the last, partial wave are cut into
-// K blocks shared evenly by up to one CTA per SM, so every SM ends at about the
-// same time.  No plan (units == 0) when the tiles fill whole waves or there is
-// too little K to share.
-struct SkPlan {
-    int64_t tile0 = 0, units = 0, rem = 0;
-    int ctas = 0;
-    int64_t grid = 0;
-    size_t ws_bytes = 0;   // FP32 partials of every stream-K CTA + one flag per stream-K tile
-};
-
-SkPlan plan_stream_k(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K) {
-    SkPlan pl;
-    const int64_t T = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-    const int64_t kb = (K + kBK - 1) / kBK;
-    const int64_t G = dev.sm_count;
-    pl.grid = T < G ? T : G;
-    if (T <= 0 || kb < 2 || G < 2) return pl;
-    const int64_t tile0 = T >= G ? (T / G) * G : 0;
-    const int64_t rem = T - tile0;
-    if (rem == 0) return pl;
-    const int64_t U = rem * kb;
-    int64_t ctas = U / kSkMinUnits;
-    if (ctas > G) ctas = G;
-    if (ctas <= rem) return pl;   // every CTA would still get a whole tile or more
-    pl.tile0 = tile0;
-    pl.rem = rem;
-    pl.units = U;
-    pl.ctas = static_cast<int>(ctas);
-    pl.grid = T >= G ? G : ctas;
-    pl.ws_bytes = static_cast<size_t>(ctas) * 256 * 128 * sizeof(float) +
-                  static_cast<size_t>((rem * 4 + 255) / 256 * 256);
-    return pl;
-}
-
-// Applies a plan to the kernel arguments when the workspace holds it (flags
-// cleared on the stream first); otherwise the GEMM runs on whole tiles only.
-// Returns the grid to launch.
-cudaError_t apply_stream_k(const DeviceInfo& dev, GemmArgs& args, void* ws, size_t ws_bytes, int64_t* grid,
-                           cudaStream_t stream) {
-    const SkPlan pl = plan_stream_k(dev, args.M, args.N, args.K);
-    *grid = pl.grid;
-    if (pl.units == 0 || ws == nullptr || ws_bytes < pl.ws_bytes) {
-        const int64_t T = ((args.M + kBM - 1) / kBM) * ((args.N + kBN - 1) / kBN);
-        *grid = T < dev.sm_count ? T : dev.sm_count;
-        return cudaSuccess;
-    }
-    uint8_t* base = static_cast<uint8_t*>(ws);
-    args.sk_tile0 = pl.tile0;
-    args.sk_units = pl.units;
-    args.sk_ctas = pl.ctas;
-    args.sk_partial = reinterpret_cast<float*>(base);
-    args.sk_flags = reinterpret_cast<unsigned int*>(base + static_cast<size_t>(pl.ctas) * 256 * 128 * sizeof(float));
-    return cudaMemsetAsync(args.sk_flags, 0, static_cast<size_t>(pl.rem) * 4, stream);
-}
 
 // Tensor maps of the dense modes: A boxes of 128 rows x 128 K-bytes; B K-major
 // [N, K] boxes of 256 rows, MN-major [K, N] boxes of 128 N-bytes x 128 K-rows.
@@ -802,7 +589,7 @@ bool make_dense_maps(CUtensorMap* ta, CUtensorMap* tb, const void* a_q, const vo
 
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
                         const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
-                        int64_t ldy, int a_fmt, int b_fmt, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                        int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream) {
     CUtensorMap ta, tb;
     if (!make_dense_maps(&ta, &tb, a_q, b_q, M, N, K, b_mn_major)) return cudaErrorInvalidValue;
     GemmArgs args{};
@@ -818,16 +605,10 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
     args.fmt_bits = (static_cast<uint32_t>(a_fmt) << 7) | (static_cast<uint32_t>(b_fmt) << 10);
     args.status = dev.status;
     args.wait_limit_ns = kDefaultWaitLimitNs;
-    int64_t grid = 0;
-    cudaError_t e = apply_stream_k(dev, args, ws, ws_bytes, &grid, stream);
-    if (e != cudaSuccess) return e;
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
     if (b_mn_major)
-        return launch_t<kBN, kStages, true, kDense>(dev, ta, tb, args, grid, stream);
-    return launch_t<kBN, kStages, false, kDense>(dev, ta, tb, args, grid, stream);
-}
-
-size_t gemm_workspace_bytes(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K) {
-    return plan_stream_k(dev, M, N, K).ws_bytes;
+        return launch_t<kBN, kStages, true, kDense>(dev, ta, tb, args, tiles, stream);
+    return launch_t<kBN, kStages, false, kDense>(dev, ta, tb, args, tiles, stream);
 }
 
 cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,

@@ -51,13 +51,9 @@ cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, 
 
 // Dense block-scaled GEMM (see mxq_gemm_bf16out).  Returns cudaErrorInvalidValue
 // when a tensor map cannot be encoded for the given shapes.
-// ws / ws_bytes: stream-K workspace (NULL or too small: whole tiles only).
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
                         const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
-                        int64_t ldy, int a_fmt, int b_fmt, void* ws, size_t ws_bytes, cudaStream_t stream);
-
-// Workspace a dense GEMM of this shape can use for stream-K on this device (0: none).
-size_t gemm_workspace_bytes(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K);
+                        int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream);
 
 // Dense GEMM whose epilogue also writes the 1x32 E4M3 quantization of the BF16
 // output (y may be null: quantized output only).

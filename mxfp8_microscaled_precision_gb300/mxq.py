@@ -74,8 +74,6 @@ def lib() -> ctypes.CDLL:
         L.mxq_gemm_bf16out.argtypes = [P, P, P, P, I64, I64, I64, S, P, I64, P]
         L.mxq_grouped_gemm.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, I64, P]
         L.mxq_gemm_mxfp8out.argtypes = [P, P, P, P, I64, I64, I64, S, P, I64, P, P, P]
-        L.mxq_gemm_workspace_bytes.argtypes, L.mxq_gemm_workspace_bytes.restype = [I64, I64, I64], SZ
-        L.mxq_gemm_bf16out_ws.argtypes = [P, P, P, P, I64, I64, I64, S, P, I64, P, SZ, P]
         L.mxq_fsdp_payload_layout.argtypes = [S, I64, I64, I32, ctypes.POINTER(I64), ctypes.POINTER(I64)]
         L.mxq_fsdp_unpack.argtypes = [S, I64, I64, I32, P, P, P, P, P, P]
         L.mxq_get_device_status.argtypes = []
@@ -84,7 +82,7 @@ def lib() -> ctypes.CDLL:
                   "mxq_grouped_gemm", "mxq_get_device_status", "mxq_debug_wait_timeout",
                   "mxq_quant_1x32_dual_batched", "mxq_quant_1x32_cols_grouped",
                   "mxq_grouped_gemm_wgrad", "mxq_gemm_bf16out_fmt", "mxq_gemm_mxfp8out",
-                  "mxq_fsdp_payload_layout", "mxq_fsdp_unpack", "mxq_gemm_bf16out_ws"):
+                  "mxq_fsdp_payload_layout", "mxq_fsdp_unpack"):
             getattr(L, f).restype = S
         _lib = L
         return L
@@ -236,27 +234,14 @@ def quant_32x32(w: torch.Tensor, layout="tiled", out=None):
     return q, s_fwd, s_bwd
 
 
-def gemm(a_q, a_s, b_q, b_s, M: int, N: int, K: int, b_mn_major: bool = False, out=None, workspace=None):
-    """y [M, N] bf16 = deq(A) deq(B)^T with tiled scales (see mxq_gemm_bf16out).
-    `workspace` (a uint8 CUDA tensor, see gemm_workspace_bytes) enables stream-K
-    scheduling of the last partial wave of tiles (mxq_gemm_bf16out_ws)."""
+def gemm(a_q, a_s, b_q, b_s, M: int, N: int, K: int, b_mn_major: bool = False, out=None):
+    """y [M, N] bf16 = deq(A) deq(B)^T with tiled scales (see mxq_gemm_bf16out)."""
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=a_q.device)
-    if workspace is None:
-        _check(lib().mxq_gemm_bf16out(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K,
-                                      1 if b_mn_major else 0, _ptr(out), out.stride(0), _stream()),
-               "mxq_gemm_bf16out")
-    else:
-        _check(lib().mxq_gemm_bf16out_ws(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K,
-                                         1 if b_mn_major else 0, _ptr(out), out.stride(0), _ptr(workspace),
-                                         workspace.numel() * workspace.element_size(), _stream()),
-               "mxq_gemm_bf16out_ws")
+    _check(lib().mxq_gemm_bf16out(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K,
+                                  1 if b_mn_major else 0, _ptr(out), out.stride(0), _stream()),
+           "mxq_gemm_bf16out")
     return out
-
-
-def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
-    """Workspace bytes mxq_gemm_bf16out_ws can use for this shape on the current device (0: none)."""
-    return int(lib().mxq_gemm_workspace_bytes(M, N, K))
 
 
 def gemm_fmt(a_q, a_s, a_fmt, b_q, b_s, b_fmt, M: int, N: int, K: int, b_mn_major: bool = False, out=None):

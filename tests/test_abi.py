@@ -110,17 +110,6 @@ def test_moe_backward_argument_errors(L):
     assert w(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 300, 1024, 128, 128, FAKE, 128, None) == 1   # G < 1
 
 
-def test_stream_k_argument_errors(L):
-    g = L.mxq_gemm_bf16out_ws
-    odd_ws = ctypes.c_void_p(0x10010)      # 16- but not 256-byte aligned
-    assert g(FAKE, FAKE, FAKE, FAKE, 64, 40, 64, 0, FAKE, 40, None, 0, None) == 2        # N % 16
-    assert g(FAKE, FAKE, FAKE, FAKE, 64, 64, 48, 0, FAKE, 64, None, 0, None) == 2        # K % 32
-    assert g(FAKE, FAKE, FAKE, FAKE, 64, 64, 64, 0, FAKE, 64, odd_ws, 1 << 20, None) == 1  # workspace alignment
-    assert g(FAKE, FAKE, FAKE, FAKE, 64, 64, 64, 0, FAKE, 60, None, 0, None) == 1        # ldy < N
-    assert g(FAKE, FAKE, FAKE, FAKE, 64, 64, 64, 3, FAKE, 64, None, 0, None) == 1        # bad flag
-    assert L.mxq_gemm_workspace_bytes(0, 64, 64) == 0
-
-
 def test_fused_quant_gemm_argument_errors(L):
     g = L.mxq_gemm_mxfp8out
     assert g(FAKE, FAKE, FAKE, FAKE, 64, 48, 64, 0, FAKE, 48, FAKE, FAKE, None) == 2    # N % 32
