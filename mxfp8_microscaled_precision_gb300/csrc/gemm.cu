@@ -218,8 +218,8 @@ __device__ __forceinline__ void store_row(const GemmArgs& p, uint32_t (&v)[4][32
                 code = static_cast<uint32_t>(e + 127);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    o[j] = scale_cvt_fp8x2<0>(bf16_lo(b[2 * j]), bf16_hi(b[2 * j]), sc) |
-                           (scale_cvt_fp8x2<0>(bf16_lo(b[2 * j + 1]), bf16_hi(b[2 * j + 1]), sc) << 16);
+                    o[j] = cvt_fp8x2<0>(bf16_lo(b[2 * j]) * sc, bf16_hi(b[2 * j]) * sc) |
+                           (cvt_fp8x2<0>(bf16_lo(b[2 * j + 1]) * sc, bf16_hi(b[2 * j + 1]) * sc) << 16);
             }
             if (grp_ok) {
                 uint4* qd = reinterpret_cast<uint4*>(p.yq + row * p.N + nc);

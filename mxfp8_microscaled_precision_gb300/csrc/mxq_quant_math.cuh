@@ -33,19 +33,6 @@ __device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
     return kFmt == 0 ? cvt_e4m3x2(lo, hi) : cvt_e5m2x2(lo, hi);
 }
 
-// (lo * s, hi * s) in one packed FP32 multiply (IEEE round to nearest per lane,
-// subnormals kept: exact here, s is a power of two), then both to FP8.
-template <int kFmt>
-__device__ __forceinline__ uint32_t scale_cvt_fp8x2(float lo, float hi, float s) {
-    uint64_t a, b, r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(lo), "f"(hi));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(b) : "f"(s));
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    float x, y;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
-    return cvt_fp8x2<kFmt>(x, y);
-}
-
 // 2^-e as a float for e in [-127, 120] (always a normal number).
 __device__ __forceinline__ float pow2_neg(int e) { return __int_as_float((127 - e) << 23); }
 

@@ -45,10 +45,10 @@ constexpr int kSmemBytes = kRing * kTileBytes + 1024 + 256;     // ring + alignm
 template <int kFmt = 0>
 __device__ __forceinline__ uint2 quant8(const uint4 v, float sc) {
     uint2 o;
-    o.x = scale_cvt_fp8x2<kFmt>(bf16_lo(v.x), bf16_hi(v.x), sc) |
-          (scale_cvt_fp8x2<kFmt>(bf16_lo(v.y), bf16_hi(v.y), sc) << 16);
-    o.y = scale_cvt_fp8x2<kFmt>(bf16_lo(v.z), bf16_hi(v.z), sc) |
-          (scale_cvt_fp8x2<kFmt>(bf16_lo(v.w), bf16_hi(v.w), sc) << 16);
+    o.x = cvt_fp8x2<kFmt>(bf16_lo(v.x) * sc, bf16_hi(v.x) * sc) |
+          (cvt_fp8x2<kFmt>(bf16_lo(v.y) * sc, bf16_hi(v.y) * sc) << 16);
+    o.y = cvt_fp8x2<kFmt>(bf16_lo(v.z) * sc, bf16_hi(v.z) * sc) |
+          (cvt_fp8x2<kFmt>(bf16_lo(v.w) * sc, bf16_hi(v.w) * sc) << 16);
     return o;
 }
 
@@ -289,8 +289,9 @@ __device__ __forceinline__ void col_pass(const uint32_t* tw, int64_t c0, int64_t
             for (int j = 0; j < 8; ++j) {
                 float f[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) f[u] = half ? bf16_hi(w[4 * j + u]) : bf16_lo(w[4 * j + u]);
-                o[j] = scale_cvt_fp8x2<kFmt>(f[0], f[1], sc) | (scale_cvt_fp8x2<kFmt>(f[2], f[3], sc) << 16);
+                for (int u = 0; u < 4; ++u)
+                    f[u] = (half ? bf16_hi(w[4 * j + u]) : bf16_lo(w[4 * j + u])) * sc;
+                o[j] = cvt_fp8x2<kFmt>(f[0], f[1]) | (cvt_fp8x2<kFmt>(f[2], f[3]) << 16);
             }
         }
         if (ok) {
