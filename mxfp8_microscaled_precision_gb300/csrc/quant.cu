@@ -241,26 +241,10 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t* __
 // row per step (conflict-free).  The group's first token is tok0 + 32 (t/64)
 // in the output (row stride out_ld, out_ld/32 scale groups); groups at or past
 // tok_limit are not written (tiled layout: their scale is padding, 0).
-// The column pass in two halves: col_load reads this thread's 32 staged words
-// (and their packed maxima) into registers, after which the staged tile may be
-// overwritten; col_store quantizes and writes them.
-__device__ __forceinline__ uint32_t col_load(const uint32_t* tw, uint32_t (&w)[32]) {
-    const int t = threadIdx.x;
-    const int p = t & 63;
-    const int gi = t >> 6;
-    uint32_t m2 = 0u;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        w[j] = tw[(32 * gi + j) * 64 + p];
-        m2 = max_u16x2(m2, w[j] & 0x7FFF7FFFu);
-    }
-    return m2;
-}
-
 template <bool kTiled, int kFmt>
-__device__ __forceinline__ void col_store(const uint32_t (&w)[32], uint32_t m2, int64_t c0, int64_t cols,
-                                          int64_t out_ld, int64_t tok0, int64_t tok_limit,
-                                          uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
+__device__ __forceinline__ void col_pass(const uint32_t* tw, int64_t c0, int64_t cols, int64_t out_ld,
+                                         int64_t tok0, int64_t tok_limit, uint8_t* __restrict__ q_col,
+                                         uint8_t* __restrict__ s_col) {
     const int t = threadIdx.x;
     const int p = t & 63;
     const int gi = t >> 6;
@@ -269,6 +253,13 @@ __device__ __forceinline__ void col_store(const uint32_t (&w)[32], uint32_t m2, 
     const int64_t ogroups = out_ld >> 5;
     const int64_t g_out = tok >> 5;
     const bool ok = cA < cols && tok < tok_limit;
+    uint32_t w[32];
+    uint32_t m2 = 0u;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        w[j] = tw[(32 * gi + j) * 64 + p];
+        m2 = max_u16x2(m2, w[j] & 0x7FFF7FFFu);
+    }
     uint8_t* q0 = q_col + cA * out_ld + tok;
     // Scale bytes of rows cA and cA+1 (same 32-row block: cA is even).
     uint8_t* s0 = kTiled ? s_col + tiled_scale_offset(cA, g_out, ogroups) : s_col + cA * ogroups + g_out;
@@ -312,15 +303,6 @@ __device__ __forceinline__ void col_store(const uint32_t (&w)[32], uint32_t m2, 
     }
 }
 
-template <bool kTiled, int kFmt>
-__device__ __forceinline__ void col_pass(const uint32_t* tw, int64_t c0, int64_t cols, int64_t out_ld,
-                                         int64_t tok0, int64_t tok_limit, uint8_t* __restrict__ q_col,
-                                         uint8_t* __restrict__ s_col) {
-    uint32_t w[32];
-    const uint32_t m2 = col_load(tw, w);
-    col_store<kTiled, kFmt>(w, m2, c0, cols, out_ld, tok0, tok_limit, q_col, s_col);
-}
-
 // Column copy (with or without the row copy): persistent, TMA-fed ring.
 // Column pass: thread t takes the column pair t % 64 and the 32-row group
 // t / 64; a warp reads 128 contiguous bytes of one staged row per step, so
@@ -344,17 +326,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_kernel(
         const uint8_t* buf = ring.buf + (i % kRing) * kTileBytes;
         int64_t b, r0, c0;
         tg.at(tile, b, r0, c0);
-        // Read everything the passes need from the slot first, then hand the slot
-        // back to TMA before the column copy is converted and written.
-        uint32_t w[32];
-        const uint32_t m2 = col_load(reinterpret_cast<const uint32_t*>(buf), w);
         if constexpr (kRow) {
             const uint4* b4 = reinterpret_cast<const uint4*>(buf) + (t >> 4) * 16 + (t & 15);
             row_pass<kTiled, kFmt>([&](int j) { return b4[j * 256]; }, r0, c0, rows, cols, q_row + b * bs.q_row,
                              s_row + b * bs.s_row);
         }
+        col_pass<kTiled, kFmt>(reinterpret_cast<const uint32_t*>(buf), c0, cols, rows, r0, rows,
+                         q_col + b * bs.q_col, s_col + b * bs.s_col);
         ring_release(ring, &tmap, i, tile, tg);
-        col_store<kTiled, kFmt>(w, m2, c0, cols, rows, r0, rows, q_col + b * bs.q_col, s_col + b * bs.s_col);
     }
     ring_drain(ring, i, tile, tg.n_tiles, guard);
 }
