@@ -242,9 +242,10 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t* __
 // in the output (row stride out_ld, out_ld/32 scale groups); groups at or past
 // tok_limit are not written (tiled layout: their scale is padding, 0).
 template <bool kTiled, int kFmt>
-__device__ __forceinline__ void col_pass(const uint32_t* tw, int64_t c0, int64_t cols, int64_t out_ld,
+__device__ __forceinline__ void col_pass(const uint32_t* tw_ptr, int64_t c0, int64_t cols, int64_t out_ld,
                                          int64_t tok0, int64_t tok_limit, uint8_t* __restrict__ q_col,
                                          uint8_t* __restrict__ s_col) {
+    const uint32_t tw = smem_u32(tw_ptr);   // the staged tile is in shared memory
     const int t = threadIdx.x;
     const int p = t & 63;
     const int gi = t >> 6;
@@ -257,7 +258,7 @@ __device__ __forceinline__ void col_pass(const uint32_t* tw, int64_t c0, int64_t
     uint32_t m2 = 0u;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-        w[j] = tw[(32 * gi + j) * 64 + p];
+        w[j] = lds32(tw + 4u * static_cast<uint32_t>((32 * gi + j) * 64 + p));
         m2 = max_u16x2(m2, w[j] & 0x7FFF7FFFu);
     }
     uint8_t* q0 = q_col + cA * out_ld + tok;
@@ -327,9 +328,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_kernel(
         int64_t b, r0, c0;
         tg.at(tile, b, r0, c0);
         if constexpr (kRow) {
-            const uint4* b4 = reinterpret_cast<const uint4*>(buf) + (t >> 4) * 16 + (t & 15);
-            row_pass<kTiled, kFmt>([&](int j) { return b4[j * 256]; }, r0, c0, rows, cols, q_row + b * bs.q_row,
-                             s_row + b * bs.s_row);
+            const uint32_t b4 = smem_u32(buf) + 16u * static_cast<uint32_t>((t >> 4) * 16 + (t & 15));
+            row_pass<kTiled, kFmt>([&](int j) { return lds128(b4 + 4096u * j); }, r0, c0, rows, cols,
+                                   q_row + b * bs.q_row, s_row + b * bs.s_row);
         }
         col_pass<kTiled, kFmt>(reinterpret_cast<const uint32_t*>(buf), c0, cols, rows, r0, rows,
                          q_col + b * bs.q_col, s_col + b * bs.s_col);
