@@ -8,6 +8,7 @@ point query, so the library needs nothing but the NVIDIA driver at run time).
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -41,10 +42,22 @@ def _stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if needed) and return the path of libmxq.so."""
+    """Compile (if needed) and return the path of libmxq.so.  Processes that
+    build at the same time (one per rank) take turns on a lock file."""
     if not force and not _stale():
         return LIB
     os.makedirs(OUT, exist_ok=True)
+    with open(os.path.join(OUT, ".build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and not _stale():   # another process built it meanwhile
+                return LIB
+            return _build(verbose)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build(verbose: bool) -> str:
     nvcc = _nvcc()
     objs = []
 
