@@ -183,7 +183,8 @@ def grouped_capacity(M_total: int, G: int) -> int:
 def quant_cols_grouped(x: torch.Tensor, offsets: torch.Tensor, capacity: int = None, layout="tiled"):
     """Token-axis quantization inside each expert (see mxq_quant_1x32_cols_grouped).
     x: bf16 [M_total, C] sorted by expert; offsets: int64 CUDA [G+1].
-    Returns (q_col [C, capacity], s_col)."""
+    Returns (q_col [C, capacity], s_col); the columns past the last expert's slot,
+    which the kernel does not write, are zero."""
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
         raise ValueError("x must be a 2-D bfloat16 CUDA tensor with unit last stride")
     if offsets.dtype != torch.int64 or not offsets.is_cuda:
@@ -192,8 +193,8 @@ def quant_cols_grouped(x: torch.Tensor, offsets: torch.Tensor, capacity: int = N
     G = offsets.numel() - 1
     if capacity is None:
         capacity = grouped_capacity(R, G)
-    q_col = torch.empty((C, capacity), dtype=torch.uint8, device=x.device)
-    s_col = _scale_tensor(C, capacity, layout, x.device)
+    q_col = torch.zeros((C, capacity), dtype=torch.uint8, device=x.device)
+    s_col = _scale_tensor(C, capacity, layout, x.device).zero_()
     _check(lib().mxq_quant_1x32_cols_grouped(_ptr(x), R, C, x.stride(0), _ptr(offsets), G, capacity,
                                              _ptr(q_col), _ptr(s_col), _layout(layout), _stream()),
            "mxq_quant_1x32_cols_grouped")
