@@ -133,6 +133,7 @@ __device__ __forceinline__ void ring_release(const Ring& r, const CUtensorMap* m
     __syncthreads();
     if (threadIdx.x == 0) {
         const int64_t next = tile + static_cast<int64_t>(kRing) * gridDim.x;
+        fence_proxy_async_smem();   // the slot's reads (and writes) come before the TMA refill
         if (next < tg.n_tiles) ring_load(r, map, i % kRing, next, tg);
     }
 }
@@ -412,6 +413,115 @@ __global__ void __launch_bounds__(kThreads) quant_cols_grouped_kernel(
     }
 }
 
+// The same token-axis quantization, persistent and fed by the TMA ring: a tile
+// is 128 tokens of one expert's slot x 128 columns, loaded from the tokens'
+// rows of x (rows past the expert's last token are zeroed in shared memory
+// before the column pass).  The slot schedule is built per CTA as above.
+struct GroupedTile {
+    int64_t pos, c0, row0, valid;   // slot position, first column, first row of x, real rows (1..128)
+};
+
+__device__ __forceinline__ GroupedTile grouped_tile(int64_t tl, int64_t tiles_c, const int64_t* s_off,
+                                                    const int64_t* s_slot, int G) {
+    GroupedTile gt;
+    gt.pos = (tl / tiles_c) * kTile;
+    gt.c0 = (tl % tiles_c) * kTile;
+    int lo = 0, hi = G;  // owner: largest g with s_slot[g] <= pos
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_slot[mid] <= gt.pos) lo = mid; else hi = mid;
+    }
+    gt.row0 = s_off[lo] + (gt.pos - s_slot[lo]);
+    const int64_t left = s_off[lo + 1] - gt.row0;
+    gt.valid = left < kTile ? left : kTile;
+    return gt;
+}
+
+template <bool kTiled>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_grouped_ring_kernel(
+    const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_t cols, const int64_t* __restrict__ offsets,
+    int G, int64_t capacity, uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, unsigned int* status,
+    uint64_t wait_limit_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    const Ring ring = ring_setup(smem_raw);
+    const WaitGuard guard{ring.abort_flag, status, wait_limit_ns};
+    int64_t* s_off = reinterpret_cast<int64_t*>(ring.buf + kRing * kTileBytes + 64);   // [G+1]
+    int64_t* s_slot = s_off + (G + 1);                                                  // [G+1]
+    const int t = threadIdx.x;
+    const int warp = t >> 5, lane = t & 31;
+    for (int g = t; g <= G; g += kThreads) {
+        int64_t o = offsets[g];
+        s_off[g] = o < 0 ? 0 : (o > rows ? rows : o);  // malformed offsets stay in bounds
+    }
+    __syncthreads();
+    if (warp == 0) {  // exclusive prefix of the slot lengths, 32 experts at a time
+        int64_t carry = 0;
+        for (int base = 0; base < G; base += 32) {
+            const int g = base + lane;
+            int64_t len = 0;
+            if (g < G) {
+                const int64_t m = s_off[g + 1] - s_off[g];
+                len = m > 0 ? (m + kTile - 1) / kTile * kTile : 0;
+            }
+            int64_t incl = len;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= d) incl += y;
+            }
+            if (g < G) s_slot[g] = carry + incl - len;
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) s_slot[G] = carry;
+    }
+    __syncthreads();
+    const int64_t used = s_slot[G] < capacity ? s_slot[G] : capacity;
+    const int64_t tiles_c = (cols + kTile - 1) / kTile;
+    const int64_t n_tiles = (used / kTile) * tiles_c;
+
+    auto issue = [&](int slot, int64_t tl) {
+        const GroupedTile gt = grouped_tile(tl, tiles_c, s_off, s_slot, G);
+        const uint32_t bar = ring.bar0 + 8u * slot;
+        mbar_arrive_expect_tx(bar, kTileBytes);
+        tma_load_3d(smem_u32(ring.buf + slot * kTileBytes), &tmap, static_cast<int32_t>(gt.c0),
+                    static_cast<int32_t>(gt.row0), 0, bar);
+    };
+    if (t == 0) {
+        for (int sl = 0; sl < kRing; ++sl) mbar_init(ring.bar0 + 8u * sl, 1);
+        *ring.abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tmap);
+        for (int sl = 0; sl < kRing; ++sl) {
+            const int64_t tl = blockIdx.x + static_cast<int64_t>(sl) * gridDim.x;
+            if (tl < n_tiles) issue(sl, tl);
+        }
+    }
+    __syncthreads();
+
+    int i = 0;
+    int64_t tl = blockIdx.x;
+    for (; tl < n_tiles; tl += gridDim.x, ++i) {
+        if (!ring_wait(ring, i, guard)) break;
+        uint8_t* buf = ring.buf + (i % kRing) * kTileBytes;
+        const GroupedTile gt = grouped_tile(tl, tiles_c, s_off, s_slot, G);
+        if (gt.valid < kTile) {   // tokens of the next expert (or past x) read as zero
+            uint4* b4 = reinterpret_cast<uint4*>(buf);
+            for (int u = static_cast<int>(gt.valid) * 16 + t; u < kTile * 16; u += kThreads)
+                b4[u] = make_uint4(0u, 0u, 0u, 0u);
+            __syncthreads();
+        }
+        col_pass<kTiled, 0>(reinterpret_cast<const uint32_t*>(buf), gt.c0, cols, capacity, gt.pos, capacity, q_col,
+                            s_col);
+        __syncthreads();
+        if (t == 0) {
+            const int64_t next = tl + static_cast<int64_t>(kRing) * gridDim.x;
+            fence_proxy_async_smem();   // the slot's reads and zeroing come before the TMA refill
+            if (next < n_tiles) issue(i % kRing, next);
+        }
+    }
+    ring_drain(ring, i, tl, n_tiles, guard);
+}
+
 // ---------------------------------------------------------------------------------
 // 32x32 block quantization of w [n, k]: one 128x128 tile (16 blocks) per CTA.
 template <bool kTiled>
@@ -571,34 +681,40 @@ cudaError_t launch_quant_1x32(const DeviceInfo& dev, const void* x, int64_t batc
 cudaError_t launch_quant_cols_grouped(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols,
                                       int64_t ld, const int64_t* offsets, int G, int64_t capacity,
                                       void* q_col, void* s_col, bool tiled, cudaStream_t stream) {
-    const size_t smem = kTile * kTile * 2 + 128 + 2 * 8 * static_cast<size_t>(G + 1);
-    auto xp = static_cast<const uint16_t*>(x);
+    const size_t smem = kRing * kTileBytes + 1024 + 64 + 2 * 8 * static_cast<size_t>(G + 1);
     auto qp = static_cast<uint8_t*>(q_col);
     auto sp = static_cast<uint8_t*>(s_col);
     const int64_t max_tiles = (capacity / kTile) * ((cols + kTile - 1) / kTile);
-    const int64_t cap = static_cast<int64_t>(dev.sm_count) * 4;
-    const unsigned grid = static_cast<unsigned>(max_tiles < cap ? max_tiles : cap);
-    if (grid == 0) return cudaSuccess;
+    if (max_tiles == 0) return cudaSuccess;
+    CUtensorMap map;
+    if (!encode_tensor_map_3d(&map, x, true, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows), 1,
+                              static_cast<uint64_t>(ld) * 2, static_cast<uint64_t>(ld) * 2 * static_cast<uint64_t>(rows),
+                              kTile, kTile))
+        return cudaErrorInvalidValue;
+    auto run = [&](auto kern, int* configured, int* per_sm) -> cudaError_t {
+        if (*configured != dev.device) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(kRing * kTileBytes + 1024 + 64 + 16 * 1025));
+            if (e != cudaSuccess) return e;
+            *configured = dev.device;
+        }
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem);
+        if (e != cudaSuccess) return e;
+        *per_sm = n < 1 ? 1 : n;
+        const int64_t cap = static_cast<int64_t>(dev.sm_count) * *per_sm;
+        const unsigned grid = static_cast<unsigned>(max_tiles < cap ? max_tiles : cap);
+        kern<<<grid, kThreads, smem, stream>>>(map, rows, cols, offsets, G, capacity, qp, sp, dev.status,
+                                               kDefaultWaitLimitNs);
+        return cudaGetLastError();
+    };
+    int per_sm = 0;
     if (tiled) {
         static thread_local int configured = -1;
-        if (configured != dev.device) {
-            cudaError_t e = cudaFuncSetAttribute(quant_cols_grouped_kernel<true>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-            if (e != cudaSuccess) return e;
-            configured = dev.device;
-        }
-        quant_cols_grouped_kernel<true><<<grid, kThreads, smem, stream>>>(xp, rows, cols, ld, offsets, G, capacity, qp, sp);
-    } else {
-        static thread_local int configured = -1;
-        if (configured != dev.device) {
-            cudaError_t e = cudaFuncSetAttribute(quant_cols_grouped_kernel<false>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-            if (e != cudaSuccess) return e;
-            configured = dev.device;
-        }
-        quant_cols_grouped_kernel<false><<<grid, kThreads, smem, stream>>>(xp, rows, cols, ld, offsets, G, capacity, qp, sp);
+        return run(quant_cols_grouped_ring_kernel<true>, &configured, &per_sm);
     }
-    return cudaGetLastError();
+    static thread_local int configured = -1;
+    return run(quant_cols_grouped_ring_kernel<false>, &configured, &per_sm);
 }
 
 cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, int64_t k, int64_t ld,
