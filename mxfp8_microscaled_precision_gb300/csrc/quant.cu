@@ -346,77 +346,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_kernel(
 // 32-token group starts at the expert's first token and is zero-padded past
 // its last.  The slots are computed from the device offsets by every CTA (in
 // shared memory); the CTAs then walk the (slot block, column block) tiles.
-template <bool kTiled>
-__global__ void __launch_bounds__(kThreads) quant_cols_grouped_kernel(
-    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
-    const int64_t* __restrict__ offsets, int G, int64_t capacity, uint8_t* __restrict__ q_col,
-    uint8_t* __restrict__ s_col) {
-    extern __shared__ uint8_t smem_raw[];
-    uint32_t* tile = reinterpret_cast<uint32_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
-    int64_t* s_off = reinterpret_cast<int64_t*>(tile + kTile * kTile / 2);  // [G+1]
-    int64_t* s_slot = s_off + (G + 1);                                      // [G+1]
-    const int t = threadIdx.x;
-    const int warp = t >> 5, lane = t & 31;
-    for (int g = t; g <= G; g += kThreads) {
-        int64_t o = offsets[g];
-        s_off[g] = o < 0 ? 0 : (o > rows ? rows : o);  // malformed offsets stay in bounds
-    }
-    __syncthreads();
-    if (warp == 0) {  // exclusive prefix of the slot lengths, 32 experts at a time
-        int64_t carry = 0;
-        for (int base = 0; base < G; base += 32) {
-            const int g = base + lane;
-            int64_t len = 0;
-            if (g < G) {
-                const int64_t m = s_off[g + 1] - s_off[g];
-                len = m > 0 ? (m + kTile - 1) / kTile * kTile : 0;
-            }
-            int64_t incl = len;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const int64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-                if (lane >= d) incl += y;
-            }
-            if (g < G) s_slot[g] = carry + incl - len;
-            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
-        }
-        if (lane == 0) s_slot[G] = carry;
-    }
-    __syncthreads();
-    const int64_t used = s_slot[G] < capacity ? s_slot[G] : capacity;
-    const int64_t tiles_c = (cols + kTile - 1) / kTile;
-    const int64_t n_tiles = (used / kTile) * tiles_c;
-    const int chunk = t & 15;
-    for (int64_t tl = blockIdx.x; tl < n_tiles; tl += gridDim.x) {
-        const int64_t pos = (tl / tiles_c) * kTile;   // slot position of this 128-token block
-        const int64_t c0 = (tl % tiles_c) * kTile;
-        int lo = 0, hi = G;  // owner: largest g with s_slot[g] <= pos
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (s_slot[mid] <= pos) lo = mid; else hi = mid;
-        }
-        const int64_t row0 = s_off[lo] + (pos - s_slot[lo]);
-        const int64_t row_end = s_off[lo + 1];
-        const int64_t col = c0 + chunk * 8;
-        const uint16_t* xp = x + row0 * ld + col;
-#pragma unroll
-        for (int j = 0; j < kLoadsPerThread; ++j) {
-            const int lr = (t >> 4) + 16 * j;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (col < cols && row0 + lr < row_end) v = __ldg(reinterpret_cast<const uint4*>(xp + lr * ld));
-            reinterpret_cast<uint4*>(tile)[lr * 16 + chunk] = v;
-        }
-        __syncthreads();
-        col_pass<kTiled, 0>(tile, c0, cols, capacity, pos, capacity, q_col, s_col);
-        __syncthreads();
-    }
-}
-
-// The same token-axis quantization, persistent and fed by the TMA ring: a tile
-// is 128 tokens of one expert's slot x 128 columns, loaded from the tokens'
-// rows of x (rows past the expert's last token are zeroed in shared memory
-// before the column pass).  The slot schedule is built per CTA as above.
+// Persistent and fed by the TMA ring: a tile is 128 tokens of one expert's
+// slot x 128 columns, loaded from the tokens' rows of x (rows past the
+// expert's last token are zeroed in shared memory before the column pass).
 struct GroupedTile {
     int64_t pos, c0, row0, valid;   // slot position, first column, first row of x, real rows (1..128)
 };
