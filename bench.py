@@ -290,6 +290,75 @@ class LinearFwdSmall(Workload):
         return time.perf_counter() - t0, "the whole step (quantization of X and W, FP64 GEMM)"
 
 
+class LinearFwdChain(Workload):
+    """Forward of one linear layer whose output feeds the next MXFP8 layer:
+    Y = X W^T in BF16 plus Y's 1x32 row quantization (the next layer's input),
+    either from the GEMM's quantizing epilogue ("fused") or by a separate
+    quantizer pass over Y ("two_pass").  Shapes of linear_train."""
+    state_keys = ("W",)
+
+    def __init__(self, fused, dev=None, M=8192, N=4096, K=4096):
+        import torch
+        from mxfp8_microscaled_precision_gb300 import mxq, workloads
+        self.fused = fused
+        self.name = "linear_fwd_chain_" + ("fused" if fused else "two_pass")
+        self.M, self.N, self.K = M, N, K
+        d = workloads.linear_train(dev or "cpu", M, N, K)
+        self.inputs = {"X": d["X"], "W": d["W"]}
+        if dev is None:
+            return
+        u8 = dict(dtype=torch.uint8, device=dev)
+        self.qx = (torch.empty((M, K), **u8), torch.empty(mxq.scale_bytes(M, K), **u8), None, None)
+        self.qw = (torch.empty((N, K), **u8), torch.empty(mxq.scale_bytes(N, K), **u8), None, None)
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.qy = (torch.empty((M, N), **u8), torch.empty(mxq.scale_bytes(M, N), **u8), None, None)
+        self.outputs = [self.y, self.qy[0], self.qy[1]]
+
+    @property
+    def gemm_flops(self):
+        return 2 * self.M * self.N * self.K
+
+    def kernels(self):
+        from mxfp8_microscaled_precision_gb300 import mxq
+        M, N, K, i = self.M, self.N, self.K, self.inputs
+        ks = [("quant_X_row", "quant", _row_bytes(M, K), lambda: mxq.quant_1x32_dual(i["X"], col=False, out=self.qx)),
+              ("quant_W_row", "quant", _row_bytes(N, K), lambda: mxq.quant_1x32_dual(i["W"], col=False, out=self.qw))]
+        if self.fused:
+            ks.append(("gemm_fwd_quantout", "gemm", 2 * M * N * K,
+                       lambda: mxq.gemm_mxfp8out(self.qx[0], self.qx[1], self.qw[0], self.qw[1], M, N, K,
+                                                 out=(self.y, self.qy[0], self.qy[1]))))
+        else:
+            ks.append(("gemm_fwd", "gemm", 2 * M * N * K,
+                       lambda: mxq.gemm(self.qx[0], self.qx[1], self.qw[0], self.qw[1], M, N, K, out=self.y)))
+            ks.append(("quant_Y_row", "quant", _row_bytes(M, N),
+                       lambda: mxq.quant_1x32_dual(self.y, col=False, out=self.qy)))
+        return ks
+
+    def cpu_sample(self, budget_s):
+        from oracle import oracle
+        import numpy as np
+        i = self.inputs
+        x = _host_bits(i["X"][:64])
+        t0 = time.perf_counter()
+        xq, xs = oracle.quant_rows(x)
+        tq = (time.perf_counter() - t0) / x.size
+        a = oracle.dequant_rows(xq, xs)
+        wq, ws = oracle.quant_rows(_host_bits(i["W"]))
+        b = oracle.dequant_rows(wq, ws)
+        rows, t_g = 0, 0.0
+        while t_g < budget_s and rows < a.shape[0]:
+            t0 = time.perf_counter()
+            y = oracle.gemm(a, b, rows=np.array([rows], dtype=np.int64))
+            oracle.quant_rows(y.reshape(1, -1))
+            t_g += time.perf_counter() - t0
+            rows += 1
+        tg = t_g / (2.0 * rows * self.N * self.K)
+        elems = self.M * self.K + self.N * self.K
+        return tq * elems + tg * self.gemm_flops, (
+            f"oracle row quant of 64 rows of X and FP64 GEMM + row quant of {rows} output rows x {self.N} x "
+            f"{self.K}; extrapolated to the full step")
+
+
 class Weight32(Workload):
     state_keys = ("W",)
 
@@ -672,6 +741,8 @@ def make_workload(name, dev=None):
         return LinearFwdSmall(dev)
     if name == "weight_32x32":
         return Weight32(dev)
+    if name in ("linear_fwd_chain_fused", "linear_fwd_chain_two_pass"):
+        return LinearFwdChain(name.endswith("fused"), dev)
     if name == "moe_grouped":
         return MoE(dev)
     if name == "moe_train":
@@ -684,7 +755,7 @@ def make_workload(name, dev=None):
 
 
 WORKLOAD_NAMES = ["linear_train", "linear_fwd_small", "weight_32x32", "moe_grouped", "moe_train", "moe_train_small",
-                  "fsdp_mxfp8", "fsdp_mxfp8_32x32",
+                  "fsdp_mxfp8", "fsdp_mxfp8_32x32", "linear_fwd_chain_fused", "linear_fwd_chain_two_pass",
                   "sweep_4096", "sweep_7168", "sweep_16384"]
 
 
