@@ -288,9 +288,9 @@ void orc_quant_32x32(const uint16_t* w, int64_t n, int64_t k, int64_t ld,
 // to a multiple of 128 and P_g = sum of L_h over h < g; everything in the slot
 // past the expert's groups is zero payload with scale code 0.  s_col holds the
 // plain scales [cols, capacity/32].  Columns past P_G are left untouched.
-void orc_quant_cols_grouped(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
-                            const int64_t* off, int32_t G, int64_t capacity,
-                            uint8_t* q_col, uint8_t* s_col) {
+void orc_quant_cols_grouped_fmt(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                                const int64_t* off, int32_t G, int64_t capacity,
+                                uint8_t* q_col, uint8_t* s_col, int fmt) {
     (void)rows;
     const int64_t cgroups = capacity / 32;
     int64_t P = 0;
@@ -307,11 +307,17 @@ void orc_quant_cols_grouped(const uint16_t* x, int64_t rows, int64_t cols, int64
                         const int64_t t = 32 * j + i;
                         return t < m ? bf16_bits_to_double(x[(lo + t) * ld + c]) : 0.0;
                     },
-                    [&](int64_t i, uint8_t b) { dst[i] = b; });
+                    [&](int64_t i, uint8_t b) { dst[i] = b; }, fmt);
             }
         }
         P += L;
     }
+}
+
+void orc_quant_cols_grouped(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                            const int64_t* off, int32_t G, int64_t capacity,
+                            uint8_t* q_col, uint8_t* s_col) {
+    orc_quant_cols_grouped_fmt(x, rows, cols, ld, off, G, capacity, q_col, s_col, 0);
 }
 
 // ---- scale layout: plain -> MMA-tiled ---------------------------------------

@@ -76,11 +76,12 @@ def _load():
     lib.orc_quant_32x32.argtypes = [P, I64, I64, I64, P, P, P]
     lib.orc_scale_tiled.argtypes = [P, I64, I64, P]
     lib.orc_quant_cols_grouped.argtypes = [P, I64, I64, I64, P, ctypes.c_int32, I64, P, P]
+    lib.orc_quant_cols_grouped_fmt.argtypes = [P, I64, I64, I64, P, ctypes.c_int32, I64, P, P, ctypes.c_int]
     lib.orc_dequant_rows.argtypes = [P, P, I64, I64, P]
     lib.orc_gemm.argtypes = [P, P, I64, I64, I64, P, I64, P]
     lib.orc_grouped_gemm.argtypes = [P, P, P, ctypes.c_int32, I64, I64, P, I64, P]
     for f in ("orc_e4m3_encode_array", "orc_bf16_from_double_array", "orc_quant_rows",
-              "orc_quant_cols_grouped", "orc_e5m2_encode_array", "orc_quant_rows_fmt",
+              "orc_quant_cols_grouped", "orc_quant_cols_grouped_fmt", "orc_e5m2_encode_array", "orc_quant_rows_fmt",
               "orc_dequant_rows_fmt",
               "orc_quant_dual", "orc_quant_32x32", "orc_scale_tiled", "orc_dequant_rows",
               "orc_gemm", "orc_grouped_gemm"):
@@ -231,9 +232,10 @@ def padded_slots(offsets: np.ndarray):
     return P, L
 
 
-def quant_cols_grouped(x_bits: np.ndarray, offsets: np.ndarray, capacity: int):
+def quant_cols_grouped(x_bits: np.ndarray, offsets: np.ndarray, capacity: int, fmt: int = 0):
     """Column (token-axis) quantization per expert with zero padding.
-    x_bits uint16 [M_total, C] (rows sorted by expert), offsets int64 [G+1].
+    x_bits uint16 [M_total, C] (rows sorted by expert), offsets int64 [G+1];
+    fmt 0 = E4M3, 1 = E5M2 payload.
     Returns (q_col [C, capacity], s_col [C, capacity/32]) -- plain scales;
     columns past the last expert's slot are returned as 0 / code 0."""
     lib = _load()
@@ -246,7 +248,7 @@ def quant_cols_grouped(x_bits: np.ndarray, offsets: np.ndarray, capacity: int):
     assert int((P[-1] + L[-1]) if G else 0) <= capacity
     q = np.zeros((C, capacity), np.uint8)
     s = np.zeros((C, capacity // 32), np.uint8)
-    lib.orc_quant_cols_grouped(_ptr(x), R, C, C, _ptr(off), G, capacity, _ptr(q), _ptr(s))
+    lib.orc_quant_cols_grouped_fmt(_ptr(x), R, C, C, _ptr(off), G, capacity, _ptr(q), _ptr(s), int(fmt))
     return q, s
 
 

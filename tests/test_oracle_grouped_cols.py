@@ -68,3 +68,29 @@ def test_grouped_cols_expert_boundary_changes_groups(orc):
     q, s = orc.quant_cols_grouped(xb, np.array([0, 16, 48]), 256)
     assert np.all(s[:, 0] == 127 + 6 - 8)          # amax 64 -> e = -2
     assert np.all(s[:, 128 // 32] == 127 - 8)      # expert 1 alone: amax 1 -> e = -8
+
+
+@pytest.mark.parametrize("sizes", [[0, 5, 0, 300, 1, 130], [33, 31, 129, 127, 0]])
+def test_grouped_cols_e5m2_equals_padded_block_row_quant(orc, sizes):
+    """The E5M2 destination type (MindSpeed RFC section 3.5.2.3) of the same
+    layout: each expert's zero-padded block, transposed, quantized by the
+    pinned E5M2 row quantizer."""
+    off = _offsets(sizes)
+    M = int(off[-1])
+    C = 64
+    g = torch.Generator().manual_seed(M + 5)
+    x = torch.randn(M, C, generator=g) * torch.pow(2.0, torch.randint(-20, 21, (M, 1), generator=g).float())
+    xb = _bits(x)
+    P, L = orc.padded_slots(off)
+    cap = int(P[-1] + L[-1]) + 128
+    q, s = orc.quant_cols_grouped(xb, off, cap, fmt=1)
+    q4, _ = orc.quant_cols_grouped(xb, off, cap, fmt=0)
+    assert not np.array_equal(q, q4)                     # the format reaches the payload
+    for e, m in enumerate(sizes):
+        if L[e] == 0:
+            continue
+        blk = np.zeros((int(L[e]), C), np.uint16)
+        blk[:m] = xb[off[e]:off[e + 1]]
+        qe, se = orc.quant_rows_fmt(np.ascontiguousarray(blk.T), 1)
+        assert np.array_equal(q[:, P[e]:P[e] + L[e]], qe)
+        assert np.array_equal(s[:, P[e] // 32:(P[e] + L[e]) // 32], se)
