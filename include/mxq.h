@@ -159,6 +159,14 @@ mxq_status mxq_quant_1x32_cols_grouped(const void* x, int64_t rows, int64_t cols
                                        void* q_col, void* s_col, mxq_scale_layout layout,
                                        mxq_stream_t stream);
 
+/* mxq_quant_1x32_cols_grouped with the payload format (E4M3 or E5M2: the RFC's
+ * dst_type, section 3.5.2.3), e.g. E5M2 output gradients for the weight
+ * gradient; the rceil rule uses the format's largest finite value. */
+mxq_status mxq_quant_1x32_cols_grouped_fmt(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                           const int64_t* group_offsets, int32_t G, int64_t capacity,
+                                           void* q_col, void* s_col, mxq_scale_layout layout,
+                                           mxq_fp8_format fmt, mxq_stream_t stream);
+
 /*
  * 32x32 block quantization (the "mxfp8-32x32" recipe; RFC sections 3.1 and
  * 3.3.3 "block_mx_quant": one payload, forward and backward scales).
@@ -301,6 +309,13 @@ mxq_status mxq_grouped_gemm(const void* a_q, const void* a_s, const void* b_q, c
                             const int64_t* group_offsets, int32_t G, int64_t M_total,
                             int64_t N, int64_t K, void* y, int64_t ldy, mxq_stream_t stream);
 
+/* mxq_grouped_gemm with the payload format of each operand (E4M3 or E5M2),
+ * e.g. E5M2 gradients against E4M3 weights in the MoE dgrad. */
+mxq_status mxq_grouped_gemm_fmt(const void* a_q, const void* a_s, mxq_fp8_format a_fmt,
+                                const void* b_q, const void* b_s, mxq_fp8_format b_fmt,
+                                const int64_t* group_offsets, int32_t G, int64_t M_total,
+                                int64_t N, int64_t K, void* y, int64_t ldy, mxq_stream_t stream);
+
 /*
  * Grouped weight-gradient GEMM for MoE experts: for every expert g
  *
@@ -318,6 +333,13 @@ mxq_status mxq_grouped_gemm_wgrad(const void* a_q, const void* a_s, const void* 
                                   const int64_t* group_offsets, int32_t G, int64_t M_total,
                                   int64_t capacity, int64_t M, int64_t N, void* y, int64_t ldy,
                                   mxq_stream_t stream);
+
+/* mxq_grouped_gemm_wgrad with the payload format of each operand (E4M3 or E5M2). */
+mxq_status mxq_grouped_gemm_wgrad_fmt(const void* a_q, const void* a_s, mxq_fp8_format a_fmt,
+                                      const void* b_q, const void* b_s, mxq_fp8_format b_fmt,
+                                      const int64_t* group_offsets, int32_t G, int64_t M_total,
+                                      int64_t capacity, int64_t M, int64_t N, void* y, int64_t ldy,
+                                      mxq_stream_t stream);
 
 /* Waits for all work on the current device, then returns MXQ_ERR_TIMEOUT if
  * any kernel of this library recorded a bounded wait that ran out since the

@@ -142,7 +142,16 @@ mxq_status mxq_quant_1x32_cols_grouped(const void* x, int64_t rows, int64_t cols
                                        const int64_t* group_offsets, int32_t G, int64_t capacity,
                                        void* q_col, void* s_col, mxq_scale_layout layout,
                                        mxq_stream_t stream) {
+    return mxq_quant_1x32_cols_grouped_fmt(x, rows, cols, ld, group_offsets, G, capacity, q_col, s_col, layout,
+                                           MXQ_FP8_E4M3, stream);
+}
+
+mxq_status mxq_quant_1x32_cols_grouped_fmt(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                           const int64_t* group_offsets, int32_t G, int64_t capacity,
+                                           void* q_col, void* s_col, mxq_scale_layout layout, mxq_fp8_format fmt,
+                                           mxq_stream_t stream) {
     if (layout != MXQ_SCALE_ROWMAJOR && layout != MXQ_SCALE_MMA_TILED) return MXQ_ERR_INVALID_ARG;
+    if (fmt != MXQ_FP8_E4M3 && fmt != MXQ_FP8_E5M2) return MXQ_ERR_INVALID_ARG;
     if (rows < 0 || cols < 0 || G < 1 || capacity < 0) return MXQ_ERR_INVALID_ARG;
     if (G > 1024) return MXQ_ERR_UNSUPPORTED_SHAPE;
     if (cols % 32 != 0 || capacity % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
@@ -157,7 +166,7 @@ mxq_status mxq_quant_1x32_cols_grouped(const void* x, int64_t rows, int64_t cols
     mxq_status st = device_ok(&dev);
     if (st != MXQ_OK) return st;
     return from_cuda(mxq::launch_quant_cols_grouped(dev, x, rows, cols, ld, group_offsets, G, capacity, q_col,
-                                                    s_col, layout == MXQ_SCALE_MMA_TILED,
+                                                    s_col, layout == MXQ_SCALE_MMA_TILED, static_cast<int>(fmt),
                                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -269,6 +278,15 @@ mxq_status mxq_fsdp_unpack(mxq_fsdp_recipe recipe, int64_t n, int64_t k, int32_t
 mxq_status mxq_grouped_gemm(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
                             const int64_t* group_offsets, int32_t G, int64_t M_total, int64_t N,
                             int64_t K, void* y, int64_t ldy, mxq_stream_t stream) {
+    return mxq_grouped_gemm_fmt(a_q, a_s, MXQ_FP8_E4M3, b_q, b_s, MXQ_FP8_E4M3, group_offsets, G, M_total, N, K, y,
+                                ldy, stream);
+}
+
+mxq_status mxq_grouped_gemm_fmt(const void* a_q, const void* a_s, mxq_fp8_format a_fmt, const void* b_q,
+                                const void* b_s, mxq_fp8_format b_fmt, const int64_t* group_offsets, int32_t G,
+                                int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy, mxq_stream_t stream) {
+    if ((a_fmt != MXQ_FP8_E4M3 && a_fmt != MXQ_FP8_E5M2) || (b_fmt != MXQ_FP8_E4M3 && b_fmt != MXQ_FP8_E5M2))
+        return MXQ_ERR_INVALID_ARG;
     if (G < 1 || M_total < 0 || N < 0 || K < 0) return MXQ_ERR_INVALID_ARG;
     if (G > 1024) return MXQ_ERR_UNSUPPORTED_SHAPE;
     if (N % 128 != 0 || K % 32 != 0 || K == 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
@@ -285,13 +303,24 @@ mxq_status mxq_grouped_gemm(const void* a_q, const void* a_s, const void* b_q, c
     mxq_status st = device_ok(&dev);
     if (st != MXQ_OK) return st;
     return from_cuda(mxq::launch_grouped_gemm(dev, a_q, a_s, b_q, b_s, group_offsets, G, M_total, N, K,
-                                              y, ldy, reinterpret_cast<cudaStream_t>(stream)));
+                                              y, ldy, static_cast<int>(a_fmt), static_cast<int>(b_fmt),
+                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mxq_status mxq_grouped_gemm_wgrad(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
                                   const int64_t* group_offsets, int32_t G, int64_t M_total,
                                   int64_t capacity, int64_t M, int64_t N, void* y, int64_t ldy,
                                   mxq_stream_t stream) {
+    return mxq_grouped_gemm_wgrad_fmt(a_q, a_s, MXQ_FP8_E4M3, b_q, b_s, MXQ_FP8_E4M3, group_offsets, G, M_total,
+                                      capacity, M, N, y, ldy, stream);
+}
+
+mxq_status mxq_grouped_gemm_wgrad_fmt(const void* a_q, const void* a_s, mxq_fp8_format a_fmt, const void* b_q,
+                                      const void* b_s, mxq_fp8_format b_fmt, const int64_t* group_offsets,
+                                      int32_t G, int64_t M_total, int64_t capacity, int64_t M, int64_t N, void* y,
+                                      int64_t ldy, mxq_stream_t stream) {
+    if ((a_fmt != MXQ_FP8_E4M3 && a_fmt != MXQ_FP8_E5M2) || (b_fmt != MXQ_FP8_E4M3 && b_fmt != MXQ_FP8_E5M2))
+        return MXQ_ERR_INVALID_ARG;
     if (G < 1 || M_total < 0 || M < 0 || N < 0 || capacity < 0) return MXQ_ERR_INVALID_ARG;
     if (G > 1024) return MXQ_ERR_UNSUPPORTED_SHAPE;
     if (N % 16 != 0 || capacity % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
@@ -314,7 +343,7 @@ mxq_status mxq_grouped_gemm_wgrad(const void* a_q, const void* a_s, const void* 
                                            reinterpret_cast<cudaStream_t>(stream)));
     }
     return from_cuda(mxq::launch_grouped_gemm_wgrad(dev, a_q, a_s, b_q, b_s, group_offsets, G, M_total,
-                                                    capacity, M, N, y, ldy,
+                                                    capacity, M, N, y, ldy, static_cast<int>(a_fmt), static_cast<int>(b_fmt),
                                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -636,8 +636,8 @@ cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void
 
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
                                 const void* b_q, const void* b_s, const int64_t* offsets, int G,
-                                int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy,
-                                cudaStream_t stream) {
+                                int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy, int a_fmt,
+                                int b_fmt, cudaStream_t stream) {
     CUtensorMap ta, tb;
     if (!make_tma_u8(&ta, a_q, static_cast<uint64_t>(M_total), static_cast<uint64_t>(K), kBM))
         return cudaErrorInvalidValue;
@@ -653,6 +653,7 @@ cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const vo
     args.b_bands = static_cast<int64_t>(G) * N / 128;
     args.offsets = offsets;
     args.G = G;
+    args.fmt_bits = (static_cast<uint32_t>(a_fmt) << 7) | (static_cast<uint32_t>(b_fmt) << 10);
     args.status = dev.status;
     args.wait_limit_ns = kDefaultWaitLimitNs;
     return launch_t<kBN, kStages, false, kGroupedRows>(dev, ta, tb, args, -1, stream);
@@ -661,7 +662,7 @@ cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const vo
 cudaError_t launch_grouped_gemm_wgrad(const DeviceInfo& dev, const void* a_q, const void* a_s,
                                       const void* b_q, const void* b_s, const int64_t* offsets, int G,
                                       int64_t M_total, int64_t capacity, int64_t M, int64_t N, void* y,
-                                      int64_t ldy, cudaStream_t stream) {
+                                      int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream) {
     CUtensorMap ta, tb;
     if (!make_tma_u8(&ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(capacity), kBM))
         return cudaErrorInvalidValue;
@@ -677,6 +678,7 @@ cudaError_t launch_grouped_gemm_wgrad(const DeviceInfo& dev, const void* a_q, co
     args.b_bands = (N + 127) / 128;
     args.offsets = offsets;
     args.G = G;
+    args.fmt_bits = (static_cast<uint32_t>(a_fmt) << 7) | (static_cast<uint32_t>(b_fmt) << 10);
     args.status = dev.status;
     args.wait_limit_ns = kDefaultWaitLimitNs;
     return launch_t<kBN, kStages, false, kGroupedK>(dev, ta, tb, args, -1, stream);

@@ -42,7 +42,7 @@ cudaError_t launch_quant_1x32(const DeviceInfo& dev, const void* x, int64_t batc
 // Token-axis 1x32 quantization inside each expert (zero-padded, 128-aligned slots).
 cudaError_t launch_quant_cols_grouped(const DeviceInfo& dev, const void* x, int64_t rows,
                                       int64_t cols, int64_t ld, const int64_t* offsets, int G,
-                                      int64_t capacity, void* q_col, void* s_col, bool tiled,
+                                      int64_t capacity, void* q_col, void* s_col, bool tiled, int fmt,
                                       cudaStream_t stream);
 
 cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, int64_t k,
@@ -72,15 +72,15 @@ cudaError_t launch_fsdp_unpack(const DeviceInfo& dev, int recipe, int64_t n, int
 
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
                                 const void* b_q, const void* b_s, const int64_t* offsets, int G,
-                                int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy,
-                                cudaStream_t stream);
+                                int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy, int a_fmt,
+                                int b_fmt, cudaStream_t stream);
 
 // Grouped contraction (MoE weight gradient): y[g] = A_g B_g^T where the K range
 // of expert g is its 128-aligned token slot; A [M, capacity], B [N, capacity].
 cudaError_t launch_grouped_gemm_wgrad(const DeviceInfo& dev, const void* a_q, const void* a_s,
                                       const void* b_q, const void* b_s, const int64_t* offsets, int G,
                                       int64_t M_total, int64_t capacity, int64_t M, int64_t N, void* y,
-                                      int64_t ldy, cudaStream_t stream);
+                                      int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream);
 
 cudaError_t launch_wait_probe(const DeviceInfo& dev, uint64_t limit_ns, cudaStream_t stream);
 

@@ -369,7 +369,7 @@ __device__ __forceinline__ GroupedTile grouped_tile(int64_t tl, int64_t tiles_c,
     return gt;
 }
 
-template <bool kTiled>
+template <bool kTiled, int kFmt>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_grouped_ring_kernel(
     const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_t cols, const int64_t* __restrict__ offsets,
     int G, int64_t capacity, uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, unsigned int* status,
@@ -442,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_grouped_ring_
                 b4[u] = make_uint4(0u, 0u, 0u, 0u);
             __syncthreads();
         }
-        col_pass<kTiled, 0>(reinterpret_cast<const uint32_t*>(buf), gt.c0, cols, capacity, gt.pos, capacity, q_col,
-                            s_col);
+        col_pass<kTiled, kFmt>(reinterpret_cast<const uint32_t*>(buf), gt.c0, cols, capacity, gt.pos, capacity,
+                               q_col, s_col);
         __syncthreads();
         if (t == 0) {
             const int64_t next = tl + static_cast<int64_t>(kRing) * gridDim.x;
@@ -612,7 +612,7 @@ cudaError_t launch_quant_1x32(const DeviceInfo& dev, const void* x, int64_t batc
 
 cudaError_t launch_quant_cols_grouped(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols,
                                       int64_t ld, const int64_t* offsets, int G, int64_t capacity,
-                                      void* q_col, void* s_col, bool tiled, cudaStream_t stream) {
+                                      void* q_col, void* s_col, bool tiled, int fmt, cudaStream_t stream) {
     const size_t smem = kRing * kTileBytes + 1024 + 64 + 2 * 8 * static_cast<size_t>(G + 1);
     auto qp = static_cast<uint8_t*>(q_col);
     auto sp = static_cast<uint8_t*>(s_col);
@@ -641,12 +641,20 @@ cudaError_t launch_quant_cols_grouped(const DeviceInfo& dev, const void* x, int6
         return cudaGetLastError();
     };
     int per_sm = 0;
+    if (tiled && fmt == 1) {
+        static thread_local int configured = -1;
+        return run(quant_cols_grouped_ring_kernel<true, 1>, &configured, &per_sm);
+    }
     if (tiled) {
         static thread_local int configured = -1;
-        return run(quant_cols_grouped_ring_kernel<true>, &configured, &per_sm);
+        return run(quant_cols_grouped_ring_kernel<true, 0>, &configured, &per_sm);
+    }
+    if (fmt == 1) {
+        static thread_local int configured = -1;
+        return run(quant_cols_grouped_ring_kernel<false, 1>, &configured, &per_sm);
     }
     static thread_local int configured = -1;
-    return run(quant_cols_grouped_ring_kernel<false>, &configured, &per_sm);
+    return run(quant_cols_grouped_ring_kernel<false, 0>, &configured, &per_sm);
 }
 
 cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, int64_t k, int64_t ld,

@@ -69,6 +69,9 @@ def lib() -> ctypes.CDLL:
         L.mxq_quant_1x32_dual_batched.argtypes = [P, I64, I64, I64, I64, I64, P, P, P, P, S, S, P]
         L.mxq_gemm_bf16out_fmt.argtypes = [P, P, S, P, P, S, I64, I64, I64, S, P, I64, P]
         L.mxq_quant_1x32_cols_grouped.argtypes = [P, I64, I64, I64, P, I32, I64, P, P, S, P]
+        L.mxq_quant_1x32_cols_grouped_fmt.argtypes = [P, I64, I64, I64, P, I32, I64, P, P, S, S, P]
+        L.mxq_grouped_gemm_fmt.argtypes = [P, P, S, P, P, S, P, I32, I64, I64, I64, P, I64, P]
+        L.mxq_grouped_gemm_wgrad_fmt.argtypes = [P, P, S, P, P, S, P, I32, I64, I64, I64, I64, P, I64, P]
         L.mxq_grouped_gemm_wgrad.argtypes = [P, P, P, P, P, I32, I64, I64, I64, I64, P, I64, P]
         L.mxq_quant_32x32.argtypes = [P, I64, I64, I64, P, P, P, S, P]
         L.mxq_gemm_bf16out.argtypes = [P, P, P, P, I64, I64, I64, S, P, I64, P]
@@ -82,7 +85,8 @@ def lib() -> ctypes.CDLL:
                   "mxq_grouped_gemm", "mxq_get_device_status", "mxq_debug_wait_timeout",
                   "mxq_quant_1x32_dual_batched", "mxq_quant_1x32_cols_grouped",
                   "mxq_grouped_gemm_wgrad", "mxq_gemm_bf16out_fmt", "mxq_gemm_mxfp8out",
-                  "mxq_fsdp_payload_layout", "mxq_fsdp_unpack"):
+                  "mxq_fsdp_payload_layout", "mxq_fsdp_unpack", "mxq_quant_1x32_cols_grouped_fmt",
+                  "mxq_grouped_gemm_fmt", "mxq_grouped_gemm_wgrad_fmt"):
             getattr(L, f).restype = S
         _lib = L
         return L
@@ -180,7 +184,7 @@ def grouped_capacity(M_total: int, G: int) -> int:
     return (M_total + 127 * G + 127) // 128 * 128
 
 
-def quant_cols_grouped(x: torch.Tensor, offsets: torch.Tensor, capacity: int = None, layout="tiled"):
+def quant_cols_grouped(x: torch.Tensor, offsets: torch.Tensor, capacity: int = None, layout="tiled", fmt="e4m3"):
     """Token-axis quantization inside each expert (see mxq_quant_1x32_cols_grouped).
     x: bf16 [M_total, C] sorted by expert; offsets: int64 CUDA [G+1].
     Returns (q_col [C, capacity], s_col); the columns past the last expert's slot,
@@ -195,13 +199,14 @@ def quant_cols_grouped(x: torch.Tensor, offsets: torch.Tensor, capacity: int = N
         capacity = grouped_capacity(R, G)
     q_col = torch.zeros((C, capacity), dtype=torch.uint8, device=x.device)
     s_col = _scale_tensor(C, capacity, layout, x.device).zero_()
-    _check(lib().mxq_quant_1x32_cols_grouped(_ptr(x), R, C, x.stride(0), _ptr(offsets), G, capacity,
-                                             _ptr(q_col), _ptr(s_col), _layout(layout), _stream()),
-           "mxq_quant_1x32_cols_grouped")
+    _check(lib().mxq_quant_1x32_cols_grouped_fmt(_ptr(x), R, C, x.stride(0), _ptr(offsets), G, capacity,
+                                                 _ptr(q_col), _ptr(s_col), _layout(layout), _fmt(fmt), _stream()),
+           "mxq_quant_1x32_cols_grouped_fmt")
     return q_col, s_col
 
 
-def grouped_gemm_wgrad(a_q, a_s, b_q, b_s, offsets: torch.Tensor, M_total: int, out=None):
+def grouped_gemm_wgrad(a_q, a_s, b_q, b_s, offsets: torch.Tensor, M_total: int, out=None, a_fmt="e4m3",
+                       b_fmt="e4m3"):
     """Per-expert y[g] = A_g B_g^T over each expert's token slot (see
     mxq_grouped_gemm_wgrad).  a_q [M, capacity], b_q [N, capacity] from
     quant_cols_grouped.  Returns y bf16 [G, M, N]."""
@@ -210,9 +215,9 @@ def grouped_gemm_wgrad(a_q, a_s, b_q, b_s, offsets: torch.Tensor, M_total: int, 
     G = offsets.numel() - 1
     if out is None:
         out = torch.empty((G, M, N), dtype=torch.bfloat16, device=a_q.device)
-    _check(lib().mxq_grouped_gemm_wgrad(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(offsets), G,
-                                        M_total, capacity, M, N, _ptr(out), out.stride(-2), _stream()),
-           "mxq_grouped_gemm_wgrad")
+    _check(lib().mxq_grouped_gemm_wgrad_fmt(_ptr(a_q), _ptr(a_s), _fmt(a_fmt), _ptr(b_q), _ptr(b_s), _fmt(b_fmt),
+                                            _ptr(offsets), G, M_total, capacity, M, N, _ptr(out), out.stride(-2),
+                                            _stream()), "mxq_grouped_gemm_wgrad_fmt")
     return out
 
 
@@ -332,7 +337,8 @@ def fsdp_unpack(recipe, gathered: torch.Tensor, n: int, k: int, world: int, out=
     return out
 
 
-def grouped_gemm(a_q, a_s, b_q, b_s, offsets: torch.Tensor, N: int, K: int, out=None):
+def grouped_gemm(a_q, a_s, b_q, b_s, offsets: torch.Tensor, N: int, K: int, out=None, a_fmt="e4m3",
+                 b_fmt="e4m3"):
     """Per-expert y[r] = deq(A)[r] deq(B_g)^T for rows of expert g
     (offsets: int64 CUDA tensor [G+1]).  Returns y [M_total, N] bf16."""
     if offsets.dtype != torch.int64 or not offsets.is_cuda:
@@ -341,9 +347,9 @@ def grouped_gemm(a_q, a_s, b_q, b_s, offsets: torch.Tensor, N: int, K: int, out=
     M_total = a_q.shape[0]
     if out is None:
         out = torch.empty((M_total, N), dtype=torch.bfloat16, device=a_q.device)
-    _check(lib().mxq_grouped_gemm(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(offsets), G,
-                                  M_total, N, K, _ptr(out), out.stride(0), _stream()),
-           "mxq_grouped_gemm")
+    _check(lib().mxq_grouped_gemm_fmt(_ptr(a_q), _ptr(a_s), _fmt(a_fmt), _ptr(b_q), _ptr(b_s), _fmt(b_fmt),
+                                      _ptr(offsets), G, M_total, N, K, _ptr(out), out.stride(0), _stream()),
+           "mxq_grouped_gemm_fmt")
     return out
 
 

@@ -41,3 +41,18 @@ def assert_gemm_close(got: torch.Tensor, ref_bits: np.ndarray, what: str = "gemm
         raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} outside tolerance; first at "
                              f"{tuple(i)}: gpu {g[tuple(i)]!r} ref {r[tuple(i)]!r} (rms {rms:.3g})")
     return float((err / np.maximum(bound, 1e-300)).max()) if r.size else 0.0
+
+
+def tiled_to_plain(s_tiled: np.ndarray, rows: int, groups: int) -> np.ndarray:
+    """Inverse of the MMA-tiled scale permutation, taken from the oracle's
+    forward map applied to index-valued inputs (the low and high index digits
+    in two passes), so that only plain [rows, groups] scales are compared."""
+    from oracle import oracle
+    idx = np.arange(rows * groups, dtype=np.int64)
+    lo = oracle.scale_tiled((idx % 251 + 1).astype(np.uint8).reshape(rows, groups))
+    hi = oracle.scale_tiled((idx // 251 % 251 + 1).astype(np.uint8).reshape(rows, groups))
+    pos = np.flatnonzero(lo)
+    plain_index = (lo[pos].astype(np.int64) - 1) + 251 * (hi[pos].astype(np.int64) - 1)
+    out = np.zeros(rows * groups, np.uint8)
+    out[plain_index] = s_tiled[pos]
+    return out.reshape(rows, groups)

@@ -108,6 +108,18 @@ def test_moe_backward_argument_errors(L):
     assert w(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 300, 1024, 128, 120, FAKE, 120, None) == 2   # N % 16
     assert w(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 300, 512, 128, 128, FAKE, 128, None) == 1    # capacity small
     assert w(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 300, 1024, 128, 128, FAKE, 128, None) == 1   # G < 1
+    cf = L.mxq_quant_1x32_cols_grouped_fmt
+    assert cf(FAKE, 300, 64, 64, FAKE, 4, 1024, FAKE, FAKE, 1, 2, None) == 1   # bad format
+    assert cf(FAKE, 300, 48, 48, FAKE, 4, 1024, FAKE, FAKE, 1, 1, None) == 2   # cols % 32
+    assert cf(FAKE, 0, 64, 64, FAKE, 4, 1024, FAKE, FAKE, 1, 1, None) == 0     # no rows
+    gf = L.mxq_grouped_gemm_fmt
+    assert gf(FAKE, FAKE, 5, FAKE, FAKE, 0, FAKE, 4, 64, 128, 64, FAKE, 128, None) == 1   # bad a format
+    assert gf(FAKE, FAKE, 1, FAKE, FAKE, 3, FAKE, 4, 64, 128, 64, FAKE, 128, None) == 1   # bad b format
+    assert gf(FAKE, FAKE, 1, FAKE, FAKE, 0, FAKE, 4, 64, 192, 64, FAKE, 192, None) == 2   # N % 128
+    assert gf(FAKE, FAKE, 1, FAKE, FAKE, 0, FAKE, 4, 0, 128, 64, FAKE, 128, None) == 0    # no rows
+    wf = L.mxq_grouped_gemm_wgrad_fmt
+    assert wf(FAKE, FAKE, 9, FAKE, FAKE, 0, FAKE, 4, 300, 1024, 128, 128, FAKE, 128, None) == 1  # bad format
+    assert wf(FAKE, FAKE, 1, FAKE, FAKE, 0, FAKE, 4, 300, 1024, 128, 120, FAKE, 120, None) == 2  # N % 16
 
 
 def test_fused_quant_gemm_argument_errors(L):

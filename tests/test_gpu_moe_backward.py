@@ -15,7 +15,7 @@ import numpy as np
 import pytest
 import torch
 
-from _util import assert_gemm_close, bits, gpu_or_skip, u8
+from _util import assert_gemm_close, bits, gpu_or_skip, tiled_to_plain, u8
 
 pytestmark = pytest.mark.gpu
 
@@ -46,20 +46,6 @@ def test_batched_dual_quant_matches_oracle(B, R, C, pad, layout):
         assert np.array_equal(u8(qc[b]), oqc) and np.array_equal(u8(sc[b]), conv(osc))
 
 
-def _tiled_to_plain(oracle, s_tiled, rows, groups):
-    """Inverse of the tiled permutation via the oracle's forward map on indices."""
-    idx_hi = np.arange(rows * groups, dtype=np.int64)
-    # map every plain position to its tiled byte with the oracle (bytes carry
-    # the low and high index bytes in two passes)
-    lo = oracle.scale_tiled((idx_hi % 251 + 1).astype(np.uint8).reshape(rows, groups))
-    hi = oracle.scale_tiled((idx_hi // 251 % 251 + 1).astype(np.uint8).reshape(rows, groups))
-    pos = np.flatnonzero(lo)
-    plain_index = (lo[pos].astype(np.int64) - 1) + 251 * (hi[pos].astype(np.int64) - 1)
-    out = np.zeros(rows * groups, np.uint8)
-    out[plain_index] = s_tiled[pos]
-    return out.reshape(rows, groups)
-
-
 @pytest.mark.parametrize("sizes", [[0, 5, 0, 300, 1, 130], [128, 256], [33, 31, 129, 127, 0, 1], [1000]])
 def test_grouped_cols_quant_matches_oracle(sizes):
     mxq, workloads, oracle = _mods()
@@ -74,7 +60,7 @@ def test_grouped_cols_quant_matches_oracle(sizes):
         q, s = mxq.quant_cols_grouped(x.cuda(), torch.from_numpy(off).cuda(), cap, layout=layout)
         torch.cuda.synchronize()
         assert np.array_equal(u8(q)[:, :used], oq[:, :used])
-        sp = u8(s) if layout == "rowmajor" else _tiled_to_plain(oracle, u8(s), C, cap // 32)
+        sp = u8(s) if layout == "rowmajor" else tiled_to_plain(u8(s), C, cap // 32)
         assert np.array_equal(sp[:, :used // 32], os_[:, :used // 32])
 
 
