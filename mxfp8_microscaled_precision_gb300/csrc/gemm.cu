@@ -19,7 +19,10 @@
 //               (128 x BN x 32 each) into the TMEM accumulator.
 //   warps 2-9   epilogue: tcgen05.ld of the FP32 accumulator, which is then
 //               released to the MMA warp; RNE to BF16 (and, in the quantizing
-//               mode, the 1x32 MXFP8 quantization), 16-byte global stores.
+//               mode, the 1x32 MXFP8 quantization); dense and grouped-
+//               contraction tiles go out through a per-warp shared-memory
+//               staging buffer (8 rows x 64 contiguous bytes per store
+//               instruction), the other modes with 16-byte stores per row.
 // Every mbarrier wait is bounded (see mxq_device.cuh).
 
 #include <cuda.h>
@@ -70,7 +73,11 @@ struct GemmArgs {
 //             for the scale factors); 8 epilogue warps drain it into
 //             registers at once and release it before converting and
 //             storing, so the next tile's MMAs start after the drain only.
-template <int BN, int STAGES>
+// Shared memory after the ring: the grouped modes' schedule tables (grouped
+// rows: clamped offsets, tile prefix, first m-tiles; grouped contraction: slot
+// starts and lengths), then, in the dense and grouped-contraction modes with
+// BN = 256, a 2 KB staging buffer per epilogue warp (see store_staged).
+template <int BN, int STAGES, int kMode>
 struct Cfg {
     static constexpr int kAccStages = BN == 128 ? 2 : 1;
     static constexpr int kEpiWarps = 4 * (BN / 128);   // each owns 32 lanes x 128 columns
@@ -87,8 +94,13 @@ struct Cfg {
     static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kOffSched = (kOffAbort + 4 + 15) / 16 * 16;
-    static constexpr int kSchedBytes = 8 * (kMaxGroups + 1) + 4 * (kMaxGroups + 1) + 4 * kMaxGroups;
-    static constexpr int kBytes = kOffSched + kSchedBytes;
+    static constexpr int kSchedBytes = kMode == kGroupedRows ? 8 * (kMaxGroups + 1) + 4 * (kMaxGroups + 1) + 4 * kMaxGroups
+                                       : kMode == kGroupedK  ? 4 * (kMaxGroups + 1) + 4 * kMaxGroups
+                                                             : 0;
+    static constexpr bool kStaged = BN == 256 && (kMode == kDense || kMode == kGroupedK);
+    static constexpr int kStageWarpBytes = 32 * 32 * 2;  // 32 rows x 32 BF16 columns
+    static constexpr int kOffStage = (kOffSched + kSchedBytes + 127) / 128 * 128;
+    static constexpr int kBytes = kOffStage + (kStaged ? kEpiWarps * kStageWarpBytes : 0);
     static constexpr int kAlloc = kBytes + 1024;        // slack for 1024-byte alignment
     // TMEM columns: accumulators, then per-stage SFA and SFB slots.
     static constexpr int kTmemSfa = kAccStages * BN;
@@ -170,6 +182,46 @@ __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs&
         ti.b_row = static_cast<int64_t>(g) * p.N + ti.n0;
     }
     return ti;
+}
+
+// One epilogue warp's share of a finished tile through its 2 KB shared-memory
+// staging buffer: lane l holds output row row0 + l (y's row numbering; the row
+// is stored when tile_row0 + l < row_hi), FP32 columns n .. n+127 in v.  Per
+// 32-column chunk each lane writes its row's 64 BF16 bytes to the buffer, then
+// the warp stores 8 rows x 64 contiguous bytes per instruction: 8 cache-line
+// halves instead of the 32 lines a row-per-lane store touches.  16-byte chunk
+// j of staged row r sits at position j ^ ((r >> 1) & 3), so both the writes
+// (one row per lane) and the reads (four lanes per row) are conflict-free.
+__device__ __forceinline__ void store_staged(const GemmArgs& p, const uint32_t (&v)[4][32], uint32_t stage,
+                                             int64_t row0, int64_t tile_row0, int64_t row_hi, int64_t n,
+                                             int lane) {
+    const uint32_t wrow = stage + 64u * static_cast<uint32_t>(lane);
+    const uint32_t wswz = static_cast<uint32_t>((lane >> 1) & 3);
+    const int rsub = lane >> 2;   // row within an 8-row group
+    const int jj = lane & 3;      // 16-byte chunk within a 64-byte row
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint4 o;
+            o.x = cvt_bf16x2(__uint_as_float(v[c][8 * j + 0]), __uint_as_float(v[c][8 * j + 1]));
+            o.y = cvt_bf16x2(__uint_as_float(v[c][8 * j + 2]), __uint_as_float(v[c][8 * j + 3]));
+            o.z = cvt_bf16x2(__uint_as_float(v[c][8 * j + 4]), __uint_as_float(v[c][8 * j + 5]));
+            o.w = cvt_bf16x2(__uint_as_float(v[c][8 * j + 6]), __uint_as_float(v[c][8 * j + 7]));
+            sts128(wrow + 16u * (static_cast<uint32_t>(j) ^ wswz), o);
+        }
+        __syncwarp();
+        const int64_t col = n + 32 * c + 8 * jj;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = 8 * i + rsub;
+            const uint4 o = lds128_ordered(stage + 64u * static_cast<uint32_t>(r) +
+                                           16u * (static_cast<uint32_t>(jj) ^ static_cast<uint32_t>((r >> 1) & 3)));
+            if (tile_row0 + r < row_hi && col + 8 <= p.N)
+                *reinterpret_cast<uint4*>(p.y + (row0 + r) * p.ldy + col) = o;
+        }
+        __syncwarp();   // the buffer is rewritten by the next chunk
+    }
 }
 
 // One epilogue thread's share of a finished tile: 128 accumulator columns
@@ -269,10 +321,10 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 }
 
 template <int BN, int STAGES, bool kMnMajor, int kMode>
-__global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
     gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tma_a,
                      const __grid_constant__ CUtensorMap tma_b, const GemmArgs p) {
-    using L = Cfg<BN, STAGES>;
+    using L = Cfg<BN, STAGES, kMode>;
     constexpr int kAcc = L::kAccStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -322,23 +374,35 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
         sch.prefix = nullptr;
         sch.first_mt = nullptr;
     } else {
-        int64_t* s_off = reinterpret_cast<int64_t*>(smem + L::kOffSched);
-        int* s_prefix = reinterpret_cast<int*>(s_off + (kMaxGroups + 1));
+        // Grouped rows keep the clamped offsets for the row masks; the grouped
+        // contraction needs only the slot tables built from them.
+        int64_t* s_off = kMode == kGroupedRows ? reinterpret_cast<int64_t*>(smem + L::kOffSched) : nullptr;
+        int* s_prefix = kMode == kGroupedRows ? reinterpret_cast<int*>(s_off + (kMaxGroups + 1))
+                                              : reinterpret_cast<int*>(smem + L::kOffSched);
         int* s_first = s_prefix + (kMaxGroups + 1);
         const int64_t row_limit = kMode == kGroupedRows ? p.M : p.M_total;
-        for (int g = threadIdx.x; g <= p.G; g += L::kThreads) {
-            int64_t o = p.offsets[g];
-            o = o < 0 ? 0 : (o > row_limit ? row_limit : o);  // keep malformed offsets in bounds
-            s_off[g] = o;
+        auto clamped_offset = [&](int g) {   // keep malformed offsets in bounds
+            const int64_t o = p.offsets[g];
+            return o < 0 ? int64_t(0) : (o > row_limit ? row_limit : o);
+        };
+        if constexpr (kMode == kGroupedRows) {
+            for (int g = threadIdx.x; g <= p.G; g += L::kThreads) s_off[g] = clamped_offset(g);
+            __syncthreads();
         }
-        __syncthreads();
         if (warp == 0) {  // tile counts and their exclusive prefix, 32 groups at a time
             int carry = 0;
             for (int base = 0; base < p.G; base += 32) {
                 const int g = base + lane;
                 int cnt = 0;
                 if (g < p.G) {
-                    const int64_t lo = s_off[g], hi = s_off[g + 1];
+                    int64_t lo, hi;
+                    if constexpr (kMode == kGroupedRows) {
+                        lo = s_off[g];
+                        hi = s_off[g + 1];
+                    } else {
+                        lo = clamped_offset(g);
+                        hi = clamped_offset(g + 1);
+                    }
                     if constexpr (kMode == kGroupedRows) {
                         const int64_t fm = lo / kBM;
                         s_first[g] = static_cast<int>(fm);
@@ -534,8 +598,12 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES>::kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[c][j] = 0u;
             }
-            store_row<kMode>(p, v, ti.m0 + 32 * quad + lane, ti.row_lo, ti.row_hi, ti.y_row0,
-                             ti.n0 + half * 128, ti.m0 < p.M);
+            if constexpr (L::kStaged)
+                store_staged(p, v, sbase + L::kOffStage + (warp - 2) * L::kStageWarpBytes,
+                             ti.y_row0 + ti.m0 + 32 * quad, ti.m0 + 32 * quad, ti.row_hi, ti.n0 + half * 128, lane);
+            else
+                store_row<kMode>(p, v, ti.m0 + 32 * quad + lane, ti.row_lo, ti.row_hi, ti.y_row0,
+                                 ti.n0 + half * 128, ti.m0 < p.M);
         }
     }
 
@@ -558,7 +626,7 @@ bool make_tma_u8(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
 template <int BN, int STAGES, bool kMnMajor, int kMode>
 cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& ta, const CUtensorMap& tb,
                      const GemmArgs& args, int64_t max_tiles, cudaStream_t stream) {
-    using L = Cfg<BN, STAGES>;
+    using L = Cfg<BN, STAGES, kMode>;
     auto kern = gemm_mxf8_kernel<BN, STAGES, kMnMajor, kMode>;
     static thread_local int configured_device = -1;  // attribute set once per device and thread
     if (configured_device != dev.device) {
