@@ -43,7 +43,7 @@ L2_FLUSH_BYTES = 256 << 20   # larger than the 129 MB L2
 L2_BYTES = 129 * 10**6
 # DRAM bytes (read + write) of one GEMM launch (the forward GEMM of the step), from
 # an ncu --set full capture of the kernel as it stands; None where not captured.
-GEMM_TRAFFIC_BYTES = {}
+GEMM_TRAFFIC_BYTES = {"linear_train": 86519808}
 
 
 def load_peaks():
