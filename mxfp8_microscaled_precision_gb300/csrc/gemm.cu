@@ -19,10 +19,10 @@
 //               (128 x BN x 32 each) into the TMEM accumulator.
 //   warps 2-9   epilogue: tcgen05.ld of the FP32 accumulator, which is then
 //               released to the MMA warp; RNE to BF16 (and, in the quantizing
-//               mode, the 1x32 MXFP8 quantization); dense and grouped-
-//               contraction tiles go out through a per-warp shared-memory
-//               staging buffer (8 rows x 64 contiguous bytes per store
-//               instruction), the other modes with 16-byte stores per row.
+//               mode, the 1x32 MXFP8 quantization); BF16 tiles go out
+//               through a per-warp shared-memory staging buffer (8 rows x 64
+//               contiguous bytes per store instruction), the quantizing
+//               epilogue with 16-byte stores per row.
 // Every mbarrier wait is bounded (see mxq_device.cuh).
 
 #include <cuda.h>
@@ -74,9 +74,9 @@ struct GemmArgs {
 //             registers at once and release it before converting and
 //             storing, so the next tile's MMAs start after the drain only.
 // Shared memory after the ring: the grouped modes' schedule tables (grouped
-// rows: clamped offsets, tile prefix, first m-tiles; grouped contraction: slot
-// starts and lengths), then, in the dense and grouped-contraction modes with
-// BN = 256, a 2 KB staging buffer per epilogue warp (see store_staged).
+// rows: tile prefix and first m-tiles; grouped contraction: slot starts and
+// lengths), then, with BN = 256 and outside the quantizing epilogue, a 2 KB
+// staging buffer per epilogue warp (see store_staged).
 template <int BN, int STAGES, int kMode>
 struct Cfg {
     static constexpr int kAccStages = BN == 128 ? 2 : 1;
@@ -94,10 +94,8 @@ struct Cfg {
     static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kOffSched = (kOffAbort + 4 + 15) / 16 * 16;
-    static constexpr int kSchedBytes = kMode == kGroupedRows ? 8 * (kMaxGroups + 1) + 4 * (kMaxGroups + 1) + 4 * kMaxGroups
-                                       : kMode == kGroupedK  ? 4 * (kMaxGroups + 1) + 4 * kMaxGroups
-                                                             : 0;
-    static constexpr bool kStaged = BN == 256 && (kMode == kDense || kMode == kGroupedK);
+    static constexpr int kSchedBytes = kMode == kGroupedRows || kMode == kGroupedK ? 4 * (kMaxGroups + 1) + 4 * kMaxGroups : 0;
+    static constexpr bool kStaged = BN == 256 && kMode != kDenseQuant;
     static constexpr int kStageWarpBytes = 32 * 32 * 2;  // 32 rows x 32 BF16 columns
     static constexpr int kOffStage = (kOffSched + kSchedBytes + 127) / 128 * 128;
     static constexpr int kBytes = kOffStage + (kStaged ? kEpiWarps * kStageWarpBytes : 0);
@@ -131,11 +129,16 @@ struct Schedule {
     int64_t m_tiles, n_tiles, total;
     int num_kb;           // K blocks of dense / grouped-row tiles
     // grouped modes only (shared memory)
-    const int64_t* off;
     const int* prefix;    // [G+1] grouped rows: tile prefix; grouped K: slot start / 128
     const int* first_mt;  // [G]   grouped rows: first m-tile; grouped K: slot length / 128
     int G;
 };
+
+// Group offset g, clamped to [0, limit] so that malformed offsets stay in bounds.
+__device__ __forceinline__ int64_t clamped_offset(const GemmArgs& p, int g, int64_t limit) {
+    const int64_t o = p.offsets[g];
+    return o < 0 ? int64_t(0) : (o > limit ? limit : o);
+}
 
 template <int BN, int kMode>
 __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs& p, int64_t t) {
@@ -177,24 +180,25 @@ __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs&
         const int64_t n_blk = local % s.n_tiles;
         ti.m0 = m_blk * kBM;
         ti.n0 = n_blk * BN;
-        ti.row_lo = max(ti.m0, s.off[g]);
-        ti.row_hi = min(ti.m0 + kBM, s.off[g + 1]);
+        ti.row_lo = max(ti.m0, clamped_offset(p, g, p.M));
+        ti.row_hi = min(ti.m0 + kBM, clamped_offset(p, g + 1, p.M));
         ti.b_row = static_cast<int64_t>(g) * p.N + ti.n0;
     }
     return ti;
 }
 
 // One epilogue warp's share of a finished tile through its 2 KB shared-memory
-// staging buffer: lane l holds output row row0 + l (y's row numbering; the row
-// is stored when tile_row0 + l < row_hi), FP32 columns n .. n+127 in v.  Per
+// staging buffer: lane l holds output row row0 + l (y's row numbering) in v,
+// FP32 columns n .. n+127.  Per
 // 32-column chunk each lane writes its row's 64 BF16 bytes to the buffer, then
 // the warp stores 8 rows x 64 contiguous bytes per instruction: 8 cache-line
-// halves instead of the 32 lines a row-per-lane store touches.  16-byte chunk
+// halves instead of the 32 lines a row-per-lane store touches.  Rows outside
+// [row_lo, row_hi) (tile-row numbering) are not stored.  16-byte chunk
 // j of staged row r sits at position j ^ ((r >> 1) & 3), so both the writes
 // (one row per lane) and the reads (four lanes per row) are conflict-free.
 __device__ __forceinline__ void store_staged(const GemmArgs& p, const uint32_t (&v)[4][32], uint32_t stage,
-                                             int64_t row0, int64_t tile_row0, int64_t row_hi, int64_t n,
-                                             int lane) {
+                                             int64_t row0, int64_t tile_row0, int64_t row_lo, int64_t row_hi,
+                                             int64_t n, int lane) {
     const uint32_t wrow = stage + 64u * static_cast<uint32_t>(lane);
     const uint32_t wswz = static_cast<uint32_t>((lane >> 1) & 3);
     const int rsub = lane >> 2;   // row within an 8-row group
@@ -217,7 +221,7 @@ __device__ __forceinline__ void store_staged(const GemmArgs& p, const uint32_t (
             const int r = 8 * i + rsub;
             const uint4 o = lds128_ordered(stage + 64u * static_cast<uint32_t>(r) +
                                            16u * (static_cast<uint32_t>(jj) ^ static_cast<uint32_t>((r >> 1) & 3)));
-            if (tile_row0 + r < row_hi && col + 8 <= p.N)
+            if (tile_row0 + r >= row_lo && tile_row0 + r < row_hi && col + 8 <= p.N)
                 *reinterpret_cast<uint4*>(p.y + (row0 + r) * p.ldy + col) = o;
         }
         __syncwarp();   // the buffer is rewritten by the next chunk
@@ -370,39 +374,21 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
     if constexpr (kMode == kDense || kMode == kDenseQuant) {
         sch.m_tiles = (p.M + kBM - 1) / kBM;
         sch.total = sch.m_tiles * sch.n_tiles;
-        sch.off = nullptr;
         sch.prefix = nullptr;
         sch.first_mt = nullptr;
     } else {
-        // Grouped rows keep the clamped offsets for the row masks; the grouped
-        // contraction needs only the slot tables built from them.
-        int64_t* s_off = kMode == kGroupedRows ? reinterpret_cast<int64_t*>(smem + L::kOffSched) : nullptr;
-        int* s_prefix = kMode == kGroupedRows ? reinterpret_cast<int*>(s_off + (kMaxGroups + 1))
-                                              : reinterpret_cast<int*>(smem + L::kOffSched);
+        // Tables built from the clamped offsets (tile_info reads the two offsets
+        // of a grouped-row tile again, clamped the same way, for its row mask).
+        int* s_prefix = reinterpret_cast<int*>(smem + L::kOffSched);
         int* s_first = s_prefix + (kMaxGroups + 1);
         const int64_t row_limit = kMode == kGroupedRows ? p.M : p.M_total;
-        auto clamped_offset = [&](int g) {   // keep malformed offsets in bounds
-            const int64_t o = p.offsets[g];
-            return o < 0 ? int64_t(0) : (o > row_limit ? row_limit : o);
-        };
-        if constexpr (kMode == kGroupedRows) {
-            for (int g = threadIdx.x; g <= p.G; g += L::kThreads) s_off[g] = clamped_offset(g);
-            __syncthreads();
-        }
         if (warp == 0) {  // tile counts and their exclusive prefix, 32 groups at a time
             int carry = 0;
             for (int base = 0; base < p.G; base += 32) {
                 const int g = base + lane;
                 int cnt = 0;
                 if (g < p.G) {
-                    int64_t lo, hi;
-                    if constexpr (kMode == kGroupedRows) {
-                        lo = s_off[g];
-                        hi = s_off[g + 1];
-                    } else {
-                        lo = clamped_offset(g);
-                        hi = clamped_offset(g + 1);
-                    }
+                    const int64_t lo = clamped_offset(p, g, row_limit), hi = clamped_offset(p, g + 1, row_limit);
                     if constexpr (kMode == kGroupedRows) {
                         const int64_t fm = lo / kBM;
                         s_first[g] = static_cast<int>(fm);
@@ -423,7 +409,6 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
             }
             if (lane == 0) s_prefix[p.G] = carry;
         }
-        sch.off = s_off;
         sch.prefix = s_prefix;
         sch.first_mt = s_first;
         sch.m_tiles = (p.M + kBM - 1) / kBM;
@@ -600,7 +585,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
             }
             if constexpr (L::kStaged)
                 store_staged(p, v, sbase + L::kOffStage + (warp - 2) * L::kStageWarpBytes,
-                             ti.y_row0 + ti.m0 + 32 * quad, ti.m0 + 32 * quad, ti.row_hi, ti.n0 + half * 128, lane);
+                             ti.y_row0 + ti.m0 + 32 * quad, ti.m0 + 32 * quad, ti.row_lo, ti.row_hi,
+                             ti.n0 + half * 128, lane);
             else
                 store_row<kMode>(p, v, ti.m0 + 32 * quad + lane, ti.row_lo, ti.row_hi, ti.y_row0,
                                  ti.n0 + half * 128, ti.m0 < p.M);
