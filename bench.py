@@ -202,6 +202,9 @@ class LinearTrain(Workload):
         bf = dict(dtype=torch.bfloat16, device=dev)
         self.y, self.dx, self.dw = torch.empty((M, N), **bf), torch.empty((M, K), **bf), torch.empty((N, K), **bf)
         self.outputs = [self.y, self.dx, self.dw]
+        gr, grs, gc, gcs = self.qg
+        self.bwd = [dict(a_q=gr, a_s=grs, b_q=self.qw[2], b_s=self.qw[3], M=M, N=K, K=N, out=self.dx),
+                    dict(a_q=gc, a_s=gcs, b_q=self.qx[2], b_s=self.qx[3], M=N, N=K, K=M, out=self.dw)]
 
     @property
     def gemm_flops(self):
@@ -218,8 +221,8 @@ class LinearTrain(Workload):
             ("quant_W_dual", "quant", _dual_bytes(N, K), lambda: mxq.quant_1x32_dual(i["W"], out=self.qw)),
             ("quant_dY_dual", "quant", _dual_bytes(M, N), lambda: mxq.quant_1x32_dual(i["dY"], out=self.qg)),
             ("gemm_fwd", "gemm", 2 * M * N * K, lambda: mxq.gemm(xr, xrs, wr, wrs, M, N, K, out=self.y)),
-            ("gemm_dgrad", "gemm", 2 * M * N * K, lambda: mxq.gemm(gr, grs, wc, wcs, M, K, N, out=self.dx)),
-            ("gemm_wgrad", "gemm", 2 * M * N * K, lambda: mxq.gemm(gc, gcs, xc, xcs, N, K, M, out=self.dw)),
+            # dgrad dX = dY W and wgrad dW = dY^T X share one launch (one last wave of tiles)
+            ("gemm_bwd", "gemm", 2 * 2 * M * N * K, lambda: mxq.gemm_multi(self.bwd)),
         ]
 
     def cpu_sample(self, budget_s):

@@ -215,6 +215,41 @@ mxq_status mxq_gemm_bf16out_fmt(const void* a_q, const void* a_s, mxq_fp8_format
                                 int64_t M, int64_t N, int64_t K, int b_mn_major,
                                 void* y, int64_t ldy, mxq_stream_t stream);
 
+/* One GEMM of mxq_gemm_bf16out_multi: y = deq(A) deq(B)^T with the fields of
+ * mxq_gemm_bf16out_fmt (caller-owned device buffers). */
+typedef struct {
+    const void* a_q;
+    const void* a_s;
+    const void* b_q;
+    const void* b_s;
+    int64_t M, N, K;
+    void* y;
+    int64_t ldy;
+    mxq_fp8_format a_fmt, b_fmt;
+} mxq_gemm_desc;
+
+/*
+ * 1 to 4 independent dense GEMMs (e.g. the dgrad and the wgrad of one linear
+ * layer's backward pass, torchtitan-npu tutorial "MXFP8 与 HiF8 架构原理速览":
+ * the backward matmuls of the MXFP8 recipe) computed by ONE persistent launch
+ * over all their output tiles.  The results are those of mxq_gemm_bf16out_fmt
+ * on each GEMM, bit for bit; only the scheduling differs: run back to back,
+ * every GEMM ends in a partly filled last wave of 128 x 256 tiles, while one
+ * launch (longest K first, the rounds alternating direction over the SMs)
+ * shares a single last wave between them.  The pages run these GEMMs as
+ * separate matmuls; this call has no counterpart there.
+ *
+ * gemms[i]    host array of count descriptors (read during the call only).
+ * b_mn_major  the B orientation of every GEMM (0 K-major, 1 MN-major).
+ * Every descriptor is checked as mxq_gemm_bf16out_fmt checks its arguments
+ * before anything is launched; the first failing one decides the status and
+ * nothing runs.  M == 0 or N == 0 GEMMs are skipped, K == 0 GEMMs write zeros.
+ * Outputs must not overlap one another or any input (not checked).
+ * count == 0 returns MXQ_OK; count > 4 or a NULL array: MXQ_ERR_INVALID_ARG.
+ */
+mxq_status mxq_gemm_bf16out_multi(const mxq_gemm_desc* gemms, int32_t count, int b_mn_major,
+                                  mxq_stream_t stream);
+
 /*
  * Block-scaled FP8 GEMM whose epilogue also quantizes its output: the BF16
  * result y (as mxq_gemm_bf16out computes it) is rounded to BF16 and each run

@@ -74,6 +74,39 @@ inline mxq_status from_cuda(cudaError_t e) {
     return MXQ_ERR_CUDA;
 }
 
+// What a validated dense GEMM asks for.
+enum DenseWork { kNothing = 0, kZeroFill = 1, kLaunch = 2 };
+
+// Argument checks of the dense BF16-output GEMMs (see mxq_gemm_bf16out).
+mxq_status check_dense(const void* a_q, const void* a_s, mxq_fp8_format a_fmt, const void* b_q, const void* b_s,
+                       mxq_fp8_format b_fmt, int64_t M, int64_t N, int64_t K, int b_mn_major, const void* y,
+                       int64_t ldy, DenseWork* work) {
+    *work = kNothing;
+    if (M < 0 || N < 0 || K < 0 || (b_mn_major != 0 && b_mn_major != 1)) return MXQ_ERR_INVALID_ARG;
+    if ((a_fmt != MXQ_FP8_E4M3 && a_fmt != MXQ_FP8_E5M2) || (b_fmt != MXQ_FP8_E4M3 && b_fmt != MXQ_FP8_E5M2))
+        return MXQ_ERR_INVALID_ARG;
+    if (K % 32 != 0 || N % 16 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (b_mn_major && N % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (M > (int64_t(1) << 31) - 128 || N > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - 128)
+        return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0) return MXQ_OK;
+    if (!y || ldy < N || ldy % 8 != 0 || !aligned16(y)) return MXQ_ERR_INVALID_ARG;
+    if (K == 0) {  // empty contraction: y = 0
+        *work = kZeroFill;
+        return MXQ_OK;
+    }
+    if (!a_q || !a_s || !b_q || !b_s) return MXQ_ERR_INVALID_ARG;
+    if (!aligned16(a_q) || !aligned16(a_s) || !aligned16(b_q) || !aligned16(b_s))
+        return MXQ_ERR_INVALID_ARG;
+    *work = kLaunch;
+    return MXQ_OK;
+}
+
+cudaError_t zero_fill(void* y, int64_t ldy, int64_t M, int64_t N, mxq_stream_t stream) {
+    return cudaMemset2DAsync(y, static_cast<size_t>(ldy) * 2, 0, static_cast<size_t>(N) * 2,
+                             static_cast<size_t>(M), reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -198,31 +231,47 @@ mxq_status mxq_gemm_bf16out(const void* a_q, const void* a_s, const void* b_q, c
 mxq_status mxq_gemm_bf16out_fmt(const void* a_q, const void* a_s, mxq_fp8_format a_fmt, const void* b_q,
                                 const void* b_s, mxq_fp8_format b_fmt, int64_t M, int64_t N, int64_t K,
                                 int b_mn_major, void* y, int64_t ldy, mxq_stream_t stream) {
-    if (M < 0 || N < 0 || K < 0 || (b_mn_major != 0 && b_mn_major != 1)) return MXQ_ERR_INVALID_ARG;
-    if ((a_fmt != MXQ_FP8_E4M3 && a_fmt != MXQ_FP8_E5M2) || (b_fmt != MXQ_FP8_E4M3 && b_fmt != MXQ_FP8_E5M2))
-        return MXQ_ERR_INVALID_ARG;
-    if (K % 32 != 0 || N % 16 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
-    if (b_mn_major && N % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
-    if (M > (int64_t(1) << 31) - 128 || N > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - 128)
-        return MXQ_ERR_UNSUPPORTED_SHAPE;
-    if (M == 0 || N == 0) return MXQ_OK;
-    if (!y || ldy < N || ldy % 8 != 0 || !aligned16(y)) return MXQ_ERR_INVALID_ARG;
+    DenseWork work;
+    mxq_status st = check_dense(a_q, a_s, a_fmt, b_q, b_s, b_fmt, M, N, K, b_mn_major, y, ldy, &work);
+    if (st != MXQ_OK || work == kNothing) return st;
     mxq::DeviceInfo dev;
-    if (K == 0) {  // empty contraction: y = 0
-        mxq_status st = device_ok(&dev);
-        if (st != MXQ_OK) return st;
-        return from_cuda(cudaMemset2DAsync(y, static_cast<size_t>(ldy) * 2, 0,
-                                           static_cast<size_t>(N) * 2, static_cast<size_t>(M),
-                                           reinterpret_cast<cudaStream_t>(stream)));
-    }
-    if (!a_q || !a_s || !b_q || !b_s) return MXQ_ERR_INVALID_ARG;
-    if (!aligned16(a_q) || !aligned16(a_s) || !aligned16(b_q) || !aligned16(b_s))
-        return MXQ_ERR_INVALID_ARG;
-    mxq_status st = device_ok(&dev);
+    st = device_ok(&dev);
     if (st != MXQ_OK) return st;
+    if (work == kZeroFill) return from_cuda(zero_fill(y, ldy, M, N, stream));
     return from_cuda(mxq::launch_gemm(dev, a_q, a_s, b_q, b_s, M, N, K, b_mn_major != 0, y, ldy,
                                       static_cast<int>(a_fmt), static_cast<int>(b_fmt),
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxq_status mxq_gemm_bf16out_multi(const mxq_gemm_desc* gemms, int32_t count, int b_mn_major,
+                                  mxq_stream_t stream) {
+    if (count < 0 || count > 4 || (count > 0 && !gemms)) return MXQ_ERR_INVALID_ARG;
+    mxq::DenseGemm launch[4];
+    int n_launch = 0;
+    bool any_zero = false;
+    for (int i = 0; i < count; ++i) {   // every GEMM is checked before anything runs
+        const mxq_gemm_desc& g = gemms[i];
+        DenseWork work;
+        const mxq_status st = check_dense(g.a_q, g.a_s, g.a_fmt, g.b_q, g.b_s, g.b_fmt, g.M, g.N, g.K, b_mn_major,
+                                          g.y, g.ldy, &work);
+        if (st != MXQ_OK) return st;
+        if (work == kZeroFill) any_zero = true;
+        if (work == kLaunch)
+            launch[n_launch++] = mxq::DenseGemm{g.a_q, g.a_s, g.b_q, g.b_s, g.M, g.N, g.K, g.y, g.ldy,
+                                                static_cast<int>(g.a_fmt), static_cast<int>(g.b_fmt)};
+    }
+    if (n_launch == 0 && !any_zero) return MXQ_OK;
+    mxq::DeviceInfo dev;
+    mxq_status st = device_ok(&dev);
+    if (st != MXQ_OK) return st;
+    for (int i = 0; i < count; ++i)
+        if (gemms[i].K == 0 && gemms[i].M > 0 && gemms[i].N > 0) {
+            const cudaError_t e = zero_fill(gemms[i].y, gemms[i].ldy, gemms[i].M, gemms[i].N, stream);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
+    if (n_launch == 0) return MXQ_OK;
+    return from_cuda(mxq::launch_gemm_multi(dev, launch, n_launch, b_mn_major != 0,
+                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mxq_status mxq_gemm_mxfp8out(const void* a_q, const void* a_s, const void* b_q, const void* b_s,

@@ -42,6 +42,7 @@ constexpr int kBK = 128;          // K elements (= bytes) per pipeline stage
 constexpr int kUmmaK = 32;        // K of one MMA instruction (FP8)
 constexpr int kRasterBand = 8;    // m-tiles per raster band (L2 reuse of B)
 constexpr int kMaxGroups = 1024;
+constexpr int kMaxProblems = 4;   // dense GEMMs of one launch
 
 // Kernel modes.
 constexpr int kDense = 0;         // y = A B^T
@@ -49,21 +50,37 @@ constexpr int kGroupedRows = 1;   // rows of A split by expert, one B per expert
 constexpr int kGroupedK = 2;      // contraction split by expert (MoE wgrad), y stacked per expert
 constexpr int kDenseQuant = 3;    // dense, epilogue also emits the 1x32 MXFP8 quantization of y
 
-struct GemmArgs {
+// One GEMM of a launch (grouped modes: the only one).
+struct Problem {
     const uint8_t* a_s;      // A scales, MMA-tiled
     const uint8_t* b_s;      // B scales, MMA-tiled
     uint16_t* y;             // bf16 output
     int64_t M, N, K, ldy;
-    int64_t M_total;         // grouped contraction: rows of the token-sorted inputs
     int64_t k_atoms;         // 4-group scale atoms per 128-row band = ceil(K/128)
     int64_t b_bands;         // 128-row bands of B scales that exist
+    int64_t m_tiles, n_tiles;
+    int64_t first_item;      // dense: the problem's first work item
+    int num_kb;              // 128-deep K blocks
+    uint32_t fmt_bits;       // operand formats in the instruction descriptor (0 = E4M3, E4M3)
+};
+
+struct GemmArgs {
+    Problem pr[kMaxProblems];
+    int nprob;
+    int64_t items;           // dense: work items (output tiles) of all problems
+    int64_t M_total;         // grouped contraction: rows of the token-sorted inputs
     const int64_t* offsets;  // grouped: [G+1] on the device
     int G;
-    uint32_t fmt_bits;       // operand formats in the instruction descriptor (0 = E4M3, E4M3)
     uint8_t* yq;             // quantizing epilogue: E4M3 payload [M, N] (row stride N)
     uint8_t* ys;             //   and its MMA-tiled scales [M, N/32]
     unsigned int* status;
     uint64_t wait_limit_ns;
+};
+
+// Tensor maps of A and B per problem (a kernel parameter: TMA reads them there).
+struct TensorMaps {
+    CUtensorMap a[kMaxProblems];
+    CUtensorMap b[kMaxProblems];
 };
 
 // Compile-time configuration of one kernel instance.
@@ -123,11 +140,11 @@ struct TileInfo {
     int64_t kb0;     // first 128-deep K block
     int nkb;         // K blocks of this tile (0: the tile is all zeros)
     int64_t y_row0;  // output row of A row 0 (grouped contraction: g * M)
+    int prob;        // problem of the tile
 };
 
 struct Schedule {
-    int64_t m_tiles, n_tiles, total;
-    int num_kb;           // K blocks of dense / grouped-row tiles
+    int64_t m_tiles, n_tiles, total;   // grouped modes (dense: per problem)
     // grouped modes only (shared memory)
     const int* prefix;    // [G+1] grouped rows: tile prefix; grouped K: slot start / 128
     const int* first_mt;  // [G]   grouped rows: first m-tile; grouped K: slot length / 128
@@ -140,33 +157,48 @@ __device__ __forceinline__ int64_t clamped_offset(const GemmArgs& p, int g, int6
     return o < 0 ? int64_t(0) : (o > limit ? limit : o);
 }
 
+// Problem of dense work item t (problems are laid out back to back).
+__device__ __forceinline__ int problem_of(const GemmArgs& p, int64_t t) {
+    int q = 0;
+    while (q + 1 < p.nprob && t >= p.pr[q + 1].first_item) ++q;
+    return q;
+}
+
 template <int BN, int kMode>
 __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs& p, int64_t t) {
     TileInfo ti;
     ti.kb0 = 0;
-    ti.nkb = s.num_kb;
     ti.y_row0 = 0;
+    ti.prob = 0;
     if constexpr (kMode != kGroupedRows) {
         int64_t g = 0;
+        int64_t m_tiles = s.m_tiles, n_tiles = s.n_tiles;
         if constexpr (kMode == kGroupedK) {
             const int64_t per = s.m_tiles * s.n_tiles;
             g = t / per;
             t -= g * per;
+        } else {
+            ti.prob = problem_of(p, t);
+            t -= p.pr[ti.prob].first_item;
+            m_tiles = p.pr[ti.prob].m_tiles;
+            n_tiles = p.pr[ti.prob].n_tiles;
         }
-        const int64_t per_band = static_cast<int64_t>(kRasterBand) * s.n_tiles;
+        const Problem& P = p.pr[ti.prob];
+        ti.nkb = P.num_kb;
+        const int64_t per_band = static_cast<int64_t>(kRasterBand) * n_tiles;
         const int64_t band = t / per_band, within = t - band * per_band;
         const int64_t mb = band * kRasterBand;
-        const int64_t bh = min(static_cast<int64_t>(kRasterBand), s.m_tiles - mb);
+        const int64_t bh = min(static_cast<int64_t>(kRasterBand), m_tiles - mb);
         const int64_t m_blk = mb + within % bh, n_blk = within / bh;
         ti.m0 = m_blk * kBM;
         ti.n0 = n_blk * BN;
         ti.row_lo = ti.m0;
-        ti.row_hi = min(ti.m0 + kBM, p.M);
+        ti.row_hi = min(ti.m0 + kBM, P.M);
         ti.b_row = ti.n0;
         if constexpr (kMode == kGroupedK) {
             ti.kb0 = s.prefix[g];
             ti.nkb = s.first_mt[g];
-            ti.y_row0 = g * p.M;
+            ti.y_row0 = g * P.M;
         }
     } else {
         int lo = 0, hi = s.G;  // largest g with prefix[g] <= t
@@ -175,14 +207,16 @@ __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs&
             if (s.prefix[mid] <= t) lo = mid; else hi = mid;
         }
         const int g = lo;
+        const Problem& P = p.pr[0];
+        ti.nkb = P.num_kb;
         const int64_t local = t - s.prefix[g];
         const int64_t m_blk = s.first_mt[g] + local / s.n_tiles;
         const int64_t n_blk = local % s.n_tiles;
         ti.m0 = m_blk * kBM;
         ti.n0 = n_blk * BN;
-        ti.row_lo = max(ti.m0, clamped_offset(p, g, p.M));
-        ti.row_hi = min(ti.m0 + kBM, clamped_offset(p, g + 1, p.M));
-        ti.b_row = static_cast<int64_t>(g) * p.N + ti.n0;
+        ti.row_lo = max(ti.m0, clamped_offset(p, g, P.M));
+        ti.row_hi = min(ti.m0 + kBM, clamped_offset(p, g + 1, P.M));
+        ti.b_row = static_cast<int64_t>(g) * P.N + ti.n0;
     }
     return ti;
 }
@@ -196,7 +230,7 @@ __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs&
 // [row_lo, row_hi) (tile-row numbering) are not stored.  16-byte chunk
 // j of staged row r sits at position j ^ ((r >> 1) & 3), so both the writes
 // (one row per lane) and the reads (four lanes per row) are conflict-free.
-__device__ __forceinline__ void store_staged(const GemmArgs& p, const uint32_t (&v)[4][32], uint32_t stage,
+__device__ __forceinline__ void store_staged(const Problem& p, const uint32_t (&v)[4][32], uint32_t stage,
                                              int64_t row0, int64_t tile_row0, int64_t row_lo, int64_t row_hi,
                                              int64_t n, int lane) {
     const uint32_t wrow = stage + 64u * static_cast<uint32_t>(lane);
@@ -235,7 +269,7 @@ __device__ __forceinline__ void store_staged(const GemmArgs& p, const uint32_t (
 // scale atom (zero for rows or groups past the matrix: the layout's padding,
 // written for every row of a band that lies in the matrix, tile_in).
 template <int kMode>
-__device__ __forceinline__ void store_row(const GemmArgs& p, uint32_t (&v)[4][32], int64_t row, int64_t row_lo,
+__device__ __forceinline__ void store_row(const GemmArgs& a, const Problem& p, uint32_t (&v)[4][32], int64_t row, int64_t row_lo,
                                           int64_t row_hi, int64_t y_row0, int64_t n, bool tile_in) {
     if constexpr (kMode == kDenseQuant) {
         // Round to BF16, then quantize each 32-column group of this row in
@@ -278,7 +312,7 @@ __device__ __forceinline__ void store_row(const GemmArgs& p, uint32_t (&v)[4][32
                            (cvt_fp8x2<0>(bf16_lo(b[2 * j + 1]) * sc, bf16_hi(b[2 * j + 1]) * sc) << 16);
             }
             if (grp_ok) {
-                uint4* qd = reinterpret_cast<uint4*>(p.yq + row * p.N + nc);
+                uint4* qd = reinterpret_cast<uint4*>(a.yq + row * p.N + nc);
                 qd[0] = make_uint4(o[0], o[1], o[2], o[3]);
                 qd[1] = make_uint4(o[4], o[5], o[6], o[7]);
             }
@@ -286,7 +320,7 @@ __device__ __forceinline__ void store_row(const GemmArgs& p, uint32_t (&v)[4][32
         }
         // The 4 groups are 4 consecutive bytes of one tiled scale atom.
         if (tile_in && g0 < ((ngroups + 3) & ~static_cast<int64_t>(3)))
-            *reinterpret_cast<uint32_t*>(p.ys + tiled_scale_offset(row, g0, ngroups)) = codes;
+            *reinterpret_cast<uint32_t*>(a.ys + tiled_scale_offset(row, g0, ngroups)) = codes;
     } else {
         (void)tile_in;
         if (row >= row_lo && row < row_hi) {
@@ -326,8 +360,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 
 template <int BN, int STAGES, bool kMnMajor, int kMode>
 __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
-    gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tma_a,
-                     const __grid_constant__ CUtensorMap tma_b, const GemmArgs p) {
+    gemm_mxf8_kernel(const __grid_constant__ TensorMaps maps, const GemmArgs p) {
     using L = Cfg<BN, STAGES, kMode>;
     constexpr int kAcc = L::kAccStages;
     extern __shared__ uint8_t smem_raw[];
@@ -359,8 +392,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tensormap(&tma_a);
-        prefetch_tensormap(&tma_b);
+        for (int q = 0; q < p.nprob; ++q) {
+            prefetch_tensormap(&maps.a[q]);
+            prefetch_tensormap(&maps.b[q]);
+        }
     }
     if (warp == 1) {
         tmem_alloc(sbase + L::kOffTmemSlot, L::kTmemCols);
@@ -368,12 +403,11 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
     }
 
     Schedule sch;
-    sch.n_tiles = (p.N + BN - 1) / BN;
+    sch.m_tiles = p.pr[0].m_tiles;
+    sch.n_tiles = p.pr[0].n_tiles;
     sch.G = p.G;
-    sch.num_kb = static_cast<int>((p.K + kBK - 1) / kBK);
     if constexpr (kMode == kDense || kMode == kDenseQuant) {
-        sch.m_tiles = (p.M + kBM - 1) / kBM;
-        sch.total = sch.m_tiles * sch.n_tiles;
+        sch.total = p.items;
         sch.prefix = nullptr;
         sch.first_mt = nullptr;
     } else {
@@ -381,7 +415,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
         // of a grouped-row tile again, clamped the same way, for its row mask).
         int* s_prefix = reinterpret_cast<int*>(smem + L::kOffSched);
         int* s_first = s_prefix + (kMaxGroups + 1);
-        const int64_t row_limit = kMode == kGroupedRows ? p.M : p.M_total;
+        const int64_t row_limit = kMode == kGroupedRows ? p.pr[0].M : p.M_total;
         if (warp == 0) {  // tile counts and their exclusive prefix, 32 groups at a time
             int carry = 0;
             for (int base = 0; base < p.G; base += 32) {
@@ -411,7 +445,6 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
         }
         sch.prefix = s_prefix;
         sch.first_mt = s_first;
-        sch.m_tiles = (p.M + kBM - 1) / kBM;
     }
     tc_fence_before();
     __syncthreads();
@@ -421,8 +454,18 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
     if constexpr (kMode == kGroupedK) {
         sch.total = static_cast<int64_t>(p.G) * sch.m_tiles * sch.n_tiles;
         // the slots must fit the K extent of the operands
-        if (static_cast<int64_t>(sch.prefix[p.G]) * kBK > p.K) sch.total = 0;
+        if (static_cast<int64_t>(sch.prefix[p.G]) * kBK > p.pr[0].K) sch.total = 0;
     }
+    // Work item of this CTA's r-th round.  Dense launches (whose problems come
+    // longest K first) take the items of odd rounds in reverse CTA order, so
+    // that CTAs that drew long tiles early draw the last short ones late; the
+    // grouped modes go round-robin.
+    auto item_of = [&](int64_t r) -> int64_t {
+        const int64_t g = gridDim.x;
+        if constexpr (kMode == kDense || kMode == kDenseQuant)
+            return r * g + ((r & 1) ? g - 1 - blockIdx.x : blockIdx.x);
+        return r * g + blockIdx.x;
+    };
 
     if (warp == 0) {
         // ---- producer -------------------------------------------------------
@@ -431,17 +474,22 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             const uint32_t full0 = full_bar(0), empty0 = empty_bar(0);
-            for (int64_t t = blockIdx.x; t < sch.total && !*abort_flag; t += gridDim.x) {
+            for (int64_t r = 0; r * gridDim.x < sch.total && !*abort_flag; ++r) {
+                const int64_t t = item_of(r);
+                if (t >= sch.total) continue;
                 const TileInfo ti = tile_info<BN, kMode>(sch, p, t);
+                const Problem& P = p.pr[ti.prob];
+                const CUtensorMap* tma_a = &maps.a[ti.prob];
+                const CUtensorMap* tma_b = &maps.b[ti.prob];
                 const int64_t b_band0 = ti.b_row / 128;
                 int sfb_atoms = 0;
 #pragma unroll
                 for (int j = 0; j < L::kSfbAtoms; ++j)
-                    if (b_band0 + j < p.b_bands) ++sfb_atoms;
+                    if (b_band0 + j < P.b_bands) ++sfb_atoms;
                 const uint32_t bytes = L::kABytes + L::kBBytes + 512u + 512u * sfb_atoms;
-                const uint8_t* sfa_src = p.a_s + ((ti.m0 / 128) * p.k_atoms + ti.kb0) * 512;
-                const uint8_t* sfb_src = p.b_s + (b_band0 * p.k_atoms + ti.kb0) * 512;
-                const int64_t sfb_band_stride = p.k_atoms * 512;
+                const uint8_t* sfa_src = P.a_s + ((ti.m0 / 128) * P.k_atoms + ti.kb0) * 512;
+                const uint8_t* sfb_src = P.b_s + (b_band0 * P.k_atoms + ti.kb0) * 512;
+                const int64_t sfb_band_stride = P.k_atoms * 512;
                 const int32_t ma = static_cast<int32_t>(ti.m0);
                 const int32_t nb = static_cast<int32_t>(ti.b_row);
                 for (int kb = 0; kb < ti.nkb; ++kb) {
@@ -451,14 +499,14 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
                     const uint32_t sa = sbase + L::kOffA + stage * L::kABytes;
                     const uint32_t sb = sbase + L::kOffB + stage * L::kBBytes;
                     const int32_t kx = static_cast<int32_t>((ti.kb0 + kb) * kBK);
-                    tma_load_2d(sa, &tma_a, kx, ma, fb);
+                    tma_load_2d(sa, tma_a, kx, ma, fb);
                     if constexpr (!kMnMajor) {
-                        tma_load_2d(sb, &tma_b, kx, nb, fb);
+                        tma_load_2d(sb, tma_b, kx, nb, fb);
                     } else {
                         // B stored [K, N]: boxes of 128 N-bytes x 128 K-rows, one per 128 columns.
 #pragma unroll
                         for (int j = 0; j < BN / 128; ++j)
-                            tma_load_2d(sb + j * 128 * kBK, &tma_b, nb + 128 * j, kx, fb);
+                            tma_load_2d(sb + j * 128 * kBK, tma_b, nb + 128 * j, kx, fb);
                     }
                     bulk_load(sbase + L::kOffSfa + stage * 512, sfa_src + kb * 512, 512u, fb);
                     for (int j = 0; j < sfb_atoms; ++j)
@@ -500,11 +548,16 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < sch.total && ok; t += gridDim.x) {
+            for (int64_t r = 0; r * gridDim.x < sch.total && ok; ++r) {
+                const int64_t t = item_of(r);
+                if (t >= sch.total) continue;
                 if (!spin_phase(tempty_bar(acc), acc_phase ^ 1u, guard)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                const int nkb = kMode == kGroupedK ? tile_info<BN, kMode>(sch, p, t).nkb : sch.num_kb;
+                const int q = kMode == kDense || kMode == kDenseQuant ? problem_of(p, t) : 0;
+                const int nkb = kMode == kGroupedK ? tile_info<BN, kMode>(sch, p, t).nkb : p.pr[q].num_kb;
+                const int64_t K = p.pr[q].K;
+                const uint32_t fmt_bits = p.pr[q].fmt_bits;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!wait_phase(full_bar(stage), phase, guard)) { ok = false; break; }
                     tc_fence_after();
@@ -520,18 +573,18 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
                     const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
                     const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
                     const int64_t k_left = kMode == kGroupedK ? static_cast<int64_t>(nkb - kb) * kBK
-                                                              : p.K - static_cast<int64_t>(kb) * kBK;
+                                                              : K - static_cast<int64_t>(kb) * kBK;
                     if (k_left >= kBK) {
 #pragma unroll
                         for (int k = 0; k < kBK / kUmmaK; ++k)
                             tc_mma_mxf8(d_tmem, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
-                                        make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k) | p.fmt_bits, sfa_t, sfb_t,
+                                        make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k) | fmt_bits, sfa_t, sfb_t,
                                         (kb > 0 || k > 0) ? 1u : 0u);
                     } else {
                         const int ksub = static_cast<int>(k_left) / kUmmaK;
                         for (int k = 0; k < ksub; ++k)
                             tc_mma_mxf8(d_tmem, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
-                                        make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k) | p.fmt_bits, sfa_t, sfb_t,
+                                        make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k) | fmt_bits, sfa_t, sfb_t,
                                         (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     tc_commit(empty_bar(stage));  // frees the slot once these MMAs are done
@@ -556,7 +609,9 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
         const int half = (warp - 2) >> 2;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int64_t t = blockIdx.x; t < sch.total; t += gridDim.x) {
+        for (int64_t r = 0; r * gridDim.x < sch.total; ++r) {
+            const int64_t t = item_of(r);
+            if (t >= sch.total) continue;
             const TileInfo ti = tile_info<BN, kMode>(sch, p, t);
             // One lane waits; the warp follows its verdict, so the .sync.aligned
             // tensor-memory loads below always run with the full warp.
@@ -583,13 +638,14 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[c][j] = 0u;
             }
+            const Problem& P = p.pr[ti.prob];
             if constexpr (L::kStaged)
-                store_staged(p, v, sbase + L::kOffStage + (warp - 2) * L::kStageWarpBytes,
+                store_staged(P, v, sbase + L::kOffStage + (warp - 2) * L::kStageWarpBytes,
                              ti.y_row0 + ti.m0 + 32 * quad, ti.m0 + 32 * quad, ti.row_lo, ti.row_hi,
                              ti.n0 + half * 128, lane);
             else
-                store_row<kMode>(p, v, ti.m0 + 32 * quad + lane, ti.row_lo, ti.row_hi, ti.y_row0,
-                                 ti.n0 + half * 128, ti.m0 < p.M);
+                store_row<kMode>(p, P, v, ti.m0 + 32 * quad + lane, ti.row_lo, ti.row_hi, ti.y_row0,
+                                 ti.n0 + half * 128, ti.m0 < P.M);
         }
     }
 
@@ -610,8 +666,8 @@ bool make_tma_u8(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
 }
 
 template <int BN, int STAGES, bool kMnMajor, int kMode>
-cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& ta, const CUtensorMap& tb,
-                     const GemmArgs& args, int64_t max_tiles, cudaStream_t stream) {
+cudaError_t launch_t(const DeviceInfo& dev, const TensorMaps& maps, const GemmArgs& args, int64_t max_tiles,
+                     cudaStream_t stream) {
     using L = Cfg<BN, STAGES, kMode>;
     auto kern = gemm_mxf8_kernel<BN, STAGES, kMnMajor, kMode>;
     static thread_local int configured_device = -1;  // attribute set once per device and thread
@@ -623,7 +679,7 @@ cudaError_t launch_t(const DeviceInfo& dev, const CUtensorMap& ta, const CUtenso
     int64_t grid = dev.sm_count;
     if (max_tiles >= 0 && max_tiles < grid) grid = max_tiles;
     if (grid <= 0) return cudaSuccess;
-    kern<<<static_cast<unsigned>(grid), L::kThreads, L::kAlloc, stream>>>(ta, tb, args);
+    kern<<<static_cast<unsigned>(grid), L::kThreads, L::kAlloc, stream>>>(maps, args);
     return cudaGetLastError();
 }
 
@@ -639,103 +695,126 @@ bool make_dense_maps(CUtensorMap* ta, CUtensorMap* tb, const void* a_q, const vo
     return make_tma_u8(tb, b_q, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK);
 }
 
+// kind::mxf8f6f4 format codes: E4M3 = 0, E5M2 = 1 (A at bits 7-9, B at 10-12).
+uint32_t fmt_bits_of(int a_fmt, int b_fmt) {
+    return (static_cast<uint32_t>(a_fmt) << 7) | (static_cast<uint32_t>(b_fmt) << 10);
+}
+
+Problem make_problem(const void* a_s, const void* b_s, void* y, int64_t M, int64_t N, int64_t K, int64_t ldy,
+                     int64_t k_atoms, int64_t b_bands, uint32_t fmt_bits) {
+    Problem q{};
+    q.a_s = static_cast<const uint8_t*>(a_s);
+    q.b_s = static_cast<const uint8_t*>(b_s);
+    q.y = static_cast<uint16_t*>(y);
+    q.M = M; q.N = N; q.K = K; q.ldy = ldy;
+    q.k_atoms = k_atoms;
+    q.b_bands = b_bands;
+    q.m_tiles = (M + kBM - 1) / kBM;
+    q.n_tiles = (N + kBN - 1) / kBN;
+    q.num_kb = static_cast<int>((K + kBK - 1) / kBK);
+    q.fmt_bits = fmt_bits;
+    return q;
+}
+
+GemmArgs base_args(const DeviceInfo& dev) {
+    GemmArgs a{};
+    a.nprob = 1;
+    a.status = dev.status;
+    a.wait_limit_ns = kDefaultWaitLimitNs;
+    return a;
+}
+
+// Dense problems of one launch, ordered by K descending (stable), their work
+// items laid out back to back.
+bool fill_dense(const DenseGemm* gemms, int count, bool b_mn_major, TensorMaps* maps, GemmArgs* args) {
+    int order[kMaxProblems];
+    for (int i = 0; i < count; ++i) order[i] = i;
+    for (int i = 1; i < count; ++i)
+        for (int j = i; j > 0 && gemms[order[j]].K > gemms[order[j - 1]].K; --j) {
+            const int t = order[j]; order[j] = order[j - 1]; order[j - 1] = t;
+        }
+    int64_t items = 0;
+    for (int i = 0; i < count; ++i) {
+        const DenseGemm& g = gemms[order[i]];
+        if (!make_dense_maps(&maps->a[i], &maps->b[i], g.a_q, g.b_q, g.M, g.N, g.K, b_mn_major)) return false;
+        args->pr[i] = make_problem(g.a_s, g.b_s, g.y, g.M, g.N, g.K, g.ldy, (g.K + 127) / 128, (g.N + 127) / 128,
+                                   fmt_bits_of(g.a_fmt, g.b_fmt));
+        args->pr[i].first_item = items;
+        items += args->pr[i].m_tiles * args->pr[i].n_tiles;
+    }
+    args->nprob = count;
+    args->items = items;
+    return true;
+}
+
 }  // namespace
+
+cudaError_t launch_gemm_multi(const DeviceInfo& dev, const DenseGemm* gemms, int count, bool b_mn_major,
+                              cudaStream_t stream) {
+    if (count < 1 || count > kMaxProblems) return cudaErrorInvalidValue;
+    TensorMaps maps;
+    GemmArgs args = base_args(dev);
+    if (!fill_dense(gemms, count, b_mn_major, &maps, &args)) return cudaErrorInvalidValue;
+    if (b_mn_major)
+        return launch_t<kBN, kStages, true, kDense>(dev, maps, args, args.items, stream);
+    return launch_t<kBN, kStages, false, kDense>(dev, maps, args, args.items, stream);
+}
 
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
                         const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
                         int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream) {
-    CUtensorMap ta, tb;
-    if (!make_dense_maps(&ta, &tb, a_q, b_q, M, N, K, b_mn_major)) return cudaErrorInvalidValue;
-    GemmArgs args{};
-    args.a_s = static_cast<const uint8_t*>(a_s);
-    args.b_s = static_cast<const uint8_t*>(b_s);
-    args.y = static_cast<uint16_t*>(y);
-    args.M = M; args.N = N; args.K = K; args.ldy = ldy;
-    args.k_atoms = (K + 127) / 128;
-    args.b_bands = (N + 127) / 128;
-    args.offsets = nullptr;
-    args.G = 0;
-    // kind::mxf8f6f4 format codes: E4M3 = 0, E5M2 = 1 (A at bits 7-9, B at 10-12)
-    args.fmt_bits = (static_cast<uint32_t>(a_fmt) << 7) | (static_cast<uint32_t>(b_fmt) << 10);
-    args.status = dev.status;
-    args.wait_limit_ns = kDefaultWaitLimitNs;
-    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-    if (b_mn_major)
-        return launch_t<kBN, kStages, true, kDense>(dev, ta, tb, args, tiles, stream);
-    return launch_t<kBN, kStages, false, kDense>(dev, ta, tb, args, tiles, stream);
+    const DenseGemm g{a_q, a_s, b_q, b_s, M, N, K, y, ldy, a_fmt, b_fmt};
+    return launch_gemm_multi(dev, &g, 1, b_mn_major, stream);
 }
 
 cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
                               const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
                               int64_t ldy, void* y_q, void* y_s, cudaStream_t stream) {
-    CUtensorMap ta, tb;
-    if (!make_dense_maps(&ta, &tb, a_q, b_q, M, N, K, b_mn_major)) return cudaErrorInvalidValue;
-    GemmArgs args{};
-    args.a_s = static_cast<const uint8_t*>(a_s);
-    args.b_s = static_cast<const uint8_t*>(b_s);
-    args.y = static_cast<uint16_t*>(y);
-    args.M = M; args.N = N; args.K = K; args.ldy = ldy;
-    args.k_atoms = (K + 127) / 128;
-    args.b_bands = (N + 127) / 128;
-    args.fmt_bits = 0;
+    TensorMaps maps;
+    GemmArgs args = base_args(dev);
+    const DenseGemm g{a_q, a_s, b_q, b_s, M, N, K, y, ldy, 0, 0};
+    if (!fill_dense(&g, 1, b_mn_major, &maps, &args)) return cudaErrorInvalidValue;
     args.yq = static_cast<uint8_t*>(y_q);
     args.ys = static_cast<uint8_t*>(y_s);
-    args.status = dev.status;
-    args.wait_limit_ns = kDefaultWaitLimitNs;
-    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
     if (b_mn_major)
-        return launch_t<kBN, kStages, true, kDenseQuant>(dev, ta, tb, args, tiles, stream);
-    return launch_t<kBN, kStages, false, kDenseQuant>(dev, ta, tb, args, tiles, stream);
+        return launch_t<kBN, kStages, true, kDenseQuant>(dev, maps, args, args.items, stream);
+    return launch_t<kBN, kStages, false, kDenseQuant>(dev, maps, args, args.items, stream);
 }
 
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
                                 const void* b_q, const void* b_s, const int64_t* offsets, int G,
                                 int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy, int a_fmt,
                                 int b_fmt, cudaStream_t stream) {
-    CUtensorMap ta, tb;
-    if (!make_tma_u8(&ta, a_q, static_cast<uint64_t>(M_total), static_cast<uint64_t>(K), kBM))
+    TensorMaps maps;
+    if (!make_tma_u8(&maps.a[0], a_q, static_cast<uint64_t>(M_total), static_cast<uint64_t>(K), kBM))
         return cudaErrorInvalidValue;
-    if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(G) * static_cast<uint64_t>(N),
+    if (!make_tma_u8(&maps.b[0], b_q, static_cast<uint64_t>(G) * static_cast<uint64_t>(N),
                      static_cast<uint64_t>(K), kBN))
         return cudaErrorInvalidValue;
-    GemmArgs args{};
-    args.a_s = static_cast<const uint8_t*>(a_s);
-    args.b_s = static_cast<const uint8_t*>(b_s);
-    args.y = static_cast<uint16_t*>(y);
-    args.M = M_total; args.N = N; args.K = K; args.ldy = ldy;
-    args.k_atoms = (K + 127) / 128;
-    args.b_bands = static_cast<int64_t>(G) * N / 128;
+    GemmArgs args = base_args(dev);
+    args.pr[0] = make_problem(a_s, b_s, y, M_total, N, K, ldy, (K + 127) / 128, static_cast<int64_t>(G) * N / 128,
+                              fmt_bits_of(a_fmt, b_fmt));
     args.offsets = offsets;
     args.G = G;
-    args.fmt_bits = (static_cast<uint32_t>(a_fmt) << 7) | (static_cast<uint32_t>(b_fmt) << 10);
-    args.status = dev.status;
-    args.wait_limit_ns = kDefaultWaitLimitNs;
-    return launch_t<kBN, kStages, false, kGroupedRows>(dev, ta, tb, args, -1, stream);
+    return launch_t<kBN, kStages, false, kGroupedRows>(dev, maps, args, -1, stream);
 }
 
 cudaError_t launch_grouped_gemm_wgrad(const DeviceInfo& dev, const void* a_q, const void* a_s,
                                       const void* b_q, const void* b_s, const int64_t* offsets, int G,
                                       int64_t M_total, int64_t capacity, int64_t M, int64_t N, void* y,
                                       int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream) {
-    CUtensorMap ta, tb;
-    if (!make_tma_u8(&ta, a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(capacity), kBM))
+    TensorMaps maps;
+    if (!make_tma_u8(&maps.a[0], a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(capacity), kBM))
         return cudaErrorInvalidValue;
-    if (!make_tma_u8(&tb, b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(capacity), kBN))
+    if (!make_tma_u8(&maps.b[0], b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(capacity), kBN))
         return cudaErrorInvalidValue;
-    GemmArgs args{};
-    args.a_s = static_cast<const uint8_t*>(a_s);
-    args.b_s = static_cast<const uint8_t*>(b_s);
-    args.y = static_cast<uint16_t*>(y);
-    args.M = M; args.N = N; args.K = capacity; args.ldy = ldy;
+    GemmArgs args = base_args(dev);
+    args.pr[0] = make_problem(a_s, b_s, y, M, N, capacity, ldy, capacity / 128, (N + 127) / 128,
+                              fmt_bits_of(a_fmt, b_fmt));
     args.M_total = M_total;
-    args.k_atoms = capacity / 128;
-    args.b_bands = (N + 127) / 128;
     args.offsets = offsets;
     args.G = G;
-    args.fmt_bits = (static_cast<uint32_t>(a_fmt) << 7) | (static_cast<uint32_t>(b_fmt) << 10);
-    args.status = dev.status;
-    args.wait_limit_ns = kDefaultWaitLimitNs;
-    return launch_t<kBN, kStages, false, kGroupedK>(dev, ta, tb, args, -1, stream);
+    return launch_t<kBN, kStages, false, kGroupedK>(dev, maps, args, -1, stream);
 }
 
 // ---- bounded-wait probe ---------------------------------------------------------------

@@ -49,6 +49,24 @@ cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, 
                                int64_t ld, void* q, void* s_fwd, void* s_bwd, bool tiled,
                                cudaStream_t stream);
 
+// One dense GEMM y = A B^T of a multi-GEMM launch (fields as in mxq_gemm_bf16out_fmt).
+struct DenseGemm {
+    const void* a_q;
+    const void* a_s;
+    const void* b_q;
+    const void* b_s;
+    int64_t M, N, K;
+    void* y;
+    int64_t ldy;
+    int a_fmt, b_fmt;
+};
+
+// 1 to 4 dense GEMMs (all with B K-major, or all MN-major) in one persistent
+// launch over their output tiles.  cudaErrorInvalidValue for a bad count or
+// shapes whose tensor maps cannot be encoded.
+cudaError_t launch_gemm_multi(const DeviceInfo& dev, const DenseGemm* gemms, int count, bool b_mn_major,
+                              cudaStream_t stream);
+
 // Dense block-scaled GEMM (see mxq_gemm_bf16out).  Returns cudaErrorInvalidValue
 // when a tensor map cannot be encoded for the given shapes.
 cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,

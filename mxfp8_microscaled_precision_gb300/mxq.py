@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
         L.mxq_quant_1x32_dual.argtypes = [P, I64, I64, I64, P, P, P, P, S, P]
         L.mxq_quant_1x32_dual_batched.argtypes = [P, I64, I64, I64, I64, I64, P, P, P, P, S, S, P]
         L.mxq_gemm_bf16out_fmt.argtypes = [P, P, S, P, P, S, I64, I64, I64, S, P, I64, P]
+        L.mxq_gemm_bf16out_multi.argtypes = [ctypes.POINTER(GemmDesc), I32, S, P]
         L.mxq_quant_1x32_cols_grouped.argtypes = [P, I64, I64, I64, P, I32, I64, P, P, S, P]
         L.mxq_quant_1x32_cols_grouped_fmt.argtypes = [P, I64, I64, I64, P, I32, I64, P, P, S, S, P]
         L.mxq_grouped_gemm_fmt.argtypes = [P, P, S, P, P, S, P, I32, I64, I64, I64, P, I64, P]
@@ -86,7 +87,7 @@ def lib() -> ctypes.CDLL:
                   "mxq_quant_1x32_dual_batched", "mxq_quant_1x32_cols_grouped",
                   "mxq_grouped_gemm_wgrad", "mxq_gemm_bf16out_fmt", "mxq_gemm_mxfp8out",
                   "mxq_fsdp_payload_layout", "mxq_fsdp_unpack", "mxq_quant_1x32_cols_grouped_fmt",
-                  "mxq_grouped_gemm_fmt", "mxq_grouped_gemm_wgrad_fmt"):
+                  "mxq_grouped_gemm_fmt", "mxq_grouped_gemm_wgrad_fmt", "mxq_gemm_bf16out_multi"):
             getattr(L, f).restype = S
         _lib = L
         return L
@@ -258,6 +259,37 @@ def gemm_fmt(a_q, a_s, a_fmt, b_q, b_s, b_fmt, M: int, N: int, K: int, b_mn_majo
                                       M, N, K, 1 if b_mn_major else 0, _ptr(out), out.stride(0), _stream()),
            "mxq_gemm_bf16out_fmt")
     return out
+
+
+class GemmDesc(ctypes.Structure):
+    """mxq_gemm_desc of include/mxq.h."""
+    _fields_ = [("a_q", ctypes.c_void_p), ("a_s", ctypes.c_void_p), ("b_q", ctypes.c_void_p),
+                ("b_s", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("y", ctypes.c_void_p), ("ldy", ctypes.c_int64), ("a_fmt", ctypes.c_int), ("b_fmt", ctypes.c_int)]
+
+
+def gemm_multi(gemms, b_mn_major: bool = False):
+    """Several independent GEMMs in one launch (see mxq_gemm_bf16out_multi).
+    gemms: list of dicts with a_q, a_s, b_q, b_s, M, N, K and optionally out,
+    a_fmt, b_fmt ("e4m3" default).  Returns the list of outputs y [M, N] bf16."""
+    if not 1 <= len(gemms) <= 4:
+        raise ValueError("gemm_multi takes 1 to 4 GEMMs")
+    descs = (GemmDesc * len(gemms))()
+    outs = []
+    for d, g in zip(descs, gemms):
+        M, N, K = g["M"], g["N"], g["K"]
+        out = g.get("out")
+        if out is None:
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=g["a_q"].device)
+        outs.append(out)
+        addr = [None if g[k] is None else g[k].data_ptr() for k in ("a_q", "a_s", "b_q", "b_s")]
+        d.a_q, d.a_s, d.b_q, d.b_s = addr
+        d.M, d.N, d.K = M, N, K
+        d.y, d.ldy = out.data_ptr(), out.stride(0)
+        d.a_fmt, d.b_fmt = _fmt(g.get("a_fmt", "e4m3")), _fmt(g.get("b_fmt", "e4m3"))
+    _check(lib().mxq_gemm_bf16out_multi(descs, len(gemms), 1 if b_mn_major else 0, _stream()),
+           "mxq_gemm_bf16out_multi")
+    return outs
 
 
 def gemm_mxfp8out(a_q, a_s, b_q, b_s, M: int, N: int, K: int, b_mn_major: bool = False,

@@ -122,6 +122,29 @@ def test_moe_backward_argument_errors(L):
     assert wf(FAKE, FAKE, 1, FAKE, FAKE, 0, FAKE, 4, 300, 1024, 128, 120, FAKE, 120, None) == 2  # N % 16
 
 
+def test_gemm_multi_argument_errors(L):
+    from mxfp8_microscaled_precision_gb300 import mxq
+    D = (mxq.GemmDesc * 2)()
+    for d in D:
+        d.a_q = d.a_s = d.b_q = d.b_s = d.y = 0x10000
+        d.M, d.N, d.K, d.ldy, d.a_fmt, d.b_fmt = 64, 128, 64, 128, 0, 0
+    f = L.mxq_gemm_bf16out_multi
+    assert f(None, 0, 0, None) == 0                # nothing to do
+    assert f(None, 1, 0, None) == 1                # no descriptors
+    assert f(D, 5, 0, None) == 1                   # more than 4
+    assert f(D, 2, 2, None) == 1                   # bad orientation flag
+    D[1].K = 48
+    assert f(D, 2, 0, None) == 2                   # K % 32 in the second GEMM: nothing runs
+    D[1].K, D[1].a_fmt = 64, 3
+    assert f(D, 2, 0, None) == 1                   # bad format
+    D[1].a_fmt, D[1].N, D[1].ldy = 0, 144, 144
+    assert f(D, 2, 1, None) == 2                   # MN-major needs N % 128
+    D[1].N, D[1].ldy, D[0].ldy = 128, 128, 100
+    assert f(D, 2, 0, None) == 1                   # ldy < N
+    D[0].ldy, D[0].M, D[1].M = 128, 0, 0
+    assert f(D, 2, 0, None) == 0                   # every GEMM empty
+
+
 def test_fused_quant_gemm_argument_errors(L):
     g = L.mxq_gemm_mxfp8out
     assert g(FAKE, FAKE, FAKE, FAKE, 64, 48, 64, 0, FAKE, 48, FAKE, FAKE, None) == 2    # N % 32
