@@ -41,9 +41,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 L2_FLUSH_BYTES = 256 << 20   # larger than the 129 MB L2
 L2_BYTES = 129 * 10**6
-# DRAM bytes (read + write) of one GEMM launch (the forward GEMM of the step), from
-# an ncu --set full capture of the kernel as it stands; None where not captured.
-GEMM_TRAFFIC_BYTES = {"linear_train": 86519808}
+# DRAM bytes (read + write) per GEMM launch of one step, averaged over the step's
+# GEMM launches like `units_per_launch` (linear_train: the forward GEMM and the
+# backward dgrad + wgrad launch), from an ncu --set full capture of the kernel as
+# it stands; None where not captured.
+GEMM_TRAFFIC_BYTES = {"linear_train": 140943104}
 
 
 def load_peaks():
