@@ -33,6 +33,9 @@ import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
+# Step entries that launch more than one kernel of the library.
+LAUNCHES_PER_ENTRY = {"quant_XW_dual": 2}
+
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
@@ -205,6 +208,9 @@ class LinearTrain(Workload):
         self.y, self.dx, self.dw = torch.empty((M, N), **bf), torch.empty((M, K), **bf), torch.empty((N, K), **bf)
         self.outputs = [self.y, self.dx, self.dw]
         gr, grs, gc, gcs = self.qg
+        # X and W are quantized on two streams: the second kernel's CTAs take the
+        # SM slots the first one frees in its last, partly filled round
+        self.side = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
         self.bwd = [dict(a_q=gr, a_s=grs, b_q=self.qw[2], b_s=self.qw[3], M=M, N=K, K=N, out=self.dx),
                     dict(a_q=gc, a_s=gcs, b_q=self.qx[2], b_s=self.qx[3], M=N, N=K, K=M, out=self.dw)]
 
@@ -219,13 +225,25 @@ class LinearTrain(Workload):
         wr, wrs, wc, wcs = self.qw
         gr, grs, gc, gcs = self.qg
         return [
-            ("quant_X_dual", "quant", _dual_bytes(M, K), lambda: mxq.quant_1x32_dual(i["X"], out=self.qx)),
-            ("quant_W_dual", "quant", _dual_bytes(N, K), lambda: mxq.quant_1x32_dual(i["W"], out=self.qw)),
+            ("quant_XW_dual", "quant", _dual_bytes(M, K) + _dual_bytes(N, K), self._quant_xw),
             ("quant_dY_dual", "quant", _dual_bytes(M, N), lambda: mxq.quant_1x32_dual(i["dY"], out=self.qg)),
             ("gemm_fwd", "gemm", 2 * M * N * K, lambda: mxq.gemm(xr, xrs, wr, wrs, M, N, K, out=self.y)),
             # dgrad dX = dY W and wgrad dW = dY^T X share one launch (one last wave of tiles)
             ("gemm_bwd", "gemm", 2 * 2 * M * N * K, lambda: mxq.gemm_multi(self.bwd)),
         ]
+
+    def _quant_xw(self):
+        import torch
+        from mxfp8_microscaled_precision_gb300 import mxq
+        cur = torch.cuda.current_stream()
+        for s in self.side:
+            s.wait_stream(cur)
+        with torch.cuda.stream(self.side[0]):
+            mxq.quant_1x32_dual(self.inputs["X"], out=self.qx)
+        with torch.cuda.stream(self.side[1]):
+            mxq.quant_1x32_dual(self.inputs["W"], out=self.qw)
+        for s in self.side:
+            cur.wait_stream(s)
 
     def cpu_sample(self, budget_s):
         """Times the oracle on row samples of each step part; returns
@@ -857,7 +875,7 @@ def run_gpu(args):
             gbs = kern[j][2] * args.steps / (sum(per_kernel[j]) / 1e3) / 1e9
             other_hbm[kern[j][0]] = {"kind": kern[j][1], "bytes_per_launch": kern[j][2],
                                      "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
-    own_launches = sum(1 for j in range(nk) if kern[j][1] != "collective")
+    own_launches = sum(LAUNCHES_PER_ENTRY.get(kern[j][0], 1) for j in range(nk) if kern[j][1] != "collective")
 
     # ---- end to end through the public API, host buffers, copies inside the timed step
     # Every step copies its inputs from pinned host memory and its outputs back. Steps
