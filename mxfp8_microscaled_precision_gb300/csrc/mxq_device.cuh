@@ -36,6 +36,14 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
+// One 256-bit global store of 8 words (dst 32-byte aligned): a whole 32-byte
+// sector in one instruction.
+__device__ __forceinline__ void stg256(void* dst, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // 16-byte shared-memory store and load ordered with other memory accesses
 // (for data exchanged between the lanes of a warp around __syncwarp).
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {

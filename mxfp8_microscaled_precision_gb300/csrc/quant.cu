@@ -263,6 +263,9 @@ __device__ __forceinline__ void col_pass(const uint32_t* tw_ptr, int64_t c0, int
         m2 = max_u16x2(m2, w[j] & 0x7FFF7FFFu);
     }
     uint8_t* q0 = q_col + cA * out_ld + tok;
+    // Runs start at multiples of 32 tokens in rows of a multiple of 32 bytes, so
+    // they are 32-byte aligned whenever the output is (uniform over the call).
+    const bool v8 = (reinterpret_cast<uintptr_t>(q_col) & 31u) == 0;
     // Scale bytes of rows cA and cA+1 (same 32-row block: cA is even).
     uint8_t* s0 = kTiled ? s_col + tiled_scale_offset(cA, g_out, ogroups) : s_col + cA * ogroups + g_out;
     const int64_t s_next = kTiled ? 16 : ogroups;
@@ -297,9 +300,13 @@ __device__ __forceinline__ void col_pass(const uint32_t* tw_ptr, int64_t c0, int
             }
         }
         if (ok) {
-            uint4* dst = reinterpret_cast<uint4*>(q0 + half * out_ld);
-            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            uint8_t* dst = q0 + half * out_ld;
+            if (v8) {   // the 32-byte run in one store (a lane writes one row per store)
+                stg256(dst, o);
+            } else {
+                reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
         }
         if (ok || kTiled) s0[half * s_next] = ok ? code : 0;
     }

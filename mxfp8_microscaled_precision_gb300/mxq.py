@@ -158,11 +158,13 @@ def _fmt(fmt) -> int:
 
 
 def quant_1x32_dual_batched(x: torch.Tensor, row: bool = True, col: bool = True, layout="tiled",
-                            fmt="e4m3"):
+                            fmt="e4m3", out=None):
     """1x32 quantization of every matrix of a 3-D bf16 CUDA tensor [B, R, C]
     (e.g. stacked expert weights; B = 1 for a single matrix) with payload
     format fmt ("e4m3" or "e5m2").  Returns (q_row [B,R,C], s_row [B, bytes],
-    q_col [B,C,R], s_col [B, bytes]); pairs not asked for are None."""
+    q_col [B,C,R], s_col [B, bytes]); pairs not asked for are None.  `out`
+    may supply the four output tensors (contiguous per matrix; None where not
+    asked for)."""
     if x.dim() == 2:
         x = x.unsqueeze(0)
     if x.dtype != torch.bfloat16 or x.dim() != 3 or not x.is_cuda or x.stride(2) != 1:
@@ -170,10 +172,13 @@ def quant_1x32_dual_batched(x: torch.Tensor, row: bool = True, col: bool = True,
     B, R, C = x.shape
     dev = x.device
     u8 = dict(dtype=torch.uint8, device=dev)
-    q_row = torch.empty((B, R, C), **u8) if row else None
-    s_row = torch.empty((B, scale_bytes(R, C, layout)), **u8) if row else None
-    q_col = torch.empty((B, C, R), **u8) if col else None
-    s_col = torch.empty((B, scale_bytes(C, R, layout)), **u8) if col else None
+    if out is not None:
+        q_row, s_row, q_col, s_col = out
+    else:
+        q_row = torch.empty((B, R, C), **u8) if row else None
+        s_row = torch.empty((B, scale_bytes(R, C, layout)), **u8) if row else None
+        q_col = torch.empty((B, C, R), **u8) if col else None
+        s_col = torch.empty((B, scale_bytes(C, R, layout)), **u8) if col else None
     _check(lib().mxq_quant_1x32_dual_batched(_ptr(x), B, R, C, x.stride(1), x.stride(0), _ptr(q_row),
                                              _ptr(s_row), _ptr(q_col), _ptr(s_col), _layout(layout),
                                              _fmt(fmt), _stream()), "mxq_quant_1x32_dual_batched")

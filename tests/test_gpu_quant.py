@@ -104,6 +104,31 @@ def test_strided_input():
     assert np.array_equal(u8(qc), oqc) and np.array_equal(u8(sc), oracle.scale_tiled(osc))
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_column_copy_at_16_byte_alignment(fmt):
+    """The column copy into a buffer 16 (not 32) bytes past an aligned address
+    (the ABI's minimum alignment, where 256-bit stores are not allowed): the
+    same bytes as into an aligned buffer and as the oracle."""
+    from oracle import oracle
+    mxq = _mxq()
+    R, C = 192, 320
+    x = torch.randn(R, C).to(torch.bfloat16)
+    xd = x.cuda()
+    base = torch.full((C * R + 64,), 0xEE, dtype=torch.uint8, device="cuda")
+    off = (32 - base.data_ptr() % 32) % 32 + 16            # 16 bytes past a 32-byte boundary
+    qc_odd = base[off:off + C * R].view(C, R)
+    assert qc_odd.data_ptr() % 32 == 16
+    sc = torch.empty(mxq.scale_bytes(C, R), dtype=torch.uint8, device="cuda")
+    _, _, qc_al, sc_al, = mxq.quant_1x32_dual_batched(xd, row=False, fmt=fmt)
+    q_b = qc_odd.view(1, C, R)
+    mxq.quant_1x32_dual_batched(xd, row=False, fmt=fmt, out=(None, None, q_b, sc.view(1, -1)))
+    torch.cuda.synchronize()
+    assert torch.equal(qc_odd, qc_al[0]) and torch.equal(sc, sc_al[0].reshape(-1))
+    assert torch.all(base[:off] == 0xEE) and torch.all(base[off + C * R:] == 0xEE), "bytes outside were written"
+    oq, _ = oracle.quant_rows_fmt(np.ascontiguousarray(bits(x).T), 1 if fmt == "e5m2" else 0)
+    assert np.array_equal(u8(qc_odd), oq)
+
+
 def test_tiled_padding_is_zero():
     """Scale bytes outside the matrix in the tiled layout are written as 0."""
     mxq = _mxq()
