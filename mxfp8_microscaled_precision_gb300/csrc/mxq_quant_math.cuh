@@ -46,10 +46,28 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
     return r;
 }
 
-// Largest |x| (as BF16 bits, sign cleared) of 8 BF16 values.
+// Per-half max(|a|, |b|) of two BF16 pairs, NaN if either is NaN (the sign bit
+// of the result is the XOR of the signs: mask it off).  One instruction.
+__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Per-half BF16 product, round to nearest even.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// BF16 bits of 2^-e for e in [-127, 126] (a normal number).
+__device__ __forceinline__ uint32_t pow2_neg_bf16(int e) { return static_cast<uint32_t>(127 - e) << 7; }
+
+// Largest |x| (as BF16 bits, sign cleared) of 8 BF16 values; a group holding a
+// NaN gives a NaN pattern, one holding an Inf (and no NaN) 0x7F80: both >= 0x7F80.
 __device__ __forceinline__ uint32_t amax8_bits(const uint4 v) {
-    const uint32_t m = max_u16x2(max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                                 max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    const uint32_t m = max_abs_bf16x2(max_abs_bf16x2(v.x, v.y), max_abs_bf16x2(v.z, v.w)) & 0x7FFF7FFFu;
     return max(m & 0xFFFFu, m >> 16);
 }
 

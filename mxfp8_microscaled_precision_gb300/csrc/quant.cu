@@ -41,14 +41,23 @@ constexpr int kTileBytes = kTile * kTile * 2;                   // 32 KB of BF16
 constexpr int kCtasPerSm = 3;                                   // ring kernels
 constexpr int kSmemBytes = kRing * kTileBytes + 1024 + 256;     // ring + alignment + barriers
 
-// Quantize 8 BF16 values (4 words) with scale 2^-e -> 8 FP8 bytes.
+// FP8 pair of the two BF16 values of a word (as FP32, exactly).
+template <int kFmt>
+__device__ __forceinline__ uint32_t cvt_pair(uint32_t w) {
+    return cvt_fp8x2<kFmt>(bf16_lo(w), bf16_hi(w));
+}
+
+// Quantize 8 finite BF16 values (4 words) with scale 2^-e -> 8 FP8 bytes; s2 is
+// 2^-e as a BF16 pair (pow2_neg_bf16 in both halves).  The BF16 product is
+// exact: x * 2^-e has x's 8 significant bits and |x * 2^-e| <= the format's
+// largest value, except when it falls below 2^-126, where both the exact and
+// the rounded product convert to a signed zero (far below half the smallest
+// E4M3 / E5M2 subnormal).
 template <int kFmt = 0>
-__device__ __forceinline__ uint2 quant8(const uint4 v, float sc) {
+__device__ __forceinline__ uint2 quant8(const uint4 v, uint32_t s2) {
     uint2 o;
-    o.x = cvt_fp8x2<kFmt>(bf16_lo(v.x) * sc, bf16_hi(v.x) * sc) |
-          (cvt_fp8x2<kFmt>(bf16_lo(v.y) * sc, bf16_hi(v.y) * sc) << 16);
-    o.y = cvt_fp8x2<kFmt>(bf16_lo(v.z) * sc, bf16_hi(v.z) * sc) |
-          (cvt_fp8x2<kFmt>(bf16_lo(v.w) * sc, bf16_hi(v.w) * sc) << 16);
+    o.x = cvt_pair<kFmt>(mul_bf16x2(v.x, s2)) | (cvt_pair<kFmt>(mul_bf16x2(v.y, s2)) << 16);
+    o.y = cvt_pair<kFmt>(mul_bf16x2(v.z, s2)) | (cvt_pair<kFmt>(mul_bf16x2(v.w, s2)) << 16);
     return o;
 }
 
@@ -189,7 +198,7 @@ __device__ __forceinline__ void row_pass(ChunkOf chunk_of, int64_t r0, int64_t c
         } else {
             const int e = rceil_exponent<kFmt>(m);
             code = static_cast<uint8_t>(e + 127);
-            out = quant8<kFmt>(v, pow2_neg(e));
+            out = quant8<kFmt>(v, pow2_neg_bf16(e) * 0x10001u);
         }
         if (valid) *reinterpret_cast<uint2*>(qp + j * qstep) = out;
         if ((chunk & 3) == 0 && (valid || kTiled)) {  // tiled padding gets 0
@@ -260,8 +269,9 @@ __device__ __forceinline__ void col_pass(const uint32_t* tw_ptr, int64_t c0, int
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         w[j] = lds32(tw + 4u * static_cast<uint32_t>((32 * gi + j) * 64 + p));
-        m2 = max_u16x2(m2, w[j] & 0x7FFF7FFFu);
+        m2 = max_abs_bf16x2(m2, w[j]);
     }
+    m2 &= 0x7FFF7FFFu;                          // column cA's amax in the low half, cA+1's in the high
     uint8_t* q0 = q_col + cA * out_ld + tok;
     // Runs start at multiples of 32 tokens in rows of a multiple of 32 bytes, so
     // they are 32-byte aligned whenever the output is (uniform over the call).
@@ -269,46 +279,65 @@ __device__ __forceinline__ void col_pass(const uint32_t* tw_ptr, int64_t c0, int
     // Scale bytes of rows cA and cA+1 (same 32-row block: cA is even).
     uint8_t* s0 = kTiled ? s_col + tiled_scale_offset(cA, g_out, ogroups) : s_col + cA * ogroups + g_out;
     const int64_t s_next = kTiled ? 16 : ogroups;
+    const uint32_t mh[2] = {m2 & 0xFFFFu, m2 >> 16};
+    uint8_t code[2];
+    uint32_t o[2][8];
+    if (mh[0] < 0x7F80u && mh[1] < 0x7F80u) {
+        // Both groups finite: scale both columns of a word with one BF16 multiply
+        // (exact, see quant8), then pair consecutive tokens of each column.
+        const int e0 = rceil_exponent<kFmt>(mh[0]), e1 = rceil_exponent<kFmt>(mh[1]);
+        code[0] = static_cast<uint8_t>(e0 + 127);
+        code[1] = static_cast<uint8_t>(e1 + 127);
+        const uint32_t s2 = pow2_neg_bf16(e0) | (pow2_neg_bf16(e1) << 16);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const uint32_t m = half ? (m2 >> 16) : (m2 & 0xFFFFu);
-        uint8_t code;
-        uint32_t o[8];
-        if (m >= 0x7F80u) {
-            code = 0xFF;
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t p0 = mul_bf16x2(w[4 * j], s2), p1 = mul_bf16x2(w[4 * j + 1], s2);
+            const uint32_t p2 = mul_bf16x2(w[4 * j + 2], s2), p3 = mul_bf16x2(w[4 * j + 3], s2);
+            o[0][j] = cvt_fp8x2<kFmt>(bf16_lo(p0), bf16_lo(p1)) | (cvt_fp8x2<kFmt>(bf16_lo(p2), bf16_lo(p3)) << 16);
+            o[1][j] = cvt_fp8x2<kFmt>(bf16_hi(p0), bf16_hi(p1)) | (cvt_fp8x2<kFmt>(bf16_hi(p2), bf16_hi(p3)) << 16);
+        }
+    } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                uint32_t bt = 0x7F7F7F7Fu;
+        for (int half = 0; half < 2; ++half) {
+            if (mh[half] >= 0x7F80u) {   // NaN or Inf in the group: 0x7F | sign per element
+                code[half] = 0xFF;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t h = half ? (w[4 * j + u] >> 16) : (w[4 * j + u] & 0xFFFFu);
-                    bt |= ((h >> 15) & 1u) << (8 * u + 7);
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t bt = 0x7F7F7F7Fu;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t h = half ? (w[4 * j + u] >> 16) : (w[4 * j + u] & 0xFFFFu);
+                        bt |= ((h >> 15) & 1u) << (8 * u + 7);
+                    }
+                    o[half][j] = bt;
                 }
-                o[j] = bt;
-            }
-        } else {
-            const int e = rceil_exponent<kFmt>(m);
-            const float sc = pow2_neg(e);
-            code = static_cast<uint8_t>(e + 127);
+            } else {
+                const int e = rceil_exponent<kFmt>(mh[half]);
+                const float sc = pow2_neg(e);
+                code[half] = static_cast<uint8_t>(e + 127);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float f[4];
+                for (int j = 0; j < 8; ++j) {
+                    float f[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    f[u] = (half ? bf16_hi(w[4 * j + u]) : bf16_lo(w[4 * j + u])) * sc;
-                o[j] = cvt_fp8x2<kFmt>(f[0], f[1]) | (cvt_fp8x2<kFmt>(f[2], f[3]) << 16);
+                    for (int u = 0; u < 4; ++u)
+                        f[u] = (half ? bf16_hi(w[4 * j + u]) : bf16_lo(w[4 * j + u])) * sc;
+                    o[half][j] = cvt_fp8x2<kFmt>(f[0], f[1]) | (cvt_fp8x2<kFmt>(f[2], f[3]) << 16);
+                }
             }
         }
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
         if (ok) {
             uint8_t* dst = q0 + half * out_ld;
             if (v8) {   // the 32-byte run in one store (a lane writes one row per store)
-                stg256(dst, o);
+                stg256(dst, o[half]);
             } else {
-                reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[half][0], o[half][1], o[half][2], o[half][3]);
+                reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[half][4], o[half][5], o[half][6], o[half][7]);
             }
         }
-        if (ok || kTiled) s0[half * s_next] = ok ? code : 0;
+        if (ok || kTiled) s0[half * s_next] = ok ? code[half] : 0;
     }
 }
 
@@ -510,7 +539,7 @@ __global__ void __launch_bounds__(kThreads) quant_32x32_kernel(const uint16_t* _
         } else {
             const int e = rceil_exponent(m);
             code = static_cast<uint8_t>(e + 127);
-            out = quant8(v[j], pow2_neg(e));
+            out = quant8(v[j], pow2_neg_bf16(e) * 0x10001u);
         }
         if (valid) *reinterpret_cast<uint2*>(qp + j * 16 * k) = out;
         if (sp && (chunk & 3) == 0 && (valid || kTiled)) {
