@@ -294,7 +294,8 @@ __device__ __forceinline__ void store_row(const GemmArgs& a, const Problem& p, u
             }
             uint32_t m2 = 0u;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) m2 = max_u16x2(m2, b[i] & 0x7FFF7FFFu);
+            for (int i = 0; i < 16; ++i) m2 = max_abs_bf16x2(m2, b[i]);
+            m2 &= 0x7FFF7FFFu;
             const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
             uint32_t o[8];
             uint32_t code;
@@ -304,12 +305,15 @@ __device__ __forceinline__ void store_row(const GemmArgs& a, const Problem& p, u
                 for (int j = 0; j < 8; ++j) o[j] = nan_bytes4(b[2 * j], b[2 * j + 1]);
             } else {
                 const int e = rceil_exponent<0>(m);
-                const float sc = pow2_neg(e);
+                // 2^-e in both BF16 halves: the BF16 product is exact (or, below 2^-126,
+                // converts to the same signed zero as the exact value)
+                const uint32_t s2 = pow2_neg_bf16(e) * 0x10001u;
                 code = static_cast<uint32_t>(e + 127);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    o[j] = cvt_fp8x2<0>(bf16_lo(b[2 * j]) * sc, bf16_hi(b[2 * j]) * sc) |
-                           (cvt_fp8x2<0>(bf16_lo(b[2 * j + 1]) * sc, bf16_hi(b[2 * j + 1]) * sc) << 16);
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t p0 = mul_bf16x2(b[2 * j], s2), p1 = mul_bf16x2(b[2 * j + 1], s2);
+                    o[j] = cvt_fp8x2<0>(bf16_lo(p0), bf16_hi(p0)) | (cvt_fp8x2<0>(bf16_lo(p1), bf16_hi(p1)) << 16);
+                }
             }
             if (grp_ok) {
                 uint4* qd = reinterpret_cast<uint4*>(a.yq + row * p.N + nc);
