@@ -207,6 +207,37 @@ def test_full_sweep_4096_forward():
     assert_gemm_close(y[torch.from_numpy(r).cuda()], oracle.gemm(xd, wd, rows=r), "sweep 4096")
 
 
+def test_full_sweep_16384_three_gemms():
+    """The largest linear layer, X, dY [16384, 16384], W [16384, 16384]: forward by the
+    single-GEMM call, dgrad and wgrad by the one-launch pair the benchmark times;
+    64 sampled output rows of each against the oracle (operand rows quantized by the
+    oracle one by one where the product needs only those rows)."""
+    mxq, workloads, oracle = _mods()
+    d = workloads.sweep(16384)
+    M = N = K = 16384
+    X, W, dY = d["X"], d["W"], d["dY"]
+    xr, xrs, xc, xcs = mxq.quant_1x32_dual(X.cuda())
+    wr, wrs, wc, wcs = mxq.quant_1x32_dual(W.cuda())
+    gr, grs, gc, gcs = mxq.quant_1x32_dual(dY.cuda())
+    y = mxq.gemm(xr, xrs, wr, wrs, M, N, K)
+    dx, dw = mxq.gemm_multi([dict(a_q=gr, a_s=grs, b_q=wc, b_s=wcs, M=M, N=K, K=N),
+                             dict(a_q=gc, a_s=gcs, b_q=xc, b_s=xcs, M=N, N=K, K=M)])
+    torch.cuda.synchronize()
+    del xr, xrs, wr, wrs, gr, grs, wc, wcs, gc, gcs, xc, xcs
+    r = _sample_rows(M, n=64, seed=5)
+    rt = torch.from_numpy(r).cuda()
+    deq_rows = lambda t: oracle.dequant_rows(*oracle.quant_rows(bits(t)))
+    w_deq = deq_rows(W)                                        # forward B: W's row copy
+    assert_gemm_close(y[rt], oracle.gemm(deq_rows(X[r]), w_deq, rows=None), "forward 16384")
+    del w_deq
+    wt_deq = deq_rows(W.t().contiguous())                      # dgrad B: W's column copy
+    assert_gemm_close(dx[rt], oracle.gemm(deq_rows(dY[r]), wt_deq, rows=None), "dgrad 16384")
+    del wt_deq
+    xt_deq = deq_rows(X.t().contiguous())                      # wgrad B: X's column copy
+    gt_rows = deq_rows(dY.t()[r].contiguous())                 # wgrad A: sampled rows of dY's column copy
+    assert_gemm_close(dw[rt], oracle.gemm(gt_rows, xt_deq, rows=None), "wgrad 16384")
+
+
 def test_small_linear_exhaustive():
     """The 256 x 512 x 512 linear forward, every output compared."""
     mxq, workloads, oracle = _mods()
