@@ -352,6 +352,48 @@ mxq_status mxq_grouped_gemm_fmt(const void* a_q, const void* a_s, mxq_fp8_format
                                 int64_t N, int64_t K, void* y, int64_t ldy, mxq_stream_t stream);
 
 /*
+ * Group-tiled A scales for mxq_grouped_gemm_group_tiled.  The rows of expert g,
+ * [group_offsets[g], group_offsets[g+1]), are tiled on their own: the
+ * MXQ_SCALE_MMA_TILED layout of that expert's [n_g, cols/32] scales (n_g rows
+ * padded to a multiple of 128 with zeros), the experts' layouts one after the
+ * other in expert order.  Expert g's first 128-row band is therefore band
+ * B_g = sum over g' < g of ceil(n_g' / 128); band b occupies bytes
+ * [b * A, (b+1) * A) with A = ceil(cols / 128) * 512.  The pages do not define
+ * this layout (nor any scale layout for the tensor cores): it exists so that
+ * a grouped GEMM's row tiles can start at every expert's first row.
+ *
+ * s_tiled    u8 MXQ_SCALE_MMA_TILED scales of a row quantization [rows, cols]
+ *            (mxq_quant_1x32_dual's s_row).
+ * group_offsets  DEVICE int64 [G+1], as for mxq_grouped_gemm (off[G] = rows).
+ * bands_cap  bands of s_out; must be >= ceil(rows/128) + G, which holds every
+ *            expert's bands for any offsets.  s_out has bands_cap * A bytes;
+ *            bands after the last expert's are not written.  Offsets that break
+ *            mxq_grouped_gemm's rule are clamped and never cause an access out of
+ *            bounds (the scales are then unspecified).
+ * Shapes: 1 <= G <= 1024; cols % 32 == 0.  One HBM-bound kernel: reads and
+ * writes about rows * cols / 32 bytes.
+ */
+mxq_status mxq_scale_regroup_rows(const void* s_tiled, int64_t rows, int64_t cols,
+                                  const int64_t* group_offsets, int32_t G, int64_t bands_cap, void* s_out,
+                                  mxq_stream_t stream);
+
+/*
+ * mxq_grouped_gemm_fmt with A's scales group-tiled (mxq_scale_regroup_rows on
+ * the same group_offsets and bands_cap = a_bands_cap).  Each expert's 128-row
+ * tiles start at its first row, so no tile spans two experts: an expert with
+ * n_g rows costs ceil(n_g / 128) row tiles instead of the up to ceil(n_g / 128)
+ * + 1 of the 128-row grid over all rows.  Results are bit-identical to
+ * mxq_grouped_gemm_fmt on the same payloads.  Arguments and errors as for
+ * mxq_grouped_gemm_fmt, plus a_bands_cap >= ceil(M_total/128) + G
+ * (MXQ_ERR_INVALID_ARG otherwise).
+ */
+mxq_status mxq_grouped_gemm_group_tiled(const void* a_q, const void* a_s, mxq_fp8_format a_fmt,
+                                        const void* b_q, const void* b_s, mxq_fp8_format b_fmt,
+                                        const int64_t* group_offsets, int32_t G, int64_t M_total, int64_t N,
+                                        int64_t K, int64_t a_bands_cap, void* y, int64_t ldy,
+                                        mxq_stream_t stream);
+
+/*
  * Grouped weight-gradient GEMM for MoE experts: for every expert g
  *
  *   y[g][m, n] = sum over the slot positions p of expert g of deq(A)[m, p] * deq(B)[n, p]

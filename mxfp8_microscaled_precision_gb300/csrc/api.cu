@@ -107,6 +107,34 @@ cudaError_t zero_fill(void* y, int64_t ldy, int64_t M, int64_t N, mxq_stream_t s
                              static_cast<size_t>(M), reinterpret_cast<cudaStream_t>(stream));
 }
 
+// Argument checks and launch of the grouped-rows GEMMs (a_bands_cap 0: A scales
+// MMA-tiled over all rows; > 0: group-tiled).
+mxq_status grouped_rows_gemm(const void* a_q, const void* a_s, mxq_fp8_format a_fmt, const void* b_q,
+                             const void* b_s, mxq_fp8_format b_fmt, const int64_t* group_offsets, int32_t G,
+                             int64_t M_total, int64_t N, int64_t K, int64_t a_bands_cap, void* y, int64_t ldy,
+                             mxq_stream_t stream) {
+    if ((a_fmt != MXQ_FP8_E4M3 && a_fmt != MXQ_FP8_E5M2) || (b_fmt != MXQ_FP8_E4M3 && b_fmt != MXQ_FP8_E5M2))
+        return MXQ_ERR_INVALID_ARG;
+    if (G < 1 || M_total < 0 || N < 0 || K < 0) return MXQ_ERR_INVALID_ARG;
+    if (G > 1024) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (N % 128 != 0 || K % 32 != 0 || K == 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (M_total > (int64_t(1) << 31) - 128 || static_cast<int64_t>(G) * N > (int64_t(1) << 31) - 256 ||
+        K > (int64_t(1) << 31) - 128)
+        return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (M_total == 0 || N == 0) return MXQ_OK;
+    if (!a_q || !a_s || !b_q || !b_s || !group_offsets || !y) return MXQ_ERR_INVALID_ARG;
+    if (ldy < N || ldy % 8 != 0) return MXQ_ERR_INVALID_ARG;
+    if (!aligned16(a_q) || !aligned16(a_s) || !aligned16(b_q) || !aligned16(b_s) || !aligned16(y) ||
+        (reinterpret_cast<uintptr_t>(group_offsets) & 7u) != 0)
+        return MXQ_ERR_INVALID_ARG;
+    mxq::DeviceInfo dev;
+    mxq_status st = device_ok(&dev);
+    if (st != MXQ_OK) return st;
+    return from_cuda(mxq::launch_grouped_gemm(dev, a_q, a_s, b_q, b_s, group_offsets, G, M_total, N, K, a_bands_cap,
+                                              y, ldy, static_cast<int>(a_fmt), static_cast<int>(b_fmt),
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -334,27 +362,36 @@ mxq_status mxq_grouped_gemm(const void* a_q, const void* a_s, const void* b_q, c
 mxq_status mxq_grouped_gemm_fmt(const void* a_q, const void* a_s, mxq_fp8_format a_fmt, const void* b_q,
                                 const void* b_s, mxq_fp8_format b_fmt, const int64_t* group_offsets, int32_t G,
                                 int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy, mxq_stream_t stream) {
-    if ((a_fmt != MXQ_FP8_E4M3 && a_fmt != MXQ_FP8_E5M2) || (b_fmt != MXQ_FP8_E4M3 && b_fmt != MXQ_FP8_E5M2))
-        return MXQ_ERR_INVALID_ARG;
-    if (G < 1 || M_total < 0 || N < 0 || K < 0) return MXQ_ERR_INVALID_ARG;
+    return grouped_rows_gemm(a_q, a_s, a_fmt, b_q, b_s, b_fmt, group_offsets, G, M_total, N, K, 0, y, ldy, stream);
+}
+
+mxq_status mxq_grouped_gemm_group_tiled(const void* a_q, const void* a_s, mxq_fp8_format a_fmt, const void* b_q,
+                                        const void* b_s, mxq_fp8_format b_fmt, const int64_t* group_offsets,
+                                        int32_t G, int64_t M_total, int64_t N, int64_t K, int64_t a_bands_cap,
+                                        void* y, int64_t ldy, mxq_stream_t stream) {
+    if (G >= 1 && M_total >= 0 && a_bands_cap < (M_total + 127) / 128 + G) return MXQ_ERR_INVALID_ARG;
+    return grouped_rows_gemm(a_q, a_s, a_fmt, b_q, b_s, b_fmt, group_offsets, G, M_total, N, K, a_bands_cap, y,
+                             ldy, stream);
+}
+
+mxq_status mxq_scale_regroup_rows(const void* s_tiled, int64_t rows, int64_t cols, const int64_t* group_offsets,
+                                  int32_t G, int64_t bands_cap, void* s_out, mxq_stream_t stream) {
+    if (G < 1 || rows < 0 || cols < 0) return MXQ_ERR_INVALID_ARG;
     if (G > 1024) return MXQ_ERR_UNSUPPORTED_SHAPE;
-    if (N % 128 != 0 || K % 32 != 0 || K == 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
-    if (M_total > (int64_t(1) << 31) - 128 || static_cast<int64_t>(G) * N > (int64_t(1) << 31) - 256 ||
-        K > (int64_t(1) << 31) - 128)
+    if (cols % 32 != 0 || rows > (int64_t(1) << 31) - 128 || cols > (int64_t(1) << 31) - 128)
         return MXQ_ERR_UNSUPPORTED_SHAPE;
-    if (M_total == 0 || N == 0) return MXQ_OK;
-    if (!a_q || !a_s || !b_q || !b_s || !group_offsets || !y) return MXQ_ERR_INVALID_ARG;
-    if (ldy < N || ldy % 8 != 0) return MXQ_ERR_INVALID_ARG;
-    if (!aligned16(a_q) || !aligned16(a_s) || !aligned16(b_q) || !aligned16(b_s) || !aligned16(y) ||
-        (reinterpret_cast<uintptr_t>(group_offsets) & 7u) != 0)
+    if (bands_cap < (rows + 127) / 128 + G) return MXQ_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return MXQ_OK;
+    if (!s_tiled || !s_out || !group_offsets) return MXQ_ERR_INVALID_ARG;
+    if (!aligned16(s_tiled) || !aligned16(s_out) || (reinterpret_cast<uintptr_t>(group_offsets) & 7u) != 0)
         return MXQ_ERR_INVALID_ARG;
     mxq::DeviceInfo dev;
     mxq_status st = device_ok(&dev);
     if (st != MXQ_OK) return st;
-    return from_cuda(mxq::launch_grouped_gemm(dev, a_q, a_s, b_q, b_s, group_offsets, G, M_total, N, K,
-                                              y, ldy, static_cast<int>(a_fmt), static_cast<int>(b_fmt),
-                                              reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(mxq::launch_scale_regroup_rows(dev, s_tiled, rows, cols, group_offsets, G, bands_cap, s_out,
+                                                    reinterpret_cast<cudaStream_t>(stream)));
 }
+
 
 mxq_status mxq_grouped_gemm_wgrad(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
                                   const int64_t* group_offsets, int32_t G, int64_t M_total,

@@ -71,6 +71,8 @@ struct GemmArgs {
     int64_t M_total;         // grouped contraction: rows of the token-sorted inputs
     const int64_t* offsets;  // grouped: [G+1] on the device
     int G;
+    int64_t a_bands_cap;     // grouped rows: 0 = A scales MMA-tiled over all rows; > 0 = group-tiled
+                             // (each group's rows tiled on their own, at most this many bands)
     uint8_t* yq;             // quantizing epilogue: E4M3 payload [M, N] (row stride N)
     uint8_t* ys;             //   and its MMA-tiled scales [M, N/32]
     unsigned int* status;
@@ -132,7 +134,8 @@ struct Cfg {
 // expert has the full m x n tile grid (rastered as dense); its K range is the
 // expert's 128-aligned token slot.
 struct TileInfo {
-    int64_t m0;      // first row of the A tile (multiple of 128)
+    int64_t m0;      // first row of the A tile (multiple of 128, or a group's first row + 128 i)
+    int64_t a_band;  // 128-row band of the A scale atoms of the tile
     int64_t n0;      // first output column
     int64_t row_lo;  // rows [row_lo, row_hi) of this tile are stored
     int64_t row_hi;
@@ -147,7 +150,8 @@ struct Schedule {
     int64_t m_tiles, n_tiles, total;   // grouped modes (dense: per problem)
     // grouped modes only (shared memory)
     const int* prefix;    // [G+1] grouped rows: tile prefix; grouped K: slot start / 128
-    const int* first_mt;  // [G]   grouped rows: first m-tile; grouped K: slot length / 128
+    const int* first_mt;  // [G]   grouped rows: first m-tile (group-tiled A scales: first band);
+                          //       grouped K: slot length / 128
     int G;
 };
 
@@ -191,6 +195,7 @@ __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs&
         const int64_t bh = min(static_cast<int64_t>(kRasterBand), m_tiles - mb);
         const int64_t m_blk = mb + within % bh, n_blk = within / bh;
         ti.m0 = m_blk * kBM;
+        ti.a_band = m_blk;
         ti.n0 = n_blk * BN;
         ti.row_lo = ti.m0;
         ti.row_hi = min(ti.m0 + kBM, P.M);
@@ -210,11 +215,19 @@ __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs&
         const Problem& P = p.pr[0];
         ti.nkb = P.num_kb;
         const int64_t local = t - s.prefix[g];
-        const int64_t m_blk = s.first_mt[g] + local / s.n_tiles;
         const int64_t n_blk = local % s.n_tiles;
-        ti.m0 = m_blk * kBM;
+        const int64_t first_row = clamped_offset(p, g, P.M);
+        if (p.a_bands_cap > 0) {   // tiles from the group's first row
+            ti.m0 = first_row + (local / s.n_tiles) * kBM;
+            ti.a_band = s.first_mt[g] + local / s.n_tiles;
+            ti.row_lo = ti.m0;
+        } else {                   // tiles on the 128-row grid of all rows
+            const int64_t m_blk = s.first_mt[g] + local / s.n_tiles;
+            ti.m0 = m_blk * kBM;
+            ti.a_band = m_blk;
+            ti.row_lo = max(ti.m0, first_row);
+        }
         ti.n0 = n_blk * BN;
-        ti.row_lo = max(ti.m0, clamped_offset(p, g, P.M));
         ti.row_hi = min(ti.m0 + kBM, clamped_offset(p, g + 1, P.M));
         ti.b_row = static_cast<int64_t>(g) * P.N + ti.n0;
     }
@@ -421,20 +434,41 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
         int* s_first = s_prefix + (kMaxGroups + 1);
         const int64_t row_limit = kMode == kGroupedRows ? p.pr[0].M : p.M_total;
         if (warp == 0) {  // tile counts and their exclusive prefix, 32 groups at a time
-            int carry = 0;
+            int carry = 0, band_carry = 0;
             for (int base = 0; base < p.G; base += 32) {
                 const int g = base + lane;
-                int cnt = 0;
+                int cnt = 0, bands = 0;
                 if (g < p.G) {
                     const int64_t lo = clamped_offset(p, g, row_limit), hi = clamped_offset(p, g + 1, row_limit);
                     if constexpr (kMode == kGroupedRows) {
-                        const int64_t fm = lo / kBM;
-                        s_first[g] = static_cast<int>(fm);
-                        cnt = hi > lo ? static_cast<int>((hi - 1) / kBM - fm + 1) * static_cast<int>(sch.n_tiles) : 0;
+                        if (p.a_bands_cap == 0) {
+                            const int64_t fm = lo / kBM;
+                            s_first[g] = static_cast<int>(fm);
+                            cnt = hi > lo ? static_cast<int>((hi - 1) / kBM - fm + 1) * static_cast<int>(sch.n_tiles) : 0;
+                        } else {
+                            bands = hi > lo ? static_cast<int>((hi - lo + kBM - 1) / kBM) : 0;
+                        }
                     } else {  // slot length in 128-token blocks
                         cnt = hi > lo ? static_cast<int>((hi - lo + kBK - 1) / kBK) : 0;
                         s_first[g] = cnt;
                     }
+                }
+                if (kMode == kGroupedRows && p.a_bands_cap > 0) {
+                    // Group-tiled A scales: group g's bands start at band B_g (the
+                    // prefix of the band counts); bands at or past the cap are dropped.
+                    int bincl = bands;
+#pragma unroll
+                    for (int d = 1; d < 32; d <<= 1) {
+                        const int y = __shfl_up_sync(0xFFFFFFFFu, bincl, d);
+                        if (lane >= d) bincl += y;
+                    }
+                    const int64_t first_band = band_carry + bincl - bands;
+                    if (g < p.G) {
+                        s_first[g] = static_cast<int>(first_band);
+                        const int64_t kept = min(static_cast<int64_t>(bands), max(int64_t(0), p.a_bands_cap - first_band));
+                        cnt = static_cast<int>(kept) * static_cast<int>(sch.n_tiles);
+                    }
+                    band_carry += __shfl_sync(0xFFFFFFFFu, bincl, 31);
                 }
                 int incl = cnt;
 #pragma unroll
@@ -491,7 +525,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
                 for (int j = 0; j < L::kSfbAtoms; ++j)
                     if (b_band0 + j < P.b_bands) ++sfb_atoms;
                 const uint32_t bytes = L::kABytes + L::kBBytes + 512u + 512u * sfb_atoms;
-                const uint8_t* sfa_src = P.a_s + ((ti.m0 / 128) * P.k_atoms + ti.kb0) * 512;
+                const uint8_t* sfa_src = P.a_s + (ti.a_band * P.k_atoms + ti.kb0) * 512;
                 const uint8_t* sfb_src = P.b_s + (b_band0 * P.k_atoms + ti.kb0) * 512;
                 const int64_t sfb_band_stride = P.k_atoms * 512;
                 const int32_t ma = static_cast<int32_t>(ti.m0);
@@ -787,8 +821,8 @@ cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void
 
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
                                 const void* b_q, const void* b_s, const int64_t* offsets, int G,
-                                int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy, int a_fmt,
-                                int b_fmt, cudaStream_t stream) {
+                                int64_t M_total, int64_t N, int64_t K, int64_t a_bands_cap, void* y,
+                                int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream) {
     TensorMaps maps;
     if (!make_tma_u8(&maps.a[0], a_q, static_cast<uint64_t>(M_total), static_cast<uint64_t>(K), kBM))
         return cudaErrorInvalidValue;
@@ -800,6 +834,7 @@ cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const vo
                               fmt_bits_of(a_fmt, b_fmt));
     args.offsets = offsets;
     args.G = G;
+    args.a_bands_cap = a_bands_cap;
     return launch_t<kBN, kStages, false, kGroupedRows>(dev, maps, args, -1, stream);
 }
 

@@ -88,10 +88,18 @@ cudaError_t launch_fsdp_unpack(const DeviceInfo& dev, int recipe, int64_t n, int
                                const void* gathered, void* q_fwd, void* s_fwd, void* q_bwd, void* s_bwd,
                                cudaStream_t stream);
 
+// a_bands_cap: 0 = A scales MMA-tiled over all rows; > 0 = group-tiled (see
+// mxq_scale_regroup_rows) in a buffer of a_bands_cap bands.
 cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
                                 const void* b_q, const void* b_s, const int64_t* offsets, int G,
-                                int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy, int a_fmt,
-                                int b_fmt, cudaStream_t stream);
+                                int64_t M_total, int64_t N, int64_t K, int64_t a_bands_cap, void* y,
+                                int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream);
+
+// Group-tiled copy of the MMA-tiled scales of a row quantization (see
+// mxq_scale_regroup_rows).
+cudaError_t launch_scale_regroup_rows(const DeviceInfo& dev, const void* s_tiled, int64_t rows, int64_t cols,
+                                      const int64_t* offsets, int G, int64_t bands_cap, void* s_out,
+                                      cudaStream_t stream);
 
 // Grouped contraction (MoE weight gradient): y[g] = A_g B_g^T where the K range
 // of expert g is its 128-aligned token slot; A [M, capacity], B [N, capacity].

@@ -693,6 +693,105 @@ cudaError_t launch_quant_cols_grouped(const DeviceInfo& dev, const void* x, int6
     return run(quant_cols_grouped_ring_kernel<false, 0>, &configured, &per_sm);
 }
 
+// ---- group-tiled scales (A operand of the grouped GEMM) ------------------------------
+
+constexpr int kRegroupThreads = 256;
+
+// Group-tiled copy of the MMA-tiled scales of a row quantization: the rows
+// [off[g], off[g+1]) of group g form ceil(n_g / 128) bands of their own, from
+// band B_g (the prefix of the band counts); bands at or past bands_cap are
+// dropped.  One warp per output atom.  Lane l's 16 bytes of an atom are the
+// scales of rows l, 32 + l, 64 + l, 96 + l of its band (word j: row 32 j + l).
+// Output row 32 j + l of band i of group g is row v = s + 32 j + l of the
+// two-band source window that starts at band (off[g] + 128 i) / 128, where
+// s = (off[g] + 128 i) % 128: source band v / 128, lane (s + l) % 32 -- the same
+// for every j -- and word (v / 32) % 4.  So each lane loads its 16 bytes of the
+// two source atoms, takes lane (s + l) % 32's eight words by shuffles and stores
+// 16 bytes: coalesced on both sides.  Rows past the group's last are zero.
+__global__ void __launch_bounds__(kRegroupThreads)
+    scale_regroup_rows_kernel(const uint4* __restrict__ src, int64_t rows, int64_t k_atoms,
+                              const int64_t* __restrict__ offsets, int G, int64_t bands_cap,
+                              uint4* __restrict__ dst) {
+    __shared__ int64_t s_off[1025];   // offsets clamped to [0, rows]
+    __shared__ int s_band[1025];      // exclusive prefix of the groups' band counts
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i <= G; i += kRegroupThreads) {
+        const int64_t o = offsets[i];
+        s_off[i] = o < 0 ? 0 : (o > rows ? rows : o);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < G; base += 32) {
+            const int g = base + lane;
+            int bands = 0;
+            if (g < G && s_off[g + 1] > s_off[g]) bands = static_cast<int>((s_off[g + 1] - s_off[g] + 127) >> 7);
+            int incl = bands;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= d) incl += y;
+            }
+            if (g < G) s_band[g] = carry + incl - bands;
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) s_band[G] = carry;
+    }
+    __syncthreads();
+    const int64_t bands = min(static_cast<int64_t>(s_band[G]), bands_cap);
+    const int64_t atoms = bands * k_atoms;
+    constexpr int kWarps = kRegroupThreads / 32;
+    for (int64_t a = static_cast<int64_t>(blockIdx.x) * kWarps + warp; a < atoms;
+         a += static_cast<int64_t>(gridDim.x) * kWarps) {
+        const int64_t b = a / k_atoms, ka = a - b * k_atoms;
+        int g = 0, hi_g = G;  // the last group whose first band is <= b (never an empty one)
+        while (hi_g - g > 1) {
+            const int mid = (g + hi_g) >> 1;
+            if (s_band[mid] <= b) g = mid; else hi_g = mid;
+        }
+        const int64_t r0 = s_off[g] + (b - s_band[g]) * 128, end = s_off[g + 1];
+        const int64_t b0 = r0 >> 7;
+        const int sh = static_cast<int>(r0 & 127);
+        const bool two = sh != 0 && (b0 + 1) * 128 < rows;
+        const uint4 x0 = src[(b0 * k_atoms + ka) * 32 + lane];
+        const uint4 x1 = two ? src[((b0 + 1) * k_atoms + ka) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+        const int u = sh + lane, from = u & 31;
+        uint32_t w0[4], w1[4];
+        w0[0] = __shfl_sync(0xFFFFFFFFu, x0.x, from);
+        w0[1] = __shfl_sync(0xFFFFFFFFu, x0.y, from);
+        w0[2] = __shfl_sync(0xFFFFFFFFu, x0.z, from);
+        w0[3] = __shfl_sync(0xFFFFFFFFu, x0.w, from);
+        w1[0] = __shfl_sync(0xFFFFFFFFu, x1.x, from);
+        w1[1] = __shfl_sync(0xFFFFFFFFu, x1.y, from);
+        w1[2] = __shfl_sync(0xFFFFFFFFu, x1.z, from);
+        w1[3] = __shfl_sync(0xFFFFFFFFu, x1.w, from);
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int v = u + 32 * j;          // row in the two-band window
+            const int k = (v >> 5) & 3;        // its word in the source lane's 16 bytes
+            const uint32_t* w = (v >> 7) ? w1 : w0;
+            const uint32_t val = k == 0 ? w[0] : k == 1 ? w[1] : k == 2 ? w[2] : w[3];
+            o[j] = r0 + 32 * j + lane < end ? val : 0u;
+        }
+        dst[a * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+cudaError_t launch_scale_regroup_rows(const DeviceInfo& dev, const void* s_tiled, int64_t rows, int64_t cols,
+                                      const int64_t* offsets, int G, int64_t bands_cap, void* s_out,
+                                      cudaStream_t stream) {
+    const int64_t k_atoms = (cols / 32 + 3) / 4;
+    const int64_t per_block = kRegroupThreads / 32;
+    int64_t grid = (bands_cap * k_atoms + per_block - 1) / per_block;
+    const int64_t most = static_cast<int64_t>(dev.sm_count) * 8;
+    if (grid > most) grid = most;
+    if (grid <= 0) return cudaSuccess;
+    scale_regroup_rows_kernel<<<static_cast<unsigned>(grid), kRegroupThreads, 0, stream>>>(
+        static_cast<const uint4*>(s_tiled), rows, k_atoms, offsets, G, bands_cap, static_cast<uint4*>(s_out));
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, int64_t k, int64_t ld,
                                void* q, void* s_fwd, void* s_bwd, bool tiled, cudaStream_t stream) {
     (void)dev;

@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
         L.mxq_quant_1x32_cols_grouped.argtypes = [P, I64, I64, I64, P, I32, I64, P, P, S, P]
         L.mxq_quant_1x32_cols_grouped_fmt.argtypes = [P, I64, I64, I64, P, I32, I64, P, P, S, S, P]
         L.mxq_grouped_gemm_fmt.argtypes = [P, P, S, P, P, S, P, I32, I64, I64, I64, P, I64, P]
+        L.mxq_grouped_gemm_group_tiled.argtypes = [P, P, S, P, P, S, P, I32, I64, I64, I64, I64, P, I64, P]
+        L.mxq_scale_regroup_rows.argtypes = [P, I64, I64, P, I32, I64, P, P]
         L.mxq_grouped_gemm_wgrad_fmt.argtypes = [P, P, S, P, P, S, P, I32, I64, I64, I64, I64, P, I64, P]
         L.mxq_grouped_gemm_wgrad.argtypes = [P, P, P, P, P, I32, I64, I64, I64, I64, P, I64, P]
         L.mxq_quant_32x32.argtypes = [P, I64, I64, I64, P, P, P, S, P]
@@ -87,7 +89,8 @@ def lib() -> ctypes.CDLL:
                   "mxq_quant_1x32_dual_batched", "mxq_quant_1x32_cols_grouped",
                   "mxq_grouped_gemm_wgrad", "mxq_gemm_bf16out_fmt", "mxq_gemm_mxfp8out",
                   "mxq_fsdp_payload_layout", "mxq_fsdp_unpack", "mxq_quant_1x32_cols_grouped_fmt",
-                  "mxq_grouped_gemm_fmt", "mxq_grouped_gemm_wgrad_fmt", "mxq_gemm_bf16out_multi"):
+                  "mxq_grouped_gemm_fmt", "mxq_grouped_gemm_wgrad_fmt", "mxq_gemm_bf16out_multi",
+                  "mxq_grouped_gemm_group_tiled", "mxq_scale_regroup_rows"):
             getattr(L, f).restype = S
         _lib = L
         return L
@@ -387,6 +390,45 @@ def grouped_gemm(a_q, a_s, b_q, b_s, offsets: torch.Tensor, N: int, K: int, out=
     _check(lib().mxq_grouped_gemm_fmt(_ptr(a_q), _ptr(a_s), _fmt(a_fmt), _ptr(b_q), _ptr(b_s), _fmt(b_fmt),
                                       _ptr(offsets), G, M_total, N, K, _ptr(out), out.stride(0), _stream()),
            "mxq_grouped_gemm_fmt")
+    return out
+
+
+def group_tiled_bands(rows: int, G: int) -> int:
+    """Bands a group-tiled scale buffer needs for any offsets: ceil(rows/128) + G."""
+    return (rows + 127) // 128 + G
+
+
+def scale_regroup_rows(s_tiled: torch.Tensor, rows: int, cols: int, offsets: torch.Tensor, bands_cap=None,
+                       out=None) -> torch.Tensor:
+    """Group-tiled copy (see mxq_scale_regroup_rows) of the MMA-tiled scales of a
+    row quantization [rows, cols]; returns uint8 [bands_cap * ceil(cols/128) * 512]."""
+    if offsets.dtype != torch.int64 or not offsets.is_cuda:
+        raise ValueError("offsets must be an int64 CUDA tensor")
+    G = offsets.numel() - 1
+    if bands_cap is None:
+        bands_cap = group_tiled_bands(rows, G)
+    if out is None:
+        out = torch.empty(bands_cap * ((cols // 32 + 3) // 4) * 512, dtype=torch.uint8, device=s_tiled.device)
+    _check(lib().mxq_scale_regroup_rows(_ptr(s_tiled), rows, cols, _ptr(offsets), G, bands_cap, _ptr(out),
+                                        _stream()), "mxq_scale_regroup_rows")
+    return out
+
+
+def grouped_gemm_group_tiled(a_q, a_s_grouped, b_q, b_s, offsets: torch.Tensor, N: int, K: int, bands_cap=None,
+                             out=None, a_fmt="e4m3", b_fmt="e4m3"):
+    """grouped_gemm with A's scales group-tiled by scale_regroup_rows (same offsets
+    and bands_cap); bit-identical results, no row tile spanning two experts."""
+    if offsets.dtype != torch.int64 or not offsets.is_cuda:
+        raise ValueError("offsets must be an int64 CUDA tensor")
+    G = offsets.numel() - 1
+    M_total = a_q.shape[0]
+    if bands_cap is None:
+        bands_cap = group_tiled_bands(M_total, G)
+    if out is None:
+        out = torch.empty((M_total, N), dtype=torch.bfloat16, device=a_q.device)
+    _check(lib().mxq_grouped_gemm_group_tiled(_ptr(a_q), _ptr(a_s_grouped), _fmt(a_fmt), _ptr(b_q), _ptr(b_s),
+                                              _fmt(b_fmt), _ptr(offsets), G, M_total, N, K, bands_cap, _ptr(out),
+                                              out.stride(0), _stream()), "mxq_grouped_gemm_group_tiled")
     return out
 
 

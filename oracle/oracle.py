@@ -264,6 +264,19 @@ def scale_tiled(s: np.ndarray) -> np.ndarray:
     return out
 
 
+def scale_group_tiled(s: np.ndarray, offsets) -> np.ndarray:
+    """Group-tiled layout of plain [rows, groups] scales: the rows
+    [offsets[g], offsets[g+1]) of each group laid out on their own by
+    scale_tiled (rows padded to 128 with zeros), the groups' layouts one after
+    the other in group order (empty groups contribute nothing).  Returns the
+    written bytes: sum over groups of ceil(n_g/128) * ceil(groups/4) * 512.
+    Not a layout of the pages: it lets a grouped GEMM's row tiles start at
+    every group's first row."""
+    s = _c(s, np.uint8)
+    parts = [scale_tiled(s[int(lo):int(hi)]) for lo, hi in zip(offsets[:-1], offsets[1:]) if hi > lo]
+    return np.concatenate(parts) if parts else np.zeros(0, np.uint8)
+
+
 def dequant_rows(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     """q[r,c] * 2^(s[r,c/32]-127) as float64 [R, C].  With s = s_fwd this is
     also the dequantized 32x32 payload (s_fwd repeats the tile exponent)."""

@@ -122,6 +122,23 @@ def test_moe_backward_argument_errors(L):
     assert wf(FAKE, FAKE, 1, FAKE, FAKE, 0, FAKE, 4, 300, 1024, 128, 120, FAKE, 120, None) == 2  # N % 16
 
 
+def test_group_tiled_argument_errors(L):
+    r = L.mxq_scale_regroup_rows
+    assert r(FAKE, 300, 256, FAKE, 4, 6, FAKE, None) == 1        # bands_cap < ceil(300/128) + 4
+    assert r(FAKE, 300, 256, FAKE, 0, 7, FAKE, None) == 1        # G < 1
+    assert r(FAKE, 300, 256, FAKE, 2000, 2003, FAKE, None) == 2  # G too big
+    assert r(FAKE, 300, 48, FAKE, 4, 7 + 1, FAKE, None) == 2     # cols % 32
+    assert r(FAKE, 300, 256, None, 4, 8, FAKE, None) == 1        # no offsets
+    assert r(FAKE, 300, 256, FAKE, 4, 8, ODD, None) == 1         # misaligned output
+    assert r(FAKE, 0, 256, FAKE, 4, 4, FAKE, None) == 0          # no rows
+    t = L.mxq_grouped_gemm_group_tiled
+    assert t(FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 4, 300, 128, 64, 6, FAKE, 128, None) == 1   # cap too small
+    assert t(FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 4, 300, 192, 64, 7, FAKE, 192, None) == 2   # N % 128
+    assert t(FAKE, FAKE, 7, FAKE, FAKE, 0, FAKE, 4, 300, 128, 64, 7, FAKE, 128, None) == 1   # bad format
+    assert t(FAKE, FAKE, 0, FAKE, FAKE, 0, None, 4, 300, 128, 64, 7, FAKE, 128, None) == 1   # no offsets
+    assert t(FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 4, 0, 128, 64, 4, FAKE, 128, None) == 0     # no rows
+
+
 def test_gemm_multi_argument_errors(L):
     from mxfp8_microscaled_precision_gb300 import mxq
     D = (mxq.GemmDesc * 2)()
