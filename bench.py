@@ -180,6 +180,24 @@ def _dual_bytes(r, c):
     return r * c * (2 + 1 + 1) + 2 * (r * c // 32)
 
 
+def _group_tiled_setup(w, offsets_cpu, ks, dev):
+    """Group-tiled A-scale buffers of the routed rows for the grouped GEMMs (one
+    per contraction length in ks), their band capacity and the bands the
+    routing fills (each expert's rows ceil(n_g / 128) bands)."""
+    import torch
+    from mxfp8_microscaled_precision_gb300 import mxq
+    off = [int(v) for v in offsets_cpu]
+    w.gt_cap = mxq.group_tiled_bands(w.Mt, w.G)
+    w.gt_bands = sum((hi - lo + 127) // 128 for lo, hi in zip(off[:-1], off[1:]) if hi > lo)
+    return [torch.empty(w.gt_cap * (k // 128) * 512, dtype=torch.uint8, device=dev) for k in ks]
+
+
+def _regroup_bytes(w, k):
+    """Algorithmic bytes of one regroup: the tiled scales of all routed rows
+    read once, the filled group-tiled bands written."""
+    return ((w.Mt + 127) // 128 + w.gt_bands) * (k // 128) * 512
+
+
 def _row_bytes(r, c):
     return r * c * (2 + 1) + r * c // 32
 
@@ -577,6 +595,7 @@ class MoE(Workload):
             return (torch.empty((r, c), **u8), torch.empty(mxq.scale_bytes(r, c), **u8), None, None)
         self.qa, self.qh = row_out(self.Mt, H), row_out(self.Mt, I)
         self.qgu, self.qdn = row_out(G * 2 * I, H), row_out(G * H, I)
+        self.sa_g, self.sh_g = _group_tiled_setup(self, d["routing"].offsets, (H, I), dev)
         bf = dict(dtype=torch.bfloat16, device=dev)
         self.y1, self.y2 = torch.empty((self.Mt, 2 * I), **bf), torch.empty((self.Mt, H), **bf)
         self.outputs = [self.y1, self.y2]
@@ -591,14 +610,20 @@ class MoE(Workload):
         return [
             ("quant_A_row", "quant", _row_bytes(Mt, H), lambda: mxq.quant_1x32_dual(i["A"], col=False, out=self.qa)),
             ("quant_H_row", "quant", _row_bytes(Mt, I), lambda: mxq.quant_1x32_dual(i["Hd"], col=False, out=self.qh)),
+            ("regroup_A_scales", "layout", _regroup_bytes(self, H),
+             lambda: mxq.scale_regroup_rows(self.qa[1], Mt, H, self.offsets, self.gt_cap, out=self.sa_g)),
+            ("regroup_H_scales", "layout", _regroup_bytes(self, I),
+             lambda: mxq.scale_regroup_rows(self.qh[1], Mt, I, self.offsets, self.gt_cap, out=self.sh_g)),
             ("quant_Wgu_row", "quant", _row_bytes(G * 2 * I, H),
              lambda: mxq.quant_1x32_dual(i["W_gate_up"], col=False, out=self.qgu)),
             ("quant_Wdn_row", "quant", _row_bytes(G * H, I),
              lambda: mxq.quant_1x32_dual(i["W_down"], col=False, out=self.qdn)),
             ("grouped_gate_up", "gemm", 2 * Mt * 2 * I * H,
-             lambda: mxq.grouped_gemm(self.qa[0], self.qa[1], self.qgu[0], self.qgu[1], self.offsets, 2 * I, H, out=self.y1)),
+             lambda: mxq.grouped_gemm_group_tiled(self.qa[0], self.sa_g, self.qgu[0], self.qgu[1], self.offsets,
+                                                  2 * I, H, self.gt_cap, out=self.y1)),
             ("grouped_down", "gemm", 2 * Mt * H * I,
-             lambda: mxq.grouped_gemm(self.qh[0], self.qh[1], self.qdn[0], self.qdn[1], self.offsets, H, I, out=self.y2)),
+             lambda: mxq.grouped_gemm_group_tiled(self.qh[0], self.sh_g, self.qdn[0], self.qdn[1], self.offsets,
+                                                  H, I, self.gt_cap, out=self.y2)),
         ]
 
     def expert0_gate_up(self):
@@ -677,6 +702,8 @@ class MoETrain(Workload):
         self.wdn = (torch.empty((G, H, I), **u8), torch.empty((G, sb(H, I)), **u8),
                     torch.empty((G, I, H), **u8), torch.empty((G, sb(I, H)), **u8))
         self.c_g1, self.c_a, self.c_g2, self.c_h = cols_g(2 * I), cols_g(H), cols_g(H), cols_g(I)
+        self.sa_g, self.sh_g, self.sg1_g, self.sg2_g = _group_tiled_setup(self, d["routing"].offsets,
+                                                                          (H, I, 2 * I, H), dev)
         self.y1, self.y2 = torch.empty((Mt, 2 * I), **bf), torch.empty((Mt, H), **bf)
         self.da, self.dh = torch.empty((Mt, H), **bf), torch.empty((Mt, I), **bf)
         self.dwgu, self.dwdn = torch.empty((G, 2 * I, H), **bf), torch.empty((G, H, I), **bf)
@@ -713,18 +740,30 @@ class MoETrain(Workload):
         return [
             ("quant_A_row", "quant", _row_bytes(Mt, H), lambda: mxq.quant_1x32_dual(i["A"], col=False, out=self.qa)),
             ("quant_H_row", "quant", _row_bytes(Mt, I), lambda: mxq.quant_1x32_dual(i["Hd"], col=False, out=self.qh)),
+            ("regroup_A_scales", "layout", _regroup_bytes(self, H),
+             lambda: mxq.scale_regroup_rows(self.qa[1], Mt, H, off, self.gt_cap, out=self.sa_g)),
+            ("regroup_H_scales", "layout", _regroup_bytes(self, I),
+             lambda: mxq.scale_regroup_rows(self.qh[1], Mt, I, off, self.gt_cap, out=self.sh_g)),
             ("quant_Wgu_dual", "quant", _dual_bytes(G * 2 * I, H), lambda: self._quant_batched(i["W_gate_up"], wgu)),
             ("quant_Wdn_dual", "quant", _dual_bytes(G * H, I), lambda: self._quant_batched(i["W_down"], wdn)),
             ("grouped_fwd_gate_up", "gemm", f_gu,
-             lambda: mxq.grouped_gemm(self.qa[0], self.qa[1], wgu[0].view(G * 2 * I, H), wgu[1].view(-1), off, 2 * I, H, out=self.y1)),
+             lambda: mxq.grouped_gemm_group_tiled(self.qa[0], self.sa_g, wgu[0].view(G * 2 * I, H), wgu[1].view(-1),
+                                                  off, 2 * I, H, self.gt_cap, out=self.y1)),
             ("grouped_fwd_down", "gemm", f_dn,
-             lambda: mxq.grouped_gemm(self.qh[0], self.qh[1], wdn[0].view(G * H, I), wdn[1].view(-1), off, H, I, out=self.y2)),
+             lambda: mxq.grouped_gemm_group_tiled(self.qh[0], self.sh_g, wdn[0].view(G * H, I), wdn[1].view(-1),
+                                                  off, H, I, self.gt_cap, out=self.y2)),
             ("quant_dY1_row", "quant", _row_bytes(Mt, 2 * I), lambda: mxq.quant_1x32_dual(i["dY1"], col=False, out=self.qg1)),
             ("quant_dY2_row", "quant", _row_bytes(Mt, H), lambda: mxq.quant_1x32_dual(i["dY2"], col=False, out=self.qg2)),
+            ("regroup_dY1_scales", "layout", _regroup_bytes(self, 2 * I),
+             lambda: mxq.scale_regroup_rows(self.qg1[1], Mt, 2 * I, off, self.gt_cap, out=self.sg1_g)),
+            ("regroup_dY2_scales", "layout", _regroup_bytes(self, H),
+             lambda: mxq.scale_regroup_rows(self.qg2[1], Mt, H, off, self.gt_cap, out=self.sg2_g)),
             ("grouped_dgrad_gate_up", "gemm", f_gu,
-             lambda: mxq.grouped_gemm(self.qg1[0], self.qg1[1], wgu[2].view(G * H, 2 * I), wgu[3].view(-1), off, H, 2 * I, out=self.da)),
+             lambda: mxq.grouped_gemm_group_tiled(self.qg1[0], self.sg1_g, wgu[2].view(G * H, 2 * I), wgu[3].view(-1),
+                                                  off, H, 2 * I, self.gt_cap, out=self.da)),
             ("grouped_dgrad_down", "gemm", f_dn,
-             lambda: mxq.grouped_gemm(self.qg2[0], self.qg2[1], wdn[2].view(G * I, H), wdn[3].view(-1), off, I, H, out=self.dh)),
+             lambda: mxq.grouped_gemm_group_tiled(self.qg2[0], self.sg2_g, wdn[2].view(G * I, H), wdn[3].view(-1),
+                                                  off, I, H, self.gt_cap, out=self.dh)),
             ("quant_dY1_cols", "quant", colsb(2 * I), lambda: self._quant_cols(i["dY1"], self.c_g1)),
             ("quant_A_cols", "quant", colsb(H), lambda: self._quant_cols(i["A"], self.c_a)),
             ("quant_dY2_cols", "quant", colsb(H), lambda: self._quant_cols(i["dY2"], self.c_g2)),

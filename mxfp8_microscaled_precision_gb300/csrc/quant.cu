@@ -696,12 +696,14 @@ cudaError_t launch_quant_cols_grouped(const DeviceInfo& dev, const void* x, int6
 // ---- group-tiled scales (A operand of the grouped GEMM) ------------------------------
 
 constexpr int kRegroupThreads = 256;
+constexpr int kAtomsPerItem = 4;   // atoms of one band per warp work item
 
 // Group-tiled copy of the MMA-tiled scales of a row quantization: the rows
 // [off[g], off[g+1]) of group g form ceil(n_g / 128) bands of their own, from
 // band B_g (the prefix of the band counts); bands at or past bands_cap are
-// dropped.  One warp per output atom.  Lane l's 16 bytes of an atom are the
-// scales of rows l, 32 + l, 64 + l, 96 + l of its band (word j: row 32 j + l).
+// dropped.  A warp handles four atoms of one output band at a time.  Lane l's
+// 16 bytes of an atom are the scales of rows l, 32 + l, 64 + l, 96 + l of its
+// band (word j: row 32 j + l).
 // Output row 32 j + l of band i of group g is row v = s + 32 j + l of the
 // two-band source window that starts at band (off[g] + 128 i) / 128, where
 // s = (off[g] + 128 i) % 128: source band v / 128, lane (s + l) % 32 -- the same
@@ -739,11 +741,14 @@ __global__ void __launch_bounds__(kRegroupThreads)
     }
     __syncthreads();
     const int64_t bands = min(static_cast<int64_t>(s_band[G]), bands_cap);
-    const int64_t atoms = bands * k_atoms;
+    // Work item: kAtomsPerItem consecutive atoms of one output band (one group
+    // lookup, all the item's loads in flight before the first shuffle).
     constexpr int kWarps = kRegroupThreads / 32;
-    for (int64_t a = static_cast<int64_t>(blockIdx.x) * kWarps + warp; a < atoms;
-         a += static_cast<int64_t>(gridDim.x) * kWarps) {
-        const int64_t b = a / k_atoms, ka = a - b * k_atoms;
+    const int64_t kgroups = (k_atoms + kAtomsPerItem - 1) / kAtomsPerItem;
+    const int64_t items = bands * kgroups;
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * kWarps + warp; it < items;
+         it += static_cast<int64_t>(gridDim.x) * kWarps) {
+        const int64_t b = it / kgroups, ka0 = (it - b * kgroups) * kAtomsPerItem;
         int g = 0, hi_g = G;  // the last group whose first band is <= b (never an empty one)
         while (hi_g - g > 1) {
             const int mid = (g + hi_g) >> 1;
@@ -753,28 +758,41 @@ __global__ void __launch_bounds__(kRegroupThreads)
         const int64_t b0 = r0 >> 7;
         const int sh = static_cast<int>(r0 & 127);
         const bool two = sh != 0 && (b0 + 1) * 128 < rows;
-        const uint4 x0 = src[(b0 * k_atoms + ka) * 32 + lane];
-        const uint4 x1 = two ? src[((b0 + 1) * k_atoms + ka) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
         const int u = sh + lane, from = u & 31;
-        uint32_t w0[4], w1[4];
-        w0[0] = __shfl_sync(0xFFFFFFFFu, x0.x, from);
-        w0[1] = __shfl_sync(0xFFFFFFFFu, x0.y, from);
-        w0[2] = __shfl_sync(0xFFFFFFFFu, x0.z, from);
-        w0[3] = __shfl_sync(0xFFFFFFFFu, x0.w, from);
-        w1[0] = __shfl_sync(0xFFFFFFFFu, x1.x, from);
-        w1[1] = __shfl_sync(0xFFFFFFFFu, x1.y, from);
-        w1[2] = __shfl_sync(0xFFFFFFFFu, x1.z, from);
-        w1[3] = __shfl_sync(0xFFFFFFFFu, x1.w, from);
-        uint32_t o[4];
+        uint4 x0[kAtomsPerItem], x1[kAtomsPerItem];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int v = u + 32 * j;          // row in the two-band window
-            const int k = (v >> 5) & 3;        // its word in the source lane's 16 bytes
-            const uint32_t* w = (v >> 7) ? w1 : w0;
-            const uint32_t val = k == 0 ? w[0] : k == 1 ? w[1] : k == 2 ? w[2] : w[3];
-            o[j] = r0 + 32 * j + lane < end ? val : 0u;
+        for (int q = 0; q < kAtomsPerItem; ++q) {
+            const int64_t ka = ka0 + q;
+            x0[q] = x1[q] = make_uint4(0u, 0u, 0u, 0u);
+            if (ka < k_atoms) {
+                x0[q] = src[(b0 * k_atoms + ka) * 32 + lane];
+                if (two) x1[q] = src[((b0 + 1) * k_atoms + ka) * 32 + lane];
+            }
         }
-        dst[a * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+        for (int q = 0; q < kAtomsPerItem; ++q) {
+            const int64_t ka = ka0 + q;
+            if (ka >= k_atoms) break;   // uniform across the warp
+            uint32_t w0[4], w1[4];
+            w0[0] = __shfl_sync(0xFFFFFFFFu, x0[q].x, from);
+            w0[1] = __shfl_sync(0xFFFFFFFFu, x0[q].y, from);
+            w0[2] = __shfl_sync(0xFFFFFFFFu, x0[q].z, from);
+            w0[3] = __shfl_sync(0xFFFFFFFFu, x0[q].w, from);
+            w1[0] = __shfl_sync(0xFFFFFFFFu, x1[q].x, from);
+            w1[1] = __shfl_sync(0xFFFFFFFFu, x1[q].y, from);
+            w1[2] = __shfl_sync(0xFFFFFFFFu, x1[q].z, from);
+            w1[3] = __shfl_sync(0xFFFFFFFFu, x1[q].w, from);
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int v = u + 32 * j;          // row in the two-band window
+                const int k = (v >> 5) & 3;        // its word in the source lane's 16 bytes
+                const uint32_t* w = (v >> 7) ? w1 : w0;
+                const uint32_t val = k == 0 ? w[0] : k == 1 ? w[1] : k == 2 ? w[2] : w[3];
+                o[j] = r0 + 32 * j + lane < end ? val : 0u;
+            }
+            dst[(b * k_atoms + ka) * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
     }
 }
 
@@ -783,8 +801,8 @@ cudaError_t launch_scale_regroup_rows(const DeviceInfo& dev, const void* s_tiled
                                       cudaStream_t stream) {
     const int64_t k_atoms = (cols / 32 + 3) / 4;
     const int64_t per_block = kRegroupThreads / 32;
-    int64_t grid = (bands_cap * k_atoms + per_block - 1) / per_block;
-    const int64_t most = static_cast<int64_t>(dev.sm_count) * 8;
+    int64_t grid = (bands_cap * ((k_atoms + kAtomsPerItem - 1) / kAtomsPerItem) + per_block - 1) / per_block;
+    const int64_t most = static_cast<int64_t>(dev.sm_count) * 3;   // resident blocks (80 registers a thread)
     if (grid > most) grid = most;
     if (grid <= 0) return cudaSuccess;
     scale_regroup_rows_kernel<<<static_cast<unsigned>(grid), kRegroupThreads, 0, stream>>>(
