@@ -62,6 +62,7 @@ struct Problem {
     int64_t first_item;      // dense: the problem's first work item
     int num_kb;              // 128-deep K blocks
     uint32_t fmt_bits;       // operand formats in the instruction descriptor (0 = E4M3, E4M3)
+    int y_tma;               // 1: TensorMaps::y of this problem maps y (32 x 32 tiled stores)
 };
 
 struct GemmArgs {
@@ -83,6 +84,7 @@ struct GemmArgs {
 struct TensorMaps {
     CUtensorMap a[kMaxProblems];
     CUtensorMap b[kMaxProblems];
+    CUtensorMap y[kMaxProblems];   // BF16 outputs, for tiled stores (Problem::y_tma)
 };
 
 // Compile-time configuration of one kernel instance.
@@ -116,7 +118,7 @@ struct Cfg {
     static constexpr int kSchedBytes = kMode == kGroupedRows || kMode == kGroupedK ? 4 * (kMaxGroups + 1) + 4 * kMaxGroups : 0;
     static constexpr bool kStaged = BN == 256 && kMode != kDenseQuant;
     static constexpr int kStageWarpBytes = 32 * 32 * 2;  // 32 rows x 32 BF16 columns
-    static constexpr int kOffStage = (kOffSched + kSchedBytes + 127) / 128 * 128;
+    static constexpr int kOffStage = (kOffSched + kSchedBytes + 1023) / 1024 * 1024;   // 64-byte swizzle atoms
     static constexpr int kBytes = kOffStage + (kStaged ? kEpiWarps * kStageWarpBytes : 0);
     static constexpr int kAlloc = kBytes + 1024;        // slack for 1024-byte alignment
     // TMEM columns: accumulators, then per-stage SFA and SFB slots.
@@ -236,40 +238,63 @@ __device__ __forceinline__ TileInfo tile_info(const Schedule& s, const GemmArgs&
 
 // One epilogue warp's share of a finished tile through its 2 KB shared-memory
 // staging buffer: lane l holds output row row0 + l (y's row numbering) in v,
-// FP32 columns n .. n+127.  Per
-// 32-column chunk each lane writes its row's 64 BF16 bytes to the buffer, then
-// the warp stores 8 rows x 64 contiguous bytes per instruction: 8 cache-line
-// halves instead of the 32 lines a row-per-lane store touches.  Rows outside
-// [row_lo, row_hi) (tile-row numbering) are not stored.  16-byte chunk
-// j of staged row r sits at position j ^ ((r >> 1) & 3), so both the writes
-// (one row per lane) and the reads (four lanes per row) are conflict-free.
+// FP32 columns n .. n+127.  Per 32-column chunk each lane writes its row's 64
+// BF16 bytes to the buffer; 16-byte chunk j of staged row r sits at position
+// j ^ ((r >> 1) & 3), which is the 64-byte swizzle of a tiled bulk copy.  When
+// all 32 rows are stored, lane 0 stores the chunk with one tiled bulk copy
+// (the tensor map clips columns past N and rows past the matrix) and the warp
+// goes on; the buffer is rewritten only after that copy has read it (`pending`
+// carries this across calls, so the wait for a tile's last chunk falls after
+// the next tile's accumulator drain).  Otherwise the warp stores 8 rows x 64
+// contiguous bytes per instruction, skipping rows outside [row_lo, row_hi)
+// (tile-row numbering); writes (one row per lane) and reads (four lanes per
+// row) of the buffer are conflict-free.
 __device__ __forceinline__ void store_staged(const Problem& p, const uint32_t (&v)[4][32], uint32_t stage,
                                              int64_t row0, int64_t tile_row0, int64_t row_lo, int64_t row_hi,
-                                             int64_t n, int lane) {
+                                             int64_t n, int lane, const CUtensorMap* ymap, bool& pending) {
     const uint32_t wrow = stage + 64u * static_cast<uint32_t>(lane);
     const uint32_t wswz = static_cast<uint32_t>((lane >> 1) & 3);
     const int rsub = lane >> 2;   // row within an 8-row group
     const int jj = lane & 3;      // 16-byte chunk within a 64-byte row
+    // All 32 rows stored: one tiled store from the buffer (its layout is the
+    // 64-byte swizzle); otherwise the rows in [row_lo, row_hi) one by one.
+    const bool whole = p.y_tma && tile_row0 >= row_lo && tile_row0 + 32 <= row_hi;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
+        uint4 o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            uint4 o;
-            o.x = cvt_bf16x2(__uint_as_float(v[c][8 * j + 0]), __uint_as_float(v[c][8 * j + 1]));
-            o.y = cvt_bf16x2(__uint_as_float(v[c][8 * j + 2]), __uint_as_float(v[c][8 * j + 3]));
-            o.z = cvt_bf16x2(__uint_as_float(v[c][8 * j + 4]), __uint_as_float(v[c][8 * j + 5]));
-            o.w = cvt_bf16x2(__uint_as_float(v[c][8 * j + 6]), __uint_as_float(v[c][8 * j + 7]));
-            sts128(wrow + 16u * (static_cast<uint32_t>(j) ^ wswz), o);
+            o[j].x = cvt_bf16x2(__uint_as_float(v[c][8 * j + 0]), __uint_as_float(v[c][8 * j + 1]));
+            o[j].y = cvt_bf16x2(__uint_as_float(v[c][8 * j + 2]), __uint_as_float(v[c][8 * j + 3]));
+            o[j].z = cvt_bf16x2(__uint_as_float(v[c][8 * j + 4]), __uint_as_float(v[c][8 * j + 5]));
+            o[j].w = cvt_bf16x2(__uint_as_float(v[c][8 * j + 6]), __uint_as_float(v[c][8 * j + 7]));
+        }
+        if (pending) {   // the previous tiled store still reads the buffer
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            pending = false;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sts128(wrow + 16u * (static_cast<uint32_t>(j) ^ wswz), o[j]);
+        if (whole) {
+            fence_proxy_async_smem();   // the buffer is read by the bulk copy (async proxy)
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(ymap, static_cast<int32_t>(n + 32 * c), static_cast<int32_t>(row0), stage);
+                bulk_commit_group();
+            }
+            pending = true;
+            continue;
         }
         __syncwarp();
         const int64_t col = n + 32 * c + 8 * jj;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = 8 * i + rsub;
-            const uint4 o = lds128_ordered(stage + 64u * static_cast<uint32_t>(r) +
+            const uint4 x = lds128_ordered(stage + 64u * static_cast<uint32_t>(r) +
                                            16u * (static_cast<uint32_t>(jj) ^ static_cast<uint32_t>((r >> 1) & 3)));
             if (tile_row0 + r >= row_lo && tile_row0 + r < row_hi && col + 8 <= p.N)
-                *reinterpret_cast<uint4*>(p.y + (row0 + r) * p.ldy + col) = o;
+                *reinterpret_cast<uint4*>(p.y + (row0 + r) * p.ldy + col) = x;
         }
         __syncwarp();   // the buffer is rewritten by the next chunk
     }
@@ -647,6 +672,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
         const int half = (warp - 2) >> 2;
         int acc = 0;
         uint32_t acc_phase = 0;
+        bool pending = false;   // a tiled store of this warp may still read its buffer
         for (int64_t r = 0; r * gridDim.x < sch.total; ++r) {
             const int64_t t = item_of(r);
             if (t >= sch.total) continue;
@@ -680,11 +706,13 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
             if constexpr (L::kStaged)
                 store_staged(P, v, sbase + L::kOffStage + (warp - 2) * L::kStageWarpBytes,
                              ti.y_row0 + ti.m0 + 32 * quad, ti.m0 + 32 * quad, ti.row_lo, ti.row_hi,
-                             ti.n0 + half * 128, lane);
+                             ti.n0 + half * 128, lane, &maps.y[ti.prob], pending);
             else
                 store_row<kMode>(p, P, v, ti.m0 + 32 * quad + lane, ti.row_lo, ti.row_hi, ti.y_row0,
                                  ti.n0 + half * 128, ti.m0 < P.M);
         }
+        if (lane == 0) bulk_wait_all();   // this warp's tiled stores complete before the CTA ends
+        __syncwarp();
     }
 
     // ---- teardown -----------------------------------------------------------
@@ -762,6 +790,17 @@ GemmArgs base_args(const DeviceInfo& dev) {
     return a;
 }
 
+// Tiled-store map of a BF16 output [rows, N] with row stride ldy; the problem
+// keeps row-by-row stores when there is no output or the rows exceed the 32-bit
+// box coordinates.
+void set_store_map(CUtensorMap* map, Problem* q, const void* y, int64_t rows, int64_t N, int64_t ldy) {
+    q->y_tma = 0;
+    if (y != nullptr && rows > 0 && rows < (int64_t(1) << 31) - 32 &&
+        encode_tensor_map_bf16_store(map, y, static_cast<uint64_t>(N), static_cast<uint64_t>(rows),
+                                     static_cast<uint64_t>(ldy)))
+        q->y_tma = 1;
+}
+
 // Dense problems of one launch, ordered by K descending (stable), their work
 // items laid out back to back.
 bool fill_dense(const DenseGemm* gemms, int count, bool b_mn_major, TensorMaps* maps, GemmArgs* args) {
@@ -777,6 +816,7 @@ bool fill_dense(const DenseGemm* gemms, int count, bool b_mn_major, TensorMaps* 
         if (!make_dense_maps(&maps->a[i], &maps->b[i], g.a_q, g.b_q, g.M, g.N, g.K, b_mn_major)) return false;
         args->pr[i] = make_problem(g.a_s, g.b_s, g.y, g.M, g.N, g.K, g.ldy, (g.K + 127) / 128, (g.N + 127) / 128,
                                    fmt_bits_of(g.a_fmt, g.b_fmt));
+        set_store_map(&maps->y[i], &args->pr[i], g.y, g.M, g.N, g.ldy);
         args->pr[i].first_item = items;
         items += args->pr[i].m_tiles * args->pr[i].n_tiles;
     }
@@ -832,6 +872,7 @@ cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const vo
     GemmArgs args = base_args(dev);
     args.pr[0] = make_problem(a_s, b_s, y, M_total, N, K, ldy, (K + 127) / 128, static_cast<int64_t>(G) * N / 128,
                               fmt_bits_of(a_fmt, b_fmt));
+    set_store_map(&maps.y[0], &args.pr[0], y, M_total, N, ldy);
     args.offsets = offsets;
     args.G = G;
     args.a_bands_cap = a_bands_cap;
@@ -850,6 +891,7 @@ cudaError_t launch_grouped_gemm_wgrad(const DeviceInfo& dev, const void* a_q, co
     GemmArgs args = base_args(dev);
     args.pr[0] = make_problem(a_s, b_s, y, M, N, capacity, ldy, capacity / 128, (N + 127) / 128,
                               fmt_bits_of(a_fmt, b_fmt));
+    set_store_map(&maps.y[0], &args.pr[0], y, static_cast<int64_t>(G) * M, N, ldy);   // y[g] stacked
     args.M_total = M_total;
     args.offsets = offsets;
     args.G = G;

@@ -27,6 +27,10 @@ bool encode_tensor_map_2d(CUtensorMap* map, const void* base, bool two_byte_elem
                           uint32_t box_outer, bool swizzle_128b);
 
 // 3-D tensor map [outer, mid, inner], box [1, box_mid, box_inner], no swizzle.
+// BF16 [rows, cols] (row stride ld elements) for 32 x 32 tiled stores with the
+// 64-byte swizzle.
+bool encode_tensor_map_bf16_store(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                                  uint64_t ld);
 bool encode_tensor_map_3d(CUtensorMap* map, const void* base, bool two_byte_elems, uint64_t inner,
                           uint64_t mid, uint64_t outer, uint64_t mid_stride_bytes,
                           uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_mid);

@@ -63,4 +63,20 @@ bool encode_tensor_map_2d(CUtensorMap* map, const void* base, bool two_byte_elem
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// BF16 matrix [rows, cols] with a row stride of ld elements, as the target of
+// tiled stores of 32 x 32 boxes from shared memory laid out with the 64-byte
+// swizzle (16-byte chunk j of box row r at chunk position j ^ ((r >> 1) & 3)).
+bool encode_tensor_map_bf16_store(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                                  uint64_t ld) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || cols == 0 || rows == 0) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {ld * 2};
+    const cuuint32_t box[2] = {32u, 32u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace mxq
