@@ -483,7 +483,6 @@ class FsdpWeight(Workload):
         d = workloads.weight_32x32(dev or "cpu")
         self.inputs = {"W_shard": d["W"][:ns].contiguous(), "X": d["X"], "dY": d["dY"]}
         if dev is None:
-            self.W_host = d["W"]
             return
         M, n, k = self.M, self.n, self.k
         u8 = dict(dtype=torch.uint8, device=dev)
@@ -553,7 +552,11 @@ class FsdpWeight(Workload):
         tq = (time.perf_counter() - t0) / w.size
         xq, xs = oracle.quant_rows(_host_bits(i["X"][:64]))
         a = oracle.dequant_rows(xq, xs)
-        wq, ws = oracle.quant_rows(_host_bits(self.W_host))
+        # the GEMM rate from output rows against this rank's shard of W (its rows
+        # are the weight's first n/world output features)
+        w_shard = i["W_shard"]
+        ns = w_shard.shape[0]
+        wq, ws = oracle.quant_rows(_host_bits(w_shard))
         b = oracle.dequant_rows(wq, ws)
         rows, t_g = 0, 0.0
         while t_g < budget_s and rows < a.shape[0]:
@@ -561,11 +564,12 @@ class FsdpWeight(Workload):
             oracle.gemm(a, b, rows=np.array([rows], dtype=np.int64))
             t_g += time.perf_counter() - t0
             rows += 1
-        tg = t_g / (2.0 * rows * self.n * self.k)
+        tg = t_g / (2.0 * rows * ns * self.k)
         elems = self.n * self.k // self.world + self.M * self.k + self.M * self.n
         return tq * elems + tg * self.gemm_flops, (
-            f"oracle {self.recipe} quant of 256 shard rows and FP64 GEMM of {rows} rows x {self.n} x {self.k}; "
-            f"extrapolated to the full step (the gather and unpack move bytes only and are not timed on the CPU)")
+            f"oracle {self.recipe} quant of 256 shard rows and FP64 GEMM of {rows} rows x {ns} x {self.k} "
+            f"(the rank's shard of W); extrapolated to the full step (the gather and unpack move bytes only "
+            f"and are not timed on the CPU)")
 
 
 class MoE(Workload):
