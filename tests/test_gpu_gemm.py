@@ -247,3 +247,24 @@ def test_small_linear_exhaustive():
     y = mxq.gemm(xq, xs, wq, ws, 256, 512, 512)
     torch.cuda.synchronize()
     assert_gemm_close(y, oracle.gemm(xd, wd), "small linear")
+
+
+@pytest.mark.parametrize("M,N,K,pad", [(300, 272, 256, 8), (1000, 4112, 512, 24), (129, 528, 128, 40)])
+def test_strided_output_clipped_stores(M, N, K, pad):
+    """Output rows ldy = N + pad apart (pad not a multiple of 32 columns), N with a
+    last 32-column chunk partly past N, ragged M: equal to the contiguous call bit
+    for bit and to the oracle; the padding columns of every row keep their bytes
+    (whole chunks leave as tiled stores clipped at N, the rest row by row)."""
+    mxq, workloads, oracle = _mods()
+    X = workloads.normal_with_outliers((M, K), seed=M + 7)
+    W = workloads.normal((N, K), 0.02, seed=N + 8)
+    xq, xs, xd = _rows_operand(X)
+    wq, ws, wd = _rows_operand(W)
+    big = torch.full((M, N + pad), 7.0, dtype=torch.bfloat16, device="cuda")
+    y = mxq.gemm(xq, xs, wq, ws, M, N, K, out=big[:, :N])
+    y1 = mxq.gemm(xq, xs, wq, ws, M, N, K)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y1.view(torch.int16)), "strided output differs"
+    assert torch.all(big[:, N:] == 7.0), "bytes past N in a row were written"
+    r = _sample_rows(M, n=min(M, 96), seed=3)
+    assert_gemm_close(y1[torch.from_numpy(r).cuda()], oracle.gemm(xd, wd, rows=r), f"strided {M}x{N}x{K}")
