@@ -165,3 +165,29 @@ def test_full_moe_forward_equals_grouped_gemm():
         assert torch.equal(y.view(torch.int16), y_grid.view(torch.int16)), f"K={K}"
         del y, y_grid
     assert mxq.get_device_status() == 0
+
+
+def test_max_experts_mostly_empty():
+    """G = 1024 (the largest supported), 60 non-empty experts of 1 to 300 rows
+    scattered among empty ones, the last expert empty: the band scan runs over
+    all 32 groups of 32 and the band lookup over 1024 experts."""
+    mxq, workloads, oracle = _mods()
+    rng = np.random.default_rng(2024)
+    sizes = np.zeros(1024, np.int64)
+    sizes[np.sort(rng.choice(1023, 60, replace=False))] = rng.integers(1, 301, 60)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    M, N, K = int(off[-1]), 128, 256
+    A = workloads.normal_with_outliers((M, K), seed=77)
+    B = workloads.normal((1024 * N, K), 0.02, seed=78, device="cuda")
+    aq, as_, _, _ = mxq.quant_1x32_dual(A.cuda(), col=False)
+    bq, bs, _, _ = mxq.quant_1x32_dual(B, col=False)
+    offd = torch.from_numpy(off).cuda()
+    sg = mxq.scale_regroup_rows(as_, M, K, offd)
+    y = mxq.grouped_gemm_group_tiled(aq, sg, bq, bs, offd, N, K)
+    y_grid = mxq.grouped_gemm(aq, as_, bq, bs, offd, N, K)
+    torch.cuda.synchronize()
+    _, osa = oracle.quant_rows(bits(A))
+    want = oracle.scale_group_tiled(osa, off)
+    assert np.array_equal(u8(sg)[:want.size], want), "group-tiled scales"
+    assert torch.equal(y.view(torch.int16), y_grid.view(torch.int16)), "differs from mxq_grouped_gemm"
+    assert mxq.get_device_status() == 0
