@@ -32,3 +32,24 @@ def test_rejects_too_few_warmup_steps():
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "1"],
                        cwd=ROOT, capture_output=True, text=True, timeout=120)
     assert r.returncode != 0
+
+
+def test_group_tiled_band_accounting():
+    """The bench's regroup bytes and buffers use the bands the oracle's group-tiled
+    layout fills (each expert ceil(n_g / 128) bands) and the capacity the C ABI
+    asks for (ceil(rows / 128) + G bands)."""
+    import numpy as np
+    import bench
+    from oracle import oracle
+
+    class W:
+        pass
+    w = W()
+    w.Mt, w.G = 1000, 4
+    off = [0, 130, 130, 700, 1000]
+    bufs = bench._group_tiled_setup(w, off, (256, 128), "cpu")
+    filled = oracle.scale_group_tiled(np.zeros((1000, 8), np.uint8), off).size
+    assert w.gt_bands * 2 * 512 == filled
+    assert w.gt_cap == (1000 + 127) // 128 + 4
+    assert bufs[0].numel() == w.gt_cap * 2 * 512 and bufs[1].numel() == w.gt_cap * 512
+    assert bench._regroup_bytes(w, 256) == ((1000 + 127) // 128 + w.gt_bands) * 2 * 512
