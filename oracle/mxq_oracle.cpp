@@ -19,16 +19,18 @@
 //    weight payload), section 3.3.1 (element type E4M3, dynamic scaling),
 //    section 3.3.3 (mxfp8 uses a dual-axis quantizer that gives separate
 //    forward and backward copies; mxfp8-32x32 gives one payload, and only
-//    the scales differ), section 3.5.2.3 (dst_type float8_e4m3fn).
+//    the scales differ), section 3.5.2.3 (process_quant_result_fn serves
+//    both recipes; its dst_type is float8_e4m3fn or float8_e5m2).
 //
-// Readings taken where the pages are silent (each one is listed in the
-// design notes as well):
+// Readings taken where the pages are silent:
 //  * E4M3 is the OCP "fn" variant (float8_e4m3fn): bias 7, no infinities,
 //    NaN = S.1111.111, largest finite 448.  Conversion is round to nearest,
 //    ties to even, saturating to +-448; the sign of zero is kept.
 //  * E8M0 code c in [0,254] means 2^(c-127); 0xFF is NaN.
 //  * The RFC also allows dst_type E5M2 (section 3.5.2.3): OCP float8_e5m2,
-//    bias 15, max finite 57344, RNE saturating; rceil then uses 57344.
+//    bias 15, max finite 57344, RNE saturating; rceil then uses 57344.  The
+//    same function serves the 32x32 recipe, so both the 1x32 and the 32x32
+//    quantizers take either format.
 //  * rceil: e = ceil(log2(amax / 448)), clamped to [-127, 127]; amax == 0
 //    gives e = -127.  Evaluated exactly: with amax = f * 2^k, f in [0.5,1),
 //    448 = 0.875 * 2^9, so e = k - 9 + (f > 0.875).
@@ -256,12 +258,13 @@ void orc_quant_dual(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
 
 // ---- 32x32 block quantization ----------------------------------------------
 // w: bf16 bits [n, k] (row stride ld), n % 32 == 0, k % 32 == 0.  Tiles of
-// 32 x 32 start at (0,0).  One payload q [n, k].  The tile exponent t[i][j]
-// (tile row i, tile column j) is written twice:
+// 32 x 32 start at (0,0).  One payload q [n, k] in format fmt (0 E4M3,
+// 1 E5M2).  The tile exponent t[i][j] (tile row i, tile column j) is written
+// twice:
 //   s_fwd [n, k/32]:  s_fwd[r][j] = t[r/32][j]   (forward, contraction over k)
 //   s_bwd [k, n/32]:  s_bwd[c][i] = t[i][c/32]   (backward, contraction over n)
-void orc_quant_32x32(const uint16_t* w, int64_t n, int64_t k, int64_t ld,
-                     uint8_t* q, uint8_t* s_fwd, uint8_t* s_bwd) {
+void orc_quant_32x32_fmt(const uint16_t* w, int64_t n, int64_t k, int64_t ld,
+                         uint8_t* q, uint8_t* s_fwd, uint8_t* s_bwd, int fmt) {
     const int64_t tn = n / 32, tk = k / 32;
 #pragma omp parallel for collapse(2) schedule(static)
     for (int64_t i = 0; i < tn; ++i) {
@@ -269,13 +272,18 @@ void orc_quant_32x32(const uint16_t* w, int64_t n, int64_t k, int64_t ld,
             uint8_t code = quant_shared_scale(
                 32 * 32,
                 [&](int64_t e) { return bf16_bits_to_double(w[(i * 32 + e / 32) * ld + j * 32 + e % 32]); },
-                [&](int64_t e, uint8_t b) { q[(i * 32 + e / 32) * k + j * 32 + e % 32] = b; });
+                [&](int64_t e, uint8_t b) { q[(i * 32 + e / 32) * k + j * 32 + e % 32] = b; }, fmt);
             for (int64_t r = 0; r < 32; ++r) {
                 if (s_fwd) s_fwd[(i * 32 + r) * tk + j] = code;
                 if (s_bwd) s_bwd[(j * 32 + r) * tn + i] = code;
             }
         }
     }
+}
+
+void orc_quant_32x32(const uint16_t* w, int64_t n, int64_t k, int64_t ld,
+                     uint8_t* q, uint8_t* s_fwd, uint8_t* s_bwd) {
+    orc_quant_32x32_fmt(w, n, k, ld, q, s_fwd, s_bwd, 0);
 }
 
 // ---- grouped column quantization (MoE weight gradient) ----------------------

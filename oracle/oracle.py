@@ -74,6 +74,7 @@ def _load():
     lib.orc_quant_rows.argtypes = [P, I64, I64, I64, P, P]
     lib.orc_quant_dual.argtypes = [P, I64, I64, I64, P, P, P, P]
     lib.orc_quant_32x32.argtypes = [P, I64, I64, I64, P, P, P]
+    lib.orc_quant_32x32_fmt.argtypes = [P, I64, I64, I64, P, P, P, ctypes.c_int]
     lib.orc_scale_tiled.argtypes = [P, I64, I64, P]
     lib.orc_quant_cols_grouped.argtypes = [P, I64, I64, I64, P, ctypes.c_int32, I64, P, P]
     lib.orc_quant_cols_grouped_fmt.argtypes = [P, I64, I64, I64, P, ctypes.c_int32, I64, P, P, ctypes.c_int]
@@ -83,7 +84,7 @@ def _load():
     for f in ("orc_e4m3_encode_array", "orc_bf16_from_double_array", "orc_quant_rows",
               "orc_quant_cols_grouped", "orc_quant_cols_grouped_fmt", "orc_e5m2_encode_array", "orc_quant_rows_fmt",
               "orc_dequant_rows_fmt",
-              "orc_quant_dual", "orc_quant_32x32", "orc_scale_tiled", "orc_dequant_rows",
+              "orc_quant_dual", "orc_quant_32x32", "orc_quant_32x32_fmt", "orc_scale_tiled", "orc_dequant_rows",
               "orc_gemm", "orc_grouped_gemm"):
         getattr(lib, f).restype = None
     _lib = lib
@@ -211,8 +212,10 @@ def quant_dual(x_bits: np.ndarray, want_row: bool = True, want_col: bool = True)
     return q_row, s_row, q_col, s_col
 
 
-def quant_32x32(w_bits: np.ndarray):
-    """32x32 block quantization.  Returns (q [N,K], s_fwd [N,K/32], s_bwd [K,N/32])."""
+def quant_32x32(w_bits: np.ndarray, fmt: int = 0):
+    """32x32 block quantization with payload format fmt (0 E4M3, 1 E5M2: the
+    RFC's dst_type, section 3.5.2.3).  Returns (q [N,K], s_fwd [N,K/32],
+    s_bwd [K,N/32])."""
     lib = _load()
     w = _c(w_bits, np.uint16)
     N, K = w.shape
@@ -220,7 +223,7 @@ def quant_32x32(w_bits: np.ndarray):
     q = np.empty((N, K), np.uint8)
     s_fwd = np.empty((N, K // 32), np.uint8)
     s_bwd = np.empty((K, N // 32), np.uint8)
-    lib.orc_quant_32x32(_ptr(w), N, K, K, _ptr(q), _ptr(s_fwd), _ptr(s_bwd))
+    lib.orc_quant_32x32_fmt(_ptr(w), N, K, K, _ptr(q), _ptr(s_fwd), _ptr(s_bwd), int(fmt))
     return q, s_fwd, s_bwd
 
 
