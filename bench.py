@@ -2,21 +2,27 @@
 """Benchmark of the MXFP8 training hot path on GB300.
 
 One step = one pass of the hot path over one batch of synthetic input.  The
-default workload is the linear layer X [8192, 4096], W [4096, 4096],
-dY [8192, 4096]: dual-axis 1x32 quantization of X, W and dY, then the
-forward (Y = X W^T), dgrad (dX = dY W) and wgrad (dW = dY^T X) block-scaled
-GEMMs with BF16 output.  Other workloads (--workload): linear_fwd_small,
-weight_32x32 (32x32 weight payload shared by forward and dgrad), moe_grouped
-(128-expert grouped GEMMs), sweep_4096 / sweep_7168 / sweep_16384.
+default workload is the largest single-GPU linear layer, M = 16384 tokens,
+K = N = 16384 (activations 0.5 Student-t(3), weights N(0, 0.02^2)): dual-axis
+1x32 quantization of X, W and dY, then the forward (Y = X W^T), dgrad
+(dX = dY W) and wgrad (dW = dY^T X) block-scaled GEMMs with BF16 output.
+The same process then times the 128-expert MoE grouped GEMMs (16384 tokens,
+top-8, gate_up and down projections with their row quantizations) and adds
+them under `moe_block` (--extra-workloads).  Other workloads (--workload):
+linear_train (8192 x 4096 x 4096), linear_fwd_small, weight_32x32 (32x32
+weight payload shared by forward and dgrad), moe_grouped, moe_train,
+fsdp_*, sweep_4096 / sweep_7168.
 
 Prints one JSON line.  `value` is the step's GEMM FLOPs divided by the step
 time (quantizers included), inputs resident in HBM, timed with CUDA events
 on the launching stream; L2 is flushed (256 MB write) between timed steps,
 outside the timed intervals.  `e2e` is the same metric through the public
 API with the inputs copied from pinned host memory and the BF16 results
-copied back inside every timed step.  `roofline` covers the GEMM kernel,
-`roofline_quant` the quantizers.  `cpu_baseline` times the oracle on a
-bounded sample.  `--impl reference` times the oracle alone (CPU).
+copied back inside every timed step.  `roofline` covers the GEMM kernel
+(peak: the larger of 2 x the measured BF16 burst and the vendor library's
+MXFP8 GEMM timed in the same run), `roofline_quant` the quantizers.
+`cpu_baseline` times the oracle on a bounded sample.  `--impl reference`
+times the oracle alone (CPU).
 
 Multi-GPU: the path has no exchange step, so N ranks run N independent
 replicas (weak scaling); the timing is the max over ranks.
@@ -45,10 +51,14 @@ FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 L2_FLUSH_BYTES = 256 << 20   # larger than the 129 MB L2
 L2_BYTES = 129 * 10**6
 # DRAM bytes (read + write) per GEMM launch of one step, averaged over the step's
-# GEMM launches like `units_per_launch` (linear_train: the forward GEMM and the
-# backward dgrad + wgrad launch), from an ncu --set full capture of the kernel as
-# it stands; None where not captured.
-GEMM_TRAFFIC_BYTES = {"linear_train": 143129088}
+# GEMM launches like `units_per_launch`, from an ncu capture of the kernel as it
+# stands; None where not captured (or captured before the kernel last changed).
+GEMM_TRAFFIC_BYTES = {}
+DEFAULT_WORKLOAD = "sweep_16384"
+DEFAULT_EXTRA = "moe_grouped"
+# Shapes (M, N, K) at which the vendor library's MXFP8 GEMM is timed for the
+# GEMM peak: its best measured rate on this machine, next to the workload's own.
+VENDOR_SHAPES = [(8192, 4096, 4096), (16384, 8192, 8192), (16384, 16384, 16384)]
 
 
 def load_peaks():
@@ -264,8 +274,10 @@ class LinearTrain(Workload):
             cur.wait_stream(s)
 
     def cpu_sample(self, budget_s):
-        """Times the oracle on row samples of each step part; returns
-        (seconds per full step extrapolated, description)."""
+        """Times the oracle on a bounded sample of each step part: the dual
+        quantization of 256 rows of X, and FP64 GEMM output rows against the
+        first 512 rows of W (output columns), one row at a time until the budget.
+        Returns (seconds per full step extrapolated from those rates, description)."""
         from oracle import oracle
         import numpy as np
         i = self.inputs
@@ -275,7 +287,8 @@ class LinearTrain(Workload):
         tq = (time.perf_counter() - t0) / x.size          # per element, dual
         qr, sr = oracle.quant_rows(_host_bits(i["X"][:64]))
         a = oracle.dequant_rows(qr, sr)
-        wq, ws = oracle.quant_rows(_host_bits(i["W"]))
+        ncols = min(512, self.N)
+        wq, ws = oracle.quant_rows(_host_bits(i["W"][:ncols]))
         b = oracle.dequant_rows(wq, ws)
         rows, t_g = 0, 0.0
         while t_g < budget_s and rows < a.shape[0]:
@@ -283,12 +296,12 @@ class LinearTrain(Workload):
             oracle.gemm(a, b, rows=np.array([rows], dtype=np.int64))
             t_g += time.perf_counter() - t0
             rows += 1
-        tg = t_g / (2.0 * rows * self.N * self.K)          # per FLOP
+        tg = t_g / (2.0 * rows * ncols * self.K)          # per FLOP
         quant_elems = self.M * self.K + self.N * self.K + self.M * self.N
         step = tq * quant_elems + tg * self.gemm_flops
         return step, (f"oracle dual quant of 256 rows of X ({x.size} elements) and FP64 GEMM of "
-                      f"{rows} output rows x {self.N} x {self.K}; extrapolated to the full step "
-                      f"({quant_elems} quantized elements, {self.gemm_flops:.4g} GEMM FLOPs)")
+                      f"{rows} output rows x {ncols} output columns x K {self.K}; rates extrapolated to the "
+                      f"full step ({quant_elems} quantized elements, {self.gemm_flops:.4g} GEMM FLOPs)")
 
 
 class LinearFwdSmall(Workload):
@@ -834,41 +847,86 @@ def workload_config(w):
     return cfg
 
 
+def cpu_model():
+    """The host CPU's model name (from /proc/cpuinfo, else the machine type)."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model", "Hardware"):
+            for line in info.splitlines():
+                if line.split(":")[0].strip() == key and ":" in line:
+                    return line.split(":", 1)[1].strip()
+        parts = sorted({line.split(":", 1)[1].strip() for line in info.splitlines()
+                        if line.startswith("CPU part") and ":" in line})
+        if parts:
+            return f"{platform.machine()} (CPU part {', '.join(parts)})"
+    except OSError:
+        pass
+    return platform.machine() or "unknown"
+
+
+def vendor_mxfp8_tflops(dev, shapes):
+    """The vendor library's MXFP8 GEMM (PyTorch _scaled_mm with float8_e4m3fn
+    operands and E8M0 block scales, cuBLASLt underneath) timed at each shape:
+    {"MxNxK": TFLOP/s}, or {"error": why}.  A denominator only: none of the
+    hot path runs here, and its outputs are not used."""
+    import torch
+    if not hasattr(torch, "float8_e8m0fnu"):
+        return {"error": "this PyTorch has no float8_e8m0fnu"}
+    out = {}
+    for (M, N, K) in shapes:
+        try:
+            a = torch.randint(-100, 100, (M, K), device=dev, dtype=torch.int8).view(torch.uint8)
+            a = (a & 0x77).view(torch.float8_e4m3fn)       # finite codes only
+            b = (torch.randint(0, 255, (N, K), device=dev, dtype=torch.uint8) & 0x77).view(torch.float8_e4m3fn)
+            sa = torch.full(((M + 127) // 128 * 128, (K // 32 + 3) // 4 * 4), 127, dtype=torch.uint8,
+                            device=dev).view(torch.float8_e8m0fnu)
+            sb = torch.full(((N + 127) // 128 * 128, (K // 32 + 3) // 4 * 4), 127, dtype=torch.uint8,
+                            device=dev).view(torch.float8_e8m0fnu)
+            f = lambda: torch._scaled_mm(a, b.t(), sa, sb, out_dtype=torch.bfloat16)
+            for _ in range(3):
+                f()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(5, min(50, int(2e12 / (2.0 * M * N * K)) + 1))
+            e0.record()
+            for _ in range(reps):
+                f()
+            e1.record()
+            torch.cuda.synchronize()
+            out[f"{M}x{N}x{K}"] = round(2.0 * M * N * K * reps / (e0.elapsed_time(e1) / 1e3) / 1e12, 1)
+            del a, b, sa, sb
+        except Exception as ex:                              # noqa: BLE001 -- a denominator, not the product
+            out[f"{M}x{N}x{K}"] = None
+            out.setdefault("error", f"{type(ex).__name__}: {str(ex).splitlines()[0][:160]}")
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---- the GPU arm ---------------------------------------------------------------------------
 
-def run_gpu(args):
+def time_device(w, args, dev, world):
+    """Warm-up, then args.steps timed steps of workload w with the inputs
+    resident in HBM (CUDA events per step and per kernel on the launching
+    stream, L2 flushed between steps) while nvidia-smi samples the clocks.
+    Returns the per-kernel and per-step times and the clock summary."""
     import torch
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    from mxfp8_microscaled_precision_gb300 import build as mbuild, mxq
-    mbuild.build()
-    mxq.lib()
-    peaks = load_peaks()
-    w = make_workload(args.workload, dev)
+    from mxfp8_microscaled_precision_gb300 import mxq
     kern = w.kernels()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-
-    def step():
-        for (_, _, _, fn) in kern:
-            fn()
-
     for _ in range(args.warmup):
         flush.fill_(1)
-        step()
+        for (_, _, _, fn) in kern:
+            fn()
     torch.cuda.synchronize()
     st = mxq.get_device_status()
     if st != 0:
-        raise SystemExit(f"device status {st} after warm-up")
-
+        raise SystemExit(f"device status {st} after warm-up of {w.name}")
     nk = len(kern)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
-    sampler = ClockSampler(dev.index if world == 1 else local)
+    sampler = ClockSampler(dev.index)
     sampler.start()
     time.sleep(0.3)
     barrier(dev)
@@ -885,39 +943,87 @@ def run_gpu(args):
     t_wall1 = time.time()
     time.sleep(0.2)
     sampler.stop()
-    clocks = sampler.summary(t_wall0 - 0.05, t_wall1 + 0.05)
-
+    st = mxq.get_device_status()
+    if st != 0:
+        raise SystemExit(f"device status {st} after the timed steps of {w.name}")
     per_kernel = [[ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps)] for j in range(nk)]
     step_ms = [ev[s][0].elapsed_time(ev[s][nk]) for s in range(args.steps)]
-    total_s = sum(step_ms) / 1e3
-    max_total_s = max_over_ranks(total_s, dev if world > 1 else None)
-    value = aggregate_value(w.gemm_flops, args.steps, world, max_total_s)
+    return {"kern": kern, "per_kernel": per_kernel, "step_ms": step_ms, "flush": flush,
+            "clocks": sampler.summary(t_wall0 - 0.05, t_wall1 + 0.05)}
 
-    kernels_ms = {kern[j][0]: statistics.mean(per_kernel[j]) for j in range(nk)}
+
+def rates(t, steps, peaks, gemm_peak):
+    """GEMM and quantizer rates of one timed workload against their peaks."""
+    kern, per_kernel = t["kern"], t["per_kernel"]
+    nk = len(kern)
     gemm_idx = [j for j in range(nk) if kern[j][1] == "gemm"]
     quant_idx = [j for j in range(nk) if kern[j][1] == "quant"]
     gemm_s = sum(sum(per_kernel[j]) for j in gemm_idx) / 1e3
     quant_s = sum(sum(per_kernel[j]) for j in quant_idx) / 1e3
-    gemm_flops = sum(kern[j][2] for j in gemm_idx) * args.steps
-    quant_bytes = sum(kern[j][2] for j in quant_idx) * args.steps
-    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
-    gemm_tflops = gemm_flops / gemm_s / 1e12
-    quant_gbs = quant_bytes / quant_s / 1e9
-    per_launch_flops = statistics.mean(kern[j][2] for j in gemm_idx)
-    roofline = {"bound": "tensor", "kernel": "gemm_mxf8_kernel", "achieved": round(gemm_tflops, 1),
-                "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
-                "traffic": GEMM_TRAFFIC_BYTES.get(w.name),
-                "units_per_launch": per_launch_flops,
-                "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 ratio)"}
-    roofline_quant = {"bound": "hbm", "kernel": "quant kernels", "achieved": round(quant_gbs, 1),
-                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
-                      "peak_source": peaks["source"] + " copy bandwidth"}
+    gemm_tflops = sum(kern[j][2] for j in gemm_idx) * steps / gemm_s / 1e12
+    quant_gbs = sum(kern[j][2] for j in quant_idx) * steps / quant_s / 1e9 if quant_idx else 0.0
     other_hbm = {}
     for j in range(nk):
         if kern[j][1] not in ("gemm", "quant"):
-            gbs = kern[j][2] * args.steps / (sum(per_kernel[j]) / 1e3) / 1e9
+            gbs = kern[j][2] * steps / (sum(per_kernel[j]) / 1e3) / 1e9
             other_hbm[kern[j][0]] = {"kind": kern[j][1], "bytes_per_launch": kern[j][2],
                                      "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    return {"gemm_tflops": gemm_tflops, "gemm_frac": gemm_tflops / gemm_peak, "quant_gbs": quant_gbs,
+            "quant_frac": quant_gbs / peaks["hbm_gbs"],
+            "per_launch_flops": statistics.mean(kern[j][2] for j in gemm_idx),
+            "kernels_ms": {kern[j][0]: round(statistics.mean(per_kernel[j]), 5) for j in range(nk)},
+            "other_hbm": other_hbm}
+
+
+def gemm_peak_of(peaks, vendor):
+    """The GEMM denominator: the larger of 2 x the measured BF16 burst (the
+    nominal FP8/BF16 ratio) and the best vendor MXFP8 rate timed in this run."""
+    fp8_nominal = peaks["bf16_tflops"] * FP8_OVER_BF16
+    best = max([v for k, v in vendor.items() if k != "error" and v], default=0.0)
+    if best > fp8_nominal:
+        return best, f"vendor MXFP8 GEMM (cuBLASLt via torch._scaled_mm) timed in this run, best of {vendor}"
+    return fp8_nominal, (f"{peaks['source']} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 ratio); "
+                         f"vendor MXFP8 in this run {vendor}")
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from mxfp8_microscaled_precision_gb300 import build as mbuild, mxq
+    mbuild.build()
+    mxq.lib()
+    peaks = load_peaks()
+    w = make_workload(args.workload, dev)
+    vendor_shapes = list(VENDOR_SHAPES)
+    if all(hasattr(w, k) for k in ("M", "N", "K")) and (w.M, w.N, w.K) not in vendor_shapes:
+        vendor_shapes.append((w.M, w.N, w.K))
+    vendor = vendor_mxfp8_tflops(dev, vendor_shapes) if not args.no_vendor_peak else {"error": "not timed"}
+    gemm_peak, gemm_peak_source = gemm_peak_of(peaks, vendor)
+    fp8_nominal = peaks["bf16_tflops"] * FP8_OVER_BF16
+
+    t = time_device(w, args, dev, world)
+    kern, stream, flush = t["kern"], torch.cuda.current_stream(), t["flush"]
+    main_clocks = t["clocks"]
+    nk = len(kern)
+    total_s = sum(t["step_ms"]) / 1e3
+    max_total_s = max_over_ranks(total_s, dev if world > 1 else None)
+    value = aggregate_value(w.gemm_flops, args.steps, world, max_total_s)
+    r = rates(t, args.steps, peaks, gemm_peak)
+    roofline = {"bound": "tensor", "kernel": "gemm_mxf8_kernel", "achieved": round(r["gemm_tflops"], 1),
+                "peak": round(gemm_peak, 1), "unit": "TFLOP/s", "frac": round(r["gemm_frac"], 4),
+                "traffic": GEMM_TRAFFIC_BYTES.get(w.name),
+                "units_per_launch": r["per_launch_flops"],
+                "peak_source": gemm_peak_source,
+                "frac_of_2x_bf16_burst": round(r["gemm_tflops"] / fp8_nominal, 4)}
+    roofline_quant = {"bound": "hbm", "kernel": "quant kernels", "achieved": round(r["quant_gbs"], 1),
+                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(r["quant_frac"], 4),
+                      "peak_source": peaks["source"] + " copy bandwidth"}
     own_launches = sum(LAUNCHES_PER_ENTRY.get(kern[j][0], 1) for j in range(nk) if kern[j][1] != "collective")
 
     # ---- end to end through the public API, host buffers, copies inside the timed step
@@ -982,11 +1088,32 @@ def run_gpu(args):
                "resident": list(w.state_keys),
                "l2": "flushed before each step's kernels" if flush_each else
                      "each step's inputs (larger than L2) arrive fresh from the host"}
-        del w2, inst
+        del w2, inst, host_in, host_out
+        st = mxq.get_device_status()
+        if st != 0:
+            raise SystemExit(f"device status {st} after the end-to-end steps")
 
-    st = mxq.get_device_status()
-    if st != 0:
-        raise SystemExit(f"device status {st} after the timed region")
+    # ---- further workloads timed in the same process (device side only)
+    extra = {}
+    extra_launches = 0
+    del t, flush
+    for name in [n for n in args.extra_workloads.split(",") if n and n != "none" and n != args.workload]:
+        torch.cuda.empty_cache()
+        wx = make_workload(name, dev)
+        tx = time_device(wx, args, dev, world)
+        rx = rates(tx, args.steps, peaks, gemm_peak)
+        tot_x = max_over_ranks(sum(tx["step_ms"]) / 1e3, dev if world > 1 else None)
+        extra[name] = {"config": workload_config(wx),
+                       "value": round(aggregate_value(wx.gemm_flops, args.steps, world, tot_x), 2),
+                       "unit": "TFLOP/s", "ms_per_step": round(tot_x / args.steps * 1e3, 4),
+                       "gemm_tflops": round(rx["gemm_tflops"], 1), "gemm_frac_peak": round(rx["gemm_frac"], 4),
+                       "gemm_frac_of_2x_bf16_burst": round(rx["gemm_tflops"] / fp8_nominal, 4),
+                       "quant_tbs": round(rx["quant_gbs"] / 1e3, 3), "quant_frac_hbm": round(rx["quant_frac"], 4),
+                       "kernels_ms": rx["kernels_ms"], "clocks": tx["clocks"]}
+        if rx["other_hbm"]:
+            extra[name]["hbm_kernels"] = rx["other_hbm"]
+        extra_launches += args.steps * sum(LAUNCHES_PER_ENTRY.get(k[0], 1) for k in tx["kern"] if k[1] != "collective")
+        del wx, tx
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -999,16 +1126,20 @@ def run_gpu(args):
                 "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (E8M0 block scales, fp32 accumulate)",
                 "data": "synthetic (seeded generators; shapes of the linear / MoE-expert workloads)",
                 "config": workload_config(w),
-                "gemm_tflops": round(gemm_tflops, 1), "gemm_frac_fp8_peak": round(gemm_tflops / fp8_peak, 4),
-                "quant_tbs": round(quant_gbs / 1e3, 3), "quant_frac_hbm": round(quant_gbs / peaks["hbm_gbs"], 4),
-                "kernels_ms": {k: round(v, 5) for k, v in kernels_ms.items()},
+                "gemm_tflops": round(r["gemm_tflops"], 1), "gemm_frac_peak": round(r["gemm_frac"], 4),
+                "quant_tbs": round(r["quant_gbs"] / 1e3, 3), "quant_frac_hbm": round(r["quant_frac"], 4),
+                "kernels_ms": r["kernels_ms"],
                 "roofline": roofline, "roofline_quant": roofline_quant,
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": own_launches * args.steps, "clocks": clocks,
-                "impl": "mxq"}
-        if other_hbm:
-            line["hbm_kernels"] = other_hbm
+                "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": own_launches * args.steps + extra_launches,
+                "gpu_launches_split": {w.name: own_launches * args.steps, "extra_workloads": extra_launches},
+                "clocks": main_clocks, "vendor_mxfp8_tflops": vendor, "impl": "mxq"}
+        if r["other_hbm"]:
+            line["hbm_kernels"] = r["other_hbm"]
         if hasattr(w, "extra"):
             line.update(w.extra())
+        for name, block in extra.items():
+            line["moe_block" if name == "moe_grouped" else "extra_" + name] = block
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -1021,7 +1152,8 @@ def cpu_baseline(w, budget_s):
     t_step, sample = w.cpu_sample(budget_s)
     cores = _omp_threads()
     return {"value": round(w.gemm_flops / t_step / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
-            "kind": "oracle", "sample": sample, "extrapolated_s_per_step": round(t_step, 3)}
+            "cpu_model": cpu_model(), "kind": "oracle", "sample": sample,
+            "extrapolated_s_per_step": round(t_step, 3)}
 
 
 def _omp_threads():
@@ -1037,29 +1169,42 @@ def _omp_threads():
 # ---- the reference arm: the oracle on the host cores ------------------------------------------
 
 def run_reference(args):
+    """The oracle timed on the host cores.  Each step is one bounded sample of
+    the workload (cpu_sample); `ms_per_step` is the measured wall time of those
+    samples, `value` the rate they give for the full step (sampled rates
+    extrapolated to the step's work), and `extrapolated_ms_per_full_step` the
+    time a whole step would take at those rates."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import torch
     from oracle import oracle
     oracle.build()
     w = make_workload(args.workload)
-    per_step_budget = max(0.05, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
-    times = []
+    per_step_budget = max(0.05, min(4.0, 100.0 / max(1, args.steps + args.warmup)))
+    ext, wall = [], []
     desc = ""
+    t_run0 = time.perf_counter()
     for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
         t, desc = w.cpu_sample(per_step_budget * 0.8)
+        dt = time.perf_counter() - t0
         if s >= args.warmup:
-            times.append(t)
-    t_step = statistics.mean(times)
-    value = w.gemm_flops / t_step / 1e12
+            ext.append(t)
+            wall.append(dt)
+    t_full = statistics.mean(ext)
+    value = w.gemm_flops / t_full / 1e12
     cores = _omp_threads()
     line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.mean(wall) * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
             "data": "synthetic", "config": workload_config(w), "impl": "reference",
-            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                             "sample": desc + "; each step is this bounded sample, time extrapolated to the full step"},
+            "extrapolated_ms_per_full_step": round(t_full * 1e3, 3),
+            "wall_s_all_steps": round(time.perf_counter() - t_run0, 3),
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "cpu_model": cpu_model(),
+                             "kind": "oracle",
+                             "sample": desc + "; each timed step is this bounded sample (ms_per_step is its "
+                                              "measured wall time; value is the sample's rate over the full "
+                                              "step's work)"},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -1067,10 +1212,15 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["mxq", "reference"], default="mxq")
-    ap.add_argument("--workload", choices=WORKLOAD_NAMES, default="linear_train")
+    ap.add_argument("--workload", choices=WORKLOAD_NAMES, default=DEFAULT_WORKLOAD)
+    ap.add_argument("--extra-workloads", default=DEFAULT_EXTRA,
+                    help="comma-separated workloads timed after the main one in the same process "
+                         "(device side only), or 'none'")
+    ap.add_argument("--no-vendor-peak", action="store_true",
+                    help="do not time the vendor MXFP8 GEMM (the GEMM peak is then 2 x the BF16 burst)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle GEMM in the CPU baseline")

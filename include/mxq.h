@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define MXQ_ABI_VERSION 1
+#define MXQ_ABI_VERSION 2
 
 typedef struct CUstream_st* mxq_stream_t; /* the same type as cudaStream_t */
 
@@ -179,10 +179,21 @@ mxq_status mxq_quant_1x32_cols_grouped_fmt(const void* x, int64_t rows, int64_t 
  *        s_bwd[c][i] = t[i][c/32].
  * where t[i][j] is the E8M0 code of 32x32 tile (i, j) (tiles start at 0,0).
  * s_fwd or s_bwd may be NULL.  Shapes: n % 32 == 0, k % 32 == 0.
+ * Errors: MXQ_ERR_INVALID_ARG (null w or q, bad ld or layout, misalignment),
+ * MXQ_ERR_UNSUPPORTED_SHAPE, MXQ_ERR_UNSUPPORTED_DEVICE, MXQ_ERR_CUDA.
  */
 mxq_status mxq_quant_32x32(const void* w, int64_t n, int64_t k, int64_t ld,
                            void* q, void* s_fwd, void* s_bwd,
                            mxq_scale_layout layout, mxq_stream_t stream);
+
+/* mxq_quant_32x32 with the payload format (RFC section 3.5.2.3: the
+ * quantizer of both recipes takes dst_type E4M3 or E5M2).  With E5M2 the tile
+ * exponent is ceil(log2(amax / 57344)) and the payload float8_e5m2 (RNE,
+ * saturating to +-57344); the scales and their layouts are as for E4M3.
+ * mxq_quant_32x32 is fmt = MXQ_FP8_E4M3.  A bad fmt: MXQ_ERR_INVALID_ARG. */
+mxq_status mxq_quant_32x32_fmt(const void* w, int64_t n, int64_t k, int64_t ld,
+                               void* q, void* s_fwd, void* s_bwd,
+                               mxq_scale_layout layout, mxq_fp8_format fmt, mxq_stream_t stream);
 
 /*
  * Block-scaled FP8 GEMM with BF16 output: forward Y = X W^T, dgrad and
@@ -196,8 +207,15 @@ mxq_status mxq_quant_32x32(const void* w, int64_t n, int64_t k, int64_t ld,
  *       payload read for dgrad -- with b_s = its backward scales [N, K/32]
  *       MMA-tiled (s_bwd of mxq_quant_32x32).
  * y     bf16 [M, N], row stride ldy (ldy >= N, ldy % 8 == 0).
- * Shapes: M >= 1; N % 16 == 0 (N % 128 == 0 when b_mn_major); K % 32 == 0
- * (K % 128 == 0 when b_mn_major).
+ * layout  the layout of a_s and b_s: must be MXQ_SCALE_MMA_TILED, the layout
+ *       the tensor cores read (every quantizer of this library writes it);
+ *       MXQ_SCALE_ROWMAJOR scales are refused with MXQ_ERR_INVALID_ARG (an
+ *       unsupported configuration, as the RFC's section 3.5.2.1 refuses one).
+ * Shapes: M >= 0; N % 16 == 0 (N % 128 == 0 when b_mn_major); K % 32 == 0
+ * (K % 128 == 0 when b_mn_major).  M == 0 or N == 0 writes nothing; K == 0
+ * writes zeros.
+ * Errors: MXQ_ERR_INVALID_ARG (null pointers, ldy, misalignment, layout),
+ * MXQ_ERR_UNSUPPORTED_SHAPE, MXQ_ERR_UNSUPPORTED_DEVICE, MXQ_ERR_CUDA.
  * Operand pairing for training (contraction axis quantized in groups of 32):
  *   forward  A = X row copy,   B = W row copy           (M tokens, N out, K in)
  *   dgrad    A = dY row copy,  B = W column copy        (N = in, K = out)
@@ -206,10 +224,11 @@ mxq_status mxq_quant_32x32(const void* w, int64_t n, int64_t k, int64_t ld,
  */
 mxq_status mxq_gemm_bf16out(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
                             int64_t M, int64_t N, int64_t K, int b_mn_major,
-                            void* y, int64_t ldy, mxq_stream_t stream);
+                            void* y, int64_t ldy, mxq_scale_layout layout, mxq_stream_t stream);
 
 /* mxq_gemm_bf16out with the payload format of each operand (E4M3 or E5M2,
- * e.g. E5M2 gradients against E4M3 weights); mxq_gemm_bf16out is E4M3 x E4M3. */
+ * e.g. E5M2 gradients against E4M3 weights); scales MMA-tiled.
+ * mxq_gemm_bf16out is E4M3 x E4M3. */
 mxq_status mxq_gemm_bf16out_fmt(const void* a_q, const void* a_s, mxq_fp8_format a_fmt,
                                 const void* b_q, const void* b_s, mxq_fp8_format b_fmt,
                                 int64_t M, int64_t N, int64_t K, int b_mn_major,
@@ -337,19 +356,44 @@ mxq_status mxq_fsdp_unpack(mxq_fsdp_recipe recipe, int64_t n, int64_t k, int32_t
  *                Empty experts are allowed.  Offsets are read on the device, so
  *                the call does not synchronize with the host; offsets that break
  *                the rule above give unspecified rows (never out-of-bounds access).
- * y              bf16 [M_total, N], row stride ldy.
- * Shapes: 1 <= G <= 1024; N % 128 == 0; K % 32 == 0; M_total >= 0.
+ * y              bf16 [M_total, N], dense (row stride N).
+ * workspace      optional DEVICE scratch owned by the caller, 16-byte aligned,
+ *                of workspace_bytes >= mxq_grouped_gemm_workspace_size(G,
+ *                M_total, N, K) bytes.  With it the call first copies A's scales
+ *                into the workspace tiled per expert (mxq_scale_regroup_rows),
+ *                so that every 128-row tile starts at an expert's first row and
+ *                no tile spans two experts; without it (workspace NULL and
+ *                workspace_bytes 0) the tiles lie on the 128-row grid of all
+ *                rows and tiles at expert boundaries are computed for each
+ *                expert they touch.  The results are bit-identical either way.
+ *                The workspace must not be used by other work until this call's
+ *                work on `stream` has finished; its contents afterwards are
+ *                unspecified.
+ * Shapes: 1 <= G <= 1024; N % 128 == 0; K % 32 == 0, K > 0; M_total >= 0
+ * (M_total == 0 writes nothing).
+ * Errors: MXQ_ERR_INVALID_ARG (null pointers, misalignment, a workspace that
+ * is too small, or only one of workspace / workspace_bytes given),
+ * MXQ_ERR_UNSUPPORTED_SHAPE, MXQ_ERR_UNSUPPORTED_DEVICE, MXQ_ERR_CUDA.
  */
 mxq_status mxq_grouped_gemm(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
                             const int64_t* group_offsets, int32_t G, int64_t M_total,
-                            int64_t N, int64_t K, void* y, int64_t ldy, mxq_stream_t stream);
+                            int64_t N, int64_t K, void* y, void* workspace, size_t workspace_bytes,
+                            mxq_stream_t stream);
+
+/* Bytes of the workspace that lets mxq_grouped_gemm (and _fmt) tile A's
+ * scales per expert, for any offsets of M_total rows over G experts:
+ * (ceil(M_total/128) + G) * ceil(K/128) * 512.  N does not enter.  0 for
+ * arguments mxq_grouped_gemm would refuse.  Host only. */
+size_t mxq_grouped_gemm_workspace_size(int32_t G, int64_t M_total, int64_t N, int64_t K);
 
 /* mxq_grouped_gemm with the payload format of each operand (E4M3 or E5M2),
- * e.g. E5M2 gradients against E4M3 weights in the MoE dgrad. */
+ * e.g. E5M2 gradients against E4M3 weights in the MoE dgrad, and an output
+ * row stride ldy (ldy >= N, ldy % 8 == 0). */
 mxq_status mxq_grouped_gemm_fmt(const void* a_q, const void* a_s, mxq_fp8_format a_fmt,
                                 const void* b_q, const void* b_s, mxq_fp8_format b_fmt,
                                 const int64_t* group_offsets, int32_t G, int64_t M_total,
-                                int64_t N, int64_t K, void* y, int64_t ldy, mxq_stream_t stream);
+                                int64_t N, int64_t K, void* y, int64_t ldy, void* workspace,
+                                size_t workspace_bytes, mxq_stream_t stream);
 
 /*
  * Group-tiled A scales for mxq_grouped_gemm_group_tiled.  The rows of expert g,
@@ -418,11 +462,15 @@ mxq_status mxq_grouped_gemm_wgrad_fmt(const void* a_q, const void* a_s, mxq_fp8_
                                       int64_t capacity, int64_t M, int64_t N, void* y, int64_t ldy,
                                       mxq_stream_t stream);
 
-/* Waits for all work on the current device, then returns MXQ_ERR_TIMEOUT if
- * any kernel of this library recorded a bounded wait that ran out since the
- * last call (and clears the record), MXQ_ERR_CUDA if the device reports an
- * error, MXQ_OK otherwise. */
-mxq_status mxq_get_device_status(void);
+/* Waits for the work queued on `stream` (synchronizes the host with it), then
+ * returns MXQ_ERR_TIMEOUT if any kernel of this library on the current device
+ * recorded a bounded wait that ran out since the last call, MXQ_ERR_CUDA if
+ * the device reports an error, MXQ_OK otherwise.  The record is read and
+ * cleared in one atomic exchange on the device, so a timeout recorded by a
+ * kernel on another stream at the same moment is never lost: it is reported
+ * by this call or by the next one.  Calls from several host threads take
+ * turns. */
+mxq_status mxq_get_device_status(mxq_stream_t stream);
 
 /* Test hook for the bounded-wait machinery: launches one small kernel that
  * waits on a barrier no thread ever completes, giving up after timeout_us

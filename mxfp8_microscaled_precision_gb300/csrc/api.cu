@@ -14,6 +14,9 @@
 
 // Device status word: kernels record a timed-out bounded wait here.
 __device__ unsigned int g_mxq_device_status = 0u;
+// What the last mxq_get_device_status found in the status word (read and
+// cleared in one atomic exchange on the device).
+__device__ unsigned int g_mxq_status_taken = 0u;
 
 namespace mxq {
 namespace {
@@ -22,6 +25,12 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 bool g_have[kMaxDevices] = {};
 DeviceInfo g_info[kMaxDevices];
+std::mutex g_status_mu;   // one mxq_get_device_status at a time per process
+
+// Moves the status word into g_mxq_status_taken and clears it, atomically: a
+// timeout recorded by a kernel still running elsewhere is either taken here
+// or stays for the next call.
+__global__ void status_take_kernel(unsigned int* status) { g_mxq_status_taken = atomicExch(status, 0u); }
 
 }  // namespace
 
@@ -30,27 +39,32 @@ cudaError_t current_device_info(DeviceInfo* info) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_have[dev]) {
-        DeviceInfo d;
-        d.device = dev;
-        if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
-            return e;
-        int optin = 0;
-        if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
-            return e;
-        d.smem_optin = static_cast<size_t>(optin);
-        if (d.cc_major == 10 && d.cc_minor == 3) {
-            void* p = nullptr;
-            if ((e = cudaGetSymbolAddress(&p, g_mxq_device_status)) != cudaSuccess) return e;
-            d.status = static_cast<unsigned int*>(p);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_have[dev]) {
+            DeviceInfo d;
+            d.device = dev;
+            if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+                (e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+                (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+                return e;
+            int optin = 0;
+            if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+                return e;
+            d.smem_optin = static_cast<size_t>(optin);
+            g_info[dev] = d;
+            g_have[dev] = true;
         }
-        g_info[dev] = d;
-        g_have[dev] = true;
+        *info = g_info[dev];
     }
-    *info = g_info[dev];
+    // The status word's address belongs to the current context, which a device
+    // reset replaces: it is looked up on every call, never cached.
+    info->status = nullptr;
+    if (info->cc_major == 10 && info->cc_minor == 3) {
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_mxq_device_status)) != cudaSuccess) return e;
+        info->status = static_cast<unsigned int*>(p);
+    }
     return cudaSuccess;
 }
 
@@ -107,12 +121,12 @@ cudaError_t zero_fill(void* y, int64_t ldy, int64_t M, int64_t N, mxq_stream_t s
                              static_cast<size_t>(M), reinterpret_cast<cudaStream_t>(stream));
 }
 
-// Argument checks and launch of the grouped-rows GEMMs (a_bands_cap 0: A scales
-// MMA-tiled over all rows; > 0: group-tiled).
-mxq_status grouped_rows_gemm(const void* a_q, const void* a_s, mxq_fp8_format a_fmt, const void* b_q,
-                             const void* b_s, mxq_fp8_format b_fmt, const int64_t* group_offsets, int32_t G,
-                             int64_t M_total, int64_t N, int64_t K, int64_t a_bands_cap, void* y, int64_t ldy,
-                             mxq_stream_t stream) {
+// Argument checks of the grouped-rows GEMMs; MXQ_OK with *launch false when
+// there is nothing to compute.
+mxq_status check_grouped_rows(const void* a_q, const void* a_s, mxq_fp8_format a_fmt, const void* b_q,
+                              const void* b_s, mxq_fp8_format b_fmt, const int64_t* group_offsets, int32_t G,
+                              int64_t M_total, int64_t N, int64_t K, const void* y, int64_t ldy, bool* launch) {
+    *launch = false;
     if ((a_fmt != MXQ_FP8_E4M3 && a_fmt != MXQ_FP8_E5M2) || (b_fmt != MXQ_FP8_E4M3 && b_fmt != MXQ_FP8_E5M2))
         return MXQ_ERR_INVALID_ARG;
     if (G < 1 || M_total < 0 || N < 0 || K < 0) return MXQ_ERR_INVALID_ARG;
@@ -127,12 +141,34 @@ mxq_status grouped_rows_gemm(const void* a_q, const void* a_s, mxq_fp8_format a_
     if (!aligned16(a_q) || !aligned16(a_s) || !aligned16(b_q) || !aligned16(b_s) || !aligned16(y) ||
         (reinterpret_cast<uintptr_t>(group_offsets) & 7u) != 0)
         return MXQ_ERR_INVALID_ARG;
+    *launch = true;
+    return MXQ_OK;
+}
+
+// Argument checks and launch of the grouped-rows GEMMs (a_bands_cap 0: A scales
+// MMA-tiled over all rows; > 0: group-tiled).
+mxq_status grouped_rows_gemm(const void* a_q, const void* a_s, mxq_fp8_format a_fmt, const void* b_q,
+                             const void* b_s, mxq_fp8_format b_fmt, const int64_t* group_offsets, int32_t G,
+                             int64_t M_total, int64_t N, int64_t K, int64_t a_bands_cap, void* y, int64_t ldy,
+                             mxq_stream_t stream) {
+    bool launch = false;
+    mxq_status st = check_grouped_rows(a_q, a_s, a_fmt, b_q, b_s, b_fmt, group_offsets, G, M_total, N, K, y, ldy,
+                                       &launch);
+    if (st != MXQ_OK || !launch) return st;
     mxq::DeviceInfo dev;
-    mxq_status st = device_ok(&dev);
+    st = device_ok(&dev);
     if (st != MXQ_OK) return st;
     return from_cuda(mxq::launch_grouped_gemm(dev, a_q, a_s, b_q, b_s, group_offsets, G, M_total, N, K, a_bands_cap,
                                               y, ldy, static_cast<int>(a_fmt), static_cast<int>(b_fmt),
                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Bands of a group-tiled A-scale buffer that hold any routing of M_total rows
+// over G experts, and its bytes.
+int64_t group_tiled_bands(int64_t M_total, int32_t G) { return (M_total + 127) / 128 + G; }
+
+int64_t group_tiled_bytes(int64_t M_total, int32_t G, int64_t K) {
+    return group_tiled_bands(M_total, G) * ((K / 32 + 3) / 4) * 512;
 }
 
 }  // namespace
@@ -233,7 +269,13 @@ mxq_status mxq_quant_1x32_cols_grouped_fmt(const void* x, int64_t rows, int64_t 
 
 mxq_status mxq_quant_32x32(const void* w, int64_t n, int64_t k, int64_t ld, void* q, void* s_fwd,
                            void* s_bwd, mxq_scale_layout layout, mxq_stream_t stream) {
+    return mxq_quant_32x32_fmt(w, n, k, ld, q, s_fwd, s_bwd, layout, MXQ_FP8_E4M3, stream);
+}
+
+mxq_status mxq_quant_32x32_fmt(const void* w, int64_t n, int64_t k, int64_t ld, void* q, void* s_fwd,
+                               void* s_bwd, mxq_scale_layout layout, mxq_fp8_format fmt, mxq_stream_t stream) {
     if (layout != MXQ_SCALE_ROWMAJOR && layout != MXQ_SCALE_MMA_TILED) return MXQ_ERR_INVALID_ARG;
+    if (fmt != MXQ_FP8_E4M3 && fmt != MXQ_FP8_E5M2) return MXQ_ERR_INVALID_ARG;
     if (n < 0 || k < 0) return MXQ_ERR_INVALID_ARG;
     if (n % 32 != 0 || k % 32 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
     if (n == 0 || k == 0) return MXQ_OK;
@@ -245,13 +287,16 @@ mxq_status mxq_quant_32x32(const void* w, int64_t n, int64_t k, int64_t ld, void
     mxq_status st = device_ok(&dev);
     if (st != MXQ_OK) return st;
     return from_cuda(mxq::launch_quant_32x32(dev, w, n, k, ld, q, s_fwd, s_bwd,
-                                             layout == MXQ_SCALE_MMA_TILED,
+                                             layout == MXQ_SCALE_MMA_TILED, static_cast<int>(fmt),
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mxq_status mxq_gemm_bf16out(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
                             int64_t M, int64_t N, int64_t K, int b_mn_major, void* y, int64_t ldy,
-                            mxq_stream_t stream) {
+                            mxq_scale_layout layout, mxq_stream_t stream) {
+    // The tensor cores read only MMA-tiled scales; the row-major layout is
+    // refused before anything else (an unsupported configuration).
+    if (layout != MXQ_SCALE_MMA_TILED) return MXQ_ERR_INVALID_ARG;
     return mxq_gemm_bf16out_fmt(a_q, a_s, MXQ_FP8_E4M3, b_q, b_s, MXQ_FP8_E4M3, M, N, K, b_mn_major, y, ldy,
                                 stream);
 }
@@ -352,17 +397,48 @@ mxq_status mxq_fsdp_unpack(mxq_fsdp_recipe recipe, int64_t n, int64_t k, int32_t
                                              q_bwd, s_bwd, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t mxq_grouped_gemm_workspace_size(int32_t G, int64_t M_total, int64_t N, int64_t K) {
+    if (G < 1 || G > 1024 || M_total < 0 || N < 0 || K <= 0 || K % 32 != 0 || M_total > (int64_t(1) << 31) - 128 ||
+        K > (int64_t(1) << 31) - 128)
+        return 0;
+    return static_cast<size_t>(group_tiled_bytes(M_total, G, K));
+}
+
 mxq_status mxq_grouped_gemm(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
                             const int64_t* group_offsets, int32_t G, int64_t M_total, int64_t N,
-                            int64_t K, void* y, int64_t ldy, mxq_stream_t stream) {
+                            int64_t K, void* y, void* workspace, size_t workspace_bytes, mxq_stream_t stream) {
     return mxq_grouped_gemm_fmt(a_q, a_s, MXQ_FP8_E4M3, b_q, b_s, MXQ_FP8_E4M3, group_offsets, G, M_total, N, K, y,
-                                ldy, stream);
+                                N, workspace, workspace_bytes, stream);
 }
 
 mxq_status mxq_grouped_gemm_fmt(const void* a_q, const void* a_s, mxq_fp8_format a_fmt, const void* b_q,
                                 const void* b_s, mxq_fp8_format b_fmt, const int64_t* group_offsets, int32_t G,
-                                int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy, mxq_stream_t stream) {
-    return grouped_rows_gemm(a_q, a_s, a_fmt, b_q, b_s, b_fmt, group_offsets, G, M_total, N, K, 0, y, ldy, stream);
+                                int64_t M_total, int64_t N, int64_t K, void* y, int64_t ldy, void* workspace,
+                                size_t workspace_bytes, mxq_stream_t stream) {
+    if ((workspace == nullptr) != (workspace_bytes == 0)) return MXQ_ERR_INVALID_ARG;
+    bool launch = false;
+    mxq_status st = check_grouped_rows(a_q, a_s, a_fmt, b_q, b_s, b_fmt, group_offsets, G, M_total, N, K, y, ldy,
+                                       &launch);
+    if (st != MXQ_OK) return st;
+    if (workspace != nullptr &&
+        (!aligned16(workspace) || workspace_bytes < static_cast<size_t>(group_tiled_bytes(M_total, G, K))))
+        return MXQ_ERR_INVALID_ARG;
+    if (!launch) return MXQ_OK;
+    mxq::DeviceInfo dev;
+    st = device_ok(&dev);
+    if (st != MXQ_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int64_t bands = 0;
+    const void* sa = a_s;
+    if (workspace != nullptr) {   // A scales group-tiled in the workspace, then tiles from each expert's first row
+        bands = group_tiled_bands(M_total, G);
+        const cudaError_t e = mxq::launch_scale_regroup_rows(dev, a_s, M_total, K, group_offsets, G, bands,
+                                                             workspace, s);
+        if (e != cudaSuccess) return from_cuda(e);
+        sa = workspace;
+    }
+    return from_cuda(mxq::launch_grouped_gemm(dev, a_q, sa, b_q, b_s, group_offsets, G, M_total, N, K, bands, y, ldy,
+                                              static_cast<int>(a_fmt), static_cast<int>(b_fmt), s));
 }
 
 mxq_status mxq_grouped_gemm_group_tiled(const void* a_q, const void* a_s, mxq_fp8_format a_fmt, const void* b_q,
@@ -433,19 +509,20 @@ mxq_status mxq_grouped_gemm_wgrad_fmt(const void* a_q, const void* a_s, mxq_fp8_
                                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
-mxq_status mxq_get_device_status(void) {
+mxq_status mxq_get_device_status(mxq_stream_t stream) {
     mxq::DeviceInfo dev;
     mxq_status st = device_ok(&dev);
     if (st != MXQ_OK) return st;
-    if (cudaDeviceSynchronize() != cudaSuccess) return MXQ_ERR_CUDA;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(mxq::g_status_mu);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MXQ_ERR_CUDA;
+    mxq::status_take_kernel<<<1, 1, 0, s>>>(dev.status);
+    if (cudaGetLastError() != cudaSuccess) return MXQ_ERR_CUDA;
     unsigned int v = 0u;
-    if (cudaMemcpyFromSymbol(&v, g_mxq_device_status, sizeof v) != cudaSuccess) return MXQ_ERR_CUDA;
-    if (v != 0u) {
-        const unsigned int zero = 0u;
-        if (cudaMemcpyToSymbol(g_mxq_device_status, &zero, sizeof zero) != cudaSuccess) return MXQ_ERR_CUDA;
-        return MXQ_ERR_TIMEOUT;
-    }
-    return MXQ_OK;
+    if (cudaMemcpyFromSymbolAsync(&v, g_mxq_status_taken, sizeof v, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return MXQ_ERR_CUDA;
+    return v != 0u ? MXQ_ERR_TIMEOUT : MXQ_OK;
 }
 
 mxq_status mxq_debug_wait_timeout(uint32_t timeout_us, mxq_stream_t stream) {

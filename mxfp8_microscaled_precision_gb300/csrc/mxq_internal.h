@@ -49,8 +49,9 @@ cudaError_t launch_quant_cols_grouped(const DeviceInfo& dev, const void* x, int6
                                       int64_t capacity, void* q_col, void* s_col, bool tiled, int fmt,
                                       cudaStream_t stream);
 
+// 32x32 block quantization (fmt: 0 = E4M3, 1 = E5M2).
 cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, int64_t k,
-                               int64_t ld, void* q, void* s_fwd, void* s_bwd, bool tiled,
+                               int64_t ld, void* q, void* s_fwd, void* s_bwd, bool tiled, int fmt,
                                cudaStream_t stream);
 
 // One dense GEMM y = A B^T of a multi-GEMM launch (fields as in mxq_gemm_bf16out_fmt).

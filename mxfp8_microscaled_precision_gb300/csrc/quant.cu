@@ -491,8 +491,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_grouped_ring_
 }
 
 // ---------------------------------------------------------------------------------
-// 32x32 block quantization of w [n, k]: one 128x128 tile (16 blocks) per CTA.
-template <bool kTiled>
+// 32x32 block quantization of w [n, k]: one 128x128 tile (16 blocks) per CTA;
+// payload E4M3 (kFmt 0) or E5M2 (kFmt 1).
+template <bool kTiled, int kFmt>
 __global__ void __launch_bounds__(kThreads) quant_32x32_kernel(const uint16_t* __restrict__ w, int64_t n,
                                                                int64_t k, int64_t ld, uint8_t* __restrict__ q,
                                                                uint8_t* __restrict__ s_fwd,
@@ -537,9 +538,9 @@ __global__ void __launch_bounds__(kThreads) quant_32x32_kernel(const uint16_t* _
             code = 0xFF;
             out = nan8(v[j]);
         } else {
-            const int e = rceil_exponent(m);
+            const int e = rceil_exponent<kFmt>(m);
             code = static_cast<uint8_t>(e + 127);
-            out = quant8(v[j], pow2_neg_bf16(e) * 0x10001u);
+            out = quant8<kFmt>(v[j], pow2_neg_bf16(e) * 0x10001u);
         }
         if (valid) *reinterpret_cast<uint2*>(qp + j * 16 * k) = out;
         if (sp && (chunk & 3) == 0 && (valid || kTiled)) {
@@ -558,7 +559,7 @@ __global__ void __launch_bounds__(kThreads) quant_32x32_kernel(const uint16_t* _
             const bool valid = c < k && gi < ngroups;
             const uint32_t m = blk_amax[b][cl >> 5];
             uint8_t code = 0;
-            if (valid) code = (m >= 0x7F80u) ? 0xFF : static_cast<uint8_t>(rceil_exponent(m) + 127);
+            if (valid) code = (m >= 0x7F80u) ? 0xFF : static_cast<uint8_t>(rceil_exponent<kFmt>(m) + 127);
             if (valid || kTiled) store_scale(s_bwd, c, gi, ngroups, kTiled, code);
         }
     }
@@ -811,7 +812,7 @@ cudaError_t launch_scale_regroup_rows(const DeviceInfo& dev, const void* s_tiled
 }
 
 cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, int64_t k, int64_t ld,
-                               void* q, void* s_fwd, void* s_bwd, bool tiled, cudaStream_t stream) {
+                               void* q, void* s_fwd, void* s_bwd, bool tiled, int fmt, cudaStream_t stream) {
     (void)dev;
     const int64_t tiles_c = (k + kTile - 1) / kTile;
     const int64_t n_tiles = tiles_c * ((n + kTile - 1) / kTile);
@@ -819,10 +820,9 @@ cudaError_t launch_quant_32x32(const DeviceInfo& dev, const void* w, int64_t n, 
     auto qp = static_cast<uint8_t*>(q);
     auto sf = static_cast<uint8_t*>(s_fwd);
     auto sb = static_cast<uint8_t*>(s_bwd);
-    if (tiled)
-        quant_32x32_kernel<true><<<static_cast<unsigned>(n_tiles), kThreads, 0, stream>>>(wp, n, k, ld, qp, sf, sb, tiles_c);
-    else
-        quant_32x32_kernel<false><<<static_cast<unsigned>(n_tiles), kThreads, 0, stream>>>(wp, n, k, ld, qp, sf, sb, tiles_c);
+    auto kern = tiled ? (fmt == 0 ? quant_32x32_kernel<true, 0> : quant_32x32_kernel<true, 1>)
+                      : (fmt == 0 ? quant_32x32_kernel<false, 0> : quant_32x32_kernel<false, 1>);
+    kern<<<static_cast<unsigned>(n_tiles), kThreads, 0, stream>>>(wp, n, k, ld, qp, sf, sb, tiles_c);
     return cudaGetLastError();
 }
 

@@ -71,18 +71,21 @@ def lib() -> ctypes.CDLL:
         L.mxq_gemm_bf16out_multi.argtypes = [ctypes.POINTER(GemmDesc), I32, S, P]
         L.mxq_quant_1x32_cols_grouped.argtypes = [P, I64, I64, I64, P, I32, I64, P, P, S, P]
         L.mxq_quant_1x32_cols_grouped_fmt.argtypes = [P, I64, I64, I64, P, I32, I64, P, P, S, S, P]
-        L.mxq_grouped_gemm_fmt.argtypes = [P, P, S, P, P, S, P, I32, I64, I64, I64, P, I64, P]
+        L.mxq_grouped_gemm_fmt.argtypes = [P, P, S, P, P, S, P, I32, I64, I64, I64, P, I64, P, SZ, P]
+        L.mxq_grouped_gemm_workspace_size.argtypes = [I32, I64, I64, I64]
+        L.mxq_grouped_gemm_workspace_size.restype = SZ
         L.mxq_grouped_gemm_group_tiled.argtypes = [P, P, S, P, P, S, P, I32, I64, I64, I64, I64, P, I64, P]
         L.mxq_scale_regroup_rows.argtypes = [P, I64, I64, P, I32, I64, P, P]
         L.mxq_grouped_gemm_wgrad_fmt.argtypes = [P, P, S, P, P, S, P, I32, I64, I64, I64, I64, P, I64, P]
         L.mxq_grouped_gemm_wgrad.argtypes = [P, P, P, P, P, I32, I64, I64, I64, I64, P, I64, P]
         L.mxq_quant_32x32.argtypes = [P, I64, I64, I64, P, P, P, S, P]
-        L.mxq_gemm_bf16out.argtypes = [P, P, P, P, I64, I64, I64, S, P, I64, P]
-        L.mxq_grouped_gemm.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, I64, P]
+        L.mxq_quant_32x32_fmt.argtypes = [P, I64, I64, I64, P, P, P, S, S, P]
+        L.mxq_gemm_bf16out.argtypes = [P, P, P, P, I64, I64, I64, S, P, I64, S, P]
+        L.mxq_grouped_gemm.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, P, SZ, P]
         L.mxq_gemm_mxfp8out.argtypes = [P, P, P, P, I64, I64, I64, S, P, I64, P, P, P]
         L.mxq_fsdp_payload_layout.argtypes = [S, I64, I64, I32, ctypes.POINTER(I64), ctypes.POINTER(I64)]
         L.mxq_fsdp_unpack.argtypes = [S, I64, I64, I32, P, P, P, P, P, P]
-        L.mxq_get_device_status.argtypes = []
+        L.mxq_get_device_status.argtypes = [P]
         L.mxq_debug_wait_timeout.argtypes = [U32, P]
         for f in ("mxq_quant_1x32_dual", "mxq_quant_32x32", "mxq_gemm_bf16out",
                   "mxq_grouped_gemm", "mxq_get_device_status", "mxq_debug_wait_timeout",
@@ -90,7 +93,7 @@ def lib() -> ctypes.CDLL:
                   "mxq_grouped_gemm_wgrad", "mxq_gemm_bf16out_fmt", "mxq_gemm_mxfp8out",
                   "mxq_fsdp_payload_layout", "mxq_fsdp_unpack", "mxq_quant_1x32_cols_grouped_fmt",
                   "mxq_grouped_gemm_fmt", "mxq_grouped_gemm_wgrad_fmt", "mxq_gemm_bf16out_multi",
-                  "mxq_grouped_gemm_group_tiled", "mxq_scale_regroup_rows"):
+                  "mxq_grouped_gemm_group_tiled", "mxq_scale_regroup_rows", "mxq_quant_32x32_fmt"):
             getattr(L, f).restype = S
         _lib = L
         return L
@@ -230,10 +233,10 @@ def grouped_gemm_wgrad(a_q, a_s, b_q, b_s, offsets: torch.Tensor, M_total: int, 
     return out
 
 
-def quant_32x32(w: torch.Tensor, layout="tiled", out=None):
-    """32x32 block quantization of a bf16 weight [n, k].  Returns
-    (q [n,k], s_fwd ([n,k/32] scales), s_bwd ([k,n/32] scales)); `out` may
-    supply the three output tensors."""
+def quant_32x32(w: torch.Tensor, layout="tiled", out=None, fmt="e4m3"):
+    """32x32 block quantization of a bf16 weight [n, k] with payload format fmt
+    ("e4m3" or "e5m2").  Returns (q [n,k], s_fwd ([n,k/32] scales), s_bwd
+    ([k,n/32] scales)); `out` may supply the three output tensors."""
     if w.dtype != torch.bfloat16 or w.dim() != 2 or not w.is_cuda or w.stride(1) != 1:
         raise ValueError("w must be a 2-D bfloat16 CUDA tensor with unit last stride")
     n, k = w.shape
@@ -244,8 +247,8 @@ def quant_32x32(w: torch.Tensor, layout="tiled", out=None):
         q = torch.empty((n, k), dtype=torch.uint8, device=dev)
         s_fwd = _scale_tensor(n, k, layout, dev)
         s_bwd = _scale_tensor(k, n, layout, dev)
-    _check(lib().mxq_quant_32x32(_ptr(w), n, k, w.stride(0), _ptr(q), _ptr(s_fwd), _ptr(s_bwd),
-                                 _layout(layout), _stream()), "mxq_quant_32x32")
+    _check(lib().mxq_quant_32x32_fmt(_ptr(w), n, k, w.stride(0), _ptr(q), _ptr(s_fwd), _ptr(s_bwd),
+                                     _layout(layout), _fmt(fmt), _stream()), "mxq_quant_32x32_fmt")
     return q, s_fwd, s_bwd
 
 
@@ -254,7 +257,7 @@ def gemm(a_q, a_s, b_q, b_s, M: int, N: int, K: int, b_mn_major: bool = False, o
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=a_q.device)
     _check(lib().mxq_gemm_bf16out(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K,
-                                  1 if b_mn_major else 0, _ptr(out), out.stride(0), _stream()),
+                                  1 if b_mn_major else 0, _ptr(out), out.stride(0), TILED, _stream()),
            "mxq_gemm_bf16out")
     return out
 
@@ -377,19 +380,33 @@ def fsdp_unpack(recipe, gathered: torch.Tensor, n: int, k: int, world: int, out=
     return out
 
 
+def grouped_gemm_workspace_size(G: int, M_total: int, N: int, K: int) -> int:
+    """Bytes of the optional grouped-GEMM workspace (see mxq_grouped_gemm_workspace_size)."""
+    return int(lib().mxq_grouped_gemm_workspace_size(G, M_total, N, K))
+
+
 def grouped_gemm(a_q, a_s, b_q, b_s, offsets: torch.Tensor, N: int, K: int, out=None, a_fmt="e4m3",
-                 b_fmt="e4m3"):
+                 b_fmt="e4m3", workspace=None):
     """Per-expert y[r] = deq(A)[r] deq(B_g)^T for rows of expert g
-    (offsets: int64 CUDA tensor [G+1]).  Returns y [M_total, N] bf16."""
+    (offsets: int64 CUDA tensor [G+1]).  Returns y [M_total, N] bf16.
+    workspace: None (row tiles on the 128-row grid), a uint8 CUDA tensor of at
+    least grouped_gemm_workspace_size bytes, or "alloc" to have one allocated
+    here; with a workspace the row tiles start at each expert's first row."""
     if offsets.dtype != torch.int64 or not offsets.is_cuda:
         raise ValueError("offsets must be an int64 CUDA tensor")
     G = offsets.numel() - 1
     M_total = a_q.shape[0]
     if out is None:
         out = torch.empty((M_total, N), dtype=torch.bfloat16, device=a_q.device)
+    if isinstance(workspace, str):
+        if workspace != "alloc":
+            raise ValueError(f"workspace must be None, a tensor or 'alloc', not {workspace!r}")
+        workspace = torch.empty(max(1, grouped_gemm_workspace_size(G, M_total, N, K)), dtype=torch.uint8,
+                                device=a_q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().mxq_grouped_gemm_fmt(_ptr(a_q), _ptr(a_s), _fmt(a_fmt), _ptr(b_q), _ptr(b_s), _fmt(b_fmt),
-                                      _ptr(offsets), G, M_total, N, K, _ptr(out), out.stride(0), _stream()),
-           "mxq_grouped_gemm_fmt")
+                                      _ptr(offsets), G, M_total, N, K, _ptr(out), out.stride(0), _ptr(workspace),
+                                      ws_bytes, _stream()), "mxq_grouped_gemm_fmt")
     return out
 
 
@@ -433,8 +450,9 @@ def grouped_gemm_group_tiled(a_q, a_s_grouped, b_q, b_s, offsets: torch.Tensor, 
 
 
 def get_device_status() -> int:
-    """Synchronizes the device; returns 0 or the recorded status (e.g. 5 = timeout)."""
-    return int(lib().mxq_get_device_status())
+    """Synchronizes with the current stream; returns 0 or the recorded status
+    (e.g. 5 = timeout), which the call clears."""
+    return int(lib().mxq_get_device_status(_stream()))
 
 
 def debug_wait_timeout(timeout_us: int) -> int:

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_and_strings(L):
-    assert L.mxq_abi_version() == 1
+    assert L.mxq_abi_version() == 2
     for s in range(6):
         assert L.mxq_status_string(s)
     assert L.mxq_scale_bytes(256, 512, 0) == 256 * 16
@@ -70,24 +70,54 @@ def test_quant_argument_errors(L):
     assert b(FAKE, 48, 64, 64, FAKE, FAKE, FAKE, 1, None) == 2            # n % 32
     assert b(FAKE, 64, 40, 40, FAKE, FAKE, FAKE, 1, None) == 2            # k % 32 (block size)
     assert b(None, 64, 64, 64, FAKE, FAKE, FAKE, 1, None) == 1
+    bf = L.mxq_quant_32x32_fmt
+    assert bf(FAKE, 64, 64, 64, FAKE, FAKE, FAKE, 1, 2, None) == 1        # bad format
+    assert bf(FAKE, 64, 40, 40, FAKE, FAKE, FAKE, 1, 1, None) == 2        # k % 32 (E5M2 too)
+    assert bf(FAKE, 0, 64, 64, FAKE, FAKE, FAKE, 1, 1, None) == 0         # empty
 
 
 def test_gemm_argument_errors(L):
     g = L.mxq_gemm_bf16out
-    assert g(FAKE, FAKE, FAKE, FAKE, 64, 128, 48, 0, FAKE, 128, None) == 2   # K % 32
-    assert g(FAKE, FAKE, FAKE, FAKE, 64, 120, 64, 0, FAKE, 120, None) == 2   # N % 16
-    assert g(FAKE, FAKE, FAKE, FAKE, 64, 144, 64, 1, FAKE, 144, None) == 2   # MN-major N % 128
-    assert g(FAKE, FAKE, FAKE, FAKE, 64, 128, 64, 2, FAKE, 128, None) == 1   # bad flag
-    assert g(FAKE, FAKE, FAKE, FAKE, 64, 128, 64, 0, FAKE, 100, None) == 1   # ldy < N
-    assert g(None, FAKE, FAKE, FAKE, 64, 128, 64, 0, FAKE, 128, None) == 1
-    assert g(FAKE, FAKE, ODD, FAKE, 64, 128, 64, 0, FAKE, 128, None) == 1
-    assert g(FAKE, FAKE, FAKE, FAKE, 0, 128, 64, 0, FAKE, 128, None) == 0    # empty
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 128, 48, 0, FAKE, 128, 1, None) == 2   # K % 32
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 120, 64, 0, FAKE, 120, 1, None) == 2   # N % 16
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 144, 64, 1, FAKE, 144, 1, None) == 2   # MN-major N % 128
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 128, 64, 2, FAKE, 128, 1, None) == 1   # bad flag
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 128, 64, 0, FAKE, 100, 1, None) == 1   # ldy < N
+    assert g(None, FAKE, FAKE, FAKE, 64, 128, 64, 0, FAKE, 128, 1, None) == 1
+    assert g(FAKE, FAKE, ODD, FAKE, 64, 128, 64, 0, FAKE, 128, 1, None) == 1
+    assert g(FAKE, FAKE, FAKE, FAKE, 0, 128, 64, 0, FAKE, 128, 1, None) == 0    # empty
+    # the tensor cores read MMA-tiled scales only: row-major scales are refused
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 128, 64, 0, FAKE, 128, 0, None) == 1
+    assert g(FAKE, FAKE, FAKE, FAKE, 0, 128, 64, 0, FAKE, 128, 0, None) == 1    # even with nothing to do
+    assert g(FAKE, FAKE, FAKE, FAKE, 64, 128, 64, 0, FAKE, 128, 9, None) == 1   # unknown layout
     gg = L.mxq_grouped_gemm
-    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 64, 128, 64, FAKE, 128, None) == 1     # G < 1
-    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 2000, 64, 128, 64, FAKE, 128, None) == 2  # G too big
-    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 192, 64, FAKE, 192, None) == 2     # N % 128
-    assert gg(FAKE, FAKE, FAKE, FAKE, None, 4, 64, 128, 64, FAKE, 128, None) == 1     # no offsets
-    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 0, 128, 64, FAKE, 128, None) == 0      # no rows
+    W = ctypes.c_size_t
+    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 64, 128, 64, FAKE, None, W(0), None) == 1     # G < 1
+    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 2000, 64, 128, 64, FAKE, None, W(0), None) == 2  # G too big
+    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 192, 64, FAKE, None, W(0), None) == 2     # N % 128
+    assert gg(FAKE, FAKE, FAKE, FAKE, None, 4, 64, 128, 64, FAKE, None, W(0), None) == 1     # no offsets
+    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 0, 128, 64, FAKE, None, W(0), None) == 0      # no rows
+    need = L.mxq_grouped_gemm_workspace_size(4, 300, 128, 64)
+    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 300, 128, 64, FAKE, FAKE, W(need - 1), None) == 1  # too small
+    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 300, 128, 64, FAKE, None, W(need), None) == 1      # bytes, no pointer
+    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 300, 128, 64, FAKE, FAKE, W(0), None) == 1         # pointer, no bytes
+    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 300, 128, 64, FAKE, ODD, W(need), None) == 1       # misaligned
+    assert gg(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 0, 128, 64, FAKE, FAKE, W(need), None) == 0        # no rows
+
+
+def test_grouped_gemm_workspace_size(L):
+    """The workspace holds A's scales tiled per expert for any routing:
+    (ceil(M_total/128) + G) bands of ceil(K/128) 512-byte atoms."""
+    ws = L.mxq_grouped_gemm_workspace_size
+    assert ws(128, 131072, 4096, 4096) == (1024 + 128) * 32 * 512
+    assert ws(128, 131072, 4096, 2048) == (1024 + 128) * 16 * 512
+    assert ws(3, 300, 256, 96) == (3 + 3) * 1 * 512          # K tail: the atom is padded
+    assert ws(1, 0, 128, 64) == 1 * 1 * 512                   # no rows still has G bands
+    assert ws(4, 300, 256, 48) == 0                           # K % 32
+    assert ws(0, 300, 256, 64) == 0 and ws(2000, 300, 256, 64) == 0
+    assert ws(4, -1, 256, 64) == 0 and ws(4, 300, 256, 0) == 0
+    from mxfp8_microscaled_precision_gb300 import mxq
+    assert mxq.grouped_gemm_workspace_size(16, 16384, 4096, 4096) == (128 + 16) * 32 * 512
 
 
 def test_moe_backward_argument_errors(L):
@@ -113,10 +143,12 @@ def test_moe_backward_argument_errors(L):
     assert cf(FAKE, 300, 48, 48, FAKE, 4, 1024, FAKE, FAKE, 1, 1, None) == 2   # cols % 32
     assert cf(FAKE, 0, 64, 64, FAKE, 4, 1024, FAKE, FAKE, 1, 1, None) == 0     # no rows
     gf = L.mxq_grouped_gemm_fmt
-    assert gf(FAKE, FAKE, 5, FAKE, FAKE, 0, FAKE, 4, 64, 128, 64, FAKE, 128, None) == 1   # bad a format
-    assert gf(FAKE, FAKE, 1, FAKE, FAKE, 3, FAKE, 4, 64, 128, 64, FAKE, 128, None) == 1   # bad b format
-    assert gf(FAKE, FAKE, 1, FAKE, FAKE, 0, FAKE, 4, 64, 192, 64, FAKE, 192, None) == 2   # N % 128
-    assert gf(FAKE, FAKE, 1, FAKE, FAKE, 0, FAKE, 4, 0, 128, 64, FAKE, 128, None) == 0    # no rows
+    Z = ctypes.c_size_t(0)
+    assert gf(FAKE, FAKE, 5, FAKE, FAKE, 0, FAKE, 4, 64, 128, 64, FAKE, 128, None, Z, None) == 1   # bad a format
+    assert gf(FAKE, FAKE, 1, FAKE, FAKE, 3, FAKE, 4, 64, 128, 64, FAKE, 128, None, Z, None) == 1   # bad b format
+    assert gf(FAKE, FAKE, 1, FAKE, FAKE, 0, FAKE, 4, 64, 192, 64, FAKE, 192, None, Z, None) == 2   # N % 128
+    assert gf(FAKE, FAKE, 1, FAKE, FAKE, 0, FAKE, 4, 0, 128, 64, FAKE, 128, None, Z, None) == 0    # no rows
+    assert gf(FAKE, FAKE, 1, FAKE, FAKE, 0, FAKE, 4, 64, 128, 64, FAKE, 120, None, Z, None) == 1   # ldy < N
     wf = L.mxq_grouped_gemm_wgrad_fmt
     assert wf(FAKE, FAKE, 9, FAKE, FAKE, 0, FAKE, 4, 300, 1024, 128, 128, FAKE, 128, None) == 1  # bad format
     assert wf(FAKE, FAKE, 1, FAKE, FAKE, 0, FAKE, 4, 300, 1024, 128, 120, FAKE, 120, None) == 2  # N % 16

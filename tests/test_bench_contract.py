@@ -24,8 +24,27 @@ def test_reference_arm_json_line():
     assert d["value"] > 0 and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    assert cb["cpu_model"]
+    # ms_per_step is the measured time of what ran: the timed steps fit in the run's own wall time
+    assert d["steps"] * d["ms_per_step"] <= d["wall_s_all_steps"] * 1e3 * 1.01
+    assert d["extrapolated_ms_per_full_step"] > 0
     e = d["e2e"]
     assert e["value"] == d["value"] and e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_default_workload_is_the_largest_single_gpu_config():
+    import bench
+    ap_default = bench.DEFAULT_WORKLOAD
+    assert ap_default == "sweep_16384" and bench.DEFAULT_EXTRA == "moe_grouped"
+
+
+def test_gemm_peak_is_not_below_the_vendor_rate():
+    import bench
+    peaks = {"bf16_tflops": 1900.0, "source": "measured"}
+    p, src = bench.gemm_peak_of(peaks, {"8192x4096x4096": 3650.0, "16384x8192x8192": 4190.0})
+    assert p == 4190.0 and "vendor" in src
+    p, src = bench.gemm_peak_of(peaks, {"error": "no e8m0"})
+    assert p == 3800.0 and "bf16" in src
 
 
 def test_rejects_too_few_warmup_steps():

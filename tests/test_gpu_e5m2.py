@@ -1,7 +1,8 @@
 """GPU parity of the E5M2 destination type (MindSpeed RFC section 3.5.2.3:
-dst_type E4M3 or E5M2): 1x32 row / column quantization bit-exact against the
-oracle, and block-scaled GEMMs with E5M2 x E5M2 and mixed E5M2 x E4M3
-operands within the GEMM tolerance."""
+dst_type E4M3 or E5M2 for the quantizer of both recipes): 1x32 row / column
+and 32x32 block quantization bit-exact against the oracle, and block-scaled
+GEMMs with E5M2 x E5M2 and mixed E5M2 x E4M3 operands (including the 32x32
+payload read forward and N-major) within the GEMM tolerance."""
 import numpy as np
 import pytest
 import torch
@@ -128,3 +129,67 @@ def test_e5m2_moe_wgrad(sizes, N, K):
         a = oracle.dequant_rows_fmt(np.ascontiguousarray(oaq[:, sl]), np.ascontiguousarray(oas[:, ss]), 1)
         b = oracle.dequant_rows(np.ascontiguousarray(obq[:, sl]), np.ascontiguousarray(obs[:, ss]))
         assert_gemm_close(dw[g], oracle.gemm(a, b), f"e5m2 moe wgrad expert {g}")
+
+
+# ---- 32x32 blocks with the E5M2 payload ---------------------------------------------------
+
+def _spread32(n, k, seed, nonfinite=False):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(n, k, generator=g, dtype=torch.float64)
+    e = torch.randint(-60, 60, (n // 32, k // 32), generator=g).double()
+    x = x * torch.pow(2.0, e).repeat_interleave(32, 0).repeat_interleave(32, 1)
+    xb = x.float().to(torch.bfloat16)
+    if n >= 64 and k >= 64:
+        xb[:32, 32:64] = 0.0
+        xb[33, 1] = -0.0
+    if nonfinite and n >= 64 and k >= 96:
+        xb[40, 70] = float("nan")
+        xb[5, 3] = float("-inf")
+    return xb
+
+
+@pytest.mark.parametrize("layout", ["tiled", "rowmajor"])
+@pytest.mark.parametrize("shape", [(64, 96), (128, 128), (384, 256), (96, 4096), (4096, 160)])
+def test_e5m2_32x32_matches_oracle(shape, layout):
+    mxq, _, oracle = _mods()
+    w = _spread32(*shape, seed=shape[0] + 5 * shape[1], nonfinite=shape == (384, 256))
+    q, sf, sb = mxq.quant_32x32(w.cuda(), layout=layout, fmt="e5m2")
+    torch.cuda.synchronize()
+    oq, osf, osb = oracle.quant_32x32(bits(w), fmt=1)
+    conv = oracle.scale_tiled if layout == "tiled" else (lambda s: s)
+    assert np.array_equal(u8(q), oq), "payload"
+    assert np.array_equal(u8(sf), conv(osf)), "s_fwd"
+    assert np.array_equal(u8(sb), conv(osb)), "s_bwd"
+
+
+def test_e5m2_32x32_full_weight():
+    """The 7168 x 7168 weight of the 32x32 path, E5M2 payload, tiled scales."""
+    mxq, workloads, oracle = _mods()
+    w = workloads.normal((7168, 7168), 0.02, seed=workloads.seed_for("weight_32x32", "W"))
+    q, sf, sb = mxq.quant_32x32(w.cuda(), fmt="e5m2")
+    torch.cuda.synchronize()
+    oq, osf, osb = oracle.quant_32x32(bits(w), fmt=1)
+    assert np.array_equal(u8(q), oq)
+    assert np.array_equal(u8(sf), oracle.scale_tiled(osf)) and np.array_equal(u8(sb), oracle.scale_tiled(osb))
+
+
+@pytest.mark.parametrize("M,n,k", [(300, 384, 256), (256, 512, 1024)])
+def test_e5m2_32x32_forward_and_mn_major_dgrad(M, n, k):
+    """The single E5M2 32x32 payload of W [n, k] read K-major with s_fwd
+    (forward, X in E4M3) and N-major with s_bwd (dgrad, dY in E5M2)."""
+    mxq, workloads, oracle = _mods()
+    W = workloads.normal((n, k), 0.02, seed=n + k + 1)
+    X = workloads.normal_with_outliers((M, k), seed=M + k)
+    dY = workloads.normal((M, n), 1e-3, seed=M + n)
+    q, sf, sb = mxq.quant_32x32(W.cuda(), fmt="e5m2")
+    xq, xs, _, _ = mxq.quant_1x32_dual(X.cuda(), col=False)
+    gq, gs, _, _ = mxq.quant_1x32_dual_batched(dY.cuda(), col=False, fmt="e5m2")
+    y = mxq.gemm_fmt(xq, xs, "e4m3", q, sf, "e5m2", M, n, k)
+    dx = mxq.gemm_fmt(gq[0], gs[0], "e5m2", q, sb, "e5m2", M, k, n, b_mn_major=True)
+    torch.cuda.synchronize()
+    oq, osf, _ = oracle.quant_32x32(bits(W), fmt=1)
+    w_deq = oracle.dequant_rows_fmt(oq, osf, 1)
+    x_deq = oracle.dequant_rows(*oracle.quant_rows(bits(X)))
+    g_deq = oracle.dequant_rows_fmt(*oracle.quant_rows_fmt(bits(dY), 1), 1)
+    assert_gemm_close(y, oracle.gemm(x_deq, w_deq), "e5m2 32x32 forward")
+    assert_gemm_close(dx, oracle.gemm(g_deq, np.ascontiguousarray(w_deq.T)), "e5m2 32x32 dgrad")

@@ -11,6 +11,10 @@ Two bars:
   one of the oracle's (the amax may cross a power of two between the two
   sums); the dequantized payload within the GEMM tolerance plus E4M3's
   rounding bound (half an ulp: 2^-4 |y| for normals, 2^-10 * scale below);
+* against the oracle's 1x32 quantizer applied to the kernel's own BF16 output
+  (the quantization of a given BF16 tensor has exactly one correct byte
+  string): payload and scales byte for byte, at every shape and both full
+  sizes;
 * against the library's own two-pass path (mxq_gemm_bf16out, then the row
   copy of mxq_quant_1x32_dual, both already pinned to the oracle): bit-exact,
   payload, scales and padding, at small and full sizes.
@@ -119,6 +123,21 @@ def test_fused_against_oracle(M, N, K, mn):
 
 
 @pytest.mark.parametrize("M,N,K,mn", SHAPES)
+def test_fused_bytes_equal_oracle_quant_of_own_output(M, N, K, mn):
+    """The quantized output is integer work on the kernel's BF16 result: the
+    oracle's 1x32 row quantizer applied to exactly those BF16 values must give
+    the same payload and scale bytes (tiled padding zero)."""
+    mxq, _, oracle = _mods()
+    ops, _ = _operands(M, N, K, seed=5 * M + N + 3 * K, mn_major=mn)
+    y, q, s = _fused(ops, M, N, K, mn)
+    torch.cuda.synchronize()
+    q_ref, s_ref = oracle.quant_rows(bits(y))
+    assert np.array_equal(u8(q), q_ref), f"fused payload {M}x{N}x{K}"
+    assert np.array_equal(_untile(u8(s), M, N // 32), s_ref), f"fused scales {M}x{N}x{K}"
+    assert np.array_equal(u8(s), oracle.scale_tiled(s_ref)), "tiled scale bytes incl. padding"
+
+
+@pytest.mark.parametrize("M,N,K,mn", SHAPES)
 def test_fused_equals_two_pass(M, N, K, mn):
     ops, _ = _operands(M, N, K, seed=11 * M + N + K, mn_major=mn)
     y2, q2, s2 = _two_pass(ops, M, N, K, mn)
@@ -172,6 +191,11 @@ def test_fused_full_size_equals_two_pass(M, N, K):
     torch.cuda.synchronize()
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
     assert torch.equal(q1, q2) and torch.equal(s1, s2)
+    # every byte against the oracle's quantization of the kernel's own BF16 output
+    q_ref, s_ref = oracle.quant_rows(bits(y1))
+    assert np.array_equal(u8(q1), q_ref), "fused payload at full size"
+    assert np.array_equal(u8(s1), oracle.scale_tiled(s_ref)), "fused tiled scales at full size"
+    del q_ref
     oxq, oxs = oracle.quant_rows(bits(X[M - 64:].cpu()))
     owq, ows = oracle.quant_rows(bits(W.cpu()))
     y_ref = oracle.gemm(oracle.dequant_rows(oxq, oxs), oracle.dequant_rows(owq, ows))

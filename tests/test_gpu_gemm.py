@@ -195,6 +195,46 @@ def test_full_weight_32x32_path():
     assert_gemm_close(dx[rt], oracle.gemm(gd, np.ascontiguousarray(w_deq.T), rows=r), "32x32 dgrad")
 
 
+def _sweep_three_gemms(K, n_rows, seed):
+    """The sweep layer M = 16384, K = N: dual quantization of X, W, dY checked
+    byte for byte against the oracle, then the forward by the single-GEMM call
+    and dgrad + wgrad by the one-launch pair the benchmark times, on sampled
+    output rows (operand rows quantized by the oracle where the product needs
+    only those rows)."""
+    mxq, workloads, oracle = _mods()
+    from _util import u8
+    d = workloads.sweep(K)
+    M = 16384
+    N = K
+    X, W, dY = d["X"], d["W"], d["dY"]
+    q = {}
+    for name, t in (("X", X), ("W", W), ("dY", dY)):
+        qr, sr, qc, sc = mxq.quant_1x32_dual(t.cuda())
+        torch.cuda.synchronize()
+        oqr, osr, oqc, osc = oracle.quant_dual(bits(t))
+        assert np.array_equal(u8(qr), oqr) and np.array_equal(u8(sr), oracle.scale_tiled(osr)), f"{name} row copy"
+        assert np.array_equal(u8(qc), oqc) and np.array_equal(u8(sc), oracle.scale_tiled(osc)), f"{name} col copy"
+        del oqr, osr, oqc, osc
+        q[name] = (qr, sr, qc, sc)
+    xr, xrs, xc, xcs = q["X"]
+    wr, wrs, wc, wcs = q["W"]
+    gr, grs, gc, gcs = q["dY"]
+    y = mxq.gemm(xr, xrs, wr, wrs, M, N, K)
+    dx, dw = mxq.gemm_multi([dict(a_q=gr, a_s=grs, b_q=wc, b_s=wcs, M=M, N=K, K=N),
+                             dict(a_q=gc, a_s=gcs, b_q=xc, b_s=xcs, M=N, N=K, K=M)])
+    torch.cuda.synchronize()
+    del q, xr, xrs, wr, wrs, gr, grs, wc, wcs, gc, gcs, xc, xcs
+    deq_rows = lambda t: oracle.dequant_rows(*oracle.quant_rows(bits(t)))
+    r = _sample_rows(M, n=n_rows, seed=seed)
+    rt = torch.from_numpy(r).cuda()
+    assert_gemm_close(y[rt], oracle.gemm(deq_rows(X[r]), deq_rows(W)), f"forward sweep {K}")
+    assert_gemm_close(dx[rt], oracle.gemm(deq_rows(dY[r]), deq_rows(W.t().contiguous())), f"dgrad sweep {K}")
+    r2 = _sample_rows(N, n=n_rows, seed=seed + 1)
+    gt_rows = deq_rows(dY.t()[r2].contiguous())
+    assert_gemm_close(dw[torch.from_numpy(r2).cuda()], oracle.gemm(gt_rows, deq_rows(X.t().contiguous())),
+                      f"wgrad sweep {K}")
+
+
 def test_full_sweep_4096_forward():
     mxq, workloads, oracle = _mods()
     d = workloads.sweep(4096)
@@ -205,6 +245,14 @@ def test_full_sweep_4096_forward():
     torch.cuda.synchronize()
     r = _sample_rows(M, seed=4)
     assert_gemm_close(y[torch.from_numpy(r).cuda()], oracle.gemm(xd, wd, rows=r), "sweep 4096")
+
+
+def test_full_sweep_4096_three_gemms():
+    _sweep_three_gemms(4096, n_rows=128, seed=41)
+
+
+def test_full_sweep_7168_three_gemms():
+    _sweep_three_gemms(7168, n_rows=96, seed=71)
 
 
 def test_full_sweep_16384_three_gemms():
@@ -236,6 +284,26 @@ def test_full_sweep_16384_three_gemms():
     xt_deq = deq_rows(X.t().contiguous())                      # wgrad B: X's column copy
     gt_rows = deq_rows(dY.t()[r].contiguous())                 # wgrad A: sampled rows of dY's column copy
     assert_gemm_close(dw[rt], oracle.gemm(gt_rows, xt_deq, rows=None), "wgrad 16384")
+
+
+def test_c_abi_gemm_layout_argument():
+    """mxq_gemm_bf16out through the C ABI: MMA-tiled scales compute, row-major
+    scales are refused before anything is launched (output untouched)."""
+    import ctypes
+    mxq, workloads, oracle = _mods()
+    M, N, K = 200, 256, 320
+    xq, xs, xd = _rows_operand(workloads.normal_with_outliers((M, K), seed=21))
+    wq, ws, wd = _rows_operand(workloads.normal((N, K), 0.02, seed=22))
+    y = torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda")
+    L = mxq.lib()
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = L.mxq_gemm_bf16out(p(xq), p(xs), p(wq), p(ws), M, N, K, 0, p(y), N, mxq.ROWMAJOR, mxq._stream())
+    torch.cuda.synchronize()
+    assert st == 1 and torch.all(y == 3.0)
+    st = L.mxq_gemm_bf16out(p(xq), p(xs), p(wq), p(ws), M, N, K, 0, p(y), N, mxq.TILED, mxq._stream())
+    torch.cuda.synchronize()
+    assert st == 0
+    assert_gemm_close(y, oracle.gemm(xd, wd), "C ABI forward")
 
 
 def test_small_linear_exhaustive():

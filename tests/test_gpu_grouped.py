@@ -110,3 +110,68 @@ def test_full_moe_gate_up_and_down_sampled():
             ref = oracle.gemm(oracle.dequant_rows(oa, osa), oracle.dequant_rows(ob, osb))
             assert_gemm_close(y[torch.from_numpy(rows).cuda()], ref, f"{name} expert {g}")
         del W, bq, bs, y
+
+
+# ---- the workspace of mxq_grouped_gemm (A scales tiled per expert) -------------------
+
+def _c_grouped(mxq, aq, as_, bq, bs, offd, G, M, N, K, y, ws):
+    import ctypes
+    p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    nbytes = 0 if ws is None else ws.numel()
+    return mxq.lib().mxq_grouped_gemm(p(aq), p(as_), p(bq), p(bs), p(offd), G, M, N, K, p(y), p(ws),
+                                      ctypes.c_size_t(nbytes), mxq._stream())
+
+
+@pytest.mark.parametrize("sizes,N,K", [
+    ([0, 5, 0, 300, 1, 130], 256, 192),
+    ([0, 1, 127, 129, 0, 256, 3], 128, 256),
+    ([37, 91, 200, 5, 0, 143, 300, 1], 512, 1024),
+    ([1] * 40, 128, 64),
+])
+def test_c_abi_grouped_workspace(sizes, N, K):
+    """mxq_grouped_gemm through the C ABI with and without its workspace: the
+    workspace (prefilled with garbage) changes only the tile schedule, so both
+    outputs are bit-identical and within the GEMM tolerance of the oracle."""
+    mxq, workloads, oracle = _mods()
+    G = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    M = int(off[-1])
+    A = workloads.normal_with_outliers((M, K), seed=M + 3)
+    B = workloads.normal((G * N, K), 0.02, seed=G + 4)
+    aq, as_, _, _ = mxq.quant_1x32_dual(A.cuda(), col=False)
+    bq, bs, _, _ = mxq.quant_1x32_dual(B.cuda(), col=False)
+    offd = torch.from_numpy(off).cuda()
+    need = mxq.grouped_gemm_workspace_size(G, M, N, K)
+    ws = torch.full((need,), 0xAB, dtype=torch.uint8, device="cuda")
+    y0 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y1 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert _c_grouped(mxq, aq, as_, bq, bs, offd, G, M, N, K, y0, None) == 0
+    assert _c_grouped(mxq, aq, as_, bq, bs, offd, G, M, N, K, y1, ws) == 0
+    assert _c_grouped(mxq, aq, as_, bq, bs, offd, G, M, N, K, y1, ws[:need - 16]) == 1   # too small
+    torch.cuda.synchronize()
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    oa, osa = oracle.quant_rows(bits(A))
+    ob, osb = oracle.quant_rows(bits(B))
+    ref = oracle.grouped_gemm(oracle.dequant_rows(oa, osa), oracle.dequant_rows(ob, osb).reshape(G, N, K), off)
+    assert_gemm_close(y1, ref, f"grouped with workspace sizes={sizes}")
+    # the workspace now holds A's scales tiled per expert (oracle layout, written bands only)
+    want = oracle.scale_group_tiled(osa, off)
+    assert np.array_equal(ws.cpu().numpy()[:want.size], want)
+
+
+def test_full_moe_with_workspace_bit_identical():
+    """The 128-expert routing (131072 rows): gate_up with the workspace equals
+    the call without it bit for bit."""
+    mxq, workloads, _ = _mods()
+    d = workloads.moe_grouped(weights=False)
+    off = d["routing"].offsets.numpy()
+    G, N, K = off.size - 1, 4096, 4096
+    offd = torch.from_numpy(off).cuda()
+    W = workloads.normal((G * N, K), 0.02, seed=workloads.seed_for("moe_grouped", "W"), device="cuda")
+    aq, as_, _, _ = mxq.quant_1x32_dual(d["A"].cuda(), col=False)
+    bq, bs, _, _ = mxq.quant_1x32_dual(W, col=False)
+    del W
+    y0 = mxq.grouped_gemm(aq, as_, bq, bs, offd, N, K)
+    y1 = mxq.grouped_gemm(aq, as_, bq, bs, offd, N, K, workspace="alloc")
+    torch.cuda.synchronize()
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))

@@ -38,3 +38,17 @@ def test_bad_arguments_raise_value_error():
         mxq.quant_1x32_dual(x)                          # 48 is not a multiple of 32
     with pytest.raises(ValueError):
         mxq.debug_wait_timeout(0)
+
+
+def test_status_on_a_side_stream():
+    """The status call synchronizes with the stream it is given: a timeout
+    recorded by a kernel on a side stream is reported by a call on that
+    stream, once."""
+    from mxfp8_microscaled_precision_gb300 import mxq
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        assert mxq.get_device_status() == 0
+        assert mxq.debug_wait_timeout(1000) == 0
+        assert mxq.get_device_status() == 5
+        assert mxq.get_device_status() == 0
+    assert mxq.get_device_status() == 0
