@@ -462,6 +462,40 @@ mxq_status mxq_grouped_gemm_wgrad_fmt(const void* a_q, const void* a_s, mxq_fp8_
                                       int64_t capacity, int64_t M, int64_t N, void* y, int64_t ldy,
                                       mxq_stream_t stream);
 
+/*
+ * mxq_grouped_gemm for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a convenience of this library.
+ *
+ * Who needs it: code that receives only its input and output buffers (for
+ * instance an operator plugged into a host framework or a serving runtime
+ * whose allocator owns all device memory and hands out nothing else), and
+ * code that must not call cudaMalloc or cudaFree, which can synchronize the
+ * whole device.  Such a caller cannot supply mxq_grouped_gemm's workspace.
+ *
+ * What it does: exactly mxq_grouped_gemm with a workspace (E4M3 x E4M3, y
+ * dense [M_total, N]; same arguments, shapes and errors), except that the
+ * workspace is a fixed array of MXQ_GROUPED_NOALLOC_MAX_WORKSPACE bytes that
+ * the library keeps in device memory.  The call itself allocates nothing.
+ *   - Limit: mxq_grouped_gemm_workspace_size(G, M_total, N, K) must not exceed
+ *     MXQ_GROUPED_NOALLOC_MAX_WORKSPACE (e.g. 131072 rows, 128 experts and
+ *     K up to 7168 fit); larger problems return MXQ_ERR_UNSUPPORTED_SHAPE
+ *     and launch nothing.
+ *   - Memory: every GPU that loads this library holds the array until the
+ *     process exits, whether or not this call is used.
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (with that device current); make that first call before any
+ *     stream capture.
+ *   - Sharing: all calls in the process use the same array, which keeps what
+ *     the last call wrote.  Nothing in it needs to start at zero: each call
+ *     rewrites every byte it later reads.  Calls whose work can overlap on the
+ *     GPU (different streams, or several host threads) race on the array and
+ *     give wrong results; order them on one stream or with events.
+ */
+#define MXQ_GROUPED_NOALLOC_MAX_WORKSPACE ((size_t)32 << 20)
+mxq_status mxq_grouped_gemm_noalloc(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
+                                    const int64_t* group_offsets, int32_t G, int64_t M_total,
+                                    int64_t N, int64_t K, void* y, mxq_stream_t stream);
+
 /* Waits for the work queued on `stream` (synchronizes the host with it), then
  * returns MXQ_ERR_TIMEOUT if any kernel of this library on the current device
  * recorded a bounded wait that ran out since the last call, MXQ_ERR_CUDA if

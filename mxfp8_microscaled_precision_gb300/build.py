@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libmxq.so")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "tensor_map.cu", "fsdp.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "tensor_map.cu", "fsdp.cu", "noalloc.cu"]
 HEADERS = ["mxq_device.cuh", "mxq_internal.h", "mxq_quant_math.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

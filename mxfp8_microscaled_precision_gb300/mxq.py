@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
         L.mxq_fsdp_payload_layout.argtypes = [S, I64, I64, I32, ctypes.POINTER(I64), ctypes.POINTER(I64)]
         L.mxq_fsdp_unpack.argtypes = [S, I64, I64, I32, P, P, P, P, P, P]
         L.mxq_get_device_status.argtypes = [P]
+        L.mxq_grouped_gemm_noalloc.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, P]
+        L.mxq_grouped_gemm_noalloc.restype = S
         L.mxq_debug_wait_timeout.argtypes = [U32, P]
         for f in ("mxq_quant_1x32_dual", "mxq_quant_32x32", "mxq_gemm_bf16out",
                   "mxq_grouped_gemm", "mxq_get_device_status", "mxq_debug_wait_timeout",
@@ -407,6 +409,27 @@ def grouped_gemm(a_q, a_s, b_q, b_s, offsets: torch.Tensor, N: int, K: int, out=
     _check(lib().mxq_grouped_gemm_fmt(_ptr(a_q), _ptr(a_s), _fmt(a_fmt), _ptr(b_q), _ptr(b_s), _fmt(b_fmt),
                                       _ptr(offsets), G, M_total, N, K, _ptr(out), out.stride(0), _ptr(workspace),
                                       ws_bytes, _stream()), "mxq_grouped_gemm_fmt")
+    return out
+
+
+# Size of the library's own workspace array used by grouped_gemm_noalloc.
+NOALLOC_MAX_WORKSPACE = 32 << 20
+
+
+def grouped_gemm_noalloc(a_q, a_s, b_q, b_s, offsets: torch.Tensor, N: int, K: int, out: torch.Tensor):
+    """grouped_gemm (E4M3) for callers that cannot allocate: the output must be
+    given (dense [M_total, N] bf16) and the workspace is the library's own
+    fixed device array (see mxq_grouped_gemm_noalloc: shared by all calls, so
+    calls must not overlap on the GPU; problems whose workspace exceeds
+    NOALLOC_MAX_WORKSPACE bytes are refused)."""
+    if offsets.dtype != torch.int64 or not offsets.is_cuda:
+        raise ValueError("offsets must be an int64 CUDA tensor")
+    G = offsets.numel() - 1
+    M_total = a_q.shape[0]
+    if out.dtype != torch.bfloat16 or tuple(out.shape) != (M_total, N) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor [M_total, N]")
+    _check(lib().mxq_grouped_gemm_noalloc(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(offsets), G, M_total,
+                                          N, K, _ptr(out), _stream()), "mxq_grouped_gemm_noalloc")
     return out
 
 
