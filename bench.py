@@ -1209,6 +1209,29 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_gemm(shape):
+    """One launch of this library's dense MXFP8 GEMM and one of the vendor's
+    (torch._scaled_mm, E4M3 operands, E8M0 scales) at M x N x K on the same
+    random operands, for a profiler to capture side by side; prints the largest
+    difference of the two BF16 outputs."""
+    import torch
+    from mxfp8_microscaled_precision_gb300 import build as mbuild, mxq
+    mbuild.build()
+    M, N, K = (int(v) for v in shape.split("x"))
+    dev = torch.device("cuda:0")
+    a = torch.randint(0, 256, (M, K), device=dev, dtype=torch.uint8) & 0x77      # finite E4M3 codes
+    b = torch.randint(0, 256, (N, K), device=dev, dtype=torch.uint8) & 0x77
+    sa = torch.full((mxq.scale_bytes(M, K),), 120, dtype=torch.uint8, device=dev)
+    sb = torch.full((mxq.scale_bytes(N, K),), 120, dtype=torch.uint8, device=dev)
+    y = mxq.gemm(a, sa, b, sb, M, N, K)
+    torch.cuda.synchronize()
+    y2 = torch._scaled_mm(a.view(torch.float8_e4m3fn), b.view(torch.float8_e4m3fn).t(),
+                          sa.view(torch.float8_e8m0fnu).view((M + 127) // 128 * 128, -1),
+                          sb.view(torch.float8_e8m0fnu).view((N + 127) // 128 * 128, -1), out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_gemm": shape, "max_abs_diff_vs_vendor": float((y.float() - y2.float()).abs().max())}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1224,7 +1247,11 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle GEMM in the CPU baseline")
+    ap.add_argument("--profile-gemm", metavar="MxNxK",
+                    help="launch this library's GEMM and the vendor's once each at this shape (for ncu) and exit")
     args = ap.parse_args(argv)
+    if args.profile_gemm:
+        return run_profile_gemm(args.profile_gemm)
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
     if args.impl == "reference":
