@@ -13,11 +13,15 @@
 //   warp 0      TMA producer: A and B tiles (128-byte swizzle) and the
 //               512-byte scale atoms, into a ring of STAGES shared-memory
 //               slots guarded by full/empty mbarriers.
-//   warp 1      allocates tensor memory; one lane issues, per stage,
+//   warp 1      allocates tensor memory; the whole warp runs the tile and
+//               stage loops (warp-uniform, so counters and descriptors live in
+//               uniform registers) and one elected lane issues, per stage,
 //               tcgen05.cp of the scale atoms into that stage's TMEM columns
 //               and the tcgen05.mma.kind::mxf8f6f4.block_scale instructions
 //               (128 x BN x 32 each) into the TMEM accumulator.
-//   warps 2-9   epilogue: tcgen05.ld of the FP32 accumulator, which is then
+//   warps 2-9   epilogue: one thread waits (suspending) for a finished
+//               accumulator while the other epilogue warps sleep on a named
+//               barrier; tcgen05.ld of the FP32 accumulator, which is then
 //               released to the MMA warp; RNE to BF16 (and, in the quantizing
 //               mode, the 1x32 MXFP8 quantization); BF16 tiles go out
 //               through a per-warp shared-memory staging buffer (8 rows x 64
@@ -114,7 +118,8 @@ struct Cfg {
     static constexpr int kNumBars = 2 * STAGES + 2 * kAccStages + 1;
     static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
-    static constexpr int kOffSched = (kOffAbort + 4 + 15) / 16 * 16;
+    static constexpr int kOffEpiFlag = kOffAbort + 4;   // accumulator-ready verdict for the epilogue warps
+    static constexpr int kOffSched = (kOffEpiFlag + 4 + 15) / 16 * 16;
     static constexpr int kSchedBytes = kMode == kGroupedRows || kMode == kGroupedK ? 4 * (kMaxGroups + 1) + 4 * kMaxGroups : 0;
     static constexpr bool kStaged = BN == 256 && kMode != kDenseQuant;
     static constexpr int kStageWarpBytes = 32 * 32 * 2;  // 32 rows x 32 BF16 columns
@@ -386,6 +391,17 @@ __device__ __forceinline__ void store_row(const GemmArgs& a, const Problem& p, u
     }
 }
 
+// True in exactly one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // Wait for the accumulator hand-off between the MMA warp and the epilogue, on
 // the critical path between tiles: busy polling without suspending the thread
 // (measured 1-4% faster than the suspending probe), bounded, then the timed wait.
@@ -419,6 +435,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + kAcc + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * kAcc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+    volatile int* epi_flag = reinterpret_cast<volatile int*>(smem + L::kOffEpiFlag);
     const WaitGuard guard{abort_flag, p.status, p.wait_limit_ns};
 
     // ---- set-up -------------------------------------------------------------
@@ -595,12 +612,12 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
         }
     } else if (warp == 1) {
         // ---- MMA issuer -----------------------------------------------------
-        if (lane == 0) {
-            // Descriptors of stage 0; other stages and K steps are offsets of them
-            // (the address field holds bytes >> 4 in the low bits).
+        // The whole warp runs the loops (warp-uniform control flow, so counters
+        // and descriptors stay in uniform registers); lane 0 waits on the
+        // barriers and broadcasts the verdict, and one elected lane issues the
+        // tensor-core instructions.
+        {
             const uint64_t a_desc0 = make_smem_desc(sbase + L::kOffA, 16, 1024, 2);
-            // N-major B (the 32x32 dgrad): 128-column chunks are kBK rows x 128 bytes
-            // apart (leading byte offset); 8-row K groups 1024 bytes apart.
             const uint64_t b_desc0 = kMnMajor ? make_smem_desc(sbase + L::kOffB, 128 * kBK, 1024, 2)
                                               : make_smem_desc(sbase + L::kOffB, 16, 1024, 2);
             const uint64_t sfa_desc0 = make_smem_desc(sbase + L::kOffSfa, 0, 128, 0);
@@ -614,7 +631,9 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
             for (int64_t r = 0; r * gridDim.x < sch.total && ok; ++r) {
                 const int64_t t = item_of(r);
                 if (t >= sch.total) continue;
-                if (!spin_phase(tempty_bar(acc), acc_phase ^ 1u, guard)) { ok = false; break; }
+                int got = 1;
+                if (lane == 0) got = spin_phase(tempty_bar(acc), acc_phase ^ 1u, guard) ? 1 : 0;
+                if (!__shfl_sync(0xFFFFFFFFu, got, 0)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 const int q = kMode == kDense || kMode == kDenseQuant ? problem_of(p, t) : 0;
@@ -622,47 +641,49 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
                 const int64_t K = p.pr[q].K;
                 const uint32_t fmt_bits = p.pr[q].fmt_bits;
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!wait_phase(full_bar(stage), phase, guard)) { ok = false; break; }
+                    int fgot = 1;
+                    if (lane == 0) fgot = wait_phase(full_bar(stage), phase, guard) ? 1 : 0;
+                    if (!__shfl_sync(0xFFFFFFFFu, fgot, 0)) { ok = false; break; }
                     tc_fence_after();
-                    // this stage's scale atoms into its tensor-memory columns
-                    tc_cp_32x128b_warpx4(tmem_base + L::kTmemSfa + 4 * stage,
-                                         sfa_desc0 + static_cast<uint64_t>((stage * 512) >> 4));
-#pragma unroll
-                    for (int a = 0; a < L::kSfbAtoms; ++a)
-                        tc_cp_32x128b_warpx4(tmem_base + L::kTmemSfb + 4 * L::kSfbAtoms * stage + 4 * a,
-                                             sfb_desc0 + static_cast<uint64_t>(((stage * L::kSfbAtoms + a) * 512) >> 4));
                     const uint32_t sfa_t = tmem_base + L::kTmemSfa + 4 * stage;
                     const uint32_t sfb_t = tmem_base + L::kTmemSfb + 4 * L::kSfbAtoms * stage;
                     const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
                     const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
+                    const uint64_t sfa_d = sfa_desc0 + static_cast<uint64_t>((stage * 512) >> 4);
+                    const uint64_t sfb_d = sfb_desc0 + static_cast<uint64_t>((stage * L::kSfbAtoms * 512) >> 4);
                     const int64_t k_left = kMode == kGroupedK ? static_cast<int64_t>(nkb - kb) * kBK
                                                               : K - static_cast<int64_t>(kb) * kBK;
-                    if (k_left >= kBK) {
+                    const int ksub = k_left >= kBK ? kBK / kUmmaK : static_cast<int>(k_left) / kUmmaK;
+                    if (elect_one()) {
+                        tc_cp_32x128b_warpx4(sfa_t, sfa_d);
+#pragma unroll
+                        for (int a = 0; a < L::kSfbAtoms; ++a)
+                            tc_cp_32x128b_warpx4(sfb_t + 4 * a, sfb_d + static_cast<uint64_t>((a * 512) >> 4));
 #pragma unroll
                         for (int k = 0; k < kBK / kUmmaK; ++k)
-                            tc_mma_mxf8(d_tmem, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
-                                        make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k) | fmt_bits, sfa_t, sfb_t,
-                                        (kb > 0 || k > 0) ? 1u : 0u);
-                    } else {
-                        const int ksub = static_cast<int>(k_left) / kUmmaK;
-                        for (int k = 0; k < ksub; ++k)
-                            tc_mma_mxf8(d_tmem, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
-                                        make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k) | fmt_bits, sfa_t, sfb_t,
-                                        (kb > 0 || k > 0) ? 1u : 0u);
+                            if (k < ksub)
+                                tc_mma_mxf8(d_tmem, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
+                                            make_idesc_mxf8(kBM, BN, kMnMajor ? 1u : 0u, k, k) | fmt_bits, sfa_t,
+                                            sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
+                        tc_commit(empty_bar(stage));  // frees the slot once these MMAs are done
                     }
-                    tc_commit(empty_bar(stage));  // frees the slot once these MMAs are done
+                    __syncwarp();
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                tc_commit(tfull_bar(acc));
+                if (elect_one()) tc_commit(tfull_bar(acc));
+                __syncwarp();
                 if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
             }
             // Drain: every MMA and copy issued above completes before teardown.
-            tc_commit(drain_bar);
-            WaitGuard g2 = guard;
-            volatile int never = 0;
-            g2.abort_flag = &never;
-            (void)mbar_wait(drain_bar, 0, g2);
+            if (lane == 0) {
+                tc_commit(drain_bar);
+                WaitGuard g2 = guard;
+                volatile int never = 0;
+                g2.abort_flag = &never;
+                (void)mbar_wait(drain_bar, 0, g2);
+            }
+            __syncwarp();
         }
     } else {
         // ---- epilogue (warps 2 .. 2+kEpiWarps-1) ------------------------------
@@ -677,11 +698,17 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
             const int64_t t = item_of(r);
             if (t >= sch.total) continue;
             const TileInfo ti = tile_info<BN, kMode>(sch, p, t);
-            // One lane waits; the warp follows its verdict, so the .sync.aligned
-            // tensor-memory loads below always run with the full warp.
-            int ok = 1;
-            if (lane == 0) ok = spin_phase(tfull_bar(acc), acc_phase, guard) ? 1 : 0;
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            // One thread waits for the finished accumulator with the suspending
+            // try_wait; the other epilogue warps sleep on named barrier 1 meanwhile
+            // (busy polling from every warp for a whole main loop measured 0-4%
+            // slower: the polls take issue slots and shared-memory bandwidth).
+            // Barrier 2 keeps the flag from being rewritten before every warp has
+            // read it.  All warps follow one verdict, so the .sync.aligned
+            // tensor-memory loads below always run with full warps.
+            if (warp == 2 && lane == 0) *epi_flag = wait_phase(tfull_bar(acc), acc_phase, guard) ? 1 : 0;
+            named_bar_sync(1, 32 * L::kEpiWarps);
+            const int ok = *epi_flag;
+            named_bar_sync(2, 32 * L::kEpiWarps);
             if (!ok) break;
             tc_fence_after();
             uint32_t v[4][32];

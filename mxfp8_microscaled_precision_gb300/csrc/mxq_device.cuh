@@ -66,6 +66,12 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     return v;
 }
 
+// Named barrier `id` (1..15) over `count` threads (a multiple of 32): the
+// warps that reach it sleep until all have arrived.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Orders this thread's view of earlier generic-proxy shared-memory accesses
 // (after a CTA barrier: every thread's) before its later async-proxy ones (TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
