@@ -391,17 +391,6 @@ __device__ __forceinline__ void store_row(const GemmArgs& a, const Problem& p, u
     }
 }
 
-// True in exactly one lane of the (converged) warp.
-__device__ __forceinline__ bool elect_one() {
-    uint32_t pred = 0;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "elect.sync _|p, 0xffffffff;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(pred));
-    return pred != 0;
-}
-
 // Wait for the accumulator hand-off between the MMA warp and the epilogue, on
 // the critical path between tiles: busy polling without suspending the thread
 // (measured 1-4% faster than the suspending probe), bounded, then the timed wait.
@@ -752,6 +741,307 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
     }
 }
 
+// ---- dense GEMMs on CTA pairs (clusters of two, tcgen05 cta_group::2) ----------------
+//
+// Output tiles of 256 x 256 per pair of SMs.  CTA rank r of the pair owns rows
+// m0 + 128 r: it loads those 128 rows of A, its 128-row half of the B tile (B
+// rows n0 + 128 r; N-major B: columns n0 + 128 r), its A scale atom and both B
+// scale atoms (every CTA's tensor core reads the scales of all 256 B rows from
+// its own tensor memory), all completing on the even CTA's full barrier.  Warp
+// 1 of the even CTA issues, per 128-deep stage, three pair scale copies and
+// four 256 x 256 x 32 pair MMAs, then a commit that frees the stage's slot in
+// both CTAs.  Against the single-CTA 128 x 256 tile this halves the shared-
+// memory operand bytes each SM stages per multiply-add and the instructions
+// the issuing thread sends per multiply-add; a stage is 33.5 KB per CTA, six
+// stages deep.  Each CTA's eight epilogue warps drain its 128 accumulator rows
+// and arrive on the even CTA's accumulator-empty barrier.
+struct PairCfg {
+    static constexpr int kStages = 6;
+    static constexpr int kEpiWarps = 8;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kABytes = 128 * kBK;          // own A rows per stage
+    static constexpr int kBBytes = 128 * kBK;          // own half of B per stage
+    static constexpr int kSfbBytes = 2 * 512;          // scale atoms of all 256 B rows
+    static constexpr int kStageBytes = kABytes + kBBytes + 512 + kSfbBytes;   // per CTA
+    static constexpr int kOffB = 0;
+    static constexpr int kOffA = kOffB + kStages * kBBytes;
+    static constexpr int kOffSfa = kOffA + kStages * kABytes;
+    static constexpr int kOffSfb = kOffSfa + kStages * 512;
+    static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
+    static constexpr int kNumBars = 2 * kStages + 3;   // full, empty, accumulator full / empty, drain
+    static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
+    static constexpr int kOffAbort = kOffTmemSlot + 4;
+    static constexpr int kOffEpiFlag = kOffAbort + 4;
+    static constexpr int kOffStage = (kOffEpiFlag + 4 + 1023) / 1024 * 1024;   // 64-byte swizzle atoms
+    static constexpr int kStageWarpBytes = 32 * 32 * 2;
+    static constexpr int kBytes = kOffStage + kEpiWarps * kStageWarpBytes;
+    static constexpr int kAlloc = kBytes + 1024;
+    static constexpr int kTmemSfa = 256;               // one 256-column accumulator, then the scales
+    static constexpr int kTmemSfb = kTmemSfa + 4 * kStages;
+    static constexpr int kTmemCols = 512;
+    static_assert(kTmemSfb + 8 * kStages <= kTmemCols, "tensor memory budget");
+    static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+// Tensor maps of a pair launch (a kernel parameter: TMA reads them there).
+// Scales: the MMA-tiled bytes of an operand viewed as rows of 256 bytes, one
+// 512-byte atom = a box of 2 rows.
+struct PairMaps {
+    CUtensorMap a[kMaxProblems];
+    CUtensorMap b[kMaxProblems];
+    CUtensorMap sfa[kMaxProblems];
+    CUtensorMap sfb[kMaxProblems];
+    CUtensorMap y[kMaxProblems];
+};
+
+// Pair tile t of a dense launch: problem, first row and first column (raster
+// bands of four 256-row tile rows, n-tiles inside a band).
+struct PairTile {
+    int prob;
+    int64_t m0, n0;
+};
+
+__device__ __forceinline__ PairTile pair_tile(const GemmArgs& p, int64_t t) {
+    PairTile pt;
+    pt.prob = problem_of(p, t);
+    const Problem& P = p.pr[pt.prob];
+    t -= P.first_item;
+    constexpr int kBand = kRasterBand / 2;
+    const int64_t per_band = static_cast<int64_t>(kBand) * P.n_tiles;
+    const int64_t band = t / per_band, within = t - band * per_band;
+    const int64_t mb = band * kBand;
+    const int64_t bh = min(static_cast<int64_t>(kBand), P.m_tiles - mb);
+    pt.m0 = (mb + within % bh) * 256;
+    pt.n0 = (within / bh) * 256;
+    return pt;
+}
+
+template <bool kMnMajor, int kMode>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1)
+    gemm_mxf8_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p) {
+    static_assert(kMode == kDense || kMode == kDenseQuant, "pair kernel: dense modes");
+    using L = PairCfg;
+    constexpr int STAGES = L::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = blockIdx.x & 1u;   // rank in the cluster of two
+    const bool leader = rank == 0;
+
+    const uint32_t bar0 = sbase + L::kOffBar;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t tfull_bar = bar0 + 8u * (2 * STAGES);
+    const uint32_t tempty_bar = bar0 + 8u * (2 * STAGES + 1);
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+    volatile int* epi_flag = reinterpret_cast<volatile int*>(smem + L::kOffEpiFlag);
+    const WaitGuard guard{abort_flag, p.status, p.wait_limit_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);      // the even CTA's producer arrives (with both CTAs' bytes)
+            mbar_init(empty_bar(s), 1);     // the even CTA's multicast commit
+        }
+        mbar_init(tfull_bar, 1);
+        mbar_init(tempty_bar, 2 * L::kEpiWarps);   // every epilogue warp of both CTAs
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        for (int q = 0; q < p.nprob; ++q) {
+            prefetch_tensormap(&maps.a[q]);
+            prefetch_tensormap(&maps.b[q]);
+            prefetch_tensormap(&maps.sfa[q]);
+            prefetch_tensormap(&maps.sfb[q]);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(sbase + L::kOffTmemSlot, L::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();   // both CTAs' barriers initialised and tensor memory allocated
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemSlot);
+
+    const int64_t total = p.items;
+    const int64_t pair_id = blockIdx.x >> 1;
+    const int64_t n_pairs = gridDim.x >> 1;
+    // Item of this pair's r-th round: problems come longest K first, odd rounds
+    // in reverse pair order (as in the single-CTA kernel).
+    auto item_of = [&](int64_t r) -> int64_t {
+        return r * n_pairs + ((r & 1) ? n_pairs - 1 - pair_id : pair_id);
+    };
+
+    if (warp == 0) {
+        // ---- producer (both CTAs) --------------------------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            const uint32_t full0 = leader ? full_bar(0) : mapa_shared(full_bar(0), 0);
+            for (int64_t r = 0; r * n_pairs < total && !*abort_flag; ++r) {
+                const int64_t t = item_of(r);
+                if (t >= total) continue;
+                const PairTile pt = pair_tile(p, t);
+                const Problem& P = p.pr[pt.prob];
+                const int32_t ma = static_cast<int32_t>(pt.m0 + 128 * rank);
+                const int32_t nb = static_cast<int32_t>(pt.n0 + 128 * rank);
+                const int32_t sfa_row = static_cast<int32_t>(2 * ((pt.m0 / 128 + rank) * P.k_atoms));
+                const int32_t sfb_row0 = static_cast<int32_t>(2 * ((pt.n0 / 128) * P.k_atoms));
+                const int32_t sfb_row1 = static_cast<int32_t>(2 * ((pt.n0 / 128 + 1) * P.k_atoms));
+                bool stop = false;
+                for (int kb = 0; kb < P.num_kb; ++kb) {
+                    if (!wait_phase(empty_bar(stage), phase ^ 1u, guard)) { stop = true; break; }
+                    const uint32_t fb = full0 + 8u * stage;
+                    if (leader) mbar_arrive_expect_tx(fb, 2u * L::kStageBytes);
+                    const uint32_t ssb = sbase + L::kOffSfb + stage * L::kSfbBytes;
+                    const int32_t kx = kb * kBK;
+                    tma_load_2d_pair(sbase + L::kOffA + stage * L::kABytes, &maps.a[pt.prob], kx, ma, fb);
+                    if constexpr (!kMnMajor)
+                        tma_load_2d_pair(sbase + L::kOffB + stage * L::kBBytes, &maps.b[pt.prob], kx, nb, fb);
+                    else   // B stored [K, N]: this CTA's 128 columns x 128 K-rows
+                        tma_load_2d_pair(sbase + L::kOffB + stage * L::kBBytes, &maps.b[pt.prob], nb, kx, fb);
+                    tma_load_2d_pair(sbase + L::kOffSfa + stage * 512, &maps.sfa[pt.prob], 0, sfa_row + 2 * kb, fb);
+                    tma_load_2d_pair(ssb, &maps.sfb[pt.prob], 0, sfb_row0 + 2 * kb, fb);
+                    tma_load_2d_pair(ssb + 512, &maps.sfb[pt.prob], 0, sfb_row1 + 2 * kb, fb);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (stop) break;
+            }
+            if (*abort_flag) {
+                // Loads in flight complete on the even CTA's barrier, which the odd
+                // CTA cannot wait on: give them a bounded while to land.
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
+            }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer (even CTA; warp-uniform loops, one elected lane issues) -----------
+        if (leader) {
+            const uint64_t a_desc0 = make_smem_desc(sbase + L::kOffA, 16, 1024, 2);
+            const uint64_t b_desc0 = kMnMajor ? make_smem_desc(sbase + L::kOffB, 128 * kBK, 1024, 2)
+                                              : make_smem_desc(sbase + L::kOffB, 16, 1024, 2);
+            const uint64_t sfa_desc0 = make_smem_desc(sbase + L::kOffSfa, 0, 128, 0);
+            const uint64_t sfb_desc0 = make_smem_desc(sbase + L::kOffSfb, 0, 128, 0);
+            constexpr uint32_t kBStepK = kMnMajor ? (kUmmaK * 128) >> 4 : kUmmaK >> 4;
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int64_t r = 0; r * n_pairs < total && ok; ++r) {
+                const int64_t t = item_of(r);
+                if (t >= total) continue;
+                int got = 1;
+                if (lane == 0) got = spin_phase(tempty_bar, acc_phase ^ 1u, guard) ? 1 : 0;
+                if (!__shfl_sync(0xFFFFFFFFu, got, 0)) { ok = false; break; }
+                tc_fence_after();
+                const int q = problem_of(p, t);
+                const int nkb = p.pr[q].num_kb;
+                const int64_t K = p.pr[q].K;
+                const uint32_t fmt_bits = p.pr[q].fmt_bits;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    int fgot = 1;
+                    if (lane == 0) fgot = wait_phase(full_bar(stage), phase, guard) ? 1 : 0;
+                    if (!__shfl_sync(0xFFFFFFFFu, fgot, 0)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem_base + L::kTmemSfa + 4 * stage;
+                    const uint32_t sfb_t = tmem_base + L::kTmemSfb + 8 * stage;
+                    const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
+                    const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
+                    const uint64_t sfa_d = sfa_desc0 + static_cast<uint64_t>((stage * 512) >> 4);
+                    const uint64_t sfb_d = sfb_desc0 + static_cast<uint64_t>((stage * L::kSfbBytes) >> 4);
+                    const int64_t k_left = K - static_cast<int64_t>(kb) * kBK;
+                    const int ksub = k_left >= kBK ? kBK / kUmmaK : static_cast<int>(k_left) / kUmmaK;
+                    if (elect_one()) {
+                        // this stage's scale atoms into its tensor-memory columns (each CTA its own)
+                        tc_cp_32x128b_warpx4_pair(sfa_t, sfa_d);
+                        tc_cp_32x128b_warpx4_pair(sfb_t, sfb_d);
+                        tc_cp_32x128b_warpx4_pair(sfb_t + 4, sfb_d + static_cast<uint64_t>(512 >> 4));
+#pragma unroll
+                        for (int k = 0; k < kBK / kUmmaK; ++k)
+                            if (k < ksub)
+                                tc_mma_mxf8_pair(tmem_base, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
+                                                 make_idesc_mxf8(256, 256, kMnMajor ? 1u : 0u, k, k) | fmt_bits,
+                                                 sfa_t, sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
+                        tc_commit_pair_multicast(empty_bar(stage), 0x3);   // frees the slot in both CTAs
+                    }
+                    __syncwarp();
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                if (elect_one()) tc_commit_pair_multicast(tfull_bar, 0x3);
+                __syncwarp();
+                acc_phase ^= 1u;
+            }
+            // Drain: every MMA and copy issued above completes before teardown.
+            if (lane == 0) {
+                tc_commit_pair(drain_bar);
+                WaitGuard g2 = guard;
+                volatile int never = 0;
+                g2.abort_flag = &never;
+                (void)mbar_wait(drain_bar, 0, g2);
+            }
+            __syncwarp();
+        }
+    } else {
+        // ---- epilogue (both CTAs; warps 2..9) ----------------------------------------
+        const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const uint32_t tempty_leader = leader ? tempty_bar : mapa_shared(tempty_bar, 0);
+        uint32_t acc_phase = 0;
+        bool pending = false;   // a tiled store of this warp may still read its buffer
+        for (int64_t r = 0; r * n_pairs < total; ++r) {
+            const int64_t t = item_of(r);
+            if (t >= total) continue;
+            const PairTile pt = pair_tile(p, t);
+            const Problem& P = p.pr[pt.prob];
+            // One thread waits (suspending), the other epilogue warps sleep on a
+            // named barrier; barrier 2 keeps the verdict until every warp read it.
+            if (warp == 2 && lane == 0) *epi_flag = wait_phase(tfull_bar, acc_phase, guard) ? 1 : 0;
+            named_bar_sync(1, 32 * L::kEpiWarps);
+            const int ok = *epi_flag;
+            named_bar_sync(2, 32 * L::kEpiWarps);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t v[4][32];
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + half * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 32 * c, v[c]);
+            tmem_ld_wait();
+            // The accumulator is in registers: hand it back to the MMA warp now.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive(tempty_bar);
+                else mbar_arrive_cluster(tempty_leader);
+            }
+            acc_phase ^= 1u;
+            const int64_t mc = pt.m0 + 128 * rank;   // this CTA's first row
+            const int64_t row_hi = min(mc + 128, P.M);
+            if constexpr (kMode == kDense)
+                store_staged(P, v, sbase + L::kOffStage + (warp - 2) * L::kStageWarpBytes, mc + 32 * quad,
+                             mc + 32 * quad, mc, row_hi, pt.n0 + half * 128, lane, &maps.y[pt.prob], pending);
+            else
+                store_row<kMode>(p, P, v, mc + 32 * quad + lane, mc, row_hi, 0, pt.n0 + half * 128, mc < P.M);
+        }
+        if (lane == 0) bulk_wait_all();   // this warp's tiled stores complete before the CTA ends
+        __syncwarp();
+    }
+
+    // ---- teardown: nothing may still target the peer when either CTA leaves ----
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc_pair(tmem_base, L::kTmemCols);
+    }
+}
+
 // Row-major u8 matrix [rows, cols] (cols contiguous), box [box_rows, 128 bytes],
 // 128-byte swizzle.
 bool make_tma_u8(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
@@ -852,11 +1142,95 @@ bool fill_dense(const DenseGemm* gemms, int count, bool b_mn_major, TensorMaps* 
     return true;
 }
 
+// MMA-tiled scales of an operand with `bands` 128-row bands of k_atoms atoms,
+// as rows of 256 bytes (one atom = a 2 x 256 box at row 2 (band k_atoms + kb)).
+bool make_tma_scales(CUtensorMap* map, const void* ptr, int64_t bands, int64_t k_atoms) {
+    return encode_tensor_map_2d(map, ptr, false, 256u, static_cast<uint64_t>(bands * k_atoms * 2), 256u, 256u,
+                                2u, false);
+}
+
+// The problems of one dense pair launch (K descending, as fill_dense orders
+// them), their 256 x 256 pair tiles laid out back to back.  False when a tensor
+// map cannot be encoded or a scale map's rows exceed its 32-bit coordinates
+// (the single-CTA kernel then runs the launch).
+bool fill_dense_pair(const DenseGemm* gemms, int count, bool b_mn_major, PairMaps* maps, GemmArgs* args) {
+    int order[kMaxProblems];
+    for (int i = 0; i < count; ++i) order[i] = i;
+    for (int i = 1; i < count; ++i)
+        for (int j = i; j > 0 && gemms[order[j]].K > gemms[order[j - 1]].K; --j) {
+            const int t = order[j]; order[j] = order[j - 1]; order[j - 1] = t;
+        }
+    int64_t items = 0;
+    for (int i = 0; i < count; ++i) {
+        const DenseGemm& g = gemms[order[i]];
+        const int64_t k_atoms = (g.K + 127) / 128;
+        const int64_t a_bands = (g.M + 127) / 128, b_bands = (g.N + 127) / 128;
+        if ((a_bands + 1) * k_atoms * 2 >= (int64_t(1) << 31) || (b_bands + 2) * k_atoms * 2 >= (int64_t(1) << 31))
+            return false;
+        if (!make_tma_u8(&maps->a[i], g.a_q, static_cast<uint64_t>(g.M), static_cast<uint64_t>(g.K), 128)) return false;
+        if (!b_mn_major) {
+            if (!make_tma_u8(&maps->b[i], g.b_q, static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.K), 128))
+                return false;
+        } else if (!make_tma_u8(&maps->b[i], g.b_q, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.N), kBK)) {
+            return false;
+        }
+        if (!make_tma_scales(&maps->sfa[i], g.a_s, a_bands, k_atoms) ||
+            !make_tma_scales(&maps->sfb[i], g.b_s, b_bands, k_atoms))
+            return false;
+        args->pr[i] = make_problem(g.a_s, g.b_s, g.y, g.M, g.N, g.K, g.ldy, k_atoms, b_bands,
+                                   fmt_bits_of(g.a_fmt, g.b_fmt));
+        args->pr[i].m_tiles = (g.M + 255) / 256;   // pair tiles
+        args->pr[i].n_tiles = (g.N + 255) / 256;
+        set_store_map(&maps->y[i], &args->pr[i], g.y, g.M, g.N, g.ldy);
+        args->pr[i].first_item = items;
+        items += args->pr[i].m_tiles * args->pr[i].n_tiles;
+    }
+    args->nprob = count;
+    args->items = items;
+    return true;
+}
+
+template <bool kMnMajor, int kMode>
+cudaError_t launch_pair_t(const DeviceInfo& dev, const PairMaps& maps, const GemmArgs& args, cudaStream_t stream) {
+    using L = PairCfg;
+    auto kern = gemm_mxf8_pair_kernel<kMnMajor, kMode>;
+    static thread_local int configured_device = -1;  // attribute set once per device and thread
+    if (configured_device != dev.device) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        if (e != cudaSuccess) return e;
+        configured_device = dev.device;
+    }
+    int64_t pairs = dev.sm_count / 2;
+    if (args.items < pairs) pairs = args.items;
+    if (pairs <= 0) return cudaSuccess;
+    kern<<<static_cast<unsigned>(2 * pairs), L::kThreads, L::kAlloc, stream>>>(maps, args);
+    return cudaGetLastError();
+}
+
+// A dense launch on CTA pairs; *done false when the pair kernel cannot take it.
+template <int kMode>
+cudaError_t try_pair(const DeviceInfo& dev, const DenseGemm* gemms, int count, bool b_mn_major, uint8_t* yq,
+                     uint8_t* ys, cudaStream_t stream, bool* done) {
+    *done = false;
+    if (dev.sm_count < 2) return cudaSuccess;
+    PairMaps maps;
+    GemmArgs args = base_args(dev);
+    if (!fill_dense_pair(gemms, count, b_mn_major, &maps, &args)) return cudaSuccess;
+    args.yq = yq;
+    args.ys = ys;
+    *done = true;
+    if (b_mn_major) return launch_pair_t<true, kMode>(dev, maps, args, stream);
+    return launch_pair_t<false, kMode>(dev, maps, args, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_multi(const DeviceInfo& dev, const DenseGemm* gemms, int count, bool b_mn_major,
                               cudaStream_t stream) {
     if (count < 1 || count > kMaxProblems) return cudaErrorInvalidValue;
+    bool done = false;
+    const cudaError_t e = try_pair<kDense>(dev, gemms, count, b_mn_major, nullptr, nullptr, stream, &done);
+    if (done || e != cudaSuccess) return e;
     TensorMaps maps;
     GemmArgs args = base_args(dev);
     if (!fill_dense(gemms, count, b_mn_major, &maps, &args)) return cudaErrorInvalidValue;
@@ -875,9 +1249,13 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const void* a_q, const void* a_s,
 cudaError_t launch_gemm_quant(const DeviceInfo& dev, const void* a_q, const void* a_s, const void* b_q,
                               const void* b_s, int64_t M, int64_t N, int64_t K, bool b_mn_major, void* y,
                               int64_t ldy, void* y_q, void* y_s, cudaStream_t stream) {
+    const DenseGemm g{a_q, a_s, b_q, b_s, M, N, K, y, ldy, 0, 0};
+    bool done = false;
+    const cudaError_t e = try_pair<kDenseQuant>(dev, &g, 1, b_mn_major, static_cast<uint8_t*>(y_q),
+                                                static_cast<uint8_t*>(y_s), stream, &done);
+    if (done || e != cudaSuccess) return e;
     TensorMaps maps;
     GemmArgs args = base_args(dev);
-    const DenseGemm g{a_q, a_s, b_q, b_s, M, N, K, y, ldy, 0, 0};
     if (!fill_dense(&g, 1, b_mn_major, &maps, &args)) return cudaErrorInvalidValue;
     args.yq = static_cast<uint8_t*>(y_q);
     args.ys = static_cast<uint8_t*>(y_s);
