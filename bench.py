@@ -160,9 +160,13 @@ class ClockSampler:
                 return None
         sm = [num(r[1]) for r in rows if num(r[1]) is not None]
         mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        capped = sum(1 for r in rows if r[8].lower().startswith("active"))
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "sm_mhz_min": min(sm) if sm else None, "sm_mhz_mean": round(statistics.mean(sm), 1) if sm else None,
+                "power_w_max": max(pw) if pw else None, "power_cap_samples": capped,
                 "reasons": reasons, "samples": len(rows)}
 
 

@@ -741,21 +741,31 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
     }
 }
 
-// ---- dense GEMMs on CTA pairs (clusters of two, tcgen05 cta_group::2) ----------------
+// ---- GEMMs on CTA pairs (clusters of two, tcgen05 cta_group::2) ----------------------
 //
-// Output tiles of 256 x 256 per pair of SMs.  CTA rank r of the pair owns rows
-// m0 + 128 r: it loads those 128 rows of A, its 128-row half of the B tile (B
-// rows n0 + 128 r; N-major B: columns n0 + 128 r), its A scale atom and both B
-// scale atoms (every CTA's tensor core reads the scales of all 256 B rows from
-// its own tensor memory), all completing on the even CTA's full barrier.  Warp
-// 1 of the even CTA issues, per 128-deep stage, three pair scale copies and
+// Output tiles of 256 x 256 per pair of SMs.  CTA rank r of the pair owns the
+// 128 rows of its half: it loads those rows of A, its 128-row half of the B
+// tile (B rows b_row + 128 r; N-major B: columns n0 + 128 r), its A scale atom
+// and both B scale atoms (every CTA's tensor core reads the scales of all 256
+// B rows from its own tensor memory), all completing on the even CTA's full
+// barrier.  Warp 1 of the even CTA runs the tile and stage loops warp-uniformly
+// and one elected lane issues, per 128-deep stage, three pair scale copies and
 // four 256 x 256 x 32 pair MMAs, then a commit that frees the stage's slot in
-// both CTAs.  Against the single-CTA 128 x 256 tile this halves the shared-
-// memory operand bytes each SM stages per multiply-add and the instructions
-// the issuing thread sends per multiply-add; a stage is 33.5 KB per CTA, six
-// stages deep.  Each CTA's eight epilogue warps drain its 128 accumulator rows
-// and arrive on the even CTA's accumulator-empty barrier.
+// both CTAs.  Against the single-CTA 128 x 256 tile this halves the operand
+// bytes each SM stages per multiply-add and the instructions issued per
+// multiply-add; a stage is 33.5 KB per CTA, six stages deep.  Each CTA's eight
+// epilogue warps drain its 128 accumulator rows and arrive on the even CTA's
+// accumulator-empty barrier.
+//
+// Modes: dense (1-4 GEMMs per launch, longest K first), dense with the
+// quantizing epilogue, grouped rows (a pair tile is two 128-row tiles of one
+// expert; when an expert has an odd number of row tiles the odd CTA of its last
+// pair tile stores nothing), grouped contraction (a pair tile is 256 x 256 of
+// one expert's weight gradient over that expert's token slot).
+template <int kMode>
 struct PairCfg {
+    static constexpr bool kGrouped = kMode == kGroupedRows || kMode == kGroupedK;
+    static constexpr int kMaxGroups = 512;             // larger G runs on the single-CTA kernel
     static constexpr int kStages = 6;
     static constexpr int kEpiWarps = 8;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -772,9 +782,12 @@ struct PairCfg {
     static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kOffEpiFlag = kOffAbort + 4;
-    static constexpr int kOffStage = (kOffEpiFlag + 4 + 1023) / 1024 * 1024;   // 64-byte swizzle atoms
+    static constexpr int kOffSched = (kOffEpiFlag + 4 + 15) / 16 * 16;
+    static constexpr int kSchedBytes = kGrouped ? 4 * (kMaxGroups + 1) + 4 * kMaxGroups : 0;
+    static constexpr int kOffStage = (kOffSched + kSchedBytes + 1023) / 1024 * 1024;   // 64-byte swizzle atoms
     static constexpr int kStageWarpBytes = 32 * 32 * 2;
-    static constexpr int kBytes = kOffStage + kEpiWarps * kStageWarpBytes;
+    static constexpr bool kStaged = kMode != kDenseQuant;
+    static constexpr int kBytes = kOffStage + (kStaged ? kEpiWarps * kStageWarpBytes : 0);
     static constexpr int kAlloc = kBytes + 1024;
     static constexpr int kTmemSfa = 256;               // one 256-column accumulator, then the scales
     static constexpr int kTmemSfb = kTmemSfa + 4 * kStages;
@@ -794,33 +807,113 @@ struct PairMaps {
     CUtensorMap y[kMaxProblems];
 };
 
-// Pair tile t of a dense launch: problem, first row and first column (raster
-// bands of four 256-row tile rows, n-tiles inside a band).
-struct PairTile {
+// What one CTA of a pair does for pair tile t.
+struct PairTileInfo {
     int prob;
-    int64_t m0, n0;
+    int64_t m0;              // this CTA's first A row (a TMA coordinate; may lie past the matrix)
+    int64_t a_band;          // this CTA's A scale band
+    int64_t row_lo, row_hi;  // A rows [row_lo, row_hi) of this CTA are stored (empty: none)
+    int64_t n0;              // first output column of the pair tile
+    int64_t b_row;           // first B row of the pair tile in the (stacked) B matrix
+    int64_t kb0;             // first 128-deep K block
+    int nkb;                 // K blocks (0: the tile is zero)
+    int64_t y_row0;          // output row of A row 0 (grouped contraction: g * M)
 };
 
-__device__ __forceinline__ PairTile pair_tile(const GemmArgs& p, int64_t t) {
-    PairTile pt;
-    pt.prob = problem_of(p, t);
-    const Problem& P = p.pr[pt.prob];
-    t -= P.first_item;
+// Raster order inside one m x n grid of pair tiles: bands of four 256-row tile
+// rows, n-tiles inside a band.
+__device__ __forceinline__ void pair_raster(int64_t local, int64_t m_tiles, int64_t n_tiles, int64_t& m0,
+                                            int64_t& n0) {
     constexpr int kBand = kRasterBand / 2;
-    const int64_t per_band = static_cast<int64_t>(kBand) * P.n_tiles;
-    const int64_t band = t / per_band, within = t - band * per_band;
+    const int64_t per_band = static_cast<int64_t>(kBand) * n_tiles;
+    const int64_t band = local / per_band, within = local - band * per_band;
     const int64_t mb = band * kBand;
-    const int64_t bh = min(static_cast<int64_t>(kBand), P.m_tiles - mb);
-    pt.m0 = (mb + within % bh) * 256;
-    pt.n0 = (within / bh) * 256;
-    return pt;
+    const int64_t bh = min(static_cast<int64_t>(kBand), m_tiles - mb);
+    m0 = (mb + within % bh) * 256;
+    n0 = (within / bh) * 256;
+}
+
+// Schedule of the grouped pair modes (shared memory, built from the device
+// offsets).  Grouped rows: prefix[g] = first pair tile of expert g (prefix[G]
+// = all), first[g] = expert g's first A band (group-tiled scales) or first
+// 128-row block.  Grouped contraction: prefix[g] = slot start / 128, first[g] =
+// slot length / 128.
+struct PairSchedule {
+    const int* prefix;
+    const int* first;
+    int64_t m_tiles, n_tiles, total;
+};
+
+template <int kMode>
+__device__ __forceinline__ PairTileInfo pair_tile_info(const PairSchedule& s, const GemmArgs& p, int64_t t,
+                                                       uint32_t rank) {
+    PairTileInfo ti;
+    ti.kb0 = 0;
+    ti.y_row0 = 0;
+    ti.prob = 0;
+    if constexpr (kMode == kDense || kMode == kDenseQuant) {
+        ti.prob = problem_of(p, t);
+        const Problem& P = p.pr[ti.prob];
+        int64_t m0p;
+        pair_raster(t - P.first_item, P.m_tiles, P.n_tiles, m0p, ti.n0);
+        ti.m0 = m0p + 128 * rank;
+        ti.a_band = ti.m0 / 128;
+        ti.row_lo = ti.m0;
+        ti.row_hi = min(ti.m0 + 128, P.M);
+        ti.b_row = ti.n0;
+        ti.nkb = P.num_kb;
+    } else if constexpr (kMode == kGroupedK) {
+        const Problem& P = p.pr[0];
+        const int64_t per = s.m_tiles * s.n_tiles;
+        const int64_t g = t / per;
+        int64_t m0p;
+        pair_raster(t - g * per, s.m_tiles, s.n_tiles, m0p, ti.n0);
+        ti.m0 = m0p + 128 * rank;
+        ti.a_band = ti.m0 / 128;
+        ti.row_lo = ti.m0;
+        ti.row_hi = min(ti.m0 + 128, P.M);
+        ti.b_row = ti.n0;
+        ti.kb0 = s.prefix[g];
+        ti.nkb = s.first[g];
+        ti.y_row0 = g * P.M;
+    } else {   // grouped rows
+        const Problem& P = p.pr[0];
+        int lo = 0, hi = p.G;  // largest g with prefix[g] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s.prefix[mid] <= t) lo = mid; else hi = mid;
+        }
+        const int g = lo;
+        const int64_t local = t - s.prefix[g];
+        ti.n0 = (local % s.n_tiles) * 256;
+        const int64_t i = 2 * (local / s.n_tiles) + rank;   // this CTA's row tile of the expert
+        const int64_t first_row = clamped_offset(p, g, P.M), end_row = clamped_offset(p, g + 1, P.M);
+        int64_t tiles;
+        if (p.a_bands_cap > 0) {   // row tiles from the expert's first row, group-tiled scales
+            tiles = (end_row - first_row + kBM - 1) / kBM;
+            tiles = min(tiles, max(int64_t(0), p.a_bands_cap - s.first[g]));
+            const int64_t ii = i < tiles ? i : 0;
+            ti.m0 = first_row + ii * kBM;
+            ti.a_band = s.first[g] + ii;
+            ti.row_lo = ti.m0;
+        } else {                   // row tiles on the 128-row grid of all rows
+            tiles = end_row > first_row ? (end_row - 1) / kBM - first_row / kBM + 1 : 0;
+            const int64_t ii = i < tiles ? i : 0;
+            ti.a_band = s.first[g] + ii;
+            ti.m0 = ti.a_band * kBM;
+            ti.row_lo = max(ti.m0, first_row);
+        }
+        ti.row_hi = i < tiles ? min(ti.m0 + kBM, end_row) : ti.row_lo;   // past the expert's tiles: nothing
+        ti.b_row = static_cast<int64_t>(g) * P.N + ti.n0;
+        ti.nkb = P.num_kb;
+    }
+    return ti;
 }
 
 template <bool kMnMajor, int kMode>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kMode>::kThreads, 1)
     gemm_mxf8_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p) {
-    static_assert(kMode == kDense || kMode == kDenseQuant, "pair kernel: dense modes");
-    using L = PairCfg;
+    using L = PairCfg<kMode>;
     constexpr int STAGES = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -862,19 +955,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
         tmem_alloc_pair(sbase + L::kOffTmemSlot, L::kTmemCols);
         tmem_relinquish_pair();
     }
+
+    PairSchedule sch;
+    sch.prefix = nullptr;
+    sch.first = nullptr;
+    sch.m_tiles = p.pr[0].m_tiles;
+    sch.n_tiles = p.pr[0].n_tiles;
+    sch.total = p.items;
+    if constexpr (L::kGrouped) {
+        // Tables from the clamped offsets (pair_tile_info reads the two offsets of
+        // a grouped-row tile again, clamped the same way, for its rows).
+        int* s_prefix = reinterpret_cast<int*>(smem + L::kOffSched);
+        int* s_first = s_prefix + (L::kMaxGroups + 1);
+        const int64_t row_limit = kMode == kGroupedRows ? p.pr[0].M : p.M_total;
+        if (warp == 0) {  // 32 groups at a time: counts, then exclusive prefixes by warp scans
+            int carry = 0, band_carry = 0;
+            for (int base = 0; base < p.G; base += 32) {
+                const int g = base + lane;
+                int cnt = 0, bands = 0;
+                int64_t lo = 0, hi = 0;
+                if (g < p.G) {
+                    lo = clamped_offset(p, g, row_limit);
+                    hi = clamped_offset(p, g + 1, row_limit);
+                }
+                if constexpr (kMode == kGroupedRows) {
+                    if (p.a_bands_cap == 0) {
+                        const int64_t tiles = hi > lo ? (hi - 1) / kBM - lo / kBM + 1 : 0;
+                        if (g < p.G) s_first[g] = static_cast<int>(lo / kBM);
+                        cnt = static_cast<int>((tiles + 1) / 2) * static_cast<int>(sch.n_tiles);
+                    } else {
+                        bands = hi > lo ? static_cast<int>((hi - lo + kBM - 1) / kBM) : 0;
+                        int bincl = bands;
+#pragma unroll
+                        for (int d = 1; d < 32; d <<= 1) {
+                            const int y = __shfl_up_sync(0xFFFFFFFFu, bincl, d);
+                            if (lane >= d) bincl += y;
+                        }
+                        const int64_t first_band = band_carry + bincl - bands;
+                        const int64_t kept = min(static_cast<int64_t>(bands), max(int64_t(0), p.a_bands_cap - first_band));
+                        if (g < p.G) s_first[g] = static_cast<int>(first_band);
+                        cnt = static_cast<int>((kept + 1) / 2) * static_cast<int>(sch.n_tiles);
+                        band_carry += __shfl_sync(0xFFFFFFFFu, bincl, 31);
+                    }
+                } else {   // slot length in 128-token blocks
+                    cnt = hi > lo ? static_cast<int>((hi - lo + kBK - 1) / kBK) : 0;
+                    if (g < p.G) s_first[g] = cnt;
+                }
+                int incl = cnt;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                    if (lane >= d) incl += y;
+                }
+                if (g < p.G) s_prefix[g] = carry + incl - cnt;
+                carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+            }
+            if (lane == 0) s_prefix[p.G] = carry;
+        }
+        sch.prefix = s_prefix;
+        sch.first = s_first;
+    }
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();   // both CTAs' barriers initialised and tensor memory allocated
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmemSlot);
-
-    const int64_t total = p.items;
+    if constexpr (kMode == kGroupedRows) sch.total = sch.prefix[p.G];
+    if constexpr (kMode == kGroupedK) {
+        sch.total = static_cast<int64_t>(p.G) * sch.m_tiles * sch.n_tiles;
+        if (static_cast<int64_t>(sch.prefix[p.G]) * kBK > p.pr[0].K) sch.total = 0;   // slots past the operands
+    }
+    const int64_t total = sch.total;
     const int64_t pair_id = blockIdx.x >> 1;
     const int64_t n_pairs = gridDim.x >> 1;
-    // Item of this pair's r-th round: problems come longest K first, odd rounds
-    // in reverse pair order (as in the single-CTA kernel).
+    // Item of this pair's r-th round: dense problems come longest K first, and
+    // dense launches take odd rounds in reverse pair order.
     auto item_of = [&](int64_t r) -> int64_t {
-        return r * n_pairs + ((r & 1) ? n_pairs - 1 - pair_id : pair_id);
+        if constexpr (kMode == kDense || kMode == kDenseQuant)
+            return r * n_pairs + ((r & 1) ? n_pairs - 1 - pair_id : pair_id);
+        return r * n_pairs + pair_id;
     };
 
     if (warp == 0) {
@@ -886,28 +1045,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
             for (int64_t r = 0; r * n_pairs < total && !*abort_flag; ++r) {
                 const int64_t t = item_of(r);
                 if (t >= total) continue;
-                const PairTile pt = pair_tile(p, t);
-                const Problem& P = p.pr[pt.prob];
-                const int32_t ma = static_cast<int32_t>(pt.m0 + 128 * rank);
-                const int32_t nb = static_cast<int32_t>(pt.n0 + 128 * rank);
-                const int32_t sfa_row = static_cast<int32_t>(2 * ((pt.m0 / 128 + rank) * P.k_atoms));
-                const int32_t sfb_row0 = static_cast<int32_t>(2 * ((pt.n0 / 128) * P.k_atoms));
-                const int32_t sfb_row1 = static_cast<int32_t>(2 * ((pt.n0 / 128 + 1) * P.k_atoms));
+                const PairTileInfo ti = pair_tile_info<kMode>(sch, p, t, rank);
+                const Problem& P = p.pr[ti.prob];
+                const CUtensorMap* ma_map = &maps.a[ti.prob];
+                const CUtensorMap* mb_map = &maps.b[ti.prob];
+                const int32_t ma = static_cast<int32_t>(ti.m0);
+                const int32_t nb = static_cast<int32_t>(ti.b_row + 128 * rank);
+                const int32_t sfa_row = static_cast<int32_t>(2 * (ti.a_band * P.k_atoms + ti.kb0));
+                const int32_t sfb_row0 = static_cast<int32_t>(2 * ((ti.b_row / 128) * P.k_atoms + ti.kb0));
+                const int32_t sfb_row1 = static_cast<int32_t>(2 * ((ti.b_row / 128 + 1) * P.k_atoms + ti.kb0));
                 bool stop = false;
-                for (int kb = 0; kb < P.num_kb; ++kb) {
+                for (int kb = 0; kb < ti.nkb; ++kb) {
                     if (!wait_phase(empty_bar(stage), phase ^ 1u, guard)) { stop = true; break; }
                     const uint32_t fb = full0 + 8u * stage;
                     if (leader) mbar_arrive_expect_tx(fb, 2u * L::kStageBytes);
                     const uint32_t ssb = sbase + L::kOffSfb + stage * L::kSfbBytes;
-                    const int32_t kx = kb * kBK;
-                    tma_load_2d_pair(sbase + L::kOffA + stage * L::kABytes, &maps.a[pt.prob], kx, ma, fb);
+                    const int32_t kx = static_cast<int32_t>((ti.kb0 + kb) * kBK);
+                    tma_load_2d_pair(sbase + L::kOffA + stage * L::kABytes, ma_map, kx, ma, fb);
                     if constexpr (!kMnMajor)
-                        tma_load_2d_pair(sbase + L::kOffB + stage * L::kBBytes, &maps.b[pt.prob], kx, nb, fb);
+                        tma_load_2d_pair(sbase + L::kOffB + stage * L::kBBytes, mb_map, kx, nb, fb);
                     else   // B stored [K, N]: this CTA's 128 columns x 128 K-rows
-                        tma_load_2d_pair(sbase + L::kOffB + stage * L::kBBytes, &maps.b[pt.prob], nb, kx, fb);
-                    tma_load_2d_pair(sbase + L::kOffSfa + stage * 512, &maps.sfa[pt.prob], 0, sfa_row + 2 * kb, fb);
-                    tma_load_2d_pair(ssb, &maps.sfb[pt.prob], 0, sfb_row0 + 2 * kb, fb);
-                    tma_load_2d_pair(ssb + 512, &maps.sfb[pt.prob], 0, sfb_row1 + 2 * kb, fb);
+                        tma_load_2d_pair(sbase + L::kOffB + stage * L::kBBytes, mb_map, nb, kx, fb);
+                    tma_load_2d_pair(sbase + L::kOffSfa + stage * 512, &maps.sfa[ti.prob], 0, sfa_row + 2 * kb, fb);
+                    tma_load_2d_pair(ssb, &maps.sfb[ti.prob], 0, sfb_row0 + 2 * kb, fb);
+                    tma_load_2d_pair(ssb + 512, &maps.sfb[ti.prob], 0, sfb_row1 + 2 * kb, fb);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (stop) break;
@@ -938,8 +1099,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 if (lane == 0) got = spin_phase(tempty_bar, acc_phase ^ 1u, guard) ? 1 : 0;
                 if (!__shfl_sync(0xFFFFFFFFu, got, 0)) { ok = false; break; }
                 tc_fence_after();
-                const int q = problem_of(p, t);
-                const int nkb = p.pr[q].num_kb;
+                const int q = kMode == kDense || kMode == kDenseQuant ? problem_of(p, t) : 0;
+                const int nkb = kMode == kGroupedK ? pair_tile_info<kMode>(sch, p, t, 0).nkb : p.pr[q].num_kb;
                 const int64_t K = p.pr[q].K;
                 const uint32_t fmt_bits = p.pr[q].fmt_bits;
                 for (int kb = 0; kb < nkb; ++kb) {
@@ -953,7 +1114,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
                     const uint64_t sfa_d = sfa_desc0 + static_cast<uint64_t>((stage * 512) >> 4);
                     const uint64_t sfb_d = sfb_desc0 + static_cast<uint64_t>((stage * L::kSfbBytes) >> 4);
-                    const int64_t k_left = K - static_cast<int64_t>(kb) * kBK;
+                    const int64_t k_left = kMode == kGroupedK ? static_cast<int64_t>(nkb - kb) * kBK
+                                                              : K - static_cast<int64_t>(kb) * kBK;
                     const int ksub = k_left >= kBK ? kBK / kUmmaK : static_cast<int>(k_left) / kUmmaK;
                     if (elect_one()) {
                         // this stage's scale atoms into its tensor-memory columns (each CTA its own)
@@ -996,8 +1158,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
         for (int64_t r = 0; r * n_pairs < total; ++r) {
             const int64_t t = item_of(r);
             if (t >= total) continue;
-            const PairTile pt = pair_tile(p, t);
-            const Problem& P = p.pr[pt.prob];
+            const PairTileInfo ti = pair_tile_info<kMode>(sch, p, t, rank);
+            const Problem& P = p.pr[ti.prob];
             // One thread waits (suspending), the other epilogue warps sleep on a
             // named barrier; barrier 2 keeps the verdict until every warp read it.
             if (warp == 2 && lane == 0) *epi_flag = wait_phase(tfull_bar, acc_phase, guard) ? 1 : 0;
@@ -1019,13 +1181,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 else mbar_arrive_cluster(tempty_leader);
             }
             acc_phase ^= 1u;
-            const int64_t mc = pt.m0 + 128 * rank;   // this CTA's first row
-            const int64_t row_hi = min(mc + 128, P.M);
-            if constexpr (kMode == kDense)
-                store_staged(P, v, sbase + L::kOffStage + (warp - 2) * L::kStageWarpBytes, mc + 32 * quad,
-                             mc + 32 * quad, mc, row_hi, pt.n0 + half * 128, lane, &maps.y[pt.prob], pending);
+            if (ti.nkb == 0) {  // no K blocks (an empty expert): the tile is zero
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[c][j] = 0u;
+            }
+            if constexpr (L::kStaged)
+                store_staged(P, v, sbase + L::kOffStage + (warp - 2) * L::kStageWarpBytes,
+                             ti.y_row0 + ti.m0 + 32 * quad, ti.m0 + 32 * quad, ti.row_lo, ti.row_hi,
+                             ti.n0 + half * 128, lane, &maps.y[ti.prob], pending);
             else
-                store_row<kMode>(p, P, v, mc + 32 * quad + lane, mc, row_hi, 0, pt.n0 + half * 128, mc < P.M);
+                store_row<kMode>(p, P, v, ti.m0 + 32 * quad + lane, ti.row_lo, ti.row_hi, 0, ti.n0 + half * 128,
+                                 ti.m0 < P.M);
         }
         if (lane == 0) bulk_wait_all();   // this warp's tiled stores complete before the CTA ends
         __syncwarp();
@@ -1149,6 +1317,14 @@ bool make_tma_scales(CUtensorMap* map, const void* ptr, int64_t bands, int64_t k
                                 2u, false);
 }
 
+// Scale maps and the scale-row range check of a pair launch: an operand with
+// `bands` 128-row bands of k_atoms atoms (rows up to two bands past the end are
+// addressed, and read as zeros).
+bool pair_scale_map(CUtensorMap* map, const void* ptr, int64_t bands, int64_t k_atoms) {
+    if ((bands + 2) * k_atoms * 2 >= (int64_t(1) << 31)) return false;
+    return make_tma_scales(map, ptr, bands, k_atoms);
+}
+
 // The problems of one dense pair launch (K descending, as fill_dense orders
 // them), their 256 x 256 pair tiles laid out back to back.  False when a tensor
 // map cannot be encoded or a scale map's rows exceed its 32-bit coordinates
@@ -1165,8 +1341,6 @@ bool fill_dense_pair(const DenseGemm* gemms, int count, bool b_mn_major, PairMap
         const DenseGemm& g = gemms[order[i]];
         const int64_t k_atoms = (g.K + 127) / 128;
         const int64_t a_bands = (g.M + 127) / 128, b_bands = (g.N + 127) / 128;
-        if ((a_bands + 1) * k_atoms * 2 >= (int64_t(1) << 31) || (b_bands + 2) * k_atoms * 2 >= (int64_t(1) << 31))
-            return false;
         if (!make_tma_u8(&maps->a[i], g.a_q, static_cast<uint64_t>(g.M), static_cast<uint64_t>(g.K), 128)) return false;
         if (!b_mn_major) {
             if (!make_tma_u8(&maps->b[i], g.b_q, static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.K), 128))
@@ -1174,8 +1348,8 @@ bool fill_dense_pair(const DenseGemm* gemms, int count, bool b_mn_major, PairMap
         } else if (!make_tma_u8(&maps->b[i], g.b_q, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.N), kBK)) {
             return false;
         }
-        if (!make_tma_scales(&maps->sfa[i], g.a_s, a_bands, k_atoms) ||
-            !make_tma_scales(&maps->sfb[i], g.b_s, b_bands, k_atoms))
+        if (!pair_scale_map(&maps->sfa[i], g.a_s, a_bands, k_atoms) ||
+            !pair_scale_map(&maps->sfb[i], g.b_s, b_bands, k_atoms))
             return false;
         args->pr[i] = make_problem(g.a_s, g.b_s, g.y, g.M, g.N, g.K, g.ldy, k_atoms, b_bands,
                                    fmt_bits_of(g.a_fmt, g.b_fmt));
@@ -1191,8 +1365,9 @@ bool fill_dense_pair(const DenseGemm* gemms, int count, bool b_mn_major, PairMap
 }
 
 template <bool kMnMajor, int kMode>
-cudaError_t launch_pair_t(const DeviceInfo& dev, const PairMaps& maps, const GemmArgs& args, cudaStream_t stream) {
-    using L = PairCfg;
+cudaError_t launch_pair_t(const DeviceInfo& dev, const PairMaps& maps, const GemmArgs& args, int64_t max_tiles,
+                          cudaStream_t stream) {
+    using L = PairCfg<kMode>;
     auto kern = gemm_mxf8_pair_kernel<kMnMajor, kMode>;
     static thread_local int configured_device = -1;  // attribute set once per device and thread
     if (configured_device != dev.device) {
@@ -1201,7 +1376,7 @@ cudaError_t launch_pair_t(const DeviceInfo& dev, const PairMaps& maps, const Gem
         configured_device = dev.device;
     }
     int64_t pairs = dev.sm_count / 2;
-    if (args.items < pairs) pairs = args.items;
+    if (max_tiles >= 0 && max_tiles < pairs) pairs = max_tiles;
     if (pairs <= 0) return cudaSuccess;
     kern<<<static_cast<unsigned>(2 * pairs), L::kThreads, L::kAlloc, stream>>>(maps, args);
     return cudaGetLastError();
@@ -1219,8 +1394,8 @@ cudaError_t try_pair(const DeviceInfo& dev, const DenseGemm* gemms, int count, b
     args.yq = yq;
     args.ys = ys;
     *done = true;
-    if (b_mn_major) return launch_pair_t<true, kMode>(dev, maps, args, stream);
-    return launch_pair_t<false, kMode>(dev, maps, args, stream);
+    if (b_mn_major) return launch_pair_t<true, kMode>(dev, maps, args, args.items, stream);
+    return launch_pair_t<false, kMode>(dev, maps, args, args.items, stream);
 }
 
 }  // namespace
@@ -1268,6 +1443,25 @@ cudaError_t launch_grouped_gemm(const DeviceInfo& dev, const void* a_q, const vo
                                 const void* b_q, const void* b_s, const int64_t* offsets, int G,
                                 int64_t M_total, int64_t N, int64_t K, int64_t a_bands_cap, void* y,
                                 int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream) {
+    if (G <= PairCfg<kGroupedRows>::kMaxGroups && dev.sm_count >= 2) {   // CTA pairs
+        PairMaps pm;
+        const int64_t k_atoms = (K + 127) / 128;
+        const int64_t a_bands = a_bands_cap > 0 ? a_bands_cap : (M_total + 127) / 128;
+        const int64_t b_bands = static_cast<int64_t>(G) * N / 128;
+        if (make_tma_u8(&pm.a[0], a_q, static_cast<uint64_t>(M_total), static_cast<uint64_t>(K), kBM) &&
+            make_tma_u8(&pm.b[0], b_q, static_cast<uint64_t>(G) * static_cast<uint64_t>(N), static_cast<uint64_t>(K),
+                        128) &&
+            pair_scale_map(&pm.sfa[0], a_s, a_bands, k_atoms) && pair_scale_map(&pm.sfb[0], b_s, b_bands, k_atoms)) {
+            GemmArgs args = base_args(dev);
+            args.pr[0] = make_problem(a_s, b_s, y, M_total, N, K, ldy, k_atoms, b_bands, fmt_bits_of(a_fmt, b_fmt));
+            args.pr[0].n_tiles = (N + 255) / 256;
+            set_store_map(&pm.y[0], &args.pr[0], y, M_total, N, ldy);
+            args.offsets = offsets;
+            args.G = G;
+            args.a_bands_cap = a_bands_cap;
+            return launch_pair_t<false, kGroupedRows>(dev, pm, args, -1, stream);
+        }
+    }
     TensorMaps maps;
     if (!make_tma_u8(&maps.a[0], a_q, static_cast<uint64_t>(M_total), static_cast<uint64_t>(K), kBM))
         return cudaErrorInvalidValue;
@@ -1288,6 +1482,25 @@ cudaError_t launch_grouped_gemm_wgrad(const DeviceInfo& dev, const void* a_q, co
                                       const void* b_q, const void* b_s, const int64_t* offsets, int G,
                                       int64_t M_total, int64_t capacity, int64_t M, int64_t N, void* y,
                                       int64_t ldy, int a_fmt, int b_fmt, cudaStream_t stream) {
+    if (G <= PairCfg<kGroupedK>::kMaxGroups && dev.sm_count >= 2) {   // CTA pairs
+        PairMaps pm;
+        const int64_t k_atoms = capacity / 128;
+        if (make_tma_u8(&pm.a[0], a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(capacity), kBM) &&
+            make_tma_u8(&pm.b[0], b_q, static_cast<uint64_t>(N), static_cast<uint64_t>(capacity), 128) &&
+            pair_scale_map(&pm.sfa[0], a_s, (M + 127) / 128, k_atoms) &&
+            pair_scale_map(&pm.sfb[0], b_s, (N + 127) / 128, k_atoms)) {
+            GemmArgs args = base_args(dev);
+            args.pr[0] = make_problem(a_s, b_s, y, M, N, capacity, ldy, k_atoms, (N + 127) / 128,
+                                      fmt_bits_of(a_fmt, b_fmt));
+            args.pr[0].m_tiles = (M + 255) / 256;   // pair tiles per expert
+            args.pr[0].n_tiles = (N + 255) / 256;
+            set_store_map(&pm.y[0], &args.pr[0], y, static_cast<int64_t>(G) * M, N, ldy);   // y[g] stacked
+            args.M_total = M_total;
+            args.offsets = offsets;
+            args.G = G;
+            return launch_pair_t<false, kGroupedK>(dev, pm, args, -1, stream);
+        }
+    }
     TensorMaps maps;
     if (!make_tma_u8(&maps.a[0], a_q, static_cast<uint64_t>(M), static_cast<uint64_t>(capacity), kBM))
         return cudaErrorInvalidValue;
