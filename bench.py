@@ -1097,6 +1097,46 @@ def run_gpu(args):
         if st != 0:
             raise SystemExit(f"device status {st} after the end-to-end steps")
 
+    # ---- the workload's quantizers timed alone (same kernels and sizes, no GEMM
+    # between them): the in-step rate above follows the GEMMs' power draw, which
+    # lowers the clock the quantizers then run at
+    quant_alone = None
+    quant_alone_launches = 0
+    quant_kern = [k for k in kern if k[1] == "quant"]
+    if quant_kern and not args.no_quant_alone:
+        # the power state the GEMMs leave takes tens of milliseconds to settle: idle first
+        torch.cuda.synchronize()
+        time.sleep(1.0)
+        ev_q = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for s in range(args.warmup):
+            flush.fill_(s & 0xFF)
+            for (_, _, _, fn) in quant_kern:
+                fn()
+        torch.cuda.synchronize()
+        sampler_q = ClockSampler(dev.index)
+        sampler_q.start()
+        time.sleep(0.3)
+        tq0 = time.time()
+        for s in range(args.steps):
+            flush.fill_(s & 0xFF)
+            ev_q[s][0].record(stream)
+            for (_, _, _, fn) in quant_kern:
+                fn()
+            ev_q[s][1].record(stream)
+        torch.cuda.synchronize()
+        tq1 = time.time()
+        time.sleep(0.2)
+        sampler_q.stop()
+        q_s = sum(e[0].elapsed_time(e[1]) for e in ev_q) / 1e3
+        q_gbs = sum(k[2] for k in quant_kern) * args.steps / q_s / 1e9
+        quant_alone = {"bound": "hbm", "kernel": "quant kernels (timed alone)", "achieved": round(q_gbs, 1),
+                       "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(q_gbs / peaks["hbm_gbs"], 4),
+                       "peak_source": peaks["source"] + " copy bandwidth",
+                       "clocks": sampler_q.summary(tq0 - 0.05, tq1 + 0.05),
+                       "how": "the step's quantizer launches only, after 1 s idle, L2 flushed before each step, "
+                              "CUDA events"}
+        quant_alone_launches = args.steps * sum(LAUNCHES_PER_ENTRY.get(k[0], 1) for k in quant_kern)
+
     # ---- further workloads timed in the same process (device side only)
     extra = {}
     extra_launches = 0
@@ -1133,10 +1173,11 @@ def run_gpu(args):
                 "gemm_tflops": round(r["gemm_tflops"], 1), "gemm_frac_peak": round(r["gemm_frac"], 4),
                 "quant_tbs": round(r["quant_gbs"] / 1e3, 3), "quant_frac_hbm": round(r["quant_frac"], 4),
                 "kernels_ms": r["kernels_ms"],
-                "roofline": roofline, "roofline_quant": roofline_quant,
+                "roofline": roofline, "roofline_quant": roofline_quant, "roofline_quant_alone": quant_alone,
                 "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": own_launches * args.steps + extra_launches,
-                "gpu_launches_split": {w.name: own_launches * args.steps, "extra_workloads": extra_launches},
+                "gpu_launches": own_launches * args.steps + extra_launches + quant_alone_launches,
+                "gpu_launches_split": {w.name: own_launches * args.steps, "extra_workloads": extra_launches,
+                                       "quant_alone": quant_alone_launches},
                 "clocks": main_clocks, "vendor_mxfp8_tflops": vendor, "impl": "mxq"}
         if r["other_hbm"]:
             line["hbm_kernels"] = r["other_hbm"]
@@ -1246,6 +1287,8 @@ def main(argv=None):
     ap.add_argument("--extra-workloads", default=DEFAULT_EXTRA,
                     help="comma-separated workloads timed after the main one in the same process "
                          "(device side only), or 'none'")
+    ap.add_argument("--no-quant-alone", action="store_true",
+                    help="do not time the workload's quantizers alone (without the GEMMs between them)")
     ap.add_argument("--no-vendor-peak", action="store_true",
                     help="do not time the vendor MXFP8 GEMM (the GEMM peak is then 2 x the BF16 burst)")
     ap.add_argument("--no-e2e", action="store_true")
