@@ -80,6 +80,7 @@ struct GemmArgs {
                              // (each group's rows tiled on their own, at most this many bands)
     uint8_t* yq;             // quantizing epilogue: E4M3 payload [M, N] (row stride N)
     uint8_t* ys;             //   and its MMA-tiled scales [M, N/32]
+    int yq_tma;              // 1: PairMaps::yq maps yq (32 x 32 tiled payload stores)
     unsigned int* status;
     uint64_t wait_limit_ns;
 };
@@ -389,6 +390,90 @@ __device__ __forceinline__ void store_row(const GemmArgs& a, const Problem& p, u
             }
         }
     }
+}
+
+// The quantizing epilogue of the pair kernel, staged like store_staged: for
+// each 32-column chunk the warp's 32 rows write their BF16 values (when y is
+// written; 64-byte swizzled rows, as store_staged) and their E4M3 payload bytes
+// (32-byte rows) to shared memory, and each leaves with one tiled bulk store;
+// the four scale codes a thread holds per 128 columns are one 4-byte word of a
+// tiled scale atom, stored directly.  The arithmetic is store_row's.  When the
+// warp's rows are not all stored (a ragged M) or a map is missing, store_row
+// takes the tile.  `pending`: this warp's last bulk stores may still read the
+// buffers.
+__device__ __forceinline__ void store_quant_staged(const GemmArgs& a, const Problem& p, uint32_t (&v)[4][32],
+                                                   uint32_t stage_y, uint32_t stage_q, int64_t row0,
+                                                   int64_t row_lo, int64_t row_hi, int64_t n, int lane,
+                                                   const CUtensorMap* ymap, const CUtensorMap* qmap,
+                                                   bool tile_in, bool& pending) {
+    const bool rows_whole = row0 >= row_lo && row0 + 32 <= row_hi;
+    const bool with_y = p.y != nullptr;
+    if (!rows_whole || !a.yq_tma || (with_y && !p.y_tma)) {
+        store_row<kDenseQuant>(a, p, v, row0 + lane, row_lo, row_hi, 0, n, tile_in);
+        return;
+    }
+    const int64_t row = row0 + lane;
+    const int64_t ngroups = p.N >> 5;
+    const int64_t g0 = n >> 5;    // a multiple of 4
+    const uint32_t wrow = stage_y + 64u * static_cast<uint32_t>(lane);
+    const uint32_t wswz = static_cast<uint32_t>((lane >> 1) & 3);
+    const uint32_t qrow = stage_q + 32u * static_cast<uint32_t>(lane);
+    uint32_t codes = 0u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int64_t nc = n + c * 32;
+        const bool grp_ok = nc < p.N;
+        uint32_t b[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            b[i] = cvt_bf16x2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1]));
+        uint32_t m2 = 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m2 = max_abs_bf16x2(m2, b[i]);
+        m2 &= 0x7FFF7FFFu;
+        const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+        uint32_t o[8];
+        uint32_t code;
+        if (m >= 0x7F80u) {  // NaN or Inf in the group
+            code = 0xFFu;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[j] = nan_bytes4(b[2 * j], b[2 * j + 1]);
+        } else {
+            const int e = rceil_exponent<0>(m);
+            const uint32_t s2 = pow2_neg_bf16(e) * 0x10001u;
+            code = static_cast<uint32_t>(e + 127);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t p0 = mul_bf16x2(b[2 * j], s2), p1 = mul_bf16x2(b[2 * j + 1], s2);
+                o[j] = cvt_fp8x2<0>(bf16_lo(p0), bf16_hi(p0)) | (cvt_fp8x2<0>(bf16_lo(p1), bf16_hi(p1)) << 16);
+            }
+        }
+        codes |= (grp_ok ? code : 0u) << (8 * c);
+        if (pending) {   // the previous chunk's bulk stores still read the buffers
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            pending = false;
+        }
+        if (with_y) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                sts128(wrow + 16u * (static_cast<uint32_t>(j) ^ wswz),
+                       make_uint4(b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]));
+        }
+        sts128(qrow, make_uint4(o[0], o[1], o[2], o[3]));
+        sts128(qrow + 16u, make_uint4(o[4], o[5], o[6], o[7]));
+        fence_proxy_async_smem();   // the buffers are read by the bulk copies (async proxy)
+        __syncwarp();
+        if (lane == 0 && grp_ok) {
+            if (with_y) tma_store_2d(ymap, static_cast<int32_t>(nc), static_cast<int32_t>(row0), stage_y);
+            tma_store_2d(qmap, static_cast<int32_t>(nc), static_cast<int32_t>(row0), stage_q);
+            bulk_commit_group();
+        }
+        pending = grp_ok;
+    }
+    // The 4 groups are 4 consecutive bytes of one tiled scale atom.
+    if (tile_in && g0 < ((ngroups + 3) & ~static_cast<int64_t>(3)))
+        *reinterpret_cast<uint32_t*>(a.ys + tiled_scale_offset(row, g0, ngroups)) = codes;
 }
 
 // Wait for the accumulator hand-off between the MMA warp and the epilogue, on
@@ -785,9 +870,10 @@ struct PairCfg {
     static constexpr int kOffSched = (kOffEpiFlag + 4 + 15) / 16 * 16;
     static constexpr int kSchedBytes = kGrouped ? 4 * (kMaxGroups + 1) + 4 * kMaxGroups : 0;
     static constexpr int kOffStage = (kOffSched + kSchedBytes + 1023) / 1024 * 1024;   // 64-byte swizzle atoms
-    static constexpr int kStageWarpBytes = 32 * 32 * 2;
-    static constexpr bool kStaged = kMode != kDenseQuant;
-    static constexpr int kBytes = kOffStage + (kStaged ? kEpiWarps * kStageWarpBytes : 0);
+    static constexpr int kStageWarpBytes = 32 * 32 * 2;                 // BF16 chunk of 32 rows
+    static constexpr int kQStageWarpBytes = kMode == kDenseQuant ? 32 * 32 : 0;   // E4M3 chunk of 32 rows
+    static constexpr int kOffQStage = kOffStage + kEpiWarps * kStageWarpBytes;
+    static constexpr int kBytes = kOffQStage + kEpiWarps * kQStageWarpBytes;
     static constexpr int kAlloc = kBytes + 1024;
     static constexpr int kTmemSfa = 256;               // one 256-column accumulator, then the scales
     static constexpr int kTmemSfb = kTmemSfa + 4 * kStages;
@@ -800,6 +886,7 @@ struct PairCfg {
 // Scales: the MMA-tiled bytes of an operand viewed as rows of 256 bytes, one
 // 512-byte atom = a box of 2 rows.
 struct PairMaps {
+    CUtensorMap yq;          // quantizing epilogue: the E4M3 payload [M, N]
     CUtensorMap a[kMaxProblems];
     CUtensorMap b[kMaxProblems];
     CUtensorMap sfa[kMaxProblems];
@@ -1187,13 +1274,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kMode>::kThr
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[c][j] = 0u;
             }
-            if constexpr (L::kStaged)
+            if constexpr (kMode == kDenseQuant)
+                store_quant_staged(p, P, v, sbase + L::kOffStage + (warp - 2) * L::kStageWarpBytes,
+                                   sbase + L::kOffQStage + (warp - 2) * L::kQStageWarpBytes, ti.m0 + 32 * quad,
+                                   ti.row_lo, ti.row_hi, ti.n0 + half * 128, lane, &maps.y[ti.prob], &maps.yq,
+                                   ti.m0 < P.M, pending);
+            else
                 store_staged(P, v, sbase + L::kOffStage + (warp - 2) * L::kStageWarpBytes,
                              ti.y_row0 + ti.m0 + 32 * quad, ti.m0 + 32 * quad, ti.row_lo, ti.row_hi,
                              ti.n0 + half * 128, lane, &maps.y[ti.prob], pending);
-            else
-                store_row<kMode>(p, P, v, ti.m0 + 32 * quad + lane, ti.row_lo, ti.row_hi, 0, ti.n0 + half * 128,
-                                 ti.m0 < P.M);
         }
         if (lane == 0) bulk_wait_all();   // this warp's tiled stores complete before the CTA ends
         __syncwarp();
@@ -1393,6 +1482,11 @@ cudaError_t try_pair(const DeviceInfo& dev, const DenseGemm* gemms, int count, b
     if (!fill_dense_pair(gemms, count, b_mn_major, &maps, &args)) return cudaSuccess;
     args.yq = yq;
     args.ys = ys;
+    args.yq_tma = 0;
+    if (yq != nullptr && gemms[0].M > 0 && gemms[0].M < (int64_t(1) << 31) - 32 &&
+        encode_tensor_map_u8_store(&maps.yq, yq, static_cast<uint64_t>(gemms[0].N),
+                                   static_cast<uint64_t>(gemms[0].M), static_cast<uint64_t>(gemms[0].N)))
+        args.yq_tma = 1;
     *done = true;
     if (b_mn_major) return launch_pair_t<true, kMode>(dev, maps, args, args.items, stream);
     return launch_pair_t<false, kMode>(dev, maps, args, args.items, stream);

@@ -31,6 +31,8 @@ bool encode_tensor_map_2d(CUtensorMap* map, const void* base, bool two_byte_elem
 // 64-byte swizzle.
 bool encode_tensor_map_bf16_store(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                                   uint64_t ld);
+// Bytes [rows, cols] (row stride ld bytes) for 32 x 32 tiled stores, no swizzle.
+bool encode_tensor_map_u8_store(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t ld);
 bool encode_tensor_map_3d(CUtensorMap* map, const void* base, bool two_byte_elems, uint64_t inner,
                           uint64_t mid, uint64_t outer, uint64_t mid_stride_bytes,
                           uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_mid);
