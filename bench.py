@@ -55,10 +55,11 @@ L2_BYTES = 129 * 10**6
 # stands; None where not captured (or captured before the kernel last changed).
 GEMM_TRAFFIC_BYTES = {
     # gemm_mxf8_pair_kernel<0,0> (ncu dram__bytes_read/write.sum, the second step's
-    # launches): forward 5.68 GB read + 0.531 GB written, dgrad + wgrad 11.53 + 1.07 GB
-    "sweep_16384": int((5.68e9 + 0.531e9 + 11.53e9 + 1.07e9) / 2),
-    # the same kernel at 8192x4096x4096: forward 52.0 + 33.6 MB, dgrad + wgrad 136.9 + 65.4 MB
-    "linear_train": int((52.0e6 + 33.6e6 + 136.9e6 + 65.4e6) / 2),
+    # launches; the kernel as it stands): forward 7.57 GB read + 0.533 GB written,
+    # dgrad + wgrad 15.32 + 1.07 GB (an earlier call of the same code read 5.68 / 11.53 GB)
+    "sweep_16384": int((7.57e9 + 0.533e9 + 15.32e9 + 1.07e9) / 2),
+    # the same kernel at 8192x4096x4096: forward 51.96 + 33.59 MB, dgrad + wgrad 137.59 + 65.59 MB
+    "linear_train": int((51.96e6 + 33.59e6 + 137.59e6 + 65.59e6) / 2),
 }
 DEFAULT_WORKLOAD = "sweep_16384"
 DEFAULT_EXTRA = "moe_grouped"
