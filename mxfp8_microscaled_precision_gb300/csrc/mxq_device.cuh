@@ -305,10 +305,14 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA).
+// Arrive on an mbarrier given by its shared::cluster address (possibly in the
+// peer CTA), release at CTA scope.  Used where the arriving thread has nothing
+// left to publish to the peer: the epilogue's tensor-memory loads have retired
+// (tcgen05.wait::ld) and tcgen05.fence::before_thread_sync orders them before
+// the arrive.  A cluster-scope release here waited for this thread's earlier
+// memory traffic and cost ~2000 cycles per tile hand-off (measured).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
-                 : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }
 
 // 2-D tiled tensor load into this CTA's shared memory whose completion is
