@@ -54,12 +54,12 @@ L2_BYTES = 129 * 10**6
 # GEMM launches like `units_per_launch`, from an ncu capture of the kernel as it
 # stands; None where not captured (or captured before the kernel last changed).
 GEMM_TRAFFIC_BYTES = {
-    # gemm_mxf8_pair_kernel<0,0> (ncu dram__bytes_read/write.sum, the second step's
-    # launches; the kernel as it stands): forward 7.57 GB read + 0.533 GB written,
-    # dgrad + wgrad 15.32 + 1.07 GB (an earlier call of the same code read 5.68 / 11.53 GB)
-    "sweep_16384": int((7.57e9 + 0.533e9 + 15.32e9 + 1.07e9) / 2),
-    # the same kernel at 8192x4096x4096: forward 51.96 + 33.59 MB, dgrad + wgrad 137.59 + 65.59 MB
-    "linear_train": int((51.96e6 + 33.59e6 + 137.59e6 + 65.59e6) / 2),
+    # gemm_mxf8_pair_kernel<0,0> as it stands (ncu dram__bytes_read/write.sum, the second
+    # step's launches): forward 9.97 GB read + 0.534 GB written, dgrad + wgrad 22.02 + 1.07 GB;
+    # the re-reads of B vary between calls (5.7-10 GB for the forward)
+    "sweep_16384": int((9.97e9 + 0.534e9 + 22.02e9 + 1.07e9) / 2),
+    # the same kernel at 8192x4096x4096: forward 51.96 + 33.93 MB, dgrad + wgrad 138.15 + 65.79 MB
+    "linear_train": int((51.96e6 + 33.93e6 + 138.15e6 + 65.79e6) / 2),
 }
 DEFAULT_WORKLOAD = "sweep_16384"
 DEFAULT_EXTRA = "moe_grouped"
