@@ -208,6 +208,87 @@ __device__ __forceinline__ void row_pass(ChunkOf chunk_of, int64_t r0, int64_t c
     }
 }
 
+// Row copy of a staged tile (the dual kernels; the tile is 128 rows of 256
+// bytes): lane l of warp w owns the 32-column group l % 4 of tile rows
+// 16 w + l / 4 and 16 w + 8 + l / 4, reads it as four 16-byte chunks, reduces,
+// scales and converts it in registers and stores it as one 32-byte run, so four
+// lanes write a row's 128 contiguous bytes.  A lane reads its chunks in the
+// order i ^ rot, rot = (group & 2) | (row & 1): the 8 lanes of a load phase (two
+// rows, four groups) then hit 8 different 16-byte bank groups.  A group's scale
+// byte goes to its place in the plain or tiled layout (tiled padding gets 0).
+template <bool kTiled, int kFmt>
+__device__ __forceinline__ void row_pass_tile(uint32_t tile, int64_t r0, int64_t c0, int64_t rows, int64_t cols,
+                                              uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row) {
+    const int t = threadIdx.x;
+    const int warp = t >> 5, lane = t & 31;
+    const int g = lane & 3;                  // 32-column group of the tile
+    const int64_t col = c0 + 32 * g;
+    const int64_t groups = cols >> 5;
+    const bool col_ok = col < cols;
+    const bool v8 = (reinterpret_cast<uintptr_t>(q_row) & 31u) == 0;   // runs are 32-byte aligned
+    const int rot = (g & 2) | ((lane >> 2) & 1);
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int r = 16 * warp + 8 * it + (lane >> 2);
+        const int64_t row = r0 + r;
+        const bool valid = col_ok && row < rows;
+        const uint32_t rowaddr = tile + static_cast<uint32_t>(r * 256 + 64 * g);
+        uint4 v[4];   // v[i]: chunk i ^ rot of the group
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = lds128(rowaddr + 16u * static_cast<uint32_t>(i ^ rot));
+        uint32_t a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = max_abs_bf16x2(max_abs_bf16x2(v[i].x, v[i].y), max_abs_bf16x2(v[i].z, v[i].w));
+        const uint32_t m2 = max_abs_bf16x2(max_abs_bf16x2(a[0], a[1]), max_abs_bf16x2(a[2], a[3])) & 0x7FFF7FFFu;
+        const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+        uint8_t code;
+        uint32_t o[8];   // o[2 i], o[2 i + 1]: the payload bytes of chunk i ^ rot
+        if (m >= 0x7F80u) {  // NaN or Inf in the group
+            code = 0xFF;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint2 n = nan8(v[i]);
+                o[2 * i] = n.x;
+                o[2 * i + 1] = n.y;
+            }
+        } else {
+            const int e = rceil_exponent<kFmt>(m);
+            code = static_cast<uint8_t>(e + 127);
+            const uint32_t s2 = pow2_neg_bf16(e) * 0x10001u;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint2 q = quant8<kFmt>(v[i], s2);
+                o[2 * i] = q.x;
+                o[2 * i + 1] = q.y;
+            }
+        }
+        // back to chunk order: undo the XOR with rot one bit at a time
+        if (rot & 1) {
+#pragma unroll
+            for (int k = 0; k < 8; k += 4) {
+                uint32_t x = o[k]; o[k] = o[k + 2]; o[k + 2] = x;
+                x = o[k + 1]; o[k + 1] = o[k + 3]; o[k + 3] = x;
+            }
+        }
+        if (rot & 2) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t x = o[k]; o[k] = o[k + 4]; o[k + 4] = x;
+            }
+        }
+        if (valid) {
+            uint8_t* dst = q_row + row * cols + col;
+            if (v8) {
+                stg256(dst, o);
+            } else {
+                reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+        }
+        if (valid || kTiled) store_scale(s_row, row, col >> 5, groups, kTiled, valid ? code : 0);
+    }
+}
+
 // Loads this thread's 8 chunks of tile (r0, c0) straight from global memory
 // (zeros outside the matrix).
 __device__ __forceinline__ void load_tile_chunks(uint4 (&v)[kLoadsPerThread], const uint16_t* __restrict__ x,
@@ -344,7 +425,7 @@ __device__ __forceinline__ void col_pass(const uint32_t* tw_ptr, int64_t c0, int
 // Column copy (with or without the row copy): persistent, TMA-fed ring.
 // Column pass: thread t takes the column pair t % 64 and the 32-row group
 // t / 64; a warp reads 128 contiguous bytes of one staged row per step, so
-// the shared-memory reads are conflict-free.
+// the shared-memory reads are conflict-free.  Row pass: row_pass_tile.
 template <bool kRow, bool kTiled, int kFmt>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_kernel(
     const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_t cols,
@@ -356,7 +437,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_kernel(
     const WaitGuard guard{ring.abort_flag, status, wait_limit_ns};
     ring_start(ring, &tmap, tg);
 
-    const int t = threadIdx.x;
     int i = 0;
     int64_t tile = blockIdx.x;
     for (; tile < tg.n_tiles; tile += gridDim.x, ++i) {
@@ -364,11 +444,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quant_cols_kernel(
         const uint8_t* buf = ring.buf + (i % kRing) * kTileBytes;
         int64_t b, r0, c0;
         tg.at(tile, b, r0, c0);
-        if constexpr (kRow) {
-            const uint32_t b4 = smem_u32(buf) + 16u * static_cast<uint32_t>((t >> 4) * 16 + (t & 15));
-            row_pass<kTiled, kFmt>([&](int j) { return lds128(b4 + 4096u * j); }, r0, c0, rows, cols,
-                                   q_row + b * bs.q_row, s_row + b * bs.s_row);
-        }
+        if constexpr (kRow)
+            row_pass_tile<kTiled, kFmt>(smem_u32(buf), r0, c0, rows, cols, q_row + b * bs.q_row, s_row + b * bs.s_row);
         col_pass<kTiled, kFmt>(reinterpret_cast<const uint32_t*>(buf), c0, cols, rows, r0, rows,
                          q_col + b * bs.q_col, s_col + b * bs.s_col);
         ring_release(ring, &tmap, i, tile, tg);
