@@ -129,6 +129,35 @@ def test_column_copy_at_16_byte_alignment(fmt):
     assert np.array_equal(u8(qc_odd), oq)
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_dual_row_copy_at_16_byte_alignment(fmt):
+    """The dual kernel's row copy into a buffer 16 (not 32) bytes past an
+    aligned address (its 32-byte runs then leave as two 16-byte stores), on a
+    ragged shape (rows and columns past the last full tile): the same bytes as
+    into an aligned buffer and as the oracle, nothing written outside."""
+    from oracle import oracle
+    mxq = _mxq()
+    R, C = 224, 352                 # multiples of 32 (the column copy's groups), not of the 128-row tile
+    x = torch.randn(R, C).to(torch.bfloat16)
+    xd = x.cuda()
+    base = torch.full((R * C + 64,), 0xEE, dtype=torch.uint8, device="cuda")
+    off = (32 - base.data_ptr() % 32) % 32 + 16
+    qr_odd = base[off:off + R * C].view(1, R, C)
+    assert qr_odd.data_ptr() % 32 == 16
+    sr = torch.empty(mxq.scale_bytes(R, C), dtype=torch.uint8, device="cuda")
+    qc = torch.empty((1, C, R), dtype=torch.uint8, device="cuda")
+    sc = torch.empty(mxq.scale_bytes(C, R), dtype=torch.uint8, device="cuda")
+    qr_al, sr_al, qc_al, sc_al = mxq.quant_1x32_dual_batched(xd, fmt=fmt)
+    mxq.quant_1x32_dual_batched(xd, fmt=fmt, out=(qr_odd, sr.view(1, -1), qc, sc.view(1, -1)))
+    torch.cuda.synchronize()
+    assert torch.equal(qr_odd, qr_al) and torch.equal(sr, sr_al[0].reshape(-1))
+    assert torch.equal(qc, qc_al) and torch.equal(sc, sc_al[0].reshape(-1))
+    assert torch.all(base[:off] == 0xEE) and torch.all(base[off + R * C:] == 0xEE), "bytes outside were written"
+    oq, os_ = oracle.quant_rows_fmt(bits(x), 1 if fmt == "e5m2" else 0)
+    assert np.array_equal(u8(qr_odd[0]), oq)
+    assert np.array_equal(u8(sr), oracle.scale_tiled(os_).reshape(-1))
+
+
 def test_tiled_padding_is_zero():
     """Scale bytes outside the matrix in the tiled layout are written as 0."""
     mxq = _mxq()
