@@ -915,6 +915,50 @@ def vendor_mxfp8_tflops(dev, shapes):
     return out
 
 
+def vendor_mxfp8_sustained(dev, shape, seconds, operands):
+    """The vendor library's MXFP8 GEMM at one shape on the workload's own
+    quantized operands (payload bytes and MMA-tiled scale bytes of A [M, K] and
+    B [N, K], so that its power draw follows the same data), launched back to
+    back for about `seconds` (the length of this run's timed region): the power
+    state a long step reaches.  {"shape", "tflops", "seconds", "clocks"} or
+    {"error": why}.  A comparison only, beside the burst peak."""
+    import torch
+    if not hasattr(torch, "float8_e8m0fnu"):
+        return {"error": "this PyTorch has no float8_e8m0fnu"}
+    M, N, K = shape
+    try:
+        a_q, a_s, b_q, b_s = operands
+        a, b = a_q.view(torch.float8_e4m3fn), b_q.view(torch.float8_e4m3fn)
+        sa = a_s.view(torch.float8_e8m0fnu).view((M + 127) // 128 * 128, -1)
+        sb = b_s.view(torch.float8_e8m0fnu).view((N + 127) // 128 * 128, -1)
+        f = lambda: torch._scaled_mm(a, b.t(), sa, sb, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        f()
+        e1.record()
+        torch.cuda.synchronize()
+        reps = max(10, int(seconds / max(e0.elapsed_time(e1) / 1e3, 1e-6)))
+        sampler = ClockSampler(dev.index)
+        sampler.start()
+        time.sleep(0.2)
+        t_w0 = time.time()
+        e0.record()
+        for _ in range(reps):
+            f()
+        e1.record()
+        torch.cuda.synchronize()
+        t_w1 = time.time()
+        sampler.stop()
+        ms = e0.elapsed_time(e1)
+        return {"shape": f"{M}x{N}x{K}", "operands": "the workload's quantized X and W", "tflops": round(2.0 * M * N * K * reps / (ms / 1e3) / 1e12, 1),
+                "seconds": round(ms / 1e3, 3), "launches": reps, "clocks": sampler.summary(t_w0 - 0.05, t_w1 + 0.05)}
+    except Exception as ex:                              # noqa: BLE001 -- a comparison, not the product
+        return {"error": f"{type(ex).__name__}: {str(ex).splitlines()[0][:160]}"}
+
+
 # ---- the GPU arm ---------------------------------------------------------------------------
 
 def time_device(w, args, dev, world):
@@ -1146,6 +1190,17 @@ def run_gpu(args):
                               "CUDA events"}
         quant_alone_launches = args.steps * sum(LAUNCHES_PER_ENTRY.get(k[0], 1) for k in quant_kern)
 
+    # ---- the vendor's MXFP8 GEMM at this workload's shape, back to back for as
+    # long as the timed region above: the same power state as a long step
+    vendor_sustained = None
+    if not args.no_vendor_peak and all(hasattr(w, k) for k in ("M", "N", "K", "qx", "qw")):
+        torch.cuda.synchronize()
+        time.sleep(1.0)
+        vendor_sustained = vendor_mxfp8_sustained(dev, (w.M, w.N, w.K), max(0.2, total_s),
+                                                  (w.qx[0], w.qx[1], w.qw[0], w.qw[1]))
+        if "tflops" in vendor_sustained:
+            roofline["frac_of_vendor_sustained"] = round(r["gemm_tflops"] / vendor_sustained["tflops"], 4)
+
     # ---- further workloads timed in the same process (device side only)
     extra = {}
     extra_launches = 0
@@ -1188,7 +1243,8 @@ def run_gpu(args):
                 "gpu_launches": own_launches * args.steps + extra_launches + quant_alone_launches,
                 "gpu_launches_split": {w.name: own_launches * args.steps, "extra_workloads": extra_launches,
                                        "quant_alone": quant_alone_launches},
-                "clocks": main_clocks, "vendor_mxfp8_tflops": vendor, "impl": "mxq"}
+                "clocks": main_clocks, "vendor_mxfp8_tflops": vendor,
+                "vendor_mxfp8_sustained": vendor_sustained, "impl": "mxq"}
         if r["other_hbm"]:
             line["hbm_kernels"] = r["other_hbm"]
         if hasattr(w, "extra"):
