@@ -9,7 +9,13 @@
 // to FSDP", section 2.2, gate_up_proj / down_proj).  With the 32x32 recipe
 // the dgrad reads the one shared weight payload N-major (RFC section 3.1).
 //
-// Design (one CTA per SM, persistent over output tiles of 128 x BN):
+// Two kernels.  Every launch the pair kernel can take runs on CTA pairs
+// (clusters of two SMs, tcgen05 cta_group::2, 256 x 256 tiles; its own section
+// below).  The single-CTA kernel takes the rest (more than 512 experts, a
+// tensor map the driver refuses to encode, a device with one SM) and is the
+// design the pair kernel extends.
+//
+// Single-CTA design (one CTA per SM, persistent over output tiles of 128 x BN):
 //   warp 0      TMA producer: A and B tiles (128-byte swizzle) and the
 //               512-byte scale atoms, into a ring of STAGES shared-memory
 //               slots guarded by full/empty mbarriers.
