@@ -54,12 +54,12 @@ L2_BYTES = 129 * 10**6
 # GEMM launches like `units_per_launch`, from an ncu capture of the kernel as it
 # stands; None where not captured (or captured before the kernel last changed).
 GEMM_TRAFFIC_BYTES = {
-    # gemm_mxf8_pair_kernel<0,0> as it stands (ncu dram__bytes_read/write.sum, the second
-    # step's launches): forward 9.97 GB read + 0.534 GB written, dgrad + wgrad 22.02 + 1.07 GB;
-    # the re-reads of B vary between calls (5.7-10 GB for the forward)
-    "sweep_16384": int((9.97e9 + 0.534e9 + 22.02e9 + 1.07e9) / 2),
-    # the same kernel at 8192x4096x4096: forward 51.96 + 33.93 MB, dgrad + wgrad 138.15 + 65.79 MB
-    "linear_train": int((51.96e6 + 33.93e6 + 138.15e6 + 65.79e6) / 2),
+    # gemm_mxf8_pair_kernel as it stands (ncu dram__bytes_read/write.sum, the second step's
+    # launches).  sweep_16384 runs on clusters of two pairs <0,0,4>: forward 5.34 GB read +
+    # 0.531 GB written, dgrad + wgrad 12.72 + 1.065 GB
+    "sweep_16384": int((5.34e9 + 0.531e9 + 12.72e9 + 1.065e9) / 2),
+    # 8192x4096x4096 on single pairs <0,0,2>: forward 51.96 + 33.95 MB, dgrad + wgrad 137.80 + 65.78 MB
+    "linear_train": int((51.96e6 + 33.95e6 + 137.80e6 + 65.78e6) / 2),
 }
 DEFAULT_WORKLOAD = "sweep_16384"
 DEFAULT_EXTRA = "moe_grouped"

@@ -39,6 +39,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 
 #include "mxq_device.cuh"
 #include "mxq_internal.h"
@@ -913,16 +914,18 @@ struct PairTileInfo {
     int64_t y_row0;          // output row of A row 0 (grouped contraction: g * M)
 };
 
-// Raster order inside one m x n grid of pair tiles: bands of four 256-row tile
-// rows, n-tiles inside a band.
+// Raster order inside one m x n grid of cluster tiles (kPairs x 256 rows by 256
+// columns): bands of 1024 rows for pairs and of 2048 rows (four tile rows) for
+// clusters of two pairs, n-tiles inside a band.
+template <int kPairs>
 __device__ __forceinline__ void pair_raster(int64_t local, int64_t m_tiles, int64_t n_tiles, int64_t& m0,
                                             int64_t& n0) {
-    constexpr int kBand = kRasterBand / 2;
+    constexpr int kBand = kPairs == 2 ? 4 : kRasterBand / 2;
     const int64_t per_band = static_cast<int64_t>(kBand) * n_tiles;
     const int64_t band = local / per_band, within = local - band * per_band;
     const int64_t mb = band * kBand;
     const int64_t bh = min(static_cast<int64_t>(kBand), m_tiles - mb);
-    m0 = (mb + within % bh) * 256;
+    m0 = (mb + within % bh) * (256 * kPairs);
     n0 = (within / bh) * 256;
 }
 
@@ -937,9 +940,11 @@ struct PairSchedule {
     int64_t m_tiles, n_tiles, total;
 };
 
-template <int kMode>
+// t is a cluster tile; pp is the pair's index in its cluster (dense modes:
+// the pairs of a cluster take consecutive 256-row tiles of one column of tiles).
+template <int kMode, int kPairs = 1>
 __device__ __forceinline__ PairTileInfo pair_tile_info(const PairSchedule& s, const GemmArgs& p, int64_t t,
-                                                       uint32_t rank) {
+                                                       uint32_t rank, uint32_t pp = 0) {
     PairTileInfo ti;
     ti.kb0 = 0;
     ti.y_row0 = 0;
@@ -948,8 +953,8 @@ __device__ __forceinline__ PairTileInfo pair_tile_info(const PairSchedule& s, co
         ti.prob = problem_of(p, t);
         const Problem& P = p.pr[ti.prob];
         int64_t m0p;
-        pair_raster(t - P.first_item, P.m_tiles, P.n_tiles, m0p, ti.n0);
-        ti.m0 = m0p + 128 * rank;
+        pair_raster<kPairs>(t - P.first_item, P.m_tiles, P.n_tiles, m0p, ti.n0);
+        ti.m0 = m0p + 256 * pp + 128 * rank;
         ti.a_band = ti.m0 / 128;
         ti.row_lo = ti.m0;
         ti.row_hi = min(ti.m0 + 128, P.M);
@@ -960,7 +965,7 @@ __device__ __forceinline__ PairTileInfo pair_tile_info(const PairSchedule& s, co
         const int64_t per = s.m_tiles * s.n_tiles;
         const int64_t g = t / per;
         int64_t m0p;
-        pair_raster(t - g * per, s.m_tiles, s.n_tiles, m0p, ti.n0);
+        pair_raster<1>(t - g * per, s.m_tiles, s.n_tiles, m0p, ti.n0);
         ti.m0 = m0p + 128 * rank;
         ti.a_band = ti.m0 / 128;
         ti.row_lo = ti.m0;
@@ -1003,18 +1008,30 @@ __device__ __forceinline__ PairTileInfo pair_tile_info(const PairSchedule& s, co
     return ti;
 }
 
-template <bool kMnMajor, int kMode>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kMode>::kThreads, 1)
+// kCluster = 2: one pair per cluster.  kCluster = 4 (dense modes): two pairs
+// per cluster take vertically adjacent pair tiles of one column of tiles, which
+// read the same B tile: each CTA loads half of its 128 B rows per stage and
+// multicasts them to itself and to the CTA of the same rank in the other pair,
+// so a cluster reads each B tile from L2 once.  A stage's slot is then written
+// by both pairs' producers, and is free when both pairs' MMAs have read it: the
+// empty barriers take a commit from each pair.
+template <bool kMnMajor, int kMode, int kCluster>
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(PairCfg<kMode>::kThreads, 1)
     gemm_mxf8_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p) {
     using L = PairCfg<kMode>;
     constexpr int STAGES = L::kStages;
+    constexpr int kPairs = kCluster / 2;
+    static_assert(kCluster == 2 || (kCluster == 4 && !L::kGrouped), "clusters of two pairs: dense modes only");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = blockIdx.x & 1u;   // rank in the cluster of two
+    const uint32_t crank = blockIdx.x % kCluster;   // rank in the (one-dimensional) cluster
+    const uint32_t rank = crank & 1u;               // rank in the pair
+    const uint32_t pp = crank >> 1;                 // the pair's index in the cluster
+    const uint32_t lead = crank & ~1u;              // cluster rank of the pair's even CTA
     const bool leader = rank == 0;
 
     const uint32_t bar0 = sbase + L::kOffBar;
@@ -1030,7 +1047,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kMode>::kThr
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);      // the even CTA's producer arrives (with both CTAs' bytes)
-            mbar_init(empty_bar(s), 1);     // the even CTA's multicast commit
+            mbar_init(empty_bar(s), kPairs);   // each pair's even CTA's multicast commit
         }
         mbar_init(tfull_bar, 1);
         mbar_init(tempty_bar, 2 * L::kEpiWarps);   // every epilogue warp of both CTAs
@@ -1119,8 +1136,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kMode>::kThr
         if (static_cast<int64_t>(sch.prefix[p.G]) * kBK > p.pr[0].K) sch.total = 0;   // slots past the operands
     }
     const int64_t total = sch.total;
-    const int64_t pair_id = blockIdx.x >> 1;
-    const int64_t n_pairs = gridDim.x >> 1;
+    const int64_t pair_id = blockIdx.x / kCluster;   // this cluster's index, and the count
+    const int64_t n_pairs = gridDim.x / kCluster;
     // Item of this pair's r-th round: dense problems come longest K first, and
     // dense launches take odd rounds in reverse pair order.
     auto item_of = [&](int64_t r) -> int64_t {
@@ -1134,11 +1151,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kMode>::kThr
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            const uint32_t full0 = leader ? full_bar(0) : mapa_shared(full_bar(0), 0);
+            const uint32_t full0 = leader ? full_bar(0) : mapa_shared(full_bar(0), lead);
             for (int64_t r = 0; r * n_pairs < total && !*abort_flag; ++r) {
                 const int64_t t = item_of(r);
                 if (t >= total) continue;
-                const PairTileInfo ti = pair_tile_info<kMode>(sch, p, t, rank);
+                const PairTileInfo ti = pair_tile_info<kMode, kPairs>(sch, p, t, rank, pp);
                 const Problem& P = p.pr[ti.prob];
                 const CUtensorMap* ma_map = &maps.a[ti.prob];
                 const CUtensorMap* mb_map = &maps.b[ti.prob];
@@ -1155,10 +1172,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kMode>::kThr
                     const uint32_t ssb = sbase + L::kOffSfb + stage * L::kSfbBytes;
                     const int32_t kx = static_cast<int32_t>((ti.kb0 + kb) * kBK);
                     tma_load_2d_pair(sbase + L::kOffA + stage * L::kABytes, ma_map, kx, ma, fb);
-                    if constexpr (!kMnMajor)
-                        tma_load_2d_pair(sbase + L::kOffB + stage * L::kBBytes, mb_map, kx, nb, fb);
-                    else   // B stored [K, N]: this CTA's 128 columns x 128 K-rows
-                        tma_load_2d_pair(sbase + L::kOffB + stage * L::kBBytes, mb_map, nb, kx, fb);
+                    if constexpr (kPairs == 1) {
+                        if constexpr (!kMnMajor)
+                            tma_load_2d_pair(sbase + L::kOffB + stage * L::kBBytes, mb_map, kx, nb, fb);
+                        else   // B stored [K, N]: this CTA's 128 columns x 128 K-rows
+                            tma_load_2d_pair(sbase + L::kOffB + stage * L::kBBytes, mb_map, nb, kx, fb);
+                    } else {   // half pp of this CTA's B (64 rows: N rows, or K rows when N-major), both pairs
+                        const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (2 + rank)));
+                        const uint32_t bdst = sbase + L::kOffB + stage * L::kBBytes + pp * (L::kBBytes / 2);
+                        if constexpr (!kMnMajor)
+                            tma_load_2d_pair_mc(bdst, mb_map, kx, nb + 64 * static_cast<int32_t>(pp), fb, mask);
+                        else
+                            tma_load_2d_pair_mc(bdst, mb_map, nb, kx + 64 * static_cast<int32_t>(pp), fb, mask);
+                    }
                     tma_load_2d_pair(sbase + L::kOffSfa + stage * 512, &maps.sfa[ti.prob], 0, sfa_row + 2 * kb, fb);
                     tma_load_2d_pair(ssb, &maps.sfb[ti.prob], 0, sfb_row0 + 2 * kb, fb);
                     tma_load_2d_pair(ssb + 512, &maps.sfb[ti.prob], 0, sfb_row1 + 2 * kb, fb);
@@ -1193,7 +1219,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kMode>::kThr
                 if (!__shfl_sync(0xFFFFFFFFu, got, 0)) { ok = false; break; }
                 tc_fence_after();
                 const int q = kMode == kDense || kMode == kDenseQuant ? problem_of(p, t) : 0;
-                const int nkb = kMode == kGroupedK ? pair_tile_info<kMode>(sch, p, t, 0).nkb : p.pr[q].num_kb;
+                const int nkb = kMode == kGroupedK ? pair_tile_info<kMode>(sch, p, t, 0u).nkb : p.pr[q].num_kb;
                 const int64_t K = p.pr[q].K;
                 const uint32_t fmt_bits = p.pr[q].fmt_bits;
                 for (int kb = 0; kb < nkb; ++kb) {
@@ -1221,13 +1247,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kMode>::kThr
                                 tc_mma_mxf8_pair(tmem_base, a_desc + ((k * kUmmaK) >> 4), b_desc + k * kBStepK,
                                                  make_idesc_mxf8(256, 256, kMnMajor ? 1u : 0u, k, k) | fmt_bits,
                                                  sfa_t, sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
-                        tc_commit_pair_multicast(empty_bar(stage), 0x3);   // frees the slot in both CTAs
+                        // frees the slot in every CTA of the cluster (each counts the commits of all pairs)
+                        tc_commit_pair_multicast(empty_bar(stage), kCluster == 4 ? 0xF : 0x3);
                     }
                     __syncwarp();
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                if (elect_one()) tc_commit_pair_multicast(tfull_bar, 0x3);
+                if (elect_one()) tc_commit_pair_multicast(tfull_bar, static_cast<uint16_t>(0x3u << lead));
                 __syncwarp();
                 acc_phase ^= 1u;
             }
@@ -1245,13 +1272,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kMode>::kThr
         // ---- epilogue (both CTAs; warps 2..9) ----------------------------------------
         const int quad = warp & 3;
         const int half = (warp - 2) >> 2;
-        const uint32_t tempty_leader = leader ? tempty_bar : mapa_shared(tempty_bar, 0);
+        const uint32_t tempty_leader = leader ? tempty_bar : mapa_shared(tempty_bar, lead);
         uint32_t acc_phase = 0;
         bool pending = false;   // a tiled store of this warp may still read its buffer
         for (int64_t r = 0; r * n_pairs < total; ++r) {
             const int64_t t = item_of(r);
             if (t >= total) continue;
-            const PairTileInfo ti = pair_tile_info<kMode>(sch, p, t, rank);
+            const PairTileInfo ti = pair_tile_info<kMode, kPairs>(sch, p, t, rank, pp);
             const Problem& P = p.pr[ti.prob];
             // One thread waits (suspending), the other epilogue warps sleep on a
             // named barrier; barrier 2 keeps the verdict until every warp read it.
@@ -1413,10 +1440,10 @@ bool make_tma_scales(CUtensorMap* map, const void* ptr, int64_t bands, int64_t k
 }
 
 // Scale maps and the scale-row range check of a pair launch: an operand with
-// `bands` 128-row bands of k_atoms atoms (rows up to two bands past the end are
-// addressed, and read as zeros).
+// `bands` 128-row bands of k_atoms atoms (rows up to three bands past the end
+// are addressed, and read as zeros).
 bool pair_scale_map(CUtensorMap* map, const void* ptr, int64_t bands, int64_t k_atoms) {
-    if ((bands + 2) * k_atoms * 2 >= (int64_t(1) << 31)) return false;
+    if ((bands + 4) * k_atoms * 2 >= (int64_t(1) << 31)) return false;
     return make_tma_scales(map, ptr, bands, k_atoms);
 }
 
@@ -1424,7 +1451,9 @@ bool pair_scale_map(CUtensorMap* map, const void* ptr, int64_t bands, int64_t k_
 // them), their 256 x 256 pair tiles laid out back to back.  False when a tensor
 // map cannot be encoded or a scale map's rows exceed its 32-bit coordinates
 // (the single-CTA kernel then runs the launch).
-bool fill_dense_pair(const DenseGemm* gemms, int count, bool b_mn_major, PairMaps* maps, GemmArgs* args) {
+bool fill_dense_pair(const DenseGemm* gemms, int count, bool b_mn_major, int pairs, PairMaps* maps,
+                     GemmArgs* args) {
+    const uint32_t b_box = static_cast<uint32_t>(128 / pairs);   // B rows (or K rows) one CTA loads per stage
     int order[kMaxProblems];
     for (int i = 0; i < count; ++i) order[i] = i;
     for (int i = 1; i < count; ++i)
@@ -1438,9 +1467,9 @@ bool fill_dense_pair(const DenseGemm* gemms, int count, bool b_mn_major, PairMap
         const int64_t a_bands = (g.M + 127) / 128, b_bands = (g.N + 127) / 128;
         if (!make_tma_u8(&maps->a[i], g.a_q, static_cast<uint64_t>(g.M), static_cast<uint64_t>(g.K), 128)) return false;
         if (!b_mn_major) {
-            if (!make_tma_u8(&maps->b[i], g.b_q, static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.K), 128))
+            if (!make_tma_u8(&maps->b[i], g.b_q, static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.K), b_box))
                 return false;
-        } else if (!make_tma_u8(&maps->b[i], g.b_q, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.N), kBK)) {
+        } else if (!make_tma_u8(&maps->b[i], g.b_q, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.N), b_box)) {
             return false;
         }
         if (!pair_scale_map(&maps->sfa[i], g.a_s, a_bands, k_atoms) ||
@@ -1448,7 +1477,7 @@ bool fill_dense_pair(const DenseGemm* gemms, int count, bool b_mn_major, PairMap
             return false;
         args->pr[i] = make_problem(g.a_s, g.b_s, g.y, g.M, g.N, g.K, g.ldy, k_atoms, b_bands,
                                    fmt_bits_of(g.a_fmt, g.b_fmt));
-        args->pr[i].m_tiles = (g.M + 255) / 256;   // pair tiles
+        args->pr[i].m_tiles = (g.M + 256 * pairs - 1) / (256 * pairs);   // cluster tiles
         args->pr[i].n_tiles = (g.N + 255) / 256;
         set_store_map(&maps->y[i], &args->pr[i], g.y, g.M, g.N, g.ldy);
         args->pr[i].first_item = items;
@@ -1459,22 +1488,73 @@ bool fill_dense_pair(const DenseGemm* gemms, int count, bool b_mn_major, PairMap
     return true;
 }
 
-template <bool kMnMajor, int kMode>
-cudaError_t launch_pair_t(const DeviceInfo& dev, const PairMaps& maps, const GemmArgs& args, int64_t max_tiles,
-                          cudaStream_t stream) {
+// Clusters of kCluster CTAs of the pair kernel that the device holds at once
+// (set up once per device and thread).  Pairs always cover every SM; clusters
+// of four need four SMs of one GPC, and a GPC whose SM count is not a multiple
+// of four leaves SMs idle (on GB300: 36 clusters, 144 of the 152 SMs).
+template <bool kMnMajor, int kMode, int kCluster>
+cudaError_t pair_clusters(const DeviceInfo& dev, int64_t* clusters) {
     using L = PairCfg<kMode>;
-    auto kern = gemm_mxf8_pair_kernel<kMnMajor, kMode>;
-    static thread_local int configured_device = -1;  // attribute set once per device and thread
+    auto kern = gemm_mxf8_pair_kernel<kMnMajor, kMode, kCluster>;
+    static thread_local int configured_device = -1;
+    static thread_local int64_t max_clusters = 0;
     if (configured_device != dev.device) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
         if (e != cudaSuccess) return e;
+        int64_t n = dev.sm_count / kCluster;
+        if (kCluster > 2 && n > 0) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(kCluster * n), 1, 1);
+            cfg.blockDim = dim3(L::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = L::kAlloc;
+            int active = 0;
+            e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
+            if (e != cudaSuccess) return e;
+            n = min(n, static_cast<int64_t>(active));
+        }
+        max_clusters = n;
         configured_device = dev.device;
     }
-    int64_t pairs = dev.sm_count / 2;
-    if (max_tiles >= 0 && max_tiles < pairs) pairs = max_tiles;
-    if (pairs <= 0) return cudaSuccess;
-    kern<<<static_cast<unsigned>(2 * pairs), L::kThreads, L::kAlloc, stream>>>(maps, args);
+    *clusters = max_clusters;
+    return cudaSuccess;
+}
+
+template <bool kMnMajor, int kMode, int kCluster = 2>
+cudaError_t launch_pair_t(const DeviceInfo& dev, const PairMaps& maps, const GemmArgs& args, int64_t max_tiles,
+                          cudaStream_t stream) {
+    using L = PairCfg<kMode>;
+    int64_t units = 0;
+    const cudaError_t e = pair_clusters<kMnMajor, kMode, kCluster>(dev, &units);
+    if (e != cudaSuccess) return e;
+    if (max_tiles >= 0 && max_tiles < units) units = max_tiles;
+    if (units <= 0) return cudaSuccess;
+    gemm_mxf8_pair_kernel<kMnMajor, kMode, kCluster>
+        <<<static_cast<unsigned>(kCluster * units), L::kThreads, L::kAlloc, stream>>>(maps, args);
     return cudaGetLastError();
+}
+
+// Pairs per cluster for a dense launch of `pair_tiles` 256 x 256 tiles.
+// Clusters of two pairs read each B tile from L2 once per cluster instead of
+// once per pair, and their launches move fewer bytes through L2 and DRAM.  Under
+// the power cap that a long run of large GEMMs reaches, the lower draw shows as a
+// higher SM clock, and that outweighs the SMs they leave idle.  In short bursts
+// at full clock the idle SMs and the coarser waves make them slower.  Launches
+// of at least kQuadMinPairTiles tiles take clusters of two pairs where the device
+// holds them; MXQ_GEMM_CLUSTER=2 or 4 overrides the choice.
+constexpr int64_t kQuadMinPairTiles = 2048;
+
+template <bool kMnMajor, int kMode>
+int dense_pairs_per_cluster(const DeviceInfo& dev, int64_t pair_tiles) {
+    const char* env = std::getenv("MXQ_GEMM_CLUSTER");
+    bool quad = pair_tiles >= kQuadMinPairTiles;
+    if (env != nullptr && (env[0] == '2' || env[0] == '4') && env[1] == '\0') quad = env[0] == '4';
+    if (!quad) return 1;
+    int64_t quads = 0;
+    if (pair_clusters<kMnMajor, kMode, 4>(dev, &quads) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    return quads > 0 ? 2 : 1;
 }
 
 // A dense launch on CTA pairs; *done false when the pair kernel cannot take it.
@@ -1483,9 +1563,13 @@ cudaError_t try_pair(const DeviceInfo& dev, const DenseGemm* gemms, int count, b
                      uint8_t* ys, cudaStream_t stream, bool* done) {
     *done = false;
     if (dev.sm_count < 2) return cudaSuccess;
+    int64_t pair_tiles = 0;
+    for (int i = 0; i < count; ++i) pair_tiles += ((gemms[i].M + 255) / 256) * ((gemms[i].N + 255) / 256);
+    const int pairs = b_mn_major ? dense_pairs_per_cluster<true, kMode>(dev, pair_tiles)
+                                 : dense_pairs_per_cluster<false, kMode>(dev, pair_tiles);
     PairMaps maps;
     GemmArgs args = base_args(dev);
-    if (!fill_dense_pair(gemms, count, b_mn_major, &maps, &args)) return cudaSuccess;
+    if (!fill_dense_pair(gemms, count, b_mn_major, pairs, &maps, &args)) return cudaSuccess;
     args.yq = yq;
     args.ys = ys;
     args.yq_tma = 0;
@@ -1494,6 +1578,10 @@ cudaError_t try_pair(const DeviceInfo& dev, const DenseGemm* gemms, int count, b
                                    static_cast<uint64_t>(gemms[0].M), static_cast<uint64_t>(gemms[0].N)))
         args.yq_tma = 1;
     *done = true;
+    if (pairs == 2) {
+        if (b_mn_major) return launch_pair_t<true, kMode, 4>(dev, maps, args, args.items, stream);
+        return launch_pair_t<false, kMode, 4>(dev, maps, args, args.items, stream);
+    }
     if (b_mn_major) return launch_pair_t<true, kMode>(dev, maps, args, args.items, stream);
     return launch_pair_t<false, kMode>(dev, maps, args, args.items, stream);
 }
