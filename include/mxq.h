@@ -221,6 +221,12 @@ mxq_status mxq_quant_32x32_fmt(const void* w, int64_t n, int64_t k, int64_t ld,
  *   dgrad    A = dY row copy,  B = W column copy        (N = in, K = out)
  *            or, 32x32, B = W payload MN-major with s_bwd
  *   wgrad    A = dY column copy, B = X column copy      (M = out, N = in, K = tokens)
+ * Schedule: launches of 2048 or more 256 x 256 output tiles (this call's and
+ * mxq_gemm_bf16out_multi's, counted over all its GEMMs) run on clusters of two
+ * SM pairs that share each B tile; smaller ones on single pairs.  The results
+ * are bit-identical either way.  The environment variable MXQ_GEMM_CLUSTER,
+ * read at each call, fixes the choice: "2" single pairs, "4" clusters of two
+ * pairs (where the device holds them).
  */
 mxq_status mxq_gemm_bf16out(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
                             int64_t M, int64_t N, int64_t K, int b_mn_major,
