@@ -1186,8 +1186,17 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(PairCfg<kMode
                             tma_load_2d_pair_mc(bdst, mb_map, nb, kx + 64 * static_cast<int32_t>(pp), fb, mask);
                     }
                     tma_load_2d_pair(sbase + L::kOffSfa + stage * 512, &maps.sfa[ti.prob], 0, sfa_row + 2 * kb, fb);
-                    tma_load_2d_pair(ssb, &maps.sfb[ti.prob], 0, sfb_row0 + 2 * kb, fb);
-                    tma_load_2d_pair(ssb + 512, &maps.sfb[ti.prob], 0, sfb_row1 + 2 * kb, fb);
+                    // Every CTA of the cluster needs the same two B scale atoms (the
+                    // scales of all 256 B rows): each CTA loads its share once and
+                    // multicasts it to all.  Pairs: atom `rank` to both CTAs.  Two
+                    // pairs: row crank & 1 of atom crank >> 1 to all four.
+                    if constexpr (kPairs == 1) {
+                        tma_load_2d_pair_mc(ssb + 512 * rank, &maps.sfb[ti.prob], 0,
+                                            (rank ? sfb_row1 : sfb_row0) + 2 * kb, fb, 0x3);
+                    } else {
+                        const int32_t srow = ((crank >> 1) ? sfb_row1 : sfb_row0) + 2 * kb + static_cast<int32_t>(crank & 1);
+                        tma_load_2d_pair_mc(ssb + 256 * crank, &maps.sfb[ti.prob], 0, srow, fb, 0xF);
+                    }
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (stop) break;
@@ -1434,17 +1443,17 @@ bool fill_dense(const DenseGemm* gemms, int count, bool b_mn_major, TensorMaps* 
 
 // MMA-tiled scales of an operand with `bands` 128-row bands of k_atoms atoms,
 // as rows of 256 bytes (one atom = a 2 x 256 box at row 2 (band k_atoms + kb)).
-bool make_tma_scales(CUtensorMap* map, const void* ptr, int64_t bands, int64_t k_atoms) {
+bool make_tma_scales(CUtensorMap* map, const void* ptr, int64_t bands, int64_t k_atoms, uint32_t box_rows = 2) {
     return encode_tensor_map_2d(map, ptr, false, 256u, static_cast<uint64_t>(bands * k_atoms * 2), 256u, 256u,
-                                2u, false);
+                                box_rows, false);
 }
 
 // Scale maps and the scale-row range check of a pair launch: an operand with
 // `bands` 128-row bands of k_atoms atoms (rows up to three bands past the end
 // are addressed, and read as zeros).
-bool pair_scale_map(CUtensorMap* map, const void* ptr, int64_t bands, int64_t k_atoms) {
+bool pair_scale_map(CUtensorMap* map, const void* ptr, int64_t bands, int64_t k_atoms, uint32_t box_rows = 2) {
     if ((bands + 4) * k_atoms * 2 >= (int64_t(1) << 31)) return false;
-    return make_tma_scales(map, ptr, bands, k_atoms);
+    return make_tma_scales(map, ptr, bands, k_atoms, box_rows);
 }
 
 // The problems of one dense pair launch (K descending, as fill_dense orders
@@ -1473,7 +1482,7 @@ bool fill_dense_pair(const DenseGemm* gemms, int count, bool b_mn_major, int pai
             return false;
         }
         if (!pair_scale_map(&maps->sfa[i], g.a_s, a_bands, k_atoms) ||
-            !pair_scale_map(&maps->sfb[i], g.b_s, b_bands, k_atoms))
+            !pair_scale_map(&maps->sfb[i], g.b_s, b_bands, k_atoms, pairs == 2 ? 1u : 2u))
             return false;
         args->pr[i] = make_problem(g.a_s, g.b_s, g.y, g.M, g.N, g.K, g.ldy, k_atoms, b_bands,
                                    fmt_bits_of(g.a_fmt, g.b_fmt));
