@@ -221,7 +221,7 @@ mxq_status mxq_quant_32x32_fmt(const void* w, int64_t n, int64_t k, int64_t ld,
  *   dgrad    A = dY row copy,  B = W column copy        (N = in, K = out)
  *            or, 32x32, B = W payload MN-major with s_bwd
  *   wgrad    A = dY column copy, B = X column copy      (M = out, N = in, K = tokens)
- * Schedule: launches of 2048 or more 256 x 256 output tiles (this call's and
+ * Schedule: launches of 1536 or more 256 x 256 output tiles (this call's and
  * mxq_gemm_bf16out_multi's, counted over all its GEMMs) run on clusters of two
  * SM pairs that share each B tile; smaller ones on single pairs.  The results
  * are bit-identical either way.  The environment variable MXQ_GEMM_CLUSTER,

@@ -1543,14 +1543,15 @@ cudaError_t launch_pair_t(const DeviceInfo& dev, const PairMaps& maps, const Gem
 }
 
 // Pairs per cluster for a dense launch of `pair_tiles` 256 x 256 tiles.
-// Clusters of two pairs read each B tile from L2 once per cluster instead of
-// once per pair, and their launches move fewer bytes through L2 and DRAM.  Under
-// the power cap that a long run of large GEMMs reaches, the lower draw shows as a
-// higher SM clock, and that outweighs the SMs they leave idle.  In short bursts
-// at full clock the idle SMs and the coarser waves make them slower.  Launches
-// of at least kQuadMinPairTiles tiles take clusters of two pairs where the device
-// holds them; MXQ_GEMM_CLUSTER=2 or 4 overrides the choice.
-constexpr int64_t kQuadMinPairTiles = 2048;
+// Clusters of two pairs read each B tile (and its scales) from L2 once per
+// cluster instead of once per pair, and their launches move fewer bytes through
+// L2 and DRAM.  Per tile that is a little faster at full clock, and under the
+// power cap that a long run of large GEMMs reaches the lower draw also buys a
+// higher SM clock.  Against that they leave 8 of GB300's 152 SMs idle, and a
+// launch of few waves loses more to the coarser last wave.  Launches of at least
+// kQuadMinPairTiles tiles (about 20 waves of pairs) take clusters of two pairs
+// where the device holds them; MXQ_GEMM_CLUSTER=2 or 4 overrides the choice.
+constexpr int64_t kQuadMinPairTiles = 1536;
 
 template <bool kMnMajor, int kMode>
 int dense_pairs_per_cluster(const DeviceInfo& dev, int64_t pair_tiles) {
