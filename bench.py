@@ -55,11 +55,11 @@ L2_BYTES = 129 * 10**6
 # stands; None where not captured (or captured before the kernel last changed).
 GEMM_TRAFFIC_BYTES = {
     # gemm_mxf8_pair_kernel as it stands (ncu dram__bytes_read/write.sum, the second step's
-    # launches).  sweep_16384 runs on clusters of two pairs <0,0,4>: forward 5.34 GB read +
-    # 0.531 GB written, dgrad + wgrad 12.72 + 1.065 GB
-    "sweep_16384": int((5.34e9 + 0.531e9 + 12.72e9 + 1.065e9) / 2),
-    # 8192x4096x4096 on single pairs <0,0,2>: forward 51.96 + 33.95 MB, dgrad + wgrad 137.80 + 65.78 MB
-    "linear_train": int((51.96e6 + 33.95e6 + 137.80e6 + 65.78e6) / 2),
+    # launches).  sweep_16384 runs on clusters of two pairs <0,0,4>: forward 3.664 GB read +
+    # 0.530 GB written, dgrad + wgrad 7.218 + 1.064 GB
+    "sweep_16384": int((3.664e9 + 0.530e9 + 7.218e9 + 1.064e9) / 2),
+    # 8192x4096x4096 on single pairs <0,0,2>: forward 51.97 + 33.52 MB, dgrad + wgrad 137.01 + 65.23 MB
+    "linear_train": int((51.97e6 + 33.52e6 + 137.01e6 + 65.23e6) / 2),
 }
 DEFAULT_WORKLOAD = "sweep_16384"
 DEFAULT_EXTRA = "moe_grouped"
