@@ -837,9 +837,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, kMode>::kThreads, 1)
 //
 // Output tiles of 256 x 256 per pair of SMs.  CTA rank r of the pair owns the
 // 128 rows of its half: it loads those rows of A, its 128-row half of the B
-// tile (B rows b_row + 128 r; N-major B: columns n0 + 128 r), its A scale atom
-// and both B scale atoms (every CTA's tensor core reads the scales of all 256
-// B rows from its own tensor memory), all completing on the even CTA's full
+// tile (B rows b_row + 128 r; N-major B: columns n0 + 128 r) and its A scale
+// atom; it also needs both B scale atoms (every CTA's tensor core reads the
+// scales of all 256 B rows from its own tensor memory), so CTA r loads atom r
+// and multicasts it to both.  All of it completes on the even CTA's full
 // barrier.  Warp 1 of the even CTA runs the tile and stage loops warp-uniformly
 // and one elected lane issues, per 128-deep stage, three pair scale copies and
 // four 256 x 256 x 32 pair MMAs, then a commit that frees the stage's slot in
